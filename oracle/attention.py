@@ -1,0 +1,101 @@
+"""GQA attention over the quantised cache (oracle side).
+
+Page "sparkle mlx_streaming/core/cache/quant_kv.py", `asym_quantized_sdpa`:
+queries are scaled, reshaped so that query head h reads kv head h // rep
+(rep = Hq / Hkv), scored against the dequantised keys, masked (a string mask
+means causal with query i at absolute position kL - qL + i), soft-maxed, and
+multiplied by the dequantised values.  The result is still in rotated value
+space; the caller applies the inverse rotation, here `o @ M_b^T`.
+
+Readings:
+
+* The queries are rotated like the keys: q' = bf16(q @ M_b) (same rule as
+  `codec.rotate`), then multiplied by the caller's scale, 1/sqrt(D).
+* Scores, softmax, P*V and the inverse rotation are carried out in float64 on
+  the exactly dequantised cache; only the final output is rounded (to
+  bfloat16).  The page's MLX kernels would round intermediates to the query
+  dtype; the method's accuracy target (bf16 I/O, fp32 accumulation) is read as
+  "no intermediate rounding".
+* Masked scores are -inf (the page uses the dtype's most negative finite
+  value; with at least one unmasked key per row the two give the same
+  softmax).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import codec
+from .bf16 import round_bf16
+
+
+def inverse_rotate(o, blocks_b) -> np.ndarray:
+    """o @ M_b^T per 4-wide block, float64."""
+    o = np.asarray(o, dtype=np.float64)
+    m = np.asarray(blocks_b, dtype=np.float64)
+    nb = m.shape[0]
+    o4 = o.reshape(o.shape[:-1] + (nb, 4))
+    out = np.einsum('...bj,bij->...bi', o4, m)
+    return out.reshape(o.shape)
+
+
+def softmax_rows(s) -> np.ndarray:
+    s = np.asarray(s, dtype=np.float64)
+    m = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def attend_slice(q_rows, k_hat, v_hat, blocks_b, scale, causal, q_pos=None):
+    """Attention for query rows of one kv head.
+
+    q_rows float32 [R, D] (bfloat16 values, unrotated); k_hat, v_hat float64 [T, D];
+    q_pos int [R]: absolute position of each row's query (causal limit t <= q_pos).
+    Returns float64 [R, D] in unrotated space.
+    """
+    qr = codec.rotate(q_rows, blocks_b).astype(np.float64) * float(scale)
+    s = qr @ k_hat.T
+    if causal:
+        t = np.arange(k_hat.shape[0])
+        s = np.where(t[None, :] <= np.asarray(q_pos)[:, None], s, -np.inf)
+    p = softmax_rows(s)
+    return inverse_rotate(p @ v_hat, blocks_b)
+
+
+def attend(q, cache, blocks_b, scale=None, causal=False, heads=None, batches=None,
+           query_index=None):
+    """Full oracle attention.
+
+    q float32 [B, Hq, L, D]; cache an `OracleCache` already holding the queries'
+    own keys/values when causal.  Returns float64 [B, Hq, L, D] (entries of
+    skipped rows left as NaN when `heads` / `batches` / `query_index` subsample).
+    """
+    q = np.asarray(q, dtype=np.float32)
+    B, Hq, L, D = q.shape
+    rep = Hq // cache.kv_heads
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.full(q.shape, np.nan, dtype=np.float64)
+    bs = range(B) if batches is None else batches
+    hs = range(Hq) if heads is None else heads
+    qi = np.arange(L) if query_index is None else np.asarray(query_index)
+    for b in bs:
+        T = int(cache.lens[b])
+        if T <= 0:
+            raise ValueError("attention over an empty sequence")
+        by_kv = {}
+        for h in hs:
+            by_kv.setdefault(h // rep, []).append(h)
+        for kvh, hl in by_kv.items():
+            kh, vh = cache.dequantized(b, kvh)
+            rows = q[b, hl][:, qi].reshape(-1, D)
+            pos = np.tile(T - L + qi, len(hl))
+            o = attend_slice(rows, kh, vh, blocks_b, scale, causal, pos)
+            o = o.reshape(len(hl), len(qi), D)
+            for j, h in enumerate(hl):
+                out[b, h, qi] = o[j]
+    return out
+
+
+def to_bf16(out64) -> np.ndarray:
+    """Final output rounding to bfloat16 (via float32), as float32 values."""
+    return round_bf16(np.asarray(out64, dtype=np.float32))
