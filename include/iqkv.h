@@ -1,0 +1,200 @@
+/*
+ * iqkv.h — C ABI of libiqkv: a rotated, asymmetric K4/V3 bit-packed KV cache
+ * and GQA decode / short-query verify attention over it, for one sm_103a GPU.
+ *
+ * Source of the method: the page "sparkle mlx_streaming/core/cache/quant_kv.py"
+ * (sections "SO(4) block rotation", "AsymmetricQuantizedKVCache",
+ * "asym_quantized_sdpa") and the page "sparkle mlx_streaming/mtp/kv_cache.py"
+ * (`commit_verified_prefix`, `_snapshot` / `_restore`, `tile_caches`,
+ * `commit_tree_row`).
+ *
+ * Conventions shared by every entry point:
+ *  - Every device buffer is allocated and owned by the caller; the library
+ *    never allocates, frees or keeps a pointer after a call returns.
+ *  - Work is enqueued asynchronously on the caller's stream (`iq_stream_t` is a
+ *    `cudaStream_t`; NULL is the legacy default stream).  No entry point
+ *    synchronises the device, except `iq_read_status`, which says so.
+ *  - bfloat16 values travel as `uint16_t` bit patterns.
+ *  - Functions return an `iq_status`; nothing is thrown across the ABI.  On an
+ *    error nothing is enqueued and nothing the caller owns is modified, and
+ *    `iq_last_error()` holds a one-line explanation (per host thread).
+ *  - Supported shapes: head_dim 256, group_size 64, k_bits 4, v_bits 3,
+ *    1 <= batch <= IQ_MAX_BATCH, kv heads >= 1, query heads a multiple of kv
+ *    heads with at most 8 query heads per kv head and 8 % rep == 0.  Anything
+ *    else returns IQ_ERR_UNSUPPORTED.
+ */
+#ifndef IQKV_H
+#define IQKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IQ_MAX_BATCH 256
+#define IQ_STEP 256 /* capacity granule, the page's `AsymmetricQuantizedKVCache.step` */
+
+typedef void* iq_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  IQ_OK = 0,
+  IQ_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer, bad mask */
+  IQ_ERR_CAPACITY = 2,    /* an append would write past the cache capacity */
+  IQ_ERR_WORKSPACE = 3,   /* workspace missing or smaller than iq_attend_workspace() */
+  IQ_ERR_UNSUPPORTED = 4, /* valid but not built: other dims / bits / group sizes */
+  IQ_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, copy, attribute) */
+  IQ_ERR_DEVICE = 6       /* a kernel reported a failure in its status word */
+} iq_status;
+
+/* Static, NUL-terminated name of a status code ("IQ_OK", ...). */
+const char* iq_status_string(int status);
+
+/* Last error message of the calling host thread ("" if none). */
+const char* iq_last_error(void);
+
+/*
+ * iq_build_rotation — the seed-fixed block-diagonal rotation
+ * (quant_kv.py, `build_block_so4`, `_quat_left`, `_quat_right_conj`).
+ *
+ * draws_host: host float32 [head_dim/4][2][4], the raw standard-normal draws of
+ *   each block's left then right quaternion, in generator order (the caller
+ *   draws them; the library normalises them in float32 and forms
+ *   L(qL) . R(qR) with float64 accumulation, rounded once to float32).
+ * rot_f32: device float32 [head_dim/4][4][4] out (the blocks of M).
+ * rot_bf16: device bf16 [head_dim/4][4][4] out (M_b = bf16(M), what the cache
+ *   and attention use).
+ * The draws are copied to the device before the call returns, so the host
+ * buffer may be reused at once.  Errors: INVALID_ARG (null, head_dim not a
+ * positive multiple of 4), UNSUPPORTED (head_dim != 256), CUDA.
+ */
+int iq_build_rotation(int head_dim, const float* draws_host, float* rot_f32,
+                      uint16_t* rot_bf16, iq_stream_t stream);
+
+/*
+ * iq_cache — plain descriptor of one quantised cache
+ * (quant_kv.py, `AsymmetricQuantizedKVCache`: keys and values each stored as a
+ * (wq, scales, biases) triple).  The caller owns every pointer.
+ *
+ *   k_codes  uint32 [B][Hkv][capacity][head_dim*k_bits/32]  (LSB-first stream)
+ *   k_scales bf16   [B][Hkv][capacity][head_dim/group_size]
+ *   k_biases bf16   [B][Hkv][capacity][head_dim/group_size]
+ *   v_codes  uint32 [B][Hkv][capacity][head_dim*v_bits/32]
+ *   v_scales, v_biases bf16 as above
+ *   lens     HOST int32 [B]: tokens held by each sequence.  This host array is
+ *            the authoritative length; the library reads it to size launches
+ *            and passes lengths to kernels by value, and updates it in
+ *            iq_cache_append / iq_cache_trim / iq_cache_gather.
+ * Device buffers must be 16-byte aligned; capacity must be a positive multiple
+ * of IQ_STEP.  Rows at or past lens[b] are stale and are never read.
+ */
+typedef struct {
+  int32_t batch, kv_heads, head_dim, group_size, k_bits, v_bits, capacity;
+  uint32_t* k_codes;
+  uint16_t* k_scales;
+  uint16_t* k_biases;
+  uint32_t* v_codes;
+  uint16_t* v_scales;
+  uint16_t* v_biases;
+  int32_t* lens;
+} iq_cache;
+
+/*
+ * iq_cache_bytes — byte sizes of the six device buffers of a cache
+ * (quant_kv.py, `_init_quant`, `_packed_words`), in descriptor order
+ * (k_codes, k_scales, k_biases, v_codes, v_scales, v_biases).
+ * Errors: INVALID_ARG, UNSUPPORTED.
+ */
+int iq_cache_bytes(int batch, int kv_heads, int head_dim, int group_size, int k_bits,
+                   int v_bits, int capacity, size_t out_bytes[6]);
+
+/* iq_cache_check — validate a descriptor (shapes, alignment, lens in [0, capacity]). */
+int iq_cache_check(const iq_cache* cache);
+
+/* iq_cache_nbytes — total bytes of the six buffers (quant_kv.py, `nbytes`). */
+size_t iq_cache_nbytes(const iq_cache* cache);
+
+/*
+ * iq_cache_append — rotate, group-quantise, bit-pack and store n new tokens per
+ * sequence at rows [lens[b], lens[b] + n) (quant_kv.py, `rotate_last` +
+ * `update_and_fetch`; quantiser scale = (max-min)/(2^b-1), bias = min,
+ * code = clamp(round-half-even((x - bias)/scale))).
+ *
+ * keys, values: device bf16 [B][Hkv][n][head_dim], contiguous, unrotated.
+ * rot_bf16: device bf16 blocks from iq_build_rotation.
+ * On success lens[b] += n for every b.  n == 0 is a no-op.
+ * Errors: INVALID_ARG, CAPACITY (some lens[b] + n > capacity; grow first —
+ * see iq_cache_gather), UNSUPPORTED, CUDA.
+ */
+int iq_cache_append(iq_cache* cache, const uint16_t* keys, const uint16_t* values, int n,
+                    const uint16_t* rot_bf16, iq_stream_t stream);
+
+/*
+ * iq_cache_trim — drop the last tokens of each sequence
+ * (quant_kv.py, `trim`: n = min(offset, n); offset -= n; return n).
+ * Host-only bookkeeping: no device work, no stream.
+ * n_host: host int32 [B], non-negative counts.  trimmed_host: host int32 [B]
+ * out (may be NULL).  Errors: INVALID_ARG (null, negative count).
+ */
+int iq_cache_trim(iq_cache* cache, const int32_t* n_host, int32_t* trimmed_host);
+
+/*
+ * iq_cache_gather — dst sequence i becomes a copy of src sequence src_of[i]:
+ * rows [0, src.lens[src_of[i]]) of every kv head and all six buffers are
+ * copied device to device and dst.lens[i] is set to that length.
+ * This one copy serves capacity growth (identity map into a larger cache,
+ * quant_kv.py `update_and_fetch` growth), snapshot and restore
+ * (kv_cache.py `_snapshot` / `_restore`: the copy never aliases),
+ * tiling a batch-1 cache to P paths (kv_cache.py `tile_caches`: all zeros) and
+ * keeping the winning path (kv_cache.py `commit_tree_row`: one index).
+ * src_of: host int32 [dst.batch].  src and dst must share kv_heads, head_dim,
+ * group_size and bits, and must not overlap in memory.
+ * Errors: INVALID_ARG, CAPACITY (dst capacity too small), UNSUPPORTED, CUDA.
+ */
+int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of,
+                    iq_stream_t stream);
+
+/*
+ * iq_attend_workspace — device scratch bytes iq_attend needs for these
+ * lengths and shapes (split-KV partial results plus a status word).
+ */
+int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_t* bytes);
+
+/*
+ * iq_attend — GQA attention of n_queries new queries per sequence over the
+ * cache (quant_kv.py, `asym_quantized_sdpa`, followed by the inverse rotation
+ * the page leaves to its caller).
+ *
+ * q: device bf16 [B][Hq][n_queries][head_dim], unrotated.  The library
+ *    rotates it with M_b (bf16 result), multiplies by `scale` (bf16 result;
+ *    1/sqrt(head_dim) is the usual value), and lets query head h read kv head
+ *    h / (Hq/Hkv).
+ * causal: 0 = every query sees all lens[b] tokens; 1 = query i sees tokens
+ *    t <= lens[b] - n_queries + i (its own token already appended).
+ * out: device [B][Hq][n_queries][head_dim], bf16 (out_f32 == 0) or float32
+ *    (out_f32 == 1), in unrotated space: out = bf16(o @ M_b^T).
+ * workspace: device buffer of at least iq_attend_workspace() bytes,
+ *    256-byte aligned; its contents on entry do not matter.
+ * Scores, softmax and P.V accumulate in float32 on tensor cores; dequantised
+ * key codes enter the products exactly; P times the value scale enters as fp16.
+ * Errors: INVALID_ARG (null, bad causal flag, empty sequence, lens[b] <
+ * n_queries when causal), WORKSPACE, UNSUPPORTED, CUDA.  A kernel-side failure
+ * (a pipeline wait that timed out) is recorded in the workspace status word and
+ * reported by iq_read_status.
+ */
+int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
+              float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
+              void* workspace, size_t workspace_bytes, iq_stream_t stream);
+
+/*
+ * iq_read_status — synchronise `stream`, read the status word that the last
+ * iq_attend on this workspace left, and clear it.  *device_status is 0 when
+ * every kernel completed normally.  Blocks the calling thread.
+ */
+int iq_read_status(void* workspace, iq_stream_t stream, int* device_status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* IQKV_H */

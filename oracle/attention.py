@@ -10,7 +10,9 @@ space; the caller applies the inverse rotation, here `o @ M_b^T`.
 Readings:
 
 * The queries are rotated like the keys: q' = bf16(q @ M_b) (same rule as
-  `codec.rotate`), then multiplied by the caller's scale, 1/sqrt(D).
+  `codec.rotate`), then multiplied by the caller's scale (1/sqrt(D)) with the
+  product rounded to bfloat16, since the page scales bfloat16 queries
+  (`queries * scale`).  For D = 256 the scale is 1/16 and the product is exact.
 * Scores, softmax, P*V and the inverse rotation are carried out in float64 on
   the exactly dequantised cache; only the final output is rounded (to
   bfloat16).  The page's MLX kernels would round intermediates to the query
@@ -52,7 +54,8 @@ def attend_slice(q_rows, k_hat, v_hat, blocks_b, scale, causal, q_pos=None):
     q_pos int [R]: absolute position of each row's query (causal limit t <= q_pos).
     Returns float64 [R, D] in unrotated space.
     """
-    qr = codec.rotate(q_rows, blocks_b).astype(np.float64) * float(scale)
+    qr = codec.rotate(q_rows, blocks_b) * np.float32(scale)
+    qr = round_bf16(qr.astype(np.float32)).astype(np.float64)
     s = qr @ k_hat.T
     if causal:
         t = np.arange(k_hat.shape[0])

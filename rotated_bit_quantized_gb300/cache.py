@@ -1,0 +1,287 @@
+"""Python face of libiqkv: rotation, quantised KV cache, attention.
+
+Argument marshalling over the C ABI only: every step of the path runs in the
+library's CUDA kernels.  Device memory comes from PyTorch (the caller's
+allocator); work is enqueued on PyTorch's current CUDA stream.
+
+Mirrors the page "sparkle mlx_streaming/core/cache/quant_kv.py"
+(`build_block_so4`, `AsymmetricQuantizedKVCache.update_and_fetch`, `trim`,
+`nbytes`, `state`, `meta_state`, `asym_quantized_sdpa`) and the page
+"sparkle mlx_streaming/mtp/kv_cache.py" (`commit_verified_prefix`,
+`_snapshot`/`_restore`, `commit_verified_snapshot`, `tile_caches`,
+`commit_tree_row`).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import numpy as np
+import torch
+
+import seeded_inputs
+
+from . import _abi
+from ._abi import IQ_STEP, IQCacheDesc, check, lib
+
+
+def _stream() -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need_cuda(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    return t.contiguous()
+
+
+class Rotation:
+    """Block-diagonal SO(4) rotation on the device (page `build_block_so4`).
+
+    `blocks_f32` [D/4, 4, 4] float32 and `blocks_bf16` [D/4, 4, 4] bfloat16
+    (M_b, what the cache and attention use).  The random draws come from
+    ``numpy.random.default_rng(seed)`` in the page's order; the library
+    normalises them and forms the blocks.
+    """
+
+    def __init__(self, seed: int = 0, head_dim: int = 256, device=None):
+        device = torch.device(device or "cuda")
+        nb = head_dim // 4
+        self.seed, self.head_dim = seed, head_dim
+        self.blocks_f32 = torch.empty((nb, 4, 4), dtype=torch.float32, device=device)
+        self.blocks_bf16 = torch.empty((nb, 4, 4), dtype=torch.bfloat16, device=device)
+        draws = np.ascontiguousarray(seeded_inputs.rotation_draws(seed, head_dim), dtype=np.float32)
+        with torch.cuda.device(device):
+            check(lib().iq_build_rotation(head_dim, draws.ctypes.data_as(ctypes.c_void_p),
+                                          _ptr(self.blocks_f32), _ptr(self.blocks_bf16), _stream()),
+                  "iq_build_rotation")
+
+
+class IQCache:
+    """Rotated K4/V3 bit-packed KV cache with one length per sequence.
+
+    Buffers follow the page's `(wq, scales, biases)` triples for keys and
+    values; `lens` (host int32 [B]) is the authoritative length of each
+    sequence.  Capacity grows in steps of 256 tokens, copying rows [0, len).
+    """
+
+    BUFFERS = ("k_codes", "k_scales", "k_biases", "v_codes", "v_scales", "v_biases")
+
+    def __init__(self, batch: int, kv_heads: int, head_dim: int = 256, group_size: int = 64,
+                 k_bits: int = 4, v_bits: int = 3, capacity: int = IQ_STEP, device=None):
+        self.batch, self.kv_heads, self.head_dim = batch, kv_heads, head_dim
+        self.group_size, self.k_bits, self.v_bits = group_size, k_bits, v_bits
+        self.device = torch.device(device or "cuda")
+        self.lens = np.zeros(batch, dtype=np.int32)
+        self._workspace = None
+        self._alloc(capacity)
+
+    # ---------------------------------------------------------------- storage
+    def _alloc(self, capacity: int):
+        sizes = (ctypes.c_size_t * 6)()
+        check(lib().iq_cache_bytes(self.batch, self.kv_heads, self.head_dim, self.group_size,
+                                   self.k_bits, self.v_bits, capacity, sizes), "iq_cache_bytes")
+        B, H = self.batch, self.kv_heads
+        dev = self.device
+        kw, vw = self.head_dim * self.k_bits // 32, self.head_dim * self.v_bits // 32
+        ng = self.head_dim // self.group_size
+        self.k_codes = torch.empty((B, H, capacity, kw), dtype=torch.int32, device=dev)
+        self.k_scales = torch.empty((B, H, capacity, ng), dtype=torch.bfloat16, device=dev)
+        self.k_biases = torch.empty((B, H, capacity, ng), dtype=torch.bfloat16, device=dev)
+        self.v_codes = torch.empty((B, H, capacity, vw), dtype=torch.int32, device=dev)
+        self.v_scales = torch.empty((B, H, capacity, ng), dtype=torch.bfloat16, device=dev)
+        self.v_biases = torch.empty((B, H, capacity, ng), dtype=torch.bfloat16, device=dev)
+        for name, n in zip(self.BUFFERS, sizes):
+            assert getattr(self, name).numel() * getattr(self, name).element_size() == n
+        self.capacity = capacity
+
+    def desc(self) -> IQCacheDesc:
+        d = IQCacheDesc(self.batch, self.kv_heads, self.head_dim, self.group_size, self.k_bits,
+                        self.v_bits, self.capacity)
+        for name in self.BUFFERS:
+            setattr(d, name, getattr(self, name).data_ptr())
+        d.lens = self.lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        return d
+
+    @property
+    def offset(self) -> int:
+        """The page's single offset: defined when every sequence has the same length."""
+        if not (self.lens == self.lens[0]).all():
+            raise ValueError("sequences have different lengths; use .lens")
+        return int(self.lens[0])
+
+    @property
+    def nbytes(self) -> int:
+        d = self.desc()
+        return int(lib().iq_cache_nbytes(ctypes.byref(d)))
+
+    @property
+    def meta_state(self):
+        return str(self.group_size), str(self.k_bits), str(self.v_bits)
+
+    def _fresh(self, batch: int, capacity: int) -> "IQCache":
+        return IQCache(batch, self.kv_heads, self.head_dim, self.group_size, self.k_bits,
+                       self.v_bits, capacity, self.device)
+
+    def _gather_from(self, src: "IQCache", src_of) -> None:
+        m = np.ascontiguousarray(src_of, dtype=np.int32)
+        ds, dd = src.desc(), self.desc()
+        with torch.cuda.device(self.device):
+            check(lib().iq_cache_gather(ctypes.byref(ds), ctypes.byref(dd),
+                                        m.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _stream()),
+                  "iq_cache_gather")
+        self.lens[:] = np.ctypeslib.as_array(dd.lens, shape=(self.batch,))
+
+    def reserve(self, capacity: int) -> None:
+        """Grow to at least `capacity` tokens (multiple of 256), keeping rows [0, len)."""
+        if capacity <= self.capacity:
+            return
+        new_cap = int(math.ceil(capacity / IQ_STEP) * IQ_STEP)
+        old = IQCache.__new__(IQCache)
+        old.__dict__.update(self.__dict__)
+        old.lens = self.lens.copy()
+        self._alloc(new_cap)
+        self._gather_from(old, np.arange(self.batch))
+
+    # ---------------------------------------------------------------- page API
+    def append(self, keys: torch.Tensor, values: torch.Tensor, rotation: Rotation) -> None:
+        """Rotate, quantise, pack and append n tokens per sequence (page `update_and_fetch`).
+
+        keys, values: bfloat16 CUDA tensors [B, Hkv, n, D], unrotated.
+        """
+        keys = _need_cuda(keys, torch.bfloat16, "keys")
+        values = _need_cuda(values, torch.bfloat16, "values")
+        n = keys.shape[2]
+        if tuple(keys.shape) != (self.batch, self.kv_heads, n, self.head_dim) or values.shape != keys.shape:
+            raise ValueError("keys/values must be [B, Hkv, n, D]")
+        need = int(self.lens.max()) + n
+        if need > self.capacity:  # grow by ceil(n/256)*256 like the page, or more if needed
+            self.reserve(max(need, self.capacity + int(math.ceil(n / IQ_STEP)) * IQ_STEP))
+        d = self.desc()
+        with torch.cuda.device(self.device):
+            check(lib().iq_cache_append(ctypes.byref(d), _ptr(keys), _ptr(values), n,
+                                        _ptr(rotation.blocks_bf16), _stream()), "iq_cache_append")
+
+    def trim(self, n) -> np.ndarray:
+        """Drop up to n tokens from each sequence; returns the counts dropped (page `trim`)."""
+        counts = np.ascontiguousarray(np.broadcast_to(np.asarray(n, dtype=np.int32), (self.batch,)))
+        out = np.zeros(self.batch, dtype=np.int32)
+        d = self.desc()
+        check(lib().iq_cache_trim(ctypes.byref(d), counts.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                  out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))), "iq_cache_trim")
+        return out
+
+    def workspace_bytes(self, q_heads: int, n_queries: int) -> int:
+        nb = ctypes.c_size_t()
+        d = self.desc()
+        check(lib().iq_attend_workspace(ctypes.byref(d), q_heads, n_queries, ctypes.byref(nb)),
+              "iq_attend_workspace")
+        return nb.value
+
+    def attend(self, q: torch.Tensor, rotation: Rotation, causal: bool = False, scale: float | None = None,
+               out: torch.Tensor | None = None, out_dtype=torch.bfloat16) -> torch.Tensor:
+        """Attention of q [B, Hq, L, D] (bf16, unrotated) over the cache (page `asym_quantized_sdpa`).
+
+        Returns [B, Hq, L, D] in unrotated space (the inverse rotation applied).
+        """
+        q = _need_cuda(q, torch.bfloat16, "q")
+        B, Hq, L, D = q.shape
+        if B != self.batch or D != self.head_dim:
+            raise ValueError("q must be [B, Hq, L, D] matching the cache")
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        if out is None:
+            out = torch.empty((B, Hq, L, D), dtype=out_dtype, device=q.device)
+        out_f32 = 1 if out.dtype == torch.float32 else 0
+        if out.dtype not in (torch.float32, torch.bfloat16) or not out.is_contiguous():
+            raise ValueError("out must be a contiguous bf16 or f32 tensor")
+        need = self.workspace_bytes(Hq, L)
+        if self._workspace is None or self._workspace.numel() < need:
+            self._workspace = torch.empty(max(need, 1 << 20), dtype=torch.uint8, device=self.device)
+        d = self.desc()
+        with torch.cuda.device(self.device):
+            check(lib().iq_attend(ctypes.byref(d), _ptr(q), Hq, L, float(scale), 1 if causal else 0,
+                                  _ptr(rotation.blocks_bf16), _ptr(out), out_f32, _ptr(self._workspace),
+                                  self._workspace.numel(), _stream()), "iq_attend")
+        return out
+
+    def device_status(self) -> int:
+        """Synchronise and return the kernels' status word (0 = all normal)."""
+        if self._workspace is None:
+            return 0
+        st = ctypes.c_int()
+        code = lib().iq_read_status(_ptr(self._workspace), _stream(), ctypes.byref(st))
+        if code not in (_abi.IQ_OK, _abi.IQ_ERR_DEVICE):
+            check(code, "iq_read_status")
+        return st.value
+
+    # ---------------------------------------------------------------- speculative decoding
+    def commit_verified_prefix(self, verified_len: int, accepted_len) -> np.ndarray:
+        """Trim the rejected suffix, verified_len - accepted_len per sequence
+        (page "kv_cache.py", `commit_verified_prefix`, trimmable-cache branch)."""
+        acc = np.broadcast_to(np.asarray(accepted_len, dtype=np.int64), (self.batch,))
+        rejected = verified_len - acc
+        if (rejected < 0).any():
+            raise ValueError("accepted_len cannot exceed verified_len")
+        return self.trim(rejected.astype(np.int32))
+
+    def snapshot(self) -> "IQCache":
+        """Independent copy of rows [0, len) (page `_snapshot`; never aliases)."""
+        cap = max(IQ_STEP, int(math.ceil(max(int(self.lens.max()), 1) / IQ_STEP) * IQ_STEP))
+        snap = self._fresh(self.batch, cap)
+        snap._gather_from(self, np.arange(self.batch))
+        return snap
+
+    def restore(self, snap: "IQCache") -> None:
+        """Install a copy of `snap` (page `_restore`: the snapshot stays intact)."""
+        if snap.batch != self.batch:
+            raise ValueError("snapshot batch differs")
+        self.reserve(int(snap.lens.max()))
+        self._gather_from(snap, np.arange(self.batch))
+
+    def tile(self, paths: int) -> None:
+        """Batch-1 cache -> batch-P cache of P identical paths (page `tile_caches`)."""
+        if self.batch != 1:
+            raise ValueError("tile needs a batch-1 cache")
+        src = IQCache.__new__(IQCache)
+        src.__dict__.update(self.__dict__)
+        src.lens = self.lens.copy()
+        self.batch = paths
+        self.lens = np.zeros(paths, dtype=np.int32)
+        self._workspace = None
+        self._alloc(src.capacity)
+        self._gather_from(src, np.zeros(paths, dtype=np.int32))
+
+    def keep_row(self, row: int) -> None:
+        """Batch-P cache -> batch-1 cache holding path `row` (page `commit_tree_row`)."""
+        src = IQCache.__new__(IQCache)
+        src.__dict__.update(self.__dict__)
+        src.lens = self.lens.copy()
+        self.batch = 1
+        self.lens = np.zeros(1, dtype=np.int32)
+        self._workspace = None
+        self._alloc(src.capacity)
+        self._gather_from(src, np.array([row], dtype=np.int32))
+
+    def commit_tree_row(self, verified_len: int, accepted_len: int, row: int) -> None:
+        """Trim the rejected suffix of every path, then keep path `row` (page `commit_tree_row`)."""
+        self.commit_verified_prefix(verified_len, accepted_len)
+        self.keep_row(row)
+
+
+def commit_verified_snapshot(cache: IQCache, snapshots, accepted_len: int,
+                             verified_len: int | None = None) -> bool:
+    """Restore the snapshot taken after `accepted_len` verified tokens
+    (page "kv_cache.py", `commit_verified_snapshot`)."""
+    if verified_len is not None and accepted_len == verified_len:
+        return True
+    if accepted_len <= 0 or accepted_len > len(snapshots):
+        return False
+    cache.restore(snapshots[accepted_len - 1])
+    return True

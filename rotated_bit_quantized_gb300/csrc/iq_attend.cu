@@ -1,0 +1,892 @@
+// libiqkv: split-KV GQA attention over the packed K4/V3 cache, and the
+// split-combine + inverse-rotation pass.
+//
+// Method source: page "sparkle mlx_streaming/core/cache/quant_kv.py",
+// `asym_quantized_sdpa` (scale the queries, GQA reshape so query head h reads
+// kv head h / rep, quantised q.K^T, causal mask at query position
+// kL - qL + i, softmax, P.V over the quantised values) and the module note
+// that the output is still in rotated value space, so the caller undoes the
+// rotation; `rotate_last` gives the query rotation.
+//
+// Kernel design (one CTA = one (sequence, kv head, query tile, key chunk)):
+//  * a producer warp streams 64-token tiles of packed K codes (2-D tensor copy
+//    with 128-byte swizzle), packed V codes and the four scale/bias rows (1-D
+//    bulk copies) into a 4-stage shared-memory ring guarded by mbarriers;
+//  * consumer warps unpack codes to fp16 in registers with bit tricks and run
+//    m16n8k16 tensor-core MMAs: S = K_codes . q (per 64-dim group, fp32
+//    accumulate), folded with the group scale/bias on CUDA cores; online
+//    softmax in fp32; O^T += V_codes^T . (P * s_v) with P transposed in
+//    registers by movmatrix; the value bias term sum_t p_t b_t on CUDA cores;
+//  * each CTA writes an un-normalised partial (O, running max, running sum);
+//    the combine kernel merges the chunks (log-sum-exp), divides, applies
+//    M_b^T and stores bf16 or fp32.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "iq_common.cuh"
+
+namespace iq {
+namespace attn {
+
+constexpr int TILE = 64;     // tokens per pipeline stage
+constexpr int NSTAGE = 4;
+constexpr int OFF_K = 0;                     // 64 rows x 128 B, 128-byte swizzle
+constexpr int OFF_V = 8192;                  // 64 rows x 96 B (+ pad for the field window)
+constexpr int OFF_KS = OFF_V + 6144 + 128;   // 64 x 8 B each
+constexpr int OFF_KB = OFF_KS + 512;
+constexpr int OFF_VS = OFF_KB + 512;
+constexpr int OFF_VB = OFF_VS + 512;
+constexpr int STAGE = 17408;                 // multiple of 1024 (swizzle atom)
+constexpr uint32_t STAGE_TX = 8192 + 6144 + 4 * 512;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float NEG_INF = -__builtin_huge_valf();
+// Row of the 16-token sub-tile that MMA token slot m (0..7) reads; slot m+8
+// reads row mu(m)+8.  Chosen so the swizzled K reads and the 96-byte-pitch V
+// reads are free of shared-memory bank conflicts.
+constexpr uint32_t MU_PACK = 0x47126530u;  // mu = {0,3,5,6,2,1,7,4}
+
+struct Params {
+  const uint32_t* k_codes;
+  const uint16_t* k_scales;
+  const uint16_t* k_biases;
+  const uint32_t* v_codes;
+  const uint16_t* v_scales;
+  const uint16_t* v_biases;
+  const uint16_t* q;
+  const uint16_t* rot;
+  float* part_o;   // [P][GT][256]
+  float* part_ml;  // [P][GT][2] (running max, running sum)
+  unsigned* status;
+  int batch, kv_heads, rep, nq, cap, nqt, chunk_tiles, maxc, causal;
+  float scale;
+  int lens[IQ_MAX_BATCH];
+};
+
+__device__ __forceinline__ int tile_limit(const Params& p, int T, int qt, int gt) {
+  if (!p.causal) return T;
+  const int rmax = min(qt * gt + gt - 1, p.rep * p.nq - 1);
+  return T - p.nq + rmax / p.rep + 1;
+}
+
+// group G's bf16 from a packed row of 4 bf16 (uint2)
+__device__ __forceinline__ float pick_bf16(uint2 v, int G) {
+  const uint32_t w = (G & 2) ? v.y : v.x;
+  return bf16_to_f32((G & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
+// 4-bit word (8 codes, LSB first) -> fp16x2 pairs (c0,c4) (c1,c5) (c2,c6) (c3,c7)
+__device__ __forceinline__ void unpack_k4(uint32_t w, uint32_t* r) {
+  constexpr uint32_t MAGIC = 0x64006400u;                       // 1024.0 in each half
+  constexpr uint32_t ONE = 0x3C003C00u, NEG1024 = 0xE400E400u;  // 1, -1024
+  constexpr uint32_t SIXTEENTH = 0x2C002C00u, NEG64 = 0xD400D400u;  // 1/16, -64
+  const uint32_t w8 = w >> 8;
+  r[0] = fma_f16x2(and_or(w, 0x000F000Fu, MAGIC), ONE, NEG1024);
+  r[1] = fma_f16x2(and_or(w, 0x00F000F0u, MAGIC), SIXTEENTH, NEG64);
+  r[2] = fma_f16x2(and_or(w8, 0x000F000Fu, MAGIC), ONE, NEG1024);
+  r[3] = fma_f16x2(and_or(w8, 0x00F000F0u, MAGIC), SIXTEENTH, NEG64);
+}
+
+// 3-bit code at bit `L` (0..7) of each 16-bit half of x -> fp16x2 codes
+template <int L>
+__device__ __forceinline__ uint32_t dq3(uint32_t x) {
+  constexpr uint32_t mask = 0x00070007u << L;
+  constexpr uint32_t sc = (15u - L) << 10;                 // 2^-L
+  constexpr uint32_t ng = 0x8000u | ((25u - L) << 10);     // -2^(10-L)
+  return fma_f16x2(and_or(x, mask, 0x64006400u), sc | (sc << 16), ng | (ng << 16));
+}
+
+// Two 24-bit fields (8 codes each; token a in fa, token b in fb) -> 8 fp16x2
+// pairs (code k of a in the low half, of b in the high half).
+__device__ __forceinline__ void unpack_v3_pair(uint32_t fa, uint32_t fb, uint32_t* h) {
+  const uint32_t x0 = __byte_perm(fa, fb, 0x5410);  // bits 0..15 of each
+  const uint32_t x1 = __byte_perm(fa, fb, 0x6521);  // bits 8..23
+  const uint32_t x2 = __byte_perm(fa, fb, 0x7632);  // bits 16..31
+  h[0] = dq3<0>(x0);
+  h[1] = dq3<3>(x0);
+  h[2] = dq3<6>(x0);
+  h[3] = dq3<1>(x1);
+  h[4] = dq3<4>(x1);
+  h[5] = dq3<7>(x1);
+  h[6] = dq3<2>(x2);
+  h[7] = dq3<5>(x2);
+}
+
+template <int NT, int DS, int STREAMS>
+struct Cfg {
+  static constexpr int GT = 8 * NT;            // query rows per CTA
+  static constexpr int GPW = 4 / DS;           // 64-dim groups per consumer warp
+  static constexpr int CW = DS * STREAMS;      // consumer warps
+  static constexpr int THREADS = (CW + 1) * 32;
+  static constexpr int OFF_QS = NSTAGE * STAGE;
+  static constexpr int OFF_QSUM = OFF_QS + GT * 512;
+  static constexpr int OFF_MBUF = OFF_QSUM + GT * 16;
+  static constexpr int OFF_LBUF = OFF_MBUF + STREAMS * GT * 4;
+  static constexpr int OFF_XBUF = OFF_LBUF + STREAMS * GT * 4;
+  static constexpr int XBUF_BYTES = DS > 1 ? STREAMS * 2 * DS * NT * 32 * 16 : 0;
+  static constexpr int OFF_BAR = OFF_XBUF + XBUF_BYTES;
+  static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + 1024;  // + alignment slack
+  static_assert(STREAMS * GT * 256 * 4 <= NSTAGE * STAGE, "stream merge buffer must fit the ring");
+  static_assert(OFF_XBUF % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+  static_assert(4 % STREAMS == 0 && 4 % DS == 0, "shape");
+};
+
+template <int NT, int DS, int STREAMS>
+__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
+    attend_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap kmap) {
+  using C = Cfg<NT, DS, STREAMS>;
+  constexpr int GT = C::GT, GPW = C::GPW, CW = C::CW, NCT = CW * 32;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + C::OFF_QS);
+  float* qsum = reinterpret_cast<float*>(smem + C::OFF_QSUM);
+  float* mbuf = reinterpret_cast<float*>(smem + C::OFF_MBUF);
+  float* lbuf = reinterpret_cast<float*>(smem + C::OFF_LBUF);
+  float4* xbuf = reinterpret_cast<float4*>(smem + C::OFF_XBUF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + NSTAGE;
+
+  const int chunk = blockIdx.x, b = blockIdx.z;
+  const int kvh = blockIdx.y / p.nqt, qt = blockIdx.y % p.nqt;
+  const int T = p.lens[b];
+  const int limit = tile_limit(p, T, qt, GT);
+  const int chunk_tok = p.chunk_tiles * TILE;
+  const int t_lo = chunk * chunk_tok;
+  if (t_lo >= limit) return;  // past this sequence's last chunk: the combine never reads it
+  const int t_hi = min(limit, t_lo + chunk_tok);
+  const int ntiles = (t_hi - t_lo + TILE - 1) / TILE;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], CW);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  const long long rowbase = (static_cast<long long>(b) * p.kv_heads + kvh) * p.cap;
+
+  // ------------------------------------------------------------ producer
+  if (warp == CW) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int k = 0;
+      for (; k < ntiles; ++k) {
+        const int st = k % NSTAGE;
+        if (k >= NSTAGE && !mbar_wait(&empty[st], ((k / NSTAGE) - 1) & 1)) {
+          atomicOr(p.status, 1u);
+          break;
+        }
+        uint8_t* sb = smem + st * STAGE;
+        const long long row0 = rowbase + t_lo + static_cast<long long>(k) * TILE;
+        mbar_arrive_expect_tx(&full[st], STAGE_TX);
+        tensor2d_g2s(sb + OFF_K, &kmap, 0, static_cast<int>(row0), &full[st], pol);
+        bulk_g2s(sb + OFF_V, p.v_codes + row0 * kVWords, 6144, &full[st], pol);
+        bulk_g2s(sb + OFF_KS, p.k_scales + row0 * kGroups, 512, &full[st], pol);
+        bulk_g2s(sb + OFF_KB, p.k_biases + row0 * kGroups, 512, &full[st], pol);
+        bulk_g2s(sb + OFF_VS, p.v_scales + row0 * kGroups, 512, &full[st], pol);
+        bulk_g2s(sb + OFF_VB, p.v_biases + row0 * kGroups, 512, &full[st], pol);
+      }
+      // never leave with copies in flight: wait for the last tile issued to each stage
+      for (int s = 0; s < NSTAGE && s < k; ++s) {
+        const int last = s + NSTAGE * ((k - 1 - s) / NSTAGE);
+        mbar_wait(&full[s], (last / NSTAGE) & 1);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int cw = warp, stream = cw / DS, dg = cw % DS;
+  const int g = lane >> 2, t = lane & 3;
+
+  // q' = bf16(q @ M_b), q'' = bf16(q' * scale); rows r <-> (query R/rep, head R%rep)
+  for (int idx = threadIdx.x; idx < GT * 64; idx += NCT) {
+    const int r = idx >> 6, blk = idx & 63;
+    const int R = qt * GT + r, i = R / p.rep, hr = R % p.rep;
+    uint32_t o01 = 0, o23 = 0;
+    if (i < p.nq) {
+      const long long qrow =
+          (static_cast<long long>(b) * p.kv_heads * p.rep + kvh * p.rep + hr) * p.nq + i;
+      const uint2 raw = *reinterpret_cast<const uint2*>(p.q + qrow * kHeadDim + blk * 4);
+      const float x[4] = {bf16_to_f32(raw.x & 0xFFFFu), bf16_to_f32(raw.x >> 16),
+                          bf16_to_f32(raw.y & 0xFFFFu), bf16_to_f32(raw.y >> 16)};
+      const uint4* r4 = reinterpret_cast<const uint4*>(p.rot + blk * 16);
+      const uint4 m01 = __ldg(r4), m23 = __ldg(r4 + 1);
+      const uint32_t mw[8] = {m01.x, m01.y, m01.z, m01.w, m23.x, m23.y, m23.z, m23.w};
+      uint32_t yb[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int e = k * 4 + j;
+          const float mkj = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
+          acc = k == 0 ? __fmul_rn(x[0], mkj) : __fadd_rn(acc, __fmul_rn(x[k], mkj));
+        }
+        yb[j] = f32_to_bf16_bits(__fmul_rn(round_bf16(acc), p.scale));
+      }
+      o01 = yb[0] | (yb[1] << 16);
+      o23 = yb[2] | (yb[3] << 16);
+    }
+    *reinterpret_cast<uint2*>(qs + r * kHeadDim + blk * 4) = make_uint2(o01, o23);
+  }
+  named_bar(1, NCT);
+  for (int r = cw; r < GT; r += CW) {
+    const uint4 v = *reinterpret_cast<const uint4*>(qs + r * kHeadDim + lane * 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s += bf16_to_f32(w[e] & 0xFFFFu) + bf16_to_f32(w[e] >> 16);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((lane & 7) == 0) qsum[r * 4 + (lane >> 3)] = s;
+  }
+  named_bar(1, NCT);
+
+  // q'' as fp16 B fragments.  Thread t covers dims 64G+16t .. +15 of group G;
+  // register pair m of its unpacked codes holds dims (m, m+4) for m < 4 and
+  // (m+4, m+8) for m >= 4; k-step s uses pairs 2s (slots 2t,2t+1) and 2s+1.
+  uint32_t qb[GPW][4][NT][2];
+  float qsr[GPW][NT][2];
+#pragma unroll
+  for (int gi = 0; gi < GPW; ++gi) {
+    const int G = dg * GPW + gi;
+    const int base = 64 * G + 16 * t;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const uint16_t* qrow = qs + (8 * j + g) * kHeadDim + base;
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int m = 2 * s + h;
+          const int lo = m < 4 ? m : m + 4;
+          qb[gi][s][j][h] = pack_f16x2(bf16_to_f32(qrow[lo]), bf16_to_f32(qrow[lo + 4]));
+        }
+      qsr[gi][j][0] = qsum[(8 * j + 2 * t) * 4 + G];
+      qsr[gi][j][1] = qsum[(8 * j + 2 * t + 1) * 4 + G];
+    }
+  }
+  int qpos[NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int R = qt * GT + 8 * j + 2 * t + e;
+      const int i = min(R / p.rep, p.nq - 1);
+      qpos[j][e] = p.causal ? T - p.nq + i : T - 1;
+    }
+
+  float O[GPW][4][NT][4];
+  float bacc[GPW][NT][2];
+  float mrow[NT][2], lrow[NT][2];
+#pragma unroll
+  for (int gi = 0; gi < GPW; ++gi)
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      bacc[gi][j][0] = bacc[gi][j][1] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) O[gi][i][j][0] = O[gi][i][j][1] = O[gi][i][j][2] = O[gi][i][j][3] = 0.f;
+    }
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    mrow[j][0] = mrow[j][1] = NEG_INF;
+    lrow[j][0] = lrow[j][1] = 0.f;
+  }
+
+  const int rS0 = (MU_PACK >> (4 * g)) & 15;  // token slot g
+  const int rS1 = rS0 + 8;                    // token slot g+8
+  const int rV0 = (MU_PACK >> (8 * t)) & 15;  // slot 2t
+  const int rV1 = (MU_PACK >> (8 * t + 4)) & 15;  // slot 2t+1
+  const int vword = (3 * g) >> 2, vshift = (24 * g) & 31;
+  int xpar = 0;
+
+  for (int k = 0; k < ntiles; ++k) {
+    const int st = k % NSTAGE;
+    if (!mbar_wait(&full[st], (k / NSTAGE) & 1)) {
+      atomicOr(p.status, 2u);
+      break;
+    }
+    const uint32_t sb = smem_u32(smem + st * STAGE);
+    const int tile_tok = t_lo + k * TILE;
+    for (int sub = stream; sub < 4; sub += STREAMS) {
+      const int tokbase = tile_tok + sub * 16;
+      if (tokbase >= t_hi) break;
+      const int rr0 = sub * 16 + rS0, rr1 = sub * 16 + rS1;
+      const uint2 ksc0 = lds64(sb + OFF_KS + rr0 * 8), ksc1 = lds64(sb + OFF_KS + rr1 * 8);
+      const uint2 kbi0 = lds64(sb + OFF_KB + rr0 * 8), kbi1 = lds64(sb + OFF_KB + rr1 * 8);
+
+      // ---- scores: per group, S_G = codes . q'' (fp32), folded with scale/bias
+      float sc[NT][4];
+#pragma unroll
+      for (int gi = 0; gi < GPW; ++gi) {
+        const int G = dg * GPW + gi;
+        const uint32_t chunk16 = 2 * G + (t >> 1);
+        const uint32_t a0 = sb + OFF_K + rr0 * 128 + ((chunk16 ^ (rr0 & 7)) << 4) + ((t & 1) << 3);
+        const uint32_t a1 = sb + OFF_K + rr1 * 128 + ((chunk16 ^ (rr1 & 7)) << 4) + ((t & 1) << 3);
+        const uint2 w0 = lds64(a0), w1 = lds64(a1);
+        uint32_t RA[8], RB[8];
+        unpack_k4(w0.x, RA);
+        unpack_k4(w0.y, RA + 4);
+        unpack_k4(w1.x, RB);
+        unpack_k4(w1.y, RB + 4);
+        float acc[NT][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint32_t A[4] = {RA[2 * s], RB[2 * s], RA[2 * s + 1], RB[2 * s + 1]};
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma_f16(acc[j], A, qb[gi][s][j][0], qb[gi][s][j][1]);
+        }
+        const float s0 = pick_bf16(ksc0, G), s1 = pick_bf16(ksc1, G);
+        const float b0 = pick_bf16(kbi0, G), b1 = pick_bf16(kbi1, G);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const float t0 = fmaf(s0, acc[j][0], b0 * qsr[gi][j][0]);
+          const float t1 = fmaf(s0, acc[j][1], b0 * qsr[gi][j][1]);
+          const float t2 = fmaf(s1, acc[j][2], b1 * qsr[gi][j][0]);
+          const float t3 = fmaf(s1, acc[j][3], b1 * qsr[gi][j][1]);
+          if (gi == 0) {
+            sc[j][0] = t0; sc[j][1] = t1; sc[j][2] = t2; sc[j][3] = t3;
+          } else {
+            sc[j][0] += t0; sc[j][1] += t1; sc[j][2] += t2; sc[j][3] += t3;
+          }
+        }
+      }
+      if constexpr (DS > 1) {  // sum the group partials of the DS warps, in group order
+        float4* xb = xbuf + (stream * 2 + xpar) * DS * NT * 32;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+          xb[(dg * NT + j) * 32 + lane] = make_float4(sc[j][0], sc[j][1], sc[j][2], sc[j][3]);
+        named_bar(2 + stream, DS * 32);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          float4 a = xb[j * 32 + lane];
+#pragma unroll
+          for (int d = 1; d < DS; ++d) {
+            const float4 v = xb[(d * NT + j) * 32 + lane];
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+          }
+          sc[j][0] = a.x; sc[j][1] = a.y; sc[j][2] = a.z; sc[j][3] = a.w;
+        }
+        xpar ^= 1;
+      }
+
+      // ---- mask (ragged tail, causal) and online softmax
+      const int tok0 = tokbase + rS0, tok1 = tokbase + rS1;
+      const bool in0 = tok0 < t_hi, in1 = tok1 < t_hi;
+      bool valid[NT][4];
+      float alpha[NT][2], msc[NT][2];
+      bool rescale = false;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        valid[j][0] = in0 && tok0 <= qpos[j][0];
+        valid[j][1] = in0 && tok0 <= qpos[j][1];
+        valid[j][2] = in1 && tok1 <= qpos[j][0];
+        valid[j][3] = in1 && tok1 <= qpos[j][1];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[j][e] = valid[j][e] ? sc[j][e] : NEG_INF;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float mx = fmaxf(sc[j][e], sc[j][e + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mnew = fmaxf(mrow[j][e], mx);
+          alpha[j][e] = mnew == NEG_INF ? 1.f : ex2_approx((mrow[j][e] - mnew) * LOG2E);
+          rescale |= mnew != mrow[j][e];
+          mrow[j][e] = mnew;
+          msc[j][e] = mnew == NEG_INF ? 0.f : mnew * LOG2E;
+        }
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          lrow[j][0] *= alpha[j][0];
+          lrow[j][1] *= alpha[j][1];
+#pragma unroll
+          for (int gi = 0; gi < GPW; ++gi) {
+            bacc[gi][j][0] *= alpha[j][0];
+            bacc[gi][j][1] *= alpha[j][1];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              O[gi][i][j][0] *= alpha[j][0];
+              O[gi][i][j][2] *= alpha[j][0];
+              O[gi][i][j][1] *= alpha[j][1];
+              O[gi][i][j][3] *= alpha[j][1];
+            }
+          }
+        }
+      }
+      float pr[NT][4];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pr[j][e] = ex2_approx(fmaf(sc[j][e], LOG2E, -msc[j][e & 1]));
+        lrow[j][0] += pr[j][0] + pr[j][2];
+        lrow[j][1] += pr[j][1] + pr[j][3];
+      }
+
+      // ---- values: O^T += V_codes^T . (P * s_v), bias term on CUDA cores
+      const uint2 vsc0 = lds64(sb + OFF_VS + rr0 * 8), vsc1 = lds64(sb + OFF_VS + rr1 * 8);
+      const uint2 vbi0 = lds64(sb + OFF_VB + rr0 * 8), vbi1 = lds64(sb + OFF_VB + rr1 * 8);
+      const uint32_t vrow0 = sb + OFF_V + (sub * 16 + rV0) * 96;
+      const uint32_t vrow1 = sb + OFF_V + (sub * 16 + rV1) * 96;
+      const uint32_t vrow2 = vrow0 + 8 * 96;
+      const uint32_t vrow3 = vrow1 + 8 * 96;
+#pragma unroll
+      for (int gi = 0; gi < GPW; ++gi) {
+        const int G = dg * GPW + gi;
+        const float vs0 = pick_bf16(vsc0, G), vs1 = pick_bf16(vsc1, G);
+        const float vb0 = pick_bf16(vbi0, G), vb1 = pick_bf16(vbi1, G);
+        uint32_t bp[NT][2];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const float q0 = valid[j][0] ? pr[j][0] * vs0 : 0.f;
+          const float q1 = valid[j][1] ? pr[j][1] * vs0 : 0.f;
+          const float q2 = valid[j][2] ? pr[j][2] * vs1 : 0.f;
+          const float q3 = valid[j][3] ? pr[j][3] * vs1 : 0.f;
+          bp[j][0] = movmatrix_trans(pack_f16x2(q0, q1));
+          bp[j][1] = movmatrix_trans(pack_f16x2(q2, q3));
+          bacc[gi][j][0] += (valid[j][0] ? pr[j][0] * vb0 : 0.f) + (valid[j][2] ? pr[j][2] * vb1 : 0.f);
+          bacc[gi][j][1] += (valid[j][1] ? pr[j][1] * vb0 : 0.f) + (valid[j][3] ? pr[j][3] * vb1 : 0.f);
+        }
+        const uint32_t wofs = (6 * G + vword) * 4;
+        const uint32_t f0 = __funnelshift_r(lds32(vrow0 + wofs), lds32(vrow0 + wofs + 4), vshift);
+        const uint32_t f1 = __funnelshift_r(lds32(vrow1 + wofs), lds32(vrow1 + wofs + 4), vshift);
+        const uint32_t f2 = __funnelshift_r(lds32(vrow2 + wofs), lds32(vrow2 + wofs + 4), vshift);
+        const uint32_t f3 = __funnelshift_r(lds32(vrow3 + wofs), lds32(vrow3 + wofs + 4), vshift);
+        uint32_t h01[8], h23[8];
+        unpack_v3_pair(f0, f1, h01);
+        unpack_v3_pair(f2, f3, h23);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t A[4] = {h01[2 * i], h01[2 * i + 1], h23[2 * i], h23[2 * i + 1]};
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma_f16(O[gi][i][j], A, bp[j][0], bp[j][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+
+  // ------------------------------------------------------------ finish the chunk
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float l = lrow[j][e];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      lrow[j][e] = l;
+#pragma unroll
+      for (int gi = 0; gi < GPW; ++gi) {
+        float bs = bacc[gi][j][e];
+        bs += __shfl_xor_sync(0xffffffffu, bs, 4);
+        bs += __shfl_xor_sync(0xffffffffu, bs, 8);
+        bs += __shfl_xor_sync(0xffffffffu, bs, 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          O[gi][i][j][e] += bs;
+          O[gi][i][j][e + 2] += bs;
+        }
+      }
+    }
+
+  const long long pidx =
+      ((static_cast<long long>(b) * p.kv_heads + kvh) * p.nqt + qt) * p.maxc + chunk;
+  float* po = p.part_o + pidx * GT * kHeadDim;
+  float* pml = p.part_ml + pidx * GT * 2;
+
+  if constexpr (STREAMS == 1) {
+#pragma unroll
+    for (int gi = 0; gi < GPW; ++gi)
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = 8 * j + 2 * t + e;
+          float* dst = po + row * kHeadDim + 64 * (dg * GPW + gi) + 8 * g;
+          reinterpret_cast<float4*>(dst)[0] =
+              make_float4(O[gi][0][j][e], O[gi][0][j][e + 2], O[gi][1][j][e], O[gi][1][j][e + 2]);
+          reinterpret_cast<float4*>(dst)[1] =
+              make_float4(O[gi][2][j][e], O[gi][2][j][e + 2], O[gi][3][j][e], O[gi][3][j][e + 2]);
+        }
+    if (dg == 0 && g == 0)
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = 8 * j + 2 * t + e;
+          pml[row * 2] = mrow[j][e];
+          pml[row * 2 + 1] = lrow[j][e];
+        }
+  } else {
+    if (dg == 0 && g == 0)
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) mbuf[stream * GT + 8 * j + 2 * t + e] = mrow[j][e];
+    named_bar(1, NCT);  // also: every consumer is done with the ring
+    float* obuf = reinterpret_cast<float*>(smem);  // [STREAMS][GT][256], aliases the ring
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int row = 8 * j + 2 * t + e;
+        float M = mbuf[row];
+#pragma unroll
+        for (int s = 1; s < STREAMS; ++s) M = fmaxf(M, mbuf[s * GT + row]);
+        const float a = mrow[j][e] == NEG_INF ? 0.f : ex2_approx((mrow[j][e] - M) * LOG2E);
+        if (dg == 0 && g == 0) lbuf[stream * GT + row] = lrow[j][e] * a;
+#pragma unroll
+        for (int gi = 0; gi < GPW; ++gi) {
+          float* dst = obuf + (stream * GT + row) * kHeadDim + 64 * (dg * GPW + gi) + 8 * g;
+          reinterpret_cast<float4*>(dst)[0] = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a,
+                                                          O[gi][1][j][e] * a, O[gi][1][j][e + 2] * a);
+          reinterpret_cast<float4*>(dst)[1] = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a,
+                                                          O[gi][3][j][e] * a, O[gi][3][j][e + 2] * a);
+        }
+      }
+    named_bar(1, NCT);
+    for (int idx = threadIdx.x; idx < GT * 64; idx += NCT) {
+      const int r = idx >> 6, c4 = idx & 63;
+      float4 a = reinterpret_cast<const float4*>(obuf + r * kHeadDim)[c4];
+#pragma unroll
+      for (int s = 1; s < STREAMS; ++s) {
+        const float4 v = reinterpret_cast<const float4*>(obuf + (s * GT + r) * kHeadDim)[c4];
+        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+      }
+      reinterpret_cast<float4*>(po + r * kHeadDim)[c4] = a;
+    }
+    for (int r = threadIdx.x; r < GT; r += NCT) {
+      float M = mbuf[r], L = lbuf[r];
+#pragma unroll
+      for (int s = 1; s < STREAMS; ++s) {
+        M = fmaxf(M, mbuf[s * GT + r]);
+        L += lbuf[s * GT + r];
+      }
+      pml[r * 2] = M;
+      pml[r * 2 + 1] = L;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ combine
+
+struct CombineParams {
+  const float* part_o;
+  const float* part_ml;
+  const uint16_t* rot;
+  void* out;
+  unsigned* status;
+  int out_f32;
+  int batch, kv_heads, rep, nq, nqt, gt, chunk_tok, maxc, causal;
+  int lens[IQ_MAX_BATCH];
+};
+
+// One warp per output row (b, query head, query).  Lane l owns dims 8l..8l+7
+// (two rotation blocks).
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int hq_total = p.kv_heads * p.rep;
+  const long long rows = static_cast<long long>(p.batch) * hq_total * p.nq;
+  if (w >= rows) return;
+  const int i = static_cast<int>(w % p.nq);
+  const int hq = static_cast<int>((w / p.nq) % hq_total);
+  const int b = static_cast<int>(w / (static_cast<long long>(p.nq) * hq_total));
+  const int kvh = hq / p.rep, hr = hq % p.rep;
+  const int R = i * p.rep + hr, qt = R / p.gt, r = R % p.gt;
+  const int T = p.lens[b];
+  int limit = T;
+  if (p.causal) limit = T - p.nq + min(qt * p.gt + p.gt - 1, p.rep * p.nq - 1) / p.rep + 1;
+  const int nch = (limit + p.chunk_tok - 1) / p.chunk_tok;
+  const long long pbase = ((static_cast<long long>(b) * p.kv_heads + kvh) * p.nqt + qt) * p.maxc;
+
+  float M = NEG_INF;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part_ml[((pbase + c) * p.gt + r) * 2]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float L = 0.f;
+  for (int c = 0; c < nch; ++c) {
+    const float* ml = p.part_ml + ((pbase + c) * p.gt + r) * 2;
+    const float m = ml[0];
+    const float wgt = m == NEG_INF ? 0.f : ex2_approx((m - M) * LOG2E);
+    L = fmaf(wgt, ml[1], L);
+    const float4* o = reinterpret_cast<const float4*>(p.part_o + ((pbase + c) * p.gt + r) * kHeadDim + 8 * lane);
+    const float4 o0 = o[0], o1 = o[1];
+    acc[0] = fmaf(wgt, o0.x, acc[0]); acc[1] = fmaf(wgt, o0.y, acc[1]);
+    acc[2] = fmaf(wgt, o0.z, acc[2]); acc[3] = fmaf(wgt, o0.w, acc[3]);
+    acc[4] = fmaf(wgt, o1.x, acc[4]); acc[5] = fmaf(wgt, o1.y, acc[5]);
+    acc[6] = fmaf(wgt, o1.z, acc[6]); acc[7] = fmaf(wgt, o1.w, acc[7]);
+  }
+  if (!(L > 0.f) && lane == 0) atomicOr(p.status, 4u);
+  float o[8];
+#pragma unroll
+  for (int d = 0; d < 8; ++d) o[d] = __fdiv_rn(acc[d], L);
+  // inverse rotation: out[4c+i] = sum_j o[4c+j] * M_b[c][i][j]
+  const uint4* r4 = reinterpret_cast<const uint4*>(p.rot) + lane * 4;
+  uint32_t mw[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = __ldg(r4 + q);
+    mw[4 * q] = v.x; mw[4 * q + 1] = v.y; mw[4 * q + 2] = v.z; mw[4 * q + 3] = v.w;
+  }
+  float y[8];
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = c * 16 + ii * 4 + j;
+        const float m = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
+        s = j == 0 ? __fmul_rn(o[4 * c], m) : fmaf(o[4 * c + j], m, s);
+      }
+      y[4 * c + ii] = s;
+    }
+  const long long orow = (static_cast<long long>(b) * hq_total + hq) * p.nq + i;
+  if (p.out_f32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHeadDim + 8 * lane);
+    dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+    dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+  } else {
+    uint4 v;
+    v.x = f32_to_bf16_bits(y[0]) | (f32_to_bf16_bits(y[1]) << 16);
+    v.y = f32_to_bf16_bits(y[2]) | (f32_to_bf16_bits(y[3]) << 16);
+    v.z = f32_to_bf16_bits(y[4]) | (f32_to_bf16_bits(y[5]) << 16);
+    v.w = f32_to_bf16_bits(y[6]) | (f32_to_bf16_bits(y[7]) << 16);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kHeadDim + 8 * lane) = v;
+  }
+}
+
+// ------------------------------------------------------------------ host plan
+
+struct Plan {
+  int nt, gt, nqt, chunk_tiles, maxc;
+  size_t part_count, bytes;
+};
+
+constexpr size_t kStatusBytes = 256;
+
+template <int NT, int DS, int STREAMS>
+int blocks_per_sm() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    using C = Cfg<NT, DS, STREAMS>;
+    int n = 0;
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS>, C::THREADS, C::SMEM) !=
+            cudaSuccess ||
+        n <= 0)
+      n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Decode (<= 8 query rows per kv head): one warp owns all four groups, four
+// token streams per CTA.  Verify / prefill (more rows): 32-row query tiles, a
+// warp per 64-dim group, one token stream.
+#define IQ_DECODE_CFG 1, 1, 4
+#define IQ_MULTI_CFG 4, 4, 1
+
+int make_plan(const iq_cache* c, int q_heads, int nq, Plan* pl) {
+  const int rep = q_heads / c->kv_heads;
+  const int rows = rep * nq;
+  pl->nt = rows <= 8 ? 1 : 4;
+  pl->gt = 8 * pl->nt;
+  pl->nqt = (rows + pl->gt - 1) / pl->gt;
+  int max_t = 0;
+  for (int b = 0; b < c->batch; ++b) max_t = c->lens[b] > max_t ? c->lens[b] : max_t;
+  const int tiles_max = (max_t + TILE - 1) / TILE;
+  const int bps = pl->nt == 1 ? blocks_per_sm<IQ_DECODE_CFG>() : blocks_per_sm<IQ_MULTI_CFG>();
+  const long long slots = static_cast<long long>(num_sms()) * bps;
+  const long long units = static_cast<long long>(c->batch) * c->kv_heads * pl->nqt;
+  long long nch = (4 * slots + units - 1) / units;
+  if (nch < 1) nch = 1;
+  int ct = static_cast<int>((tiles_max + nch - 1) / nch);
+  if (ct < 4) ct = 4;
+  pl->chunk_tiles = ct;
+  pl->maxc = (tiles_max + ct - 1) / ct;
+  pl->part_count = static_cast<size_t>(units) * pl->maxc;
+  pl->bytes = kStatusBytes + pl->part_count * pl->gt * (kHeadDim + 2) * sizeof(float);
+  return IQ_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+int validate(const iq_cache* c, const uint16_t* q, int q_heads, int nq, int causal, const void* rot,
+             const void* out) {
+  int st = iq_cache_check(c);
+  if (st != IQ_OK) return st;
+  if (!q || !rot || !out) return fail(IQ_ERR_INVALID_ARG, "null q/rotation/out");
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16 ||
+      reinterpret_cast<uintptr_t>(rot) % 16)
+    return fail(IQ_ERR_INVALID_ARG, "q/out/rotation not 16-byte aligned");
+  if (causal != 0 && causal != 1) return fail(IQ_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (nq < 1) return fail(IQ_ERR_INVALID_ARG, "n_queries must be >= 1");
+  if (q_heads < 1 || q_heads % c->kv_heads) return fail(IQ_ERR_INVALID_ARG, "q_heads must be a multiple of kv_heads");
+  const int rep = q_heads / c->kv_heads;
+  if (rep > 8 || 8 % rep) return fail(IQ_ERR_UNSUPPORTED, "query heads per kv head must divide 8");
+  for (int b = 0; b < c->batch; ++b) {
+    if (c->lens[b] < 1) return fail(IQ_ERR_INVALID_ARG, "attention over an empty sequence");
+    if (causal && c->lens[b] < nq) return fail(IQ_ERR_INVALID_ARG, "causal: lens[b] < n_queries");
+  }
+  if (static_cast<long long>(c->batch) * c->kv_heads * c->capacity >= (1LL << 31))
+    return fail(IQ_ERR_UNSUPPORTED, "cache rows exceed 2^31");
+  return IQ_OK;
+}
+
+template <int NT, int DS, int STREAMS>
+int launch_attend(const Params& prm, const CUtensorMap& map, dim3 grid, cudaStream_t s) {
+  using C = Cfg<NT, DS, STREAMS>;
+  blocks_per_sm<NT, DS, STREAMS>();  // sets the shared-memory attribute once
+  attend_kernel<NT, DS, STREAMS><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
+  IQ_CUDA(cudaGetLastError());
+  return IQ_OK;
+}
+
+}  // namespace attn
+}  // namespace iq
+
+using namespace iq;
+using namespace iq::attn;
+
+extern "C" {
+
+int iq_attend_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* bytes) {
+  clear_error();
+  int st = iq_cache_check(c);
+  if (st != IQ_OK) return st;
+  if (!bytes) return fail(IQ_ERR_INVALID_ARG, "null bytes");
+  if (n_queries < 1 || q_heads < 1 || q_heads % c->kv_heads)
+    return fail(IQ_ERR_INVALID_ARG, "bad head or query count");
+  Plan pl;
+  make_plan(c, q_heads, n_queries, &pl);
+  *bytes = pl.bytes;
+  return IQ_OK;
+}
+
+int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
+              const uint16_t* rot_bf16, void* out, int out_f32, void* workspace, size_t workspace_bytes,
+              iq_stream_t stream) {
+  clear_error();
+  int st = validate(c, q, q_heads, n_queries, causal, rot_bf16, out);
+  if (st != IQ_OK) return st;
+  Plan pl;
+  make_plan(c, q_heads, n_queries, &pl);
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256) return fail(IQ_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
+  if (workspace_bytes < pl.bytes) return fail(IQ_ERR_WORKSPACE, "workspace smaller than iq_attend_workspace()");
+  auto encode = encode_fn();
+  if (!encode) return fail(IQ_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kKWords),
+                              static_cast<cuuint64_t>(c->batch) * c->kv_heads * c->capacity};
+  const cuuint64_t strides[1] = {kKWords * 4};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKWords), static_cast<cuuint32_t>(TILE)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, c->k_codes, dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(IQ_ERR_CUDA, "cuTensorMapEncodeTiled failed for the key codes");
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  unsigned* status = reinterpret_cast<unsigned*>(ws);
+  float* part_o = reinterpret_cast<float*>(ws + kStatusBytes);
+  float* part_ml = part_o + pl.part_count * pl.gt * kHeadDim;
+  IQ_CUDA(cudaMemsetAsync(status, 0, sizeof(unsigned), s));
+
+  Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.k_codes = c->k_codes;
+  prm.k_scales = c->k_scales;
+  prm.k_biases = c->k_biases;
+  prm.v_codes = c->v_codes;
+  prm.v_scales = c->v_scales;
+  prm.v_biases = c->v_biases;
+  prm.q = q;
+  prm.rot = rot_bf16;
+  prm.part_o = part_o;
+  prm.part_ml = part_ml;
+  prm.status = status;
+  prm.batch = c->batch;
+  prm.kv_heads = c->kv_heads;
+  prm.rep = q_heads / c->kv_heads;
+  prm.nq = n_queries;
+  prm.cap = c->capacity;
+  prm.nqt = pl.nqt;
+  prm.chunk_tiles = pl.chunk_tiles;
+  prm.maxc = pl.maxc;
+  prm.causal = causal;
+  prm.scale = scale;
+  for (int b = 0; b < c->batch; ++b) prm.lens[b] = c->lens[b];
+  dim3 grid(pl.maxc, c->kv_heads * pl.nqt, c->batch);
+  st = pl.nt == 1 ? launch_attend<IQ_DECODE_CFG>(prm, map, grid, s) : launch_attend<IQ_MULTI_CFG>(prm, map, grid, s);
+  if (st != IQ_OK) return st;
+
+  CombineParams cp;
+  std::memset(&cp, 0, sizeof(cp));
+  cp.part_o = part_o;
+  cp.part_ml = part_ml;
+  cp.rot = rot_bf16;
+  cp.out = out;
+  cp.status = status;
+  cp.out_f32 = out_f32 ? 1 : 0;
+  cp.batch = c->batch;
+  cp.kv_heads = c->kv_heads;
+  cp.rep = prm.rep;
+  cp.nq = n_queries;
+  cp.nqt = pl.nqt;
+  cp.gt = pl.gt;
+  cp.chunk_tok = pl.chunk_tiles * TILE;
+  cp.maxc = pl.maxc;
+  cp.causal = causal;
+  for (int b = 0; b < c->batch; ++b) cp.lens[b] = c->lens[b];
+  const long long rows = static_cast<long long>(c->batch) * q_heads * n_queries;
+  const long long blocks = (rows * 32 + 255) / 256;
+  combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(cp);
+  IQ_CUDA(cudaGetLastError());
+  return IQ_OK;
+}
+
+int iq_read_status(void* workspace, iq_stream_t stream, int* device_status) {
+  clear_error();
+  if (!workspace || !device_status) return fail(IQ_ERR_INVALID_ARG, "null pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  IQ_CUDA(cudaStreamSynchronize(s));
+  IQ_CUDA(cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost));
+  IQ_CUDA(cudaMemset(workspace, 0, sizeof(unsigned)));
+  *device_status = static_cast<int>(v);
+  return v ? fail(IQ_ERR_DEVICE, "a kernel reported a failure (status bits set)") : IQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,412 @@
+// libiqkv: rotation build, cache bookkeeping, append (rotate + quantise + pack)
+// and row gather.
+//
+// Method source: page "sparkle mlx_streaming/core/cache/quant_kv.py"
+// (`_quat_left`, `_quat_right_conj`, `build_block_so4`, `rotate_last`,
+// `_packed_words`, `AsymmetricQuantizedKVCache`), and page
+// "sparkle mlx_streaming/mtp/kv_cache.py" (`_snapshot`/`_restore`,
+// `tile_caches`, `commit_tree_row`), which the row gather serves.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "iq_common.cuh"
+
+namespace iq {
+
+static thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(IQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+void clear_error() { g_last_error.clear(); }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// ------------------------------------------------------------------ rotation
+
+// One thread per 4x4 block.  Normalisation in float32 with explicit IEEE
+// operations (sum of squares in index order, correctly rounded sqrt and
+// division); block entries L(qL).R(qR) summed in float64 over k = 0..3 in
+// order, rounded once to float32; then rounded to bfloat16 for M_b.
+struct RotationDraws {
+  float v[kHeadDim / 4][2][4];
+};
+
+__global__ void rotation_kernel(const __grid_constant__ RotationDraws draws, float* __restrict__ rot,
+                                uint16_t* __restrict__ rotb, int nblocks) {
+  int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblocks) return;
+  float q[2][4];
+  for (int s = 0; s < 2; ++s) {
+    float v[4];
+    for (int i = 0; i < 4; ++i) v[i] = draws.v[b][s][i];
+    float acc = __fmul_rn(v[0], v[0]);
+    for (int i = 1; i < 4; ++i) acc = __fadd_rn(acc, __fmul_rn(v[i], v[i]));
+    float nrm = __fsqrt_rn(acc);
+    for (int i = 0; i < 4; ++i) q[s][i] = __fdiv_rn(v[i], nrm);
+  }
+  const double w = q[0][0], x = q[0][1], y = q[0][2], z = q[0][3];
+  // left-multiplication matrix of qL (page `_quat_left`)
+  const double L[4][4] = {{w, -x, -y, -z}, {x, w, -z, y}, {y, z, w, -x}, {z, -y, x, w}};
+  const double rw = q[1][0], rx = q[1][1], ry = q[1][2], rz = q[1][3];
+  // page `_quat_right_conj`, entries exactly as printed
+  const double R[4][4] = {{rw, rx, ry, rz}, {-rx, rw, rz, -ry}, {-ry, -rz, rw, rx}, {-rz, ry, -rx, rw}};
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 4; ++j) {
+      double acc = 0.0;
+      for (int k = 0; k < 4; ++k) acc = __dadd_rn(acc, __dmul_rn(L[i][k], R[k][j]));
+      float f = __double2float_rn(acc);
+      rot[b * 16 + i * 4 + j] = f;
+      rotb[b * 16 + i * 4 + j] = static_cast<uint16_t>(f32_to_bf16_bits(f));
+    }
+}
+
+// ------------------------------------------------------------------ append
+
+struct AppendParams {
+  const uint16_t* keys;
+  const uint16_t* values;
+  uint32_t* k_codes;
+  uint16_t* k_scales;
+  uint16_t* k_biases;
+  uint32_t* v_codes;
+  uint16_t* v_scales;
+  uint16_t* v_biases;
+  const uint16_t* rot;
+  int batch, heads, n, cap;
+  int lens[IQ_MAX_BATCH];
+};
+
+// One warp per (row, K-or-V).  Lane l owns dims 8l..8l+7 (two rotation
+// blocks); 64-dim group g is lanes 8g..8g+7.
+__global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
+  const int lane = threadIdx.x & 31;
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+
+  // M_b blocks 2*lane and 2*lane+1 (32 bf16 = 64 bytes)
+  float m[2][4][4];
+  {
+    const uint4* r4 = reinterpret_cast<const uint4*>(p.rot) + lane * 4;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 v = __ldg(r4 + c);
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int idx = c * 8 + e * 2;  // bf16 index within the two blocks
+        m[idx >> 4][(idx >> 2) & 3][idx & 3] = bf16_to_f32(w[e] & 0xFFFFu);
+        m[(idx + 1) >> 4][((idx + 1) >> 2) & 3][(idx + 1) & 3] = bf16_to_f32(w[e] >> 16);
+      }
+    }
+  }
+
+  const long long rows = static_cast<long long>(p.batch) * p.heads * p.n;
+  for (long long item = gwarp; item < 2 * rows; item += nwarps) {
+    const bool is_v = item & 1;
+    const long long row = item >> 1;
+    const int i = static_cast<int>(row % p.n);
+    const long long bh = row / p.n;
+    const int b = static_cast<int>(bh / p.heads);
+    const uint16_t* src = (is_v ? p.values : p.keys) + row * kHeadDim + lane * 8;
+    uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+    uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = bf16_to_f32(rw[e] & 0xFFFFu);
+      x[2 * e + 1] = bf16_to_f32(rw[e] >> 16);
+    }
+    // rotate: y[4c+j] = bf16( sum_{i=0..3} x[4c+i] * M_b[c][i][j] ), f32 sum in order
+    float y[8];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float acc = __fmul_rn(x[4 * c], m[c][0][j]);
+#pragma unroll
+        for (int k = 1; k < 4; ++k) acc = __fadd_rn(acc, __fmul_rn(x[4 * c + k], m[c][k][j]));
+        y[4 * c + j] = round_bf16(acc);
+      }
+    float mn = y[0], mx = y[0];
+#pragma unroll
+    for (int e = 1; e < 8; ++e) {
+      mn = fminf(mn, y[e]);
+      mx = fmaxf(mx, y[e]);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const int levels = is_v ? 7 : 15;
+    const float scale = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(levels));
+    const uint32_t s_bits = f32_to_bf16_bits(scale);
+    const float s_hat = bf16_to_f32(s_bits);
+    uint32_t code[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      int c = 0;
+      if (s_hat != 0.0f) {
+        c = __float2int_rn(__fdiv_rn(__fsub_rn(y[e], mn), s_hat));
+        c = min(max(c, 0), levels);
+      }
+      code[e] = static_cast<uint32_t>(c);
+    }
+    const long long dst = bh * p.cap + p.lens[b] + i;
+    if (!is_v) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w |= code[e] << (4 * e);
+      p.k_codes[dst * kKWords + lane] = w;
+    } else {
+      uint32_t v24 = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v24 |= code[e] << (3 * e);
+      // output word w covers stream bits [32w, 32w+32): lanes a = 32w/24 and a+1
+      const int a = lane < kVWords ? (4 * lane) / 3 : 0;
+      const int off = lane < kVWords ? 32 * lane - 24 * a : 0;  // 0, 8 or 16
+      const uint32_t lo = __shfl_sync(0xffffffffu, v24, a);
+      const uint32_t hi = __shfl_sync(0xffffffffu, v24, min(a + 1, 31));
+      if (lane < kVWords) p.v_codes[dst * kVWords + lane] = (lo >> off) | (hi << (24 - off));
+    }
+    // scales and biases of the 4 groups: lanes 0, 8, 16, 24 hold them
+    const uint32_t b_bits = f32_to_bf16_bits(mn);
+    uint32_t sg[4], bg[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      sg[g] = __shfl_sync(0xffffffffu, s_bits, 8 * g);
+      bg[g] = __shfl_sync(0xffffffffu, b_bits, 8 * g);
+    }
+    if (lane < 2) {
+      const uint32_t* v = lane == 0 ? sg : bg;
+      uint16_t* base = lane == 0 ? (is_v ? p.v_scales : p.k_scales) : (is_v ? p.v_biases : p.k_biases);
+      uint2 pk = make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+      *reinterpret_cast<uint2*>(base + dst * kGroups) = pk;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ gather
+
+struct GatherParams {
+  const void* src[6];
+  void* dst[6];
+  int row_units[6];  // 8-byte units per row of each buffer
+  int dst_batch, heads, src_cap, dst_cap;
+  int src_of[IQ_MAX_BATCH];
+  int len[IQ_MAX_BATCH];
+};
+
+// blockIdx.y = dst sequence * heads + head, blockIdx.z = buffer.
+__global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherParams p) {
+  const int seq = blockIdx.y / p.heads, h = blockIdx.y % p.heads, buf = blockIdx.z;
+  const long long units = static_cast<long long>(p.len[seq]) * p.row_units[buf];
+  const uint2* s = static_cast<const uint2*>(p.src[buf]) +
+                   (static_cast<long long>(p.src_of[seq]) * p.heads + h) * p.src_cap * p.row_units[buf];
+  uint2* d = static_cast<uint2*>(p.dst[buf]) +
+             (static_cast<long long>(seq) * p.heads + h) * p.dst_cap * p.row_units[buf];
+  for (long long u = blockIdx.x * 256LL + threadIdx.x; u < units; u += 256LL * gridDim.x) d[u] = s[u];
+}
+
+}  // namespace iq
+
+using namespace iq;
+
+// ------------------------------------------------------------------ C ABI
+
+extern "C" {
+
+const char* iq_status_string(int status) {
+  switch (status) {
+    case IQ_OK: return "IQ_OK";
+    case IQ_ERR_INVALID_ARG: return "IQ_ERR_INVALID_ARG";
+    case IQ_ERR_CAPACITY: return "IQ_ERR_CAPACITY";
+    case IQ_ERR_WORKSPACE: return "IQ_ERR_WORKSPACE";
+    case IQ_ERR_UNSUPPORTED: return "IQ_ERR_UNSUPPORTED";
+    case IQ_ERR_CUDA: return "IQ_ERR_CUDA";
+    case IQ_ERR_DEVICE: return "IQ_ERR_DEVICE";
+    default: return "IQ_ERR_UNKNOWN";
+  }
+}
+
+const char* iq_last_error(void) { return g_last_error.c_str(); }
+
+int iq_build_rotation(int head_dim, const float* draws_host, float* rot_f32, uint16_t* rot_bf16,
+                      iq_stream_t stream) {
+  clear_error();
+  if (!draws_host || !rot_f32 || !rot_bf16) return fail(IQ_ERR_INVALID_ARG, "null pointer");
+  if (head_dim <= 0 || head_dim % 4) return fail(IQ_ERR_INVALID_ARG, "head_dim must be a positive multiple of 4");
+  if (head_dim != kHeadDim) return fail(IQ_ERR_UNSUPPORTED, "only head_dim 256 is built");
+  const int nb = head_dim / 4;
+  // The draws travel as a by-value kernel parameter, so the host buffer may be
+  // reused as soon as this call returns.
+  RotationDraws d;
+  std::memcpy(d.v, draws_host, sizeof(d.v));
+  rotation_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(d, rot_f32, rot_bf16, nb);
+  IQ_CUDA(cudaGetLastError());
+  return IQ_OK;
+}
+
+int iq_cache_bytes(int batch, int kv_heads, int head_dim, int group_size, int k_bits, int v_bits,
+                   int capacity, size_t out_bytes[6]) {
+  clear_error();
+  if (!out_bytes) return fail(IQ_ERR_INVALID_ARG, "null out_bytes");
+  if (batch <= 0 || kv_heads <= 0 || capacity <= 0 || capacity % IQ_STEP)
+    return fail(IQ_ERR_INVALID_ARG, "batch, kv_heads > 0 and capacity a positive multiple of 256 required");
+  if (head_dim != kHeadDim || group_size != kGroup || k_bits != 4 || v_bits != 3)
+    return fail(IQ_ERR_UNSUPPORTED, "only head_dim 256, group 64, k_bits 4, v_bits 3 are built");
+  if (batch > IQ_MAX_BATCH) return fail(IQ_ERR_UNSUPPORTED, "batch above IQ_MAX_BATCH");
+  const size_t rows = static_cast<size_t>(batch) * kv_heads * capacity;
+  const size_t ng = head_dim / group_size;
+  out_bytes[0] = rows * (head_dim * k_bits / 32) * 4;
+  out_bytes[1] = out_bytes[2] = rows * ng * 2;
+  out_bytes[3] = rows * (head_dim * v_bits / 32) * 4;
+  out_bytes[4] = out_bytes[5] = rows * ng * 2;
+  return IQ_OK;
+}
+
+int iq_cache_check(const iq_cache* c) {
+  clear_error();
+  if (!c) return fail(IQ_ERR_INVALID_ARG, "null cache");
+  size_t bytes[6];
+  int st = iq_cache_bytes(c->batch, c->kv_heads, c->head_dim, c->group_size, c->k_bits, c->v_bits,
+                          c->capacity, bytes);
+  if (st != IQ_OK) return st;
+  const void* ptrs[6] = {c->k_codes, c->k_scales, c->k_biases, c->v_codes, c->v_scales, c->v_biases};
+  for (int i = 0; i < 6; ++i) {
+    if (!ptrs[i]) return fail(IQ_ERR_INVALID_ARG, "null cache buffer");
+    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16) return fail(IQ_ERR_INVALID_ARG, "cache buffer not 16-byte aligned");
+  }
+  if (!c->lens) return fail(IQ_ERR_INVALID_ARG, "null lens");
+  for (int b = 0; b < c->batch; ++b)
+    if (c->lens[b] < 0 || c->lens[b] > c->capacity) return fail(IQ_ERR_INVALID_ARG, "lens[b] outside [0, capacity]");
+  return IQ_OK;
+}
+
+size_t iq_cache_nbytes(const iq_cache* c) {
+  size_t bytes[6];
+  if (!c || iq_cache_bytes(c->batch, c->kv_heads, c->head_dim, c->group_size, c->k_bits, c->v_bits,
+                           c->capacity, bytes) != IQ_OK)
+    return 0;
+  size_t t = 0;
+  for (int i = 0; i < 6; ++i) t += bytes[i];
+  return t;
+}
+
+int iq_cache_append(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n,
+                    const uint16_t* rot_bf16, iq_stream_t stream) {
+  int st = iq_cache_check(c);
+  if (st != IQ_OK) return st;
+  if (n < 0) return fail(IQ_ERR_INVALID_ARG, "negative token count");
+  if (n == 0) return IQ_OK;
+  if (!keys || !values || !rot_bf16) return fail(IQ_ERR_INVALID_ARG, "null keys/values/rotation");
+  if (reinterpret_cast<uintptr_t>(keys) % 16 || reinterpret_cast<uintptr_t>(values) % 16 ||
+      reinterpret_cast<uintptr_t>(rot_bf16) % 16)
+    return fail(IQ_ERR_INVALID_ARG, "keys/values/rotation not 16-byte aligned");
+  for (int b = 0; b < c->batch; ++b)
+    if (static_cast<long long>(c->lens[b]) + n > c->capacity)
+      return fail(IQ_ERR_CAPACITY, "append past capacity (grow the cache first)");
+  AppendParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.keys = keys;
+  p.values = values;
+  p.k_codes = c->k_codes;
+  p.k_scales = c->k_scales;
+  p.k_biases = c->k_biases;
+  p.v_codes = c->v_codes;
+  p.v_scales = c->v_scales;
+  p.v_biases = c->v_biases;
+  p.rot = rot_bf16;
+  p.batch = c->batch;
+  p.heads = c->kv_heads;
+  p.n = n;
+  p.cap = c->capacity;
+  for (int b = 0; b < c->batch; ++b) p.lens[b] = c->lens[b];
+  const long long items = 2LL * c->batch * c->kv_heads * n;
+  long long blocks = (items + 7) / 8;
+  const long long max_blocks = static_cast<long long>(num_sms()) * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
+  append_kernel<<<static_cast<int>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  IQ_CUDA(cudaGetLastError());
+  for (int b = 0; b < c->batch; ++b) c->lens[b] += n;
+  return IQ_OK;
+}
+
+int iq_cache_trim(iq_cache* c, const int32_t* n_host, int32_t* trimmed_host) {
+  clear_error();
+  if (!c || !c->lens || !n_host) return fail(IQ_ERR_INVALID_ARG, "null pointer");
+  if (c->batch <= 0 || c->batch > IQ_MAX_BATCH) return fail(IQ_ERR_INVALID_ARG, "bad batch");
+  for (int b = 0; b < c->batch; ++b)
+    if (n_host[b] < 0) return fail(IQ_ERR_INVALID_ARG, "negative trim count");
+  for (int b = 0; b < c->batch; ++b) {
+    const int32_t t = n_host[b] < c->lens[b] ? n_host[b] : c->lens[b];
+    c->lens[b] -= t;
+    if (trimmed_host) trimmed_host[b] = t;
+  }
+  return IQ_OK;
+}
+
+int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of, iq_stream_t stream) {
+  int st = iq_cache_check(src);
+  if (st != IQ_OK) return st;
+  st = iq_cache_check(dst);
+  if (st != IQ_OK) return st;
+  if (!src_of) return fail(IQ_ERR_INVALID_ARG, "null src_of");
+  if (src->kv_heads != dst->kv_heads || src->head_dim != dst->head_dim ||
+      src->group_size != dst->group_size || src->k_bits != dst->k_bits || src->v_bits != dst->v_bits)
+    return fail(IQ_ERR_INVALID_ARG, "src and dst shapes differ");
+  GatherParams p;
+  std::memset(&p, 0, sizeof(p));
+  int max_len = 0;
+  for (int i = 0; i < dst->batch; ++i) {
+    if (src_of[i] < 0 || src_of[i] >= src->batch) return fail(IQ_ERR_INVALID_ARG, "src_of index out of range");
+    p.src_of[i] = src_of[i];
+    p.len[i] = src->lens[src_of[i]];
+    if (p.len[i] > dst->capacity) return fail(IQ_ERR_CAPACITY, "dst capacity below a source length");
+    if (p.len[i] > max_len) max_len = p.len[i];
+  }
+  const void* sp[6] = {src->k_codes, src->k_scales, src->k_biases, src->v_codes, src->v_scales, src->v_biases};
+  void* dp[6] = {dst->k_codes, dst->k_scales, dst->k_biases, dst->v_codes, dst->v_scales, dst->v_biases};
+  const int units[6] = {kKWords / 2, 1, 1, kVWords / 2, 1, 1};
+  for (int i = 0; i < 6; ++i) {
+    if (sp[i] == dp[i]) return fail(IQ_ERR_INVALID_ARG, "src and dst share a buffer");
+    p.src[i] = sp[i];
+    p.dst[i] = dp[i];
+    p.row_units[i] = units[i];
+  }
+  p.dst_batch = dst->batch;
+  p.heads = dst->kv_heads;
+  p.src_cap = src->capacity;
+  p.dst_cap = dst->capacity;
+  if (max_len > 0) {
+    int gx = (max_len * 16 + 255) / 256;
+    if (gx > 64) gx = 64;
+    dim3 grid(gx, dst->batch * dst->kv_heads, 6);
+    gather_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    IQ_CUDA(cudaGetLastError());
+  }
+  for (int i = 0; i < dst->batch; ++i) dst->lens[i] = p.len[i];
+  return IQ_OK;
+}
+
+}  // extern "C"
