@@ -1,0 +1,362 @@
+"""Benchmark: batched decode over the rotated K4/V3 quantised KV cache.
+
+Workload (default): 32 sequences, 16 query heads / 2 kv heads, head_dim 256,
+each sequence holding a 32768-token K4/V3 cache (keys with x20 outlier
+channels, values ~N(0,1)); one step = append one new token per sequence (K1
+append kernel) + attend one bf16 query per sequence (split-KV attention +
+combine).  Metric: KV tokens scanned per second (B x tokens attended per step),
+whole job.  Inputs are resident in HBM before the timed region; the cache
+(537 MB read per step) is larger than the 129 MB L2, so no flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica on its own GPU (the path has
+no exchange step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "quantized-KV decode attention: KV tokens/s and HBM GB/s vs ~8 TB/s roofline"
+UNIT = "KV tokens/s"
+K_ROW, V_ROW = 144, 112  # algorithmic bytes per token-head: codes + bf16 scales/biases
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the measured work runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def physical_gpu(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [x for x in vis.split(",") if x.strip()]
+    if local < len(parts) and parts[local].strip().isdigit():
+        return int(parts[local])
+    return local
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def make_workload(wid: int, steps_total: int, dev):
+    """Device-resident cache holding the prefill, plus per-step inputs (host and device)."""
+    from rotated_bit_quantized_gb300 import IQCache, Rotation
+    w = si.WORKLOADS[wid]
+    B, Hkv, Hq = w["B"], w["Hkv"], w["Hq"]
+    rot = Rotation(0, 256, dev)
+    cache = IQCache(B, Hkv, device=dev, capacity=256)
+    cache.reserve(w["prefill"] + w["append"] * steps_total + 256)
+    full_k, full_v = si.kv_tokens(w["seed"], B, Hkv, w["prefill"], outliers=w["outliers"])
+    chunk = 4096
+    for lo in range(0, w["prefill"], chunk):  # upload in slices to bound device temporaries
+        hi = min(lo + chunk, w["prefill"])
+        cache.append(full_k[:, :, lo:hi].to(dev), full_v[:, :, lo:hi].to(dev), rot)
+    del full_k, full_v
+    steps = []
+    for s in range(steps_total):
+        k, v = si.kv_tokens(w["seed"], B, Hkv, w["append"], outliers=w["outliers"], step=s)
+        q = si.queries(w["seed"], B, Hq, w["queries"], step=s)
+        steps.append((k.pin_memory(), v.pin_memory(), q.pin_memory()))
+    torch.cuda.synchronize(dev)
+    return w, rot, cache, steps
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from rotated_bit_quantized_gb300 import build as b
+    b.build()
+    W, K = args.warmup, args.steps
+    w, rot, cache, steps = make_workload(args.workload, W + K, dev)
+    B, Hkv, Hq, L = w["B"], w["Hkv"], w["Hq"], w["queries"]
+    base_len = cache.lens.copy()
+    dsteps = [(k.to(dev), v.to(dev), q.to(dev)) for k, v, q in steps]
+    out = torch.empty((B, Hq, L, 256), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    accept = (si.accepted_lengths(W + K, B, w["append"], w["accept_seed"])
+              if "accept_seed" in w else None)
+
+    def step(i, ev=None):
+        k, v, q = dsteps[i]
+        cache.append(k, v, rot)
+        if ev is not None:
+            ev[0].record(stream)
+        cache.attend(q, rot, causal=w["causal"], out=out)
+        if ev is not None:
+            ev[1].record(stream)
+        if accept is not None:  # speculative verify: keep the accepted prefix only
+            cache.commit_verified_prefix(w["append"], accept[i])
+
+    # ---- device-resident run
+    for i in range(W):
+        step(i)
+    cache.trim(cache.lens - base_len)  # timed steps start from the 32768-token cache
+    torch.cuda.synchronize(dev)
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tokens = 0
+    gpu_index = physical_gpu(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index) as clk:
+        time.sleep(0.25)
+        start.record(stream)
+        for i in range(K):
+            tokens += int(cache.lens.sum()) + B * w["append"]
+            step(W + i, attn_ev[i])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        # keep sampling a little so short timed regions still get clock samples under load
+        extra_t0 = time.time()
+        while time.time() - extra_t0 < 0.6:
+            cache.attend(dsteps[W + K - 1][2], rot, causal=w["causal"], out=out)
+            torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(stop)
+    attn_ms = [a.elapsed_time(bq) for a, bq in attn_ev]
+    status = cache.device_status()
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+
+    # ---- end to end through the public API with host buffers
+    cache.trim(cache.lens - base_len)
+    host_out = torch.empty((B, Hq, L, 256), dtype=torch.bfloat16).pin_memory()
+    dk = torch.empty_like(dsteps[0][0])
+    dv = torch.empty_like(dsteps[0][1])
+    dq = torch.empty_like(dsteps[0][2])
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_tokens = 0
+    e0.record(stream)
+    for i in range(K):
+        k, v, q = steps[W + i]
+        dk.copy_(k, non_blocking=True)
+        dv.copy_(v, non_blocking=True)
+        dq.copy_(q, non_blocking=True)
+        cache.append(dk, dv, rot)
+        cache.attend(dq, rot, causal=w["causal"], out=out)
+        host_out.copy_(out, non_blocking=True)
+        e_tokens += int(cache.lens.sum())
+        if accept is not None:
+            cache.commit_verified_prefix(w["append"], accept[W + i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1)
+    te = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e_ms_max = float(te.item())
+
+    if rank == 0:
+        hbm, peak_kind = peaks()
+        token_heads = tokens * Hkv / K  # per step, per rank
+        attn_avg_s = statistics.mean(attn_ms) / 1e3
+        achieved = token_heads * (K_ROW + V_ROW) / attn_avg_s / 1e9
+        h2d = (dsteps[0][0].numel() + dsteps[0][1].numel() + dsteps[0][2].numel()) * 2
+        d2h = out.numel() * 2
+        cpu = None if args.no_cpu_baseline else cpu_baseline_sample(args.workload, budget_s=args.cpu_seconds)
+        rec = {
+            "metric": METRIC, "value": ws * tokens / (ms_max / 1e3), "unit": UNIT, "n_gpus": ws,
+            "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded N(0,1); keys with x20 outlier channels)",
+            "config": {"workload": f"{w['name']}: B={B} seqs, Hq={Hq}/Hkv={Hkv}, head_dim=256, "
+                                   f"{w['prefill']}-token K4/V3 cache, append {w['append']} + attend "
+                                   f"{L} query per step",
+                       "parallelism": f"replicas x{ws}",
+                       "l2": "no flush: the cache read per step (537 MB) exceeds the 129 MB L2"},
+            "roofline": {"bound": "hbm", "kernel": "iq_attend (attend_kernel + combine_kernel)",
+                         "achieved": achieved, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "bytes_per_token_head": K_ROW + V_ROW, "token_heads_per_launch": token_heads,
+                         "avg_launch_us": attn_avg_s * 1e6},
+            "e2e": {"value": ws * e_tokens / (e_ms_max / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * K,
+            "clocks": clk.summary(),
+            "device_status": status,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(rec), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def cpu_baseline_sample(wid: int, budget_s: float = 15.0, sequences=None):
+    """The oracle as it stands, on a bounded sample of the workload's step:
+    append one token and attend one query for a few sequences.  Returns the
+    record for the JSON line (KV tokens/s)."""
+    from oracle import attention, rotation as orot
+    from oracle.cache import OracleCache
+    w = si.WORKLOADS[wid]
+    Hkv, Hq = w["Hkv"], w["Hq"]
+    mb = orot.blocks_bf16(orot.build_blocks(si.rotation_draws(0, 256)))
+    seqs = sequences if sequences is not None else list(range(w["B"]))
+    tokens, spent, done = 0, 0.0, 0
+    for b in seqs:
+        oc = OracleCache(1, Hkv)
+        k = np.stack([si.kv_slice(w["seed"], b, h, w["prefill"], outliers=w["outliers"])[0].float().numpy()
+                      for h in range(Hkv)])[None]
+        v = np.stack([si.kv_slice(w["seed"], b, h, w["prefill"], outliers=w["outliers"])[1].float().numpy()
+                      for h in range(Hkv)])[None]
+        oc.append(k, v, mb)  # prefill: setup, not timed
+        ks = np.stack([si.kv_slice(w["seed"], b, h, w["append"], outliers=w["outliers"], step=0)[0].float().numpy()
+                       for h in range(Hkv)])[None]
+        vs = np.stack([si.kv_slice(w["seed"], b, h, w["append"], outliers=w["outliers"], step=0)[1].float().numpy()
+                       for h in range(Hkv)])[None]
+        q = si.queries(w["seed"], w["B"], Hq, w["queries"], step=0)[b:b + 1].float().numpy()
+        t0 = time.perf_counter()
+        oc.append(ks, vs, mb)
+        attention.attend(q, oc, mb, causal=w["causal"])
+        spent += time.perf_counter() - t0
+        tokens += int(oc.lens[0])
+        done += 1
+        if spent >= budget_s:
+            break
+    cores = len(os.sched_getaffinity(0))
+    return {"value": tokens / spent, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {w['B']} sequences of one step (append 1 + attend over "
+                      f"{w['prefill'] + w['append']} tokens, {Hkv} kv heads); NumPy oracle, "
+                      f"BLAS threads up to {cores}; prefill encode untimed",
+            "seconds": spent}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    W, K = args.warmup, args.steps
+    w = si.WORKLOADS[args.workload]
+    per_step_budget = max(1.0, args.cpu_seconds / max(1, K + W))
+    vals = []
+    for i in range(W + K):
+        r = cpu_baseline_sample(args.workload, budget_s=per_step_budget, sequences=[i % w["B"]])
+        if i >= W:
+            vals.append(r)
+    tok = sum(r["value"] * r["seconds"] for r in vals)
+    sec = sum(r["seconds"] for r in vals)
+    value = tok / sec
+    cores = len(os.sched_getaffinity(0))
+    rec = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+           "warmup": W, "ms_per_step": 1e3 * sec / K, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64 (NumPy oracle)", "data": "synthetic",
+           "config": {"workload": f"{w['name']} (each step: one sequence of B={w['B']}, append "
+                                  f"{w['append']} + attend over {w['prefill'] + w['append']} tokens)"},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": "one sequence per step, prefill encode untimed"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(rec), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=4, choices=[2, 4, 5])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

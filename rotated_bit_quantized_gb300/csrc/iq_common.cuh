@@ -33,7 +33,7 @@ constexpr int kGroup = 64;
 constexpr int kKWords = 32;   // 256 dims * 4 bits / 32
 constexpr int kVWords = 24;   // 256 dims * 3 bits / 32
 constexpr int kGroups = 4;    // 256 / 64
-constexpr uint32_t kSpinLimit = 1u << 26;  // bounded waits: ~seconds, then report
+constexpr uint32_t kSpinLimit = 1u << 22;  // bounded waits (~seconds), then report
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);

@@ -118,6 +118,15 @@ def kv_tokens(data_seed: int, batch: int, kv_heads: int, n: int, head_dim: int =
     return k, v
 
 
+def kv_slice(data_seed: int, b: int, h: int, n: int, head_dim: int = 256,
+             outliers: bool = False, step: int | None = None):
+    """K and V tokens of the single slice (b, h) as CPU bfloat16 tensors [n, D];
+    identical to ``kv_tokens(...)[.][b, h]``."""
+    stream = STREAM_PREFILL if step is None else STREAM_STEP
+    k, v = _slice_tokens(data_seed, b, h, n, head_dim, outliers, stream, step)
+    return to_bf16(k), to_bf16(v)
+
+
 def queries(data_seed: int, batch: int, q_heads: int, n: int, head_dim: int = 256,
             step: int = 0) -> torch.Tensor:
     """Queries as a CPU bfloat16 tensor [B, Hq, n, D], ~N(0, 1)."""
@@ -136,3 +145,20 @@ def accepted_lengths(steps: int, batch: int, draft: int = 4, seed: int = 50) -> 
 def garbage_like(shape, seed: int = 7) -> np.ndarray:
     """Random 32-bit words used to pre-fill buffers whose stale rows must never be read."""
     return np.random.default_rng(seed).integers(0, 2 ** 32, size=shape, dtype=np.uint32)
+
+
+# The five workloads (sizes and seeds only).  `prefill` tokens are appended in
+# one call; each of `steps` steps appends `append` tokens per sequence and then
+# attends `queries` new queries per sequence (`causal` as stated).
+WORKLOADS = {
+    1: dict(name="tiny", B=1, Hq=1, Hkv=1, prefill=256, outliers=False, steps=0, append=0,
+            queries=1, causal=False, seed=1),
+    2: dict(name="single_stream_decode", B=1, Hq=16, Hkv=2, prefill=4096, outliers=True, steps=0,
+            append=0, queries=1, causal=False, seed=2),
+    3: dict(name="chunked_prefill", B=1, Hq=16, Hkv=2, prefill=0, outliers=True, steps=16,
+            append=2048, queries=2048, causal=True, trim_after=1000, seed=3),
+    4: dict(name="batched_decode", B=32, Hq=16, Hkv=2, prefill=32768, outliers=True, steps=64,
+            append=1, queries=1, causal=True, seed=4),
+    5: dict(name="spec_verify", B=8, Hq=16, Hkv=2, prefill=131072, outliers=True, steps=32,
+            append=4, queries=4, causal=True, accept_seed=50, seed=5),
+}

@@ -1,0 +1,107 @@
+"""The C-ABI library loads, exports every symbol of include/iqkv.h, and rejects
+bad arguments on the host before touching a device.  Runs without a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from rotated_bit_quantized_gb300 import build
+    build.build()
+    from rotated_bit_quantized_gb300 import _abi
+    return _abi.lib()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "iqkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(iq_[a-z_0-9]+)\s*\(", text))
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = header_functions()
+    from rotated_bit_quantized_gb300 import _abi
+    assert declared == set(_abi.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    assert L.iq_status_string(0) == b"IQ_OK"
+    assert L.iq_status_string(2) == b"IQ_ERR_CAPACITY"
+    assert L.iq_status_string(99) == b"IQ_ERR_UNKNOWN"
+
+
+def test_cache_bytes(L):
+    out = (ctypes.c_size_t * 6)()
+    assert L.iq_cache_bytes(2, 3, 256, 64, 4, 3, 512, out) == 0
+    rows = 2 * 3 * 512
+    assert list(out) == [rows * 128, rows * 8, rows * 8, rows * 96, rows * 8, rows * 8]
+    assert L.iq_cache_bytes(2, 3, 256, 64, 4, 3, 500, out) == 1        # not a multiple of 256
+    assert L.iq_cache_bytes(2, 3, 128, 64, 4, 3, 512, out) == 4        # other head_dim
+    assert L.iq_cache_bytes(2, 3, 256, 64, 2, 3, 512, out) == 4        # other bits
+    assert L.iq_cache_bytes(300, 3, 256, 64, 4, 3, 512, out) == 4      # batch above maximum
+    assert b"256" in L.iq_last_error() or L.iq_last_error()
+
+
+def fake_desc(batch=2, cap=256, lens=(3, 4), align=0):
+    from rotated_bit_quantized_gb300._abi import IQCacheDesc
+    d = IQCacheDesc(batch, 2, 256, 64, 4, 3, cap)
+    base = 0x10000000 + align
+    for i, name in enumerate(("k_codes", "k_scales", "k_biases", "v_codes", "v_scales", "v_biases")):
+        setattr(d, name, base + i * 0x1000000)
+    arr = np.array(lens, dtype=np.int32)
+    d.lens = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    return d, arr
+
+
+def test_check_and_trim_host_only(L):
+    d, lens = fake_desc()
+    assert L.iq_cache_check(ctypes.byref(d)) == 0
+    d2, _ = fake_desc(align=4)
+    assert L.iq_cache_check(ctypes.byref(d2)) == 1
+    d3, _ = fake_desc(lens=(3, 300))
+    assert L.iq_cache_check(ctypes.byref(d3)) == 1
+    n = np.array([5, 1], dtype=np.int32)
+    out = np.zeros(2, dtype=np.int32)
+    P = ctypes.POINTER(ctypes.c_int32)
+    assert L.iq_cache_trim(ctypes.byref(d), n.ctypes.data_as(P), out.ctypes.data_as(P)) == 0
+    assert out.tolist() == [3, 1] and lens.tolist() == [0, 3]
+    neg = np.array([-1, 0], dtype=np.int32)
+    assert L.iq_cache_trim(ctypes.byref(d), neg.ctypes.data_as(P), out.ctypes.data_as(P)) == 1
+    assert lens.tolist() == [0, 3]
+    assert L.iq_cache_nbytes(ctypes.byref(d)) == 2 * 2 * 256 * 256
+
+
+def test_append_and_attend_reject_before_launch(L):
+    d, lens = fake_desc(lens=(250, 10))
+    p = ctypes.c_void_p(0x20000000)
+    # capacity: 250 + 7 > 256
+    assert L.iq_cache_append(ctypes.byref(d), p, p, 7, p, None) == 2
+    assert lens.tolist() == [250, 10]
+    assert L.iq_cache_append(ctypes.byref(d), p, p, -1, p, None) == 1
+    assert L.iq_cache_append(ctypes.byref(d), None, p, 1, p, None) == 1
+    out = ctypes.c_size_t()
+    assert L.iq_attend_workspace(ctypes.byref(d), 16, 1, ctypes.byref(out)) == 0 and out.value > 256
+    # bad causal flag, rep not dividing 8, causal with too few tokens, missing workspace
+    assert L.iq_attend(ctypes.byref(d), p, 16, 1, 0.0625, 2, p, p, 0, p, out.value, None) == 1
+    assert L.iq_attend(ctypes.byref(d), p, 6, 1, 0.0625, 0, p, p, 0, p, out.value, None) == 4
+    assert L.iq_attend(ctypes.byref(d), p, 16, 20, 0.0625, 1, p, p, 0, p, out.value, None) == 1
+    assert L.iq_attend(ctypes.byref(d), p, 16, 1, 0.0625, 0, p, p, 0, None, 0, None) == 3
+    assert L.iq_attend(ctypes.byref(d), p, 16, 1, 0.0625, 0, p, p, 0, p, 16, None) == 3
+    d0, _ = fake_desc(lens=(0, 4))
+    assert L.iq_attend(ctypes.byref(d0), p, 16, 1, 0.0625, 0, p, p, 0, p, out.value, None) == 1
+
+
+def test_rotation_rejects(L):
+    draws = np.zeros((64, 2, 4), dtype=np.float32)
+    p = ctypes.c_void_p(0x20000000)
+    assert L.iq_build_rotation(255, draws.ctypes.data, p, p, None) == 1
+    assert L.iq_build_rotation(128, draws.ctypes.data, p, p, None) == 4
+    assert L.iq_build_rotation(256, None, p, p, None) == 1
