@@ -188,6 +188,36 @@ int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queri
               void* workspace, size_t workspace_bytes, iq_stream_t stream);
 
 /*
+ * iq_attend_noalloc — iq_attend for callers that cannot allocate device
+ * memory.  (The source pages have no counterpart: this is a library service.)
+ *
+ * Some callers cannot call cudaMalloc for a workspace: a serving process whose
+ * allocator already owns all of HBM (weights and KV pool), a plugin that only
+ * receives the buffers its host hands it, or a decode loop where an allocation
+ * (which can synchronise the device) would break the latency budget.  This
+ * entry point computes exactly what iq_attend computes, with its scratch in a
+ * library-owned device array of IQ_NOALLOC_SCRATCH_BYTES (64 MiB) that every
+ * GPU using this entry point keeps until the process exits.  It allocates
+ * nothing and calls no allocating routine; the caller still passes q and out.
+ *
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ * Sharing: every call uses the same array and it keeps the last call's
+ * contents (the status word is cleared by each call; the partials are written
+ * before they are read).  Calls that can run at the same time on the GPU
+ * (different streams without ordering) race on the array: serialise them.
+ * Errors: as iq_attend, plus WORKSPACE when the call needs more scratch than
+ * IQ_NOALLOC_SCRATCH_BYTES (use iq_attend with a caller workspace then).
+ * Kernel-side failures land in the shared status word, which this entry point
+ * does not report; use iq_attend + iq_read_status where that matters.
+ */
+#define IQ_NOALLOC_SCRATCH_BYTES (64u << 20)
+int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
+                      float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
+                      iq_stream_t stream);
+
+/*
  * iq_read_status — synchronise `stream`, read the status word that the last
  * iq_attend on this workspace left, and clear it.  *device_status is 0 when
  * every kernel completed normally.  Blocks the calling thread.

@@ -20,10 +20,12 @@ IQ_ERR_CUDA = 5
 IQ_ERR_DEVICE = 6
 IQ_MAX_BATCH = 256
 IQ_STEP = 256
+IQ_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 EXPORTS = ("iq_status_string", "iq_last_error", "iq_build_rotation", "iq_cache_bytes",
            "iq_cache_check", "iq_cache_nbytes", "iq_cache_append", "iq_cache_trim",
-           "iq_cache_gather", "iq_attend_workspace", "iq_attend", "iq_read_status")
+           "iq_cache_gather", "iq_attend_workspace", "iq_attend", "iq_read_status",
+           "iq_attend_noalloc")
 
 
 class IQCacheDesc(ctypes.Structure):
@@ -68,6 +70,7 @@ def lib() -> ctypes.CDLL:
         L.iq_attend_workspace.argtypes = [DESC, I, I, ctypes.POINTER(S)]
         L.iq_attend.argtypes = [DESC, P, I, I, ctypes.c_float, I, P, P, I, P, S, P]
         L.iq_read_status.argtypes = [P, P, ctypes.POINTER(I)]
+        L.iq_attend_noalloc.argtypes = [DESC, P, I, I, ctypes.c_float, I, P, P, I, P]
         for name in EXPORTS:
             if name not in ("iq_status_string", "iq_last_error", "iq_cache_nbytes"):
                 getattr(L, name).restype = I

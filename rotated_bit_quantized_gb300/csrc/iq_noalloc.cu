@@ -1,0 +1,73 @@
+// libiqkv: iq_attend_noalloc — attention for callers that cannot allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc: a serving process that has already
+// handed all of HBM to its own arena (weights + KV pool), a plugin that only
+// sees the buffers its host gives it, or a latency-critical decode loop where
+// an allocation (which may synchronise the device) is not acceptable.  For
+// them this entry point runs the same split-KV attention as iq_attend, with
+// its scratch (the split partials and the status word) in a library-owned,
+// file-scope device array instead of a caller workspace.
+//
+// The array is IQ_NOALLOC_SCRATCH_BYTES large and lives for as long as the
+// library is loaded on a device.  Its address is looked up once per device,
+// on the first call made with that device current.  Every call shares the
+// array, so calls that may run at the same time on the GPU (different streams,
+// no ordering between them) race on it and must not overlap.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "iq_common.cuh"
+
+namespace iq {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[IQ_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device (set-up on the
+// first call per device).  In host code the array's name is only a host-side
+// stand-in, so the real address must come from cudaGetSymbolAddress.
+int scratch_address(void** out) {
+  int dev = -1;
+  IQ_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return fail(IQ_ERR_UNSUPPORTED, "device index above 63");
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return IQ_OK;
+}
+
+}  // namespace
+}  // namespace iq
+
+extern "C" int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
+                                 float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
+                                 iq_stream_t stream) {
+  size_t need = 0;
+  int st = iq_attend_workspace(cache, q_heads, n_queries, &need);
+  if (st != IQ_OK) return st;
+  if (need > IQ_NOALLOC_SCRATCH_BYTES)
+    return iq::fail(IQ_ERR_WORKSPACE,
+                    "iq_attend_noalloc: this call needs " + std::to_string(need) +
+                        " bytes of scratch, above the built-in " +
+                        std::to_string(static_cast<size_t>(IQ_NOALLOC_SCRATCH_BYTES)) +
+                        "; use iq_attend with a caller workspace");
+  void* scratch = nullptr;
+  st = iq::scratch_address(&scratch);
+  if (st != IQ_OK) return st;
+  // iq_attend clears the status word at the start of every call; the split
+  // partials are written before they are read, so nothing else needs zeroing.
+  return iq_attend(cache, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, scratch,
+                   IQ_NOALLOC_SCRATCH_BYTES, stream);
+}
