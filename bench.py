@@ -256,14 +256,14 @@ def run_ours(args):
                                    f"{L} query per step",
                        "parallelism": f"replicas x{ws}",
                        "l2": "no flush: the cache read per step (537 MB) exceeds the 129 MB L2"},
-            "roofline": {"bound": "hbm", "kernel": "iq_attend (attend_kernel + combine_kernel)",
+            "roofline": {"bound": "hbm", "kernel": "attend_kernel (iq_attend: split-KV attention with fused combine)",
                          "achieved": achieved, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": None,
                          "bytes_per_token_head": K_ROW + V_ROW, "token_heads_per_launch": token_heads,
                          "avg_launch_us": attn_avg_s * 1e6},
             "e2e": {"value": ws * e_tokens / (e_ms_max / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * K,
+            "gpu_launches": 2 * K,  # append_kernel + attend_kernel per step
             "clocks": clk.summary(),
             "device_status": status,
             "cpu_baseline": cpu,

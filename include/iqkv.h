@@ -157,7 +157,8 @@ int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of,
 
 /*
  * iq_attend_workspace — device scratch bytes iq_attend needs for these
- * lengths and shapes (split-KV partial results plus a status word).
+ * lengths and shapes (status word, per-unit chunk counters and the split-KV
+ * partial results).
  */
 int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_t* bytes);
 
@@ -196,7 +197,7 @@ int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queri
  * receives the buffers its host hands it, or a decode loop where an allocation
  * (which can synchronise the device) would break the latency budget.  This
  * entry point computes exactly what iq_attend computes, with its scratch in a
- * library-owned device array of IQ_NOALLOC_SCRATCH_BYTES (64 MiB) that every
+ * library-owned device array of IQ_NOALLOC_SCRATCH_BYTES (16 MiB) that every
  * GPU using this entry point keeps until the process exits.  It allocates
  * nothing and calls no allocating routine; the caller still passes q and out.
  *
@@ -212,7 +213,7 @@ int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queri
  * Kernel-side failures land in the shared status word, which this entry point
  * does not report; use iq_attend + iq_read_status where that matters.
  */
-#define IQ_NOALLOC_SCRATCH_BYTES (64u << 20)
+#define IQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
                       float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
                       iq_stream_t stream);

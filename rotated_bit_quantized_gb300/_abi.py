@@ -20,7 +20,7 @@ IQ_ERR_CUDA = 5
 IQ_ERR_DEVICE = 6
 IQ_MAX_BATCH = 256
 IQ_STEP = 256
-IQ_NOALLOC_SCRATCH_BYTES = 64 << 20
+IQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 EXPORTS = ("iq_status_string", "iq_last_error", "iq_build_rotation", "iq_cache_bytes",
            "iq_cache_check", "iq_cache_nbytes", "iq_cache_append", "iq_cache_trim",

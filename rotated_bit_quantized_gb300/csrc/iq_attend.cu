@@ -1,5 +1,5 @@
-// libiqkv: split-KV GQA attention over the packed K4/V3 cache, and the
-// split-combine + inverse-rotation pass.
+// libiqkv: GQA attention over the packed K4/V3 cache (persistent stream-K
+// kernel with the split combine and the inverse rotation fused in).
 //
 // Method source: page "sparkle mlx_streaming/core/cache/quant_kv.py",
 // `asym_quantized_sdpa` (scale the queries, GQA reshape so query head h reads
@@ -8,24 +8,36 @@
 // that the output is still in rotated value space, so the caller undoes the
 // rotation; `rotate_last` gives the query rotation.
 //
-// Kernel design (one CTA = one (sequence, kv head, query tile, key chunk)):
-//  * a producer warp streams 64-token tiles of packed K codes (2-D tensor copy
-//    with 128-byte swizzle), packed V codes and the four scale/bias rows (1-D
-//    bulk copies) into a 4-stage shared-memory ring guarded by mbarriers;
+// Work decomposition.  A "unit" is (sequence, kv head, tile of 8*NT query
+// rows); its keys form a run of 64-token tiles.  All units' tiles are laid
+// end to end and split evenly over a persistent grid (at most one CTA per
+// resident slot), so every CTA streams the same number of tiles; a CTA whose
+// range crosses unit boundaries finishes one unit segment and starts the
+// next.  Each segment writes an un-normalised partial (O, running max in log2
+// units, running sum); the CTA that finishes a unit's last segment (an atomic
+// counter per unit) merges the unit's partials (log-sum-exp), divides,
+// applies M_b^T and stores bf16 or fp32.
+//
+// Inside a CTA:
+//  * a producer warp streams the tiles (packed K codes by a 2-D tensor copy with
+//    128-byte swizzle; packed V codes and the four scale/bias rows by 1-D bulk
+//    copies) into a 4-stage shared-memory ring guarded by mbarriers, running
+//    ahead across unit boundaries;
 //  * consumer warps unpack codes to fp16 in registers with bit tricks and run
 //    m16n8k16 tensor-core MMAs: S = K_codes . q (per 64-dim group, fp32
 //    accumulate), folded with the group scale/bias on CUDA cores; online
-//    softmax in fp32; O^T += V_codes^T . (P * s_v) with P transposed in
-//    registers by movmatrix; the value bias term sum_t p_t b_t on CUDA cores;
-//  * each CTA writes an un-normalised partial (O, running max, running sum);
-//    the combine kernel merges the chunks (log-sum-exp), divides, applies
-//    M_b^T and stores bf16 or fp32.
+//    softmax in fp32 with a lazily moving reference max; O^T += (V_codes - 4)^T
+//    . (P * s_v) with P transposed in registers by movmatrix; the value bias
+//    term sum_t p_t (b_t + 4 s_t) on CUDA cores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
+#include <vector>
 
 #include "iq_common.cuh"
 
@@ -42,8 +54,18 @@ constexpr int OFF_VS = OFF_KB + 512;
 constexpr int OFF_VB = OFF_VS + 512;
 constexpr int STAGE = 17408;                 // multiple of 1024 (swizzle atom)
 constexpr uint32_t STAGE_TX = 8192 + 6144 + 4 * 512;
+constexpr int UNIT_CAP = 1024;   // units per launch (their tile prefix travels by value)
+constexpr int MIN_TILES_PER_CTA = 8;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float NEG_INF = -__builtin_huge_valf();
+// Lazy running max: the reference max of a row moves only when a score exceeds
+// it by more than 2^TAU (log2 units), so p = 2^(s - m) stays below 2^TAU and
+// p * s_v stays inside fp16 for value scales below 2^(16 - TAU).
+constexpr float TAU = 6.0f;
+// Value codes enter the P.V product centred: c - VCENTRE in [-4, 3] (exact in
+// fp16), which halves the worst-case effect of rounding P * s_v to fp16; the
+// VCENTRE * s_v part joins the fp32 bias term.
+constexpr float VCENTRE = 4.0f;
 // Row of the 16-token sub-tile that MMA token slot m (0..7) reads; slot m+8
 // reads row mu(m)+8.  Chosen so the swizzled K reads and the 96-byte-pitch V
 // reads are free of shared-memory bank conflicts.
@@ -58,18 +80,28 @@ struct Params {
   const uint16_t* v_biases;
   const uint16_t* q;
   const uint16_t* rot;
-  float* part_o;   // [P][GT][256]
-  float* part_ml;  // [P][GT][2] (running max, running sum)
+  float* part_o;       // [slots][GT][256]
+  float* part_ml;      // [slots][GT][2] (running max in log2 units, running sum)
   unsigned* status;
-  int batch, kv_heads, rep, nq, cap, nqt, chunk_tiles, maxc, causal;
+  unsigned* counters;  // [units]: finished segments per unit
+  void* out;
+  int out_f32;
+  int batch, kv_heads, rep, nq, cap, nqt, causal;
+  int unit_base, num_units, grid;  // this launch covers units [unit_base, unit_base + num_units)
   float scale;
   int lens[IQ_MAX_BATCH];
+  int prefix[UNIT_CAP + 1];  // tile prefix over this launch's units
 };
 
 __device__ __forceinline__ int tile_limit(const Params& p, int T, int qt, int gt) {
   if (!p.causal) return T;
   const int rmax = min(qt * gt + gt - 1, p.rep * p.nq - 1);
   return T - p.nq + rmax / p.rep + 1;
+}
+
+// CTA that owns global tile x when W tiles are split evenly over G CTAs
+__device__ __forceinline__ int cta_of(long long x, long long W, int G) {
+  return static_cast<int>(((x + 1) * G - 1) / W);
 }
 
 // group G's bf16 from a packed row of 4 bf16 (uint2)
@@ -90,12 +122,12 @@ __device__ __forceinline__ void unpack_k4(uint32_t w, uint32_t* r) {
   r[3] = fma_f16x2(and_or(w8, 0x00F000F0u, MAGIC), SIXTEENTH, NEG64);
 }
 
-// 3-bit code at bit `L` (0..7) of each 16-bit half of x -> fp16x2 codes
+// 3-bit code at bit `L` (0..7) of each 16-bit half of x -> fp16x2 (code - 4)
 template <int L>
 __device__ __forceinline__ uint32_t dq3(uint32_t x) {
   constexpr uint32_t mask = 0x00070007u << L;
-  constexpr uint32_t sc = (15u - L) << 10;                 // 2^-L
-  constexpr uint32_t ng = 0x8000u | ((25u - L) << 10);     // -2^(10-L)
+  constexpr uint32_t sc = (15u - L) << 10;                          // 2^-L
+  constexpr uint32_t ng = 0x8000u | ((25u - L) << 10) | (4u << L);  // -(2^(10-L) + 4)
   return fma_f16x2(and_or(x, mask, 0x64006400u), sc | (sc << 16), ng | (ng << 16));
 }
 
@@ -117,7 +149,7 @@ __device__ __forceinline__ void unpack_v3_pair(uint32_t fa, uint32_t fb, uint32_
 
 template <int NT, int DS, int STREAMS>
 struct Cfg {
-  static constexpr int GT = 8 * NT;            // query rows per CTA
+  static constexpr int GT = 8 * NT;            // query rows per unit
   static constexpr int GPW = 4 / DS;           // 64-dim groups per consumer warp
   static constexpr int CW = DS * STREAMS;      // consumer warps
   static constexpr int THREADS = (CW + 1) * 32;
@@ -127,10 +159,12 @@ struct Cfg {
   static constexpr int OFF_LBUF = OFF_MBUF + STREAMS * GT * 4;
   static constexpr int OFF_XBUF = OFF_LBUF + STREAMS * GT * 4;
   static constexpr int XBUF_BYTES = DS > 1 ? STREAMS * 2 * DS * NT * 32 * 16 : 0;
-  static constexpr int OFF_BAR = OFF_XBUF + XBUF_BYTES;
-  static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + 1024;  // + alignment slack
-  static_assert(STREAMS * GT * 256 * 4 <= NSTAGE * STAGE, "stream merge buffer must fit the ring");
-  static_assert(OFF_XBUF % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+  static constexpr int OFF_OBUF = OFF_XBUF + XBUF_BYTES;
+  static constexpr int OBUF_BYTES = STREAMS > 1 ? STREAMS * GT * 256 * 4 : 0;
+  static constexpr int OFF_BAR = OFF_OBUF + OBUF_BYTES;
+  static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8;
+  static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
+  static_assert(OFF_XBUF % 16 == 0 && OFF_OBUF % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
   static_assert(4 % STREAMS == 0 && 4 % DS == 0, "shape");
 };
 
@@ -146,18 +180,26 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
   float* mbuf = reinterpret_cast<float*>(smem + C::OFF_MBUF);
   float* lbuf = reinterpret_cast<float*>(smem + C::OFF_LBUF);
   float4* xbuf = reinterpret_cast<float4*>(smem + C::OFF_XBUF);
+  float* obuf = reinterpret_cast<float*>(smem + C::OFF_OBUF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + NSTAGE;
+  int* s_flag = reinterpret_cast<int*>(smem + C::OFF_FLAG);
 
-  const int chunk = blockIdx.x, b = blockIdx.z;
-  const int kvh = blockIdx.y / p.nqt, qt = blockIdx.y % p.nqt;
-  const int T = p.lens[b];
-  const int limit = tile_limit(p, T, qt, GT);
-  const int chunk_tok = p.chunk_tiles * TILE;
-  const int t_lo = chunk * chunk_tok;
-  if (t_lo >= limit) return;  // past this sequence's last chunk: the combine never reads it
-  const int t_hi = min(limit, t_lo + chunk_tok);
-  const int ntiles = (t_hi - t_lo + TILE - 1) / TILE;
+  // ---- this CTA's even share of the launch's tiles
+  const int G = p.grid;
+  const long long W = p.prefix[p.num_units];
+  const int k_cta = blockIdx.x;
+  const long long g0 = W * k_cta / G, g1 = W * (k_cta + 1) / G;
+  if (g0 >= g1) return;
+  int u0 = 0;  // unit holding tile g0: last u with prefix[u] <= g0
+  {
+    int lo = 0, hi = p.num_units - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.prefix[mid] <= g0) lo = mid; else hi = mid - 1;
+    }
+    u0 = lo;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -169,21 +211,24 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
   }
   __syncthreads();
 
-  const long long rowbase = (static_cast<long long>(b) * p.kv_heads + kvh) * p.cap;
-
   // ------------------------------------------------------------ producer
   if (warp == CW) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int k = 0;
-      for (; k < ntiles; ++k) {
-        const int st = k % NSTAGE;
-        if (k >= NSTAGE && !mbar_wait(&empty[st], ((k / NSTAGE) - 1) & 1)) {
+      int u = u0;
+      long long k = 0;
+      for (long long gt = g0; gt < g1; ++gt, ++k) {
+        while (gt >= p.prefix[u + 1]) ++u;
+        const int ug = p.unit_base + u;
+        const int b = ug / (p.kv_heads * p.nqt), kvh = (ug / p.nqt) % p.kv_heads;
+        const int st = static_cast<int>(k % NSTAGE);
+        if (k >= NSTAGE && !mbar_wait(&empty[st], static_cast<uint32_t>((k / NSTAGE) - 1) & 1)) {
           atomicOr(p.status, 1u);
           break;
         }
         uint8_t* sb = smem + st * STAGE;
-        const long long row0 = rowbase + t_lo + static_cast<long long>(k) * TILE;
+        const long long row0 = (static_cast<long long>(b) * p.kv_heads + kvh) * p.cap +
+                               (gt - p.prefix[u]) * TILE;
         mbar_arrive_expect_tx(&full[st], STAGE_TX);
         tensor2d_g2s(sb + OFF_K, &kmap, 0, static_cast<int>(row0), &full[st], pol);
         bulk_g2s(sb + OFF_V, p.v_codes + row0 * kVWords, 6144, &full[st], pol);
@@ -193,9 +238,9 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
         bulk_g2s(sb + OFF_VB, p.v_biases + row0 * kGroups, 512, &full[st], pol);
       }
       // never leave with copies in flight: wait for the last tile issued to each stage
-      for (int s = 0; s < NSTAGE && s < k; ++s) {
-        const int last = s + NSTAGE * ((k - 1 - s) / NSTAGE);
-        mbar_wait(&full[s], (last / NSTAGE) & 1);
+      for (long long s = 0; s < NSTAGE && s < k; ++s) {
+        const long long last = s + NSTAGE * ((k - 1 - s) / NSTAGE);
+        mbar_wait(&full[s], static_cast<uint32_t>(last / NSTAGE) & 1);
       }
     }
     return;
@@ -204,187 +249,197 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
   // ------------------------------------------------------------ consumers
   const int cw = warp, stream = cw / DS, dg = cw % DS;
   const int g = lane >> 2, t = lane & 3;
-
-  // q' = bf16(q @ M_b), q'' = bf16(q' * scale); rows r <-> (query R/rep, head R%rep)
-  for (int idx = threadIdx.x; idx < GT * 64; idx += NCT) {
-    const int r = idx >> 6, blk = idx & 63;
-    const int R = qt * GT + r, i = R / p.rep, hr = R % p.rep;
-    uint32_t o01 = 0, o23 = 0;
-    if (i < p.nq) {
-      const long long qrow =
-          (static_cast<long long>(b) * p.kv_heads * p.rep + kvh * p.rep + hr) * p.nq + i;
-      const uint2 raw = *reinterpret_cast<const uint2*>(p.q + qrow * kHeadDim + blk * 4);
-      const float x[4] = {bf16_to_f32(raw.x & 0xFFFFu), bf16_to_f32(raw.x >> 16),
-                          bf16_to_f32(raw.y & 0xFFFFu), bf16_to_f32(raw.y >> 16)};
-      const uint4* r4 = reinterpret_cast<const uint4*>(p.rot + blk * 16);
-      const uint4 m01 = __ldg(r4), m23 = __ldg(r4 + 1);
-      const uint32_t mw[8] = {m01.x, m01.y, m01.z, m01.w, m23.x, m23.y, m23.z, m23.w};
-      uint32_t yb[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int e = k * 4 + j;
-          const float mkj = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
-          acc = k == 0 ? __fmul_rn(x[0], mkj) : __fadd_rn(acc, __fmul_rn(x[k], mkj));
-        }
-        yb[j] = f32_to_bf16_bits(__fmul_rn(round_bf16(acc), p.scale));
-      }
-      o01 = yb[0] | (yb[1] << 16);
-      o23 = yb[2] | (yb[3] << 16);
-    }
-    *reinterpret_cast<uint2*>(qs + r * kHeadDim + blk * 4) = make_uint2(o01, o23);
-  }
-  named_bar(1, NCT);
-  for (int r = cw; r < GT; r += CW) {
-    const uint4 v = *reinterpret_cast<const uint4*>(qs + r * kHeadDim + lane * 8);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float s = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s += bf16_to_f32(w[e] & 0xFFFFu) + bf16_to_f32(w[e] >> 16);
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if ((lane & 7) == 0) qsum[r * 4 + (lane >> 3)] = s;
-  }
-  named_bar(1, NCT);
-
-  // q'' as fp16 B fragments.  Thread t covers dims 64G+16t .. +15 of group G;
-  // register pair m of its unpacked codes holds dims (m, m+4) for m < 4 and
-  // (m+4, m+8) for m >= 4; k-step s uses pairs 2s (slots 2t,2t+1) and 2s+1.
-  uint32_t qb[GPW][4][NT][2];
-  float qsr[GPW][NT][2];
-#pragma unroll
-  for (int gi = 0; gi < GPW; ++gi) {
-    const int G = dg * GPW + gi;
-    const int base = 64 * G + 16 * t;
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const uint16_t* qrow = qs + (8 * j + g) * kHeadDim + base;
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int m = 2 * s + h;
-          const int lo = m < 4 ? m : m + 4;
-          qb[gi][s][j][h] = pack_f16x2(bf16_to_f32(qrow[lo]), bf16_to_f32(qrow[lo + 4]));
-        }
-      qsr[gi][j][0] = qsum[(8 * j + 2 * t) * 4 + G];
-      qsr[gi][j][1] = qsum[(8 * j + 2 * t + 1) * 4 + G];
-    }
-  }
-  int qpos[NT][2];
-#pragma unroll
-  for (int j = 0; j < NT; ++j)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int R = qt * GT + 8 * j + 2 * t + e;
-      const int i = min(R / p.rep, p.nq - 1);
-      qpos[j][e] = p.causal ? T - p.nq + i : T - 1;
-    }
-
-  float O[GPW][4][NT][4];
-  float bacc[GPW][NT][2];
-  float mrow[NT][2], lrow[NT][2];
-#pragma unroll
-  for (int gi = 0; gi < GPW; ++gi)
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      bacc[gi][j][0] = bacc[gi][j][1] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) O[gi][i][j][0] = O[gi][i][j][1] = O[gi][i][j][2] = O[gi][i][j][3] = 0.f;
-    }
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    mrow[j][0] = mrow[j][1] = NEG_INF;
-    lrow[j][0] = lrow[j][1] = 0.f;
-  }
-
-  const int rS0 = (MU_PACK >> (4 * g)) & 15;  // token slot g
-  const int rS1 = rS0 + 8;                    // token slot g+8
-  const int rV0 = (MU_PACK >> (8 * t)) & 15;  // slot 2t
+  const int rS0 = (MU_PACK >> (4 * g)) & 15;      // token slot g
+  const int rV0 = (MU_PACK >> (8 * t)) & 15;      // slot 2t
   const int rV1 = (MU_PACK >> (8 * t + 4)) & 15;  // slot 2t+1
   const int vword = (3 * g) >> 2, vshift = (24 * g) & 31;
+  const uint32_t kswz = ((t & 1) << 3);
+
+  // per-unit state
+  int b = 0, kvh = 0, qt = 0, T = 0, limit = 0, qmin = 0;
+  int qpos[NT][2];
+  uint32_t qb[GPW][4][NT][2];
+  float qsr[GPW][NT][2];
+  float O[GPW][4][NT][4];
+  float bacc[GPW][NT][2];
+  float msc[NT][2], lrow[NT][2];  // reference max (log2 units), partial row sum
   int xpar = 0;
 
-  for (int k = 0; k < ntiles; ++k) {
-    const int st = k % NSTAGE;
-    if (!mbar_wait(&full[st], (k / NSTAGE) & 1)) {
-      atomicOr(p.status, 2u);
-      break;
+  // ---- start unit u: rotate and scale its queries, load the MMA fragments, reset the state
+  auto begin_unit = [&](int u) {
+    const int ug = p.unit_base + u;
+    b = ug / (p.kv_heads * p.nqt);
+    kvh = (ug / p.nqt) % p.kv_heads;
+    qt = ug % p.nqt;
+    T = p.lens[b];
+    limit = tile_limit(p, T, qt, GT);
+    qmin = p.causal ? T - p.nq + (qt * GT) / p.rep : T - 1;
+    named_bar(1, NCT);  // every consumer is done with the previous unit's qs / qsum
+    // q' = bf16(q @ M_b), q'' = bf16(q' * scale); rows r <-> (query R/rep, head R%rep)
+    for (int idx = threadIdx.x; idx < GT * 64; idx += NCT) {
+      const int r = idx >> 6, blk = idx & 63;
+      const int R = qt * GT + r, i = R / p.rep, hr = R % p.rep;
+      uint32_t o01 = 0, o23 = 0;
+      if (i < p.nq) {
+        const long long qrow =
+            (static_cast<long long>(b) * p.kv_heads * p.rep + kvh * p.rep + hr) * p.nq + i;
+        const uint2 raw = *reinterpret_cast<const uint2*>(p.q + qrow * kHeadDim + blk * 4);
+        const float x[4] = {bf16_to_f32(raw.x & 0xFFFFu), bf16_to_f32(raw.x >> 16),
+                            bf16_to_f32(raw.y & 0xFFFFu), bf16_to_f32(raw.y >> 16)};
+        const uint4* r4 = reinterpret_cast<const uint4*>(p.rot + blk * 16);
+        const uint4 m01 = __ldg(r4), m23 = __ldg(r4 + 1);
+        const uint32_t mw[8] = {m01.x, m01.y, m01.z, m01.w, m23.x, m23.y, m23.z, m23.w};
+        uint32_t yb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float acc = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int e = k * 4 + j;
+            const float mkj = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
+            acc = k == 0 ? __fmul_rn(x[0], mkj) : __fadd_rn(acc, __fmul_rn(x[k], mkj));
+          }
+          yb[j] = f32_to_bf16_bits(__fmul_rn(round_bf16(acc), p.scale));
+        }
+        o01 = yb[0] | (yb[1] << 16);
+        o23 = yb[2] | (yb[3] << 16);
+      }
+      *reinterpret_cast<uint2*>(qs + r * kHeadDim + blk * 4) = make_uint2(o01, o23);
     }
-    const uint32_t sb = smem_u32(smem + st * STAGE);
-    const int tile_tok = t_lo + k * TILE;
-    for (int sub = stream; sub < 4; sub += STREAMS) {
-      const int tokbase = tile_tok + sub * 16;
-      if (tokbase >= t_hi) break;
-      const int rr0 = sub * 16 + rS0, rr1 = sub * 16 + rS1;
-      const uint2 ksc0 = lds64(sb + OFF_KS + rr0 * 8), ksc1 = lds64(sb + OFF_KS + rr1 * 8);
-      const uint2 kbi0 = lds64(sb + OFF_KB + rr0 * 8), kbi1 = lds64(sb + OFF_KB + rr1 * 8);
+    named_bar(1, NCT);
+    for (int r = cw; r < GT; r += CW) {
+      const uint4 v = *reinterpret_cast<const uint4*>(qs + r * kHeadDim + lane * 8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s += bf16_to_f32(w[e] & 0xFFFFu) + bf16_to_f32(w[e] >> 16);
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if ((lane & 7) == 0) qsum[r * 4 + (lane >> 3)] = s;
+    }
+    named_bar(1, NCT);
+    // q'' as fp16 B fragments.  Thread t covers dims 64G+16t .. +15 of group G;
+    // register pair m of its unpacked codes holds dims (m, m+4) for m < 4 and
+    // (m+4, m+8) for m >= 4; k-step s uses pairs 2s (slots 2t,2t+1) and 2s+1.
+#pragma unroll
+    for (int gi = 0; gi < GPW; ++gi) {
+      const int Gr = dg * GPW + gi;
+      const int base = 64 * Gr + 16 * t;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const uint16_t* qrow = qs + (8 * j + g) * kHeadDim + base;
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int m = 2 * s + h;
+            const int lo = m < 4 ? m : m + 4;
+            qb[gi][s][j][h] = pack_f16x2(bf16_to_f32(qrow[lo]), bf16_to_f32(qrow[lo + 4]));
+          }
+        qsr[gi][j][0] = qsum[(8 * j + 2 * t) * 4 + Gr];
+        qsr[gi][j][1] = qsum[(8 * j + 2 * t + 1) * 4 + Gr];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int R = qt * GT + 8 * j + 2 * t + e;
+        const int i = min(R / p.rep, p.nq - 1);
+        qpos[j][e] = p.causal ? T - p.nq + i : T - 1;
+      }
+#pragma unroll
+    for (int gi = 0; gi < GPW; ++gi)
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        bacc[gi][j][0] = bacc[gi][j][1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) O[gi][i][j][0] = O[gi][i][j][1] = O[gi][i][j][2] = O[gi][i][j][3] = 0.f;
+      }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      msc[j][0] = msc[j][1] = NEG_INF;
+      lrow[j][0] = lrow[j][1] = 0.f;
+    }
+  };
 
-      // ---- scores: per group, S_G = codes . q'' (fp32), folded with scale/bias
-      float sc[NT][4];
+  // ---- one 16-token sub-tile.  FULL: every token is inside the unit's range
+  // and visible to every row (no masking work at all).
+  auto subtile = [&](auto full_tag, int sub, int tokbase, uint32_t sb) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    const int rr0 = sub * 16 + rS0, rr1 = rr0 + 8;
+    const uint2 ksc0 = lds64(sb + OFF_KS + rr0 * 8), ksc1 = lds64(sb + OFF_KS + rr1 * 8);
+    const uint2 kbi0 = lds64(sb + OFF_KB + rr0 * 8), kbi1 = lds64(sb + OFF_KB + rr1 * 8);
+
+    // scores: per group, S_G = codes . q'' (fp32), folded with scale/bias
+    float sc[NT][4];
 #pragma unroll
-      for (int gi = 0; gi < GPW; ++gi) {
-        const int G = dg * GPW + gi;
-        const uint32_t chunk16 = 2 * G + (t >> 1);
-        const uint32_t a0 = sb + OFF_K + rr0 * 128 + ((chunk16 ^ (rr0 & 7)) << 4) + ((t & 1) << 3);
-        const uint32_t a1 = sb + OFF_K + rr1 * 128 + ((chunk16 ^ (rr1 & 7)) << 4) + ((t & 1) << 3);
-        const uint2 w0 = lds64(a0), w1 = lds64(a1);
-        uint32_t RA[8], RB[8];
-        unpack_k4(w0.x, RA);
-        unpack_k4(w0.y, RA + 4);
-        unpack_k4(w1.x, RB);
-        unpack_k4(w1.y, RB + 4);
-        float acc[NT][4];
+    for (int gi = 0; gi < GPW; ++gi) {
+      const int Gr = dg * GPW + gi;
+      const uint32_t chunk16 = 2 * Gr + (t >> 1);
+      const uint32_t a0 = sb + OFF_K + rr0 * 128 + ((chunk16 ^ (rr0 & 7)) << 4) + kswz;
+      const uint32_t a1 = sb + OFF_K + rr1 * 128 + ((chunk16 ^ (rr1 & 7)) << 4) + kswz;
+      const uint2 w0 = lds64(a0), w1 = lds64(a1);
+      uint32_t RA[8], RB[8];
+      unpack_k4(w0.x, RA);
+      unpack_k4(w0.y, RA + 4);
+      unpack_k4(w1.x, RB);
+      unpack_k4(w1.y, RB + 4);
+      float acc[NT][4];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+      for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const uint32_t A[4] = {RA[2 * s], RB[2 * s], RA[2 * s + 1], RB[2 * s + 1]};
+      for (int s = 0; s < 4; ++s) {
+        const uint32_t A[4] = {RA[2 * s], RB[2 * s], RA[2 * s + 1], RB[2 * s + 1]};
 #pragma unroll
-          for (int j = 0; j < NT; ++j) mma_f16(acc[j], A, qb[gi][s][j][0], qb[gi][s][j][1]);
-        }
-        const float s0 = pick_bf16(ksc0, G), s1 = pick_bf16(ksc1, G);
-        const float b0 = pick_bf16(kbi0, G), b1 = pick_bf16(kbi1, G);
+        for (int j = 0; j < NT; ++j) mma_f16(acc[j], A, qb[gi][s][j][0], qb[gi][s][j][1]);
+      }
+      const float s0 = pick_bf16(ksc0, Gr), s1 = pick_bf16(ksc1, Gr);
+      const float b0 = pick_bf16(kbi0, Gr), b1 = pick_bf16(kbi1, Gr);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const float t0 = fmaf(s0, acc[j][0], b0 * qsr[gi][j][0]);
-          const float t1 = fmaf(s0, acc[j][1], b0 * qsr[gi][j][1]);
-          const float t2 = fmaf(s1, acc[j][2], b1 * qsr[gi][j][0]);
-          const float t3 = fmaf(s1, acc[j][3], b1 * qsr[gi][j][1]);
+      for (int j = 0; j < NT; ++j) {
+        if constexpr (DS == 1) {
           if (gi == 0) {
-            sc[j][0] = t0; sc[j][1] = t1; sc[j][2] = t2; sc[j][3] = t3;
+            sc[j][0] = s0 * acc[j][0]; sc[j][1] = s0 * acc[j][1];
+            sc[j][2] = s1 * acc[j][2]; sc[j][3] = s1 * acc[j][3];
           } else {
-            sc[j][0] += t0; sc[j][1] += t1; sc[j][2] += t2; sc[j][3] += t3;
+            sc[j][0] = fmaf(s0, acc[j][0], sc[j][0]); sc[j][1] = fmaf(s0, acc[j][1], sc[j][1]);
+            sc[j][2] = fmaf(s1, acc[j][2], sc[j][2]); sc[j][3] = fmaf(s1, acc[j][3], sc[j][3]);
           }
+          sc[j][0] = fmaf(b0, qsr[gi][j][0], sc[j][0]); sc[j][1] = fmaf(b0, qsr[gi][j][1], sc[j][1]);
+          sc[j][2] = fmaf(b1, qsr[gi][j][0], sc[j][2]); sc[j][3] = fmaf(b1, qsr[gi][j][1], sc[j][3]);
+        } else {
+          sc[j][0] = fmaf(s0, acc[j][0], b0 * qsr[gi][j][0]);
+          sc[j][1] = fmaf(s0, acc[j][1], b0 * qsr[gi][j][1]);
+          sc[j][2] = fmaf(s1, acc[j][2], b1 * qsr[gi][j][0]);
+          sc[j][3] = fmaf(s1, acc[j][3], b1 * qsr[gi][j][1]);
         }
       }
-      if constexpr (DS > 1) {  // sum the group partials of the DS warps, in group order
-        float4* xb = xbuf + (stream * 2 + xpar) * DS * NT * 32;
+    }
+    if constexpr (DS > 1) {  // sum the group partials of the DS warps, in group order
+      float4* xb = xbuf + (stream * 2 + xpar) * DS * NT * 32;
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
-          xb[(dg * NT + j) * 32 + lane] = make_float4(sc[j][0], sc[j][1], sc[j][2], sc[j][3]);
-        named_bar(2 + stream, DS * 32);
+      for (int j = 0; j < NT; ++j)
+        xb[(dg * NT + j) * 32 + lane] = make_float4(sc[j][0], sc[j][1], sc[j][2], sc[j][3]);
+      named_bar(2 + stream, DS * 32);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          float4 a = xb[j * 32 + lane];
+      for (int j = 0; j < NT; ++j) {
+        float4 a = xb[j * 32 + lane];
 #pragma unroll
-          for (int d = 1; d < DS; ++d) {
-            const float4 v = xb[(d * NT + j) * 32 + lane];
-            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-          }
-          sc[j][0] = a.x; sc[j][1] = a.y; sc[j][2] = a.z; sc[j][3] = a.w;
+        for (int d = 1; d < DS; ++d) {
+          const float4 v = xb[(d * NT + j) * 32 + lane];
+          a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
         }
-        xpar ^= 1;
+        sc[j][0] = a.x; sc[j][1] = a.y; sc[j][2] = a.z; sc[j][3] = a.w;
       }
+      xpar ^= 1;
+    }
 
-      // ---- mask (ragged tail, causal) and online softmax
-      const int tok0 = tokbase + rS0, tok1 = tokbase + rS1;
-      const bool in0 = tok0 < t_hi, in1 = tok1 < t_hi;
-      bool valid[NT][4];
-      float alpha[NT][2], msc[NT][2];
-      bool rescale = false;
+    // mask (ragged tail, causal): only on sub-tiles that need it
+    bool valid[NT][4];
+    if constexpr (!FULL) {
+      const int tok0 = tokbase + rS0, tok1 = tok0 + 8;
+      const bool in0 = tok0 < limit, in1 = tok1 < limit;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         valid[j][0] = in0 && tok0 <= qpos[j][0];
@@ -393,290 +448,347 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
         valid[j][3] = in1 && tok1 <= qpos[j][1];
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[j][e] = valid[j][e] ? sc[j][e] : NEG_INF;
+      }
+    }
+
+    // online softmax with a lazily moving reference max
+    float x[NT][4];
+    bool trig = false;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[j][e] = fmaf(sc[j][e], LOG2E, -msc[j][e & 1]);
+        trig |= !(x[j][e] <= TAU);
+      }
+    if (__any_sync(0xffffffffu, trig)) {
+      float alpha[NT][2];
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           float mx = fmaxf(sc[j][e], sc[j][e + 2]);
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mnew = fmaxf(mrow[j][e], mx);
-          alpha[j][e] = mnew == NEG_INF ? 1.f : ex2_approx((mrow[j][e] - mnew) * LOG2E);
-          rescale |= mnew != mrow[j][e];
-          mrow[j][e] = mnew;
-          msc[j][e] = mnew == NEG_INF ? 0.f : mnew * LOG2E;
+          const float mnew = fmaxf(msc[j][e], mx * LOG2E);
+          alpha[j][e] = mnew == NEG_INF ? 1.f : ex2_approx(msc[j][e] - mnew);
+          msc[j][e] = mnew;
         }
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          lrow[j][0] *= alpha[j][0];
-          lrow[j][1] *= alpha[j][1];
-#pragma unroll
-          for (int gi = 0; gi < GPW; ++gi) {
-            bacc[gi][j][0] *= alpha[j][0];
-            bacc[gi][j][1] *= alpha[j][1];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              O[gi][i][j][0] *= alpha[j][0];
-              O[gi][i][j][2] *= alpha[j][0];
-              O[gi][i][j][1] *= alpha[j][1];
-              O[gi][i][j][3] *= alpha[j][1];
-            }
-          }
-        }
-      }
-      float pr[NT][4];
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
+        lrow[j][0] *= alpha[j][0];
+        lrow[j][1] *= alpha[j][1];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pr[j][e] = ex2_approx(fmaf(sc[j][e], LOG2E, -msc[j][e & 1]));
-        lrow[j][0] += pr[j][0] + pr[j][2];
-        lrow[j][1] += pr[j][1] + pr[j][3];
+        for (int gi = 0; gi < GPW; ++gi) {
+          bacc[gi][j][0] *= alpha[j][0];
+          bacc[gi][j][1] *= alpha[j][1];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            O[gi][i][j][0] *= alpha[j][0];
+            O[gi][i][j][2] *= alpha[j][0];
+            O[gi][i][j][1] *= alpha[j][1];
+            O[gi][i][j][3] *= alpha[j][1];
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float m = msc[j][e & 1];
+          x[j][e] = fmaf(sc[j][e], LOG2E, m == NEG_INF ? 0.f : -m);
+        }
       }
+    }
+    float pr[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pr[j][e] = ex2_approx(x[j][e]);
+      lrow[j][0] += pr[j][0] + pr[j][2];
+      lrow[j][1] += pr[j][1] + pr[j][3];
+    }
 
-      // ---- values: O^T += V_codes^T . (P * s_v), bias term on CUDA cores
-      const uint2 vsc0 = lds64(sb + OFF_VS + rr0 * 8), vsc1 = lds64(sb + OFF_VS + rr1 * 8);
-      const uint2 vbi0 = lds64(sb + OFF_VB + rr0 * 8), vbi1 = lds64(sb + OFF_VB + rr1 * 8);
-      const uint32_t vrow0 = sb + OFF_V + (sub * 16 + rV0) * 96;
-      const uint32_t vrow1 = sb + OFF_V + (sub * 16 + rV1) * 96;
-      const uint32_t vrow2 = vrow0 + 8 * 96;
-      const uint32_t vrow3 = vrow1 + 8 * 96;
+    // values: O^T += (V_codes - 4)^T . (P * s_v); bias term on CUDA cores
+    const uint2 vsc0 = lds64(sb + OFF_VS + rr0 * 8), vsc1 = lds64(sb + OFF_VS + rr1 * 8);
+    const uint2 vbi0 = lds64(sb + OFF_VB + rr0 * 8), vbi1 = lds64(sb + OFF_VB + rr1 * 8);
+    const uint32_t vrow0 = sb + OFF_V + (sub * 16 + rV0) * 96;
+    const uint32_t vrow1 = sb + OFF_V + (sub * 16 + rV1) * 96;
+    const uint32_t vrow2 = vrow0 + 8 * 96;
+    const uint32_t vrow3 = vrow1 + 8 * 96;
 #pragma unroll
-      for (int gi = 0; gi < GPW; ++gi) {
-        const int G = dg * GPW + gi;
-        const float vs0 = pick_bf16(vsc0, G), vs1 = pick_bf16(vsc1, G);
-        const float vb0 = pick_bf16(vbi0, G), vb1 = pick_bf16(vbi1, G);
-        uint32_t bp[NT][2];
+    for (int gi = 0; gi < GPW; ++gi) {
+      const int Gr = dg * GPW + gi;
+      const float vs0 = pick_bf16(vsc0, Gr), vs1 = pick_bf16(vsc1, Gr);
+      const float vb0 = fmaf(VCENTRE, vs0, pick_bf16(vbi0, Gr));
+      const float vb1 = fmaf(VCENTRE, vs1, pick_bf16(vbi1, Gr));
+      uint32_t bp[NT][2];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const float q0 = valid[j][0] ? pr[j][0] * vs0 : 0.f;
-          const float q1 = valid[j][1] ? pr[j][1] * vs0 : 0.f;
-          const float q2 = valid[j][2] ? pr[j][2] * vs1 : 0.f;
-          const float q3 = valid[j][3] ? pr[j][3] * vs1 : 0.f;
-          bp[j][0] = movmatrix_trans(pack_f16x2(q0, q1));
-          bp[j][1] = movmatrix_trans(pack_f16x2(q2, q3));
+      for (int j = 0; j < NT; ++j) {
+        float q0 = pr[j][0] * vs0, q1 = pr[j][1] * vs0, q2 = pr[j][2] * vs1, q3 = pr[j][3] * vs1;
+        if constexpr (FULL) {
+          bacc[gi][j][0] = fmaf(pr[j][0], vb0, fmaf(pr[j][2], vb1, bacc[gi][j][0]));
+          bacc[gi][j][1] = fmaf(pr[j][1], vb0, fmaf(pr[j][3], vb1, bacc[gi][j][1]));
+        } else {  // masked tokens may hold stale (even NaN) scales: select, never multiply
+          q0 = valid[j][0] ? q0 : 0.f;
+          q1 = valid[j][1] ? q1 : 0.f;
+          q2 = valid[j][2] ? q2 : 0.f;
+          q3 = valid[j][3] ? q3 : 0.f;
           bacc[gi][j][0] += (valid[j][0] ? pr[j][0] * vb0 : 0.f) + (valid[j][2] ? pr[j][2] * vb1 : 0.f);
           bacc[gi][j][1] += (valid[j][1] ? pr[j][1] * vb0 : 0.f) + (valid[j][3] ? pr[j][3] * vb1 : 0.f);
         }
-        const uint32_t wofs = (6 * G + vword) * 4;
-        const uint32_t f0 = __funnelshift_r(lds32(vrow0 + wofs), lds32(vrow0 + wofs + 4), vshift);
-        const uint32_t f1 = __funnelshift_r(lds32(vrow1 + wofs), lds32(vrow1 + wofs + 4), vshift);
-        const uint32_t f2 = __funnelshift_r(lds32(vrow2 + wofs), lds32(vrow2 + wofs + 4), vshift);
-        const uint32_t f3 = __funnelshift_r(lds32(vrow3 + wofs), lds32(vrow3 + wofs + 4), vshift);
-        uint32_t h01[8], h23[8];
-        unpack_v3_pair(f0, f1, h01);
-        unpack_v3_pair(f2, f3, h23);
+        bp[j][0] = movmatrix_trans(pack_f16x2(q0, q1));
+        bp[j][1] = movmatrix_trans(pack_f16x2(q2, q3));
+      }
+      const uint32_t wofs = (6 * Gr + vword) * 4;
+      const uint32_t f0 = __funnelshift_r(lds32(vrow0 + wofs), lds32(vrow0 + wofs + 4), vshift);
+      const uint32_t f1 = __funnelshift_r(lds32(vrow1 + wofs), lds32(vrow1 + wofs + 4), vshift);
+      const uint32_t f2 = __funnelshift_r(lds32(vrow2 + wofs), lds32(vrow2 + wofs + 4), vshift);
+      const uint32_t f3 = __funnelshift_r(lds32(vrow3 + wofs), lds32(vrow3 + wofs + 4), vshift);
+      uint32_t h01[8], h23[8];
+      unpack_v3_pair(f0, f1, h01);
+      unpack_v3_pair(f2, f3, h23);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t A[4] = {h01[2 * i], h01[2 * i + 1], h23[2 * i], h23[2 * i + 1]};
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t A[4] = {h01[2 * i], h01[2 * i + 1], h23[2 * i], h23[2 * i + 1]};
 #pragma unroll
-          for (int j = 0; j < NT; ++j) mma_f16(O[gi][i][j], A, bp[j][0], bp[j][1]);
-        }
+        for (int j = 0; j < NT; ++j) mma_f16(O[gi][i][j], A, bp[j][0], bp[j][1]);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-  }
+  };
 
-  // ------------------------------------------------------------ finish the chunk
-#pragma unroll
-  for (int j = 0; j < NT; ++j)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float l = lrow[j][e];
-      l += __shfl_xor_sync(0xffffffffu, l, 4);
-      l += __shfl_xor_sync(0xffffffffu, l, 8);
-      l += __shfl_xor_sync(0xffffffffu, l, 16);
-      lrow[j][e] = l;
-#pragma unroll
-      for (int gi = 0; gi < GPW; ++gi) {
-        float bs = bacc[gi][j][e];
-        bs += __shfl_xor_sync(0xffffffffu, bs, 4);
-        bs += __shfl_xor_sync(0xffffffffu, bs, 8);
-        bs += __shfl_xor_sync(0xffffffffu, bs, 16);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          O[gi][i][j][e] += bs;
-          O[gi][i][j][e + 2] += bs;
-        }
-      }
-    }
-
-  const long long pidx =
-      ((static_cast<long long>(b) * p.kv_heads + kvh) * p.nqt + qt) * p.maxc + chunk;
-  float* po = p.part_o + pidx * GT * kHeadDim;
-  float* pml = p.part_ml + pidx * GT * 2;
-
-  if constexpr (STREAMS == 1) {
-#pragma unroll
-    for (int gi = 0; gi < GPW; ++gi)
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = 8 * j + 2 * t + e;
-          float* dst = po + row * kHeadDim + 64 * (dg * GPW + gi) + 8 * g;
-          reinterpret_cast<float4*>(dst)[0] =
-              make_float4(O[gi][0][j][e], O[gi][0][j][e + 2], O[gi][1][j][e], O[gi][1][j][e + 2]);
-          reinterpret_cast<float4*>(dst)[1] =
-              make_float4(O[gi][2][j][e], O[gi][2][j][e + 2], O[gi][3][j][e], O[gi][3][j][e + 2]);
-        }
-    if (dg == 0 && g == 0)
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = 8 * j + 2 * t + e;
-          pml[row * 2] = mrow[j][e];
-          pml[row * 2 + 1] = lrow[j][e];
-        }
-  } else {
-    if (dg == 0 && g == 0)
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) mbuf[stream * GT + 8 * j + 2 * t + e] = mrow[j][e];
-    named_bar(1, NCT);  // also: every consumer is done with the ring
-    float* obuf = reinterpret_cast<float*>(smem);  // [STREAMS][GT][256], aliases the ring
+  // ---- finish unit u's segment: partial store; the unit's last segment combines
+  auto end_unit = [&](int u) {
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int row = 8 * j + 2 * t + e;
-        float M = mbuf[row];
-#pragma unroll
-        for (int s = 1; s < STREAMS; ++s) M = fmaxf(M, mbuf[s * GT + row]);
-        const float a = mrow[j][e] == NEG_INF ? 0.f : ex2_approx((mrow[j][e] - M) * LOG2E);
-        if (dg == 0 && g == 0) lbuf[stream * GT + row] = lrow[j][e] * a;
+        float l = lrow[j][e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        lrow[j][e] = l;
 #pragma unroll
         for (int gi = 0; gi < GPW; ++gi) {
-          float* dst = obuf + (stream * GT + row) * kHeadDim + 64 * (dg * GPW + gi) + 8 * g;
-          reinterpret_cast<float4*>(dst)[0] = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a,
-                                                          O[gi][1][j][e] * a, O[gi][1][j][e + 2] * a);
-          reinterpret_cast<float4*>(dst)[1] = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a,
-                                                          O[gi][3][j][e] * a, O[gi][3][j][e + 2] * a);
+          float bs = bacc[gi][j][e];
+          bs += __shfl_xor_sync(0xffffffffu, bs, 4);
+          bs += __shfl_xor_sync(0xffffffffu, bs, 8);
+          bs += __shfl_xor_sync(0xffffffffu, bs, 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            O[gi][i][j][e] += bs;
+            O[gi][i][j][e + 2] += bs;
+          }
         }
       }
+    const long long slot = static_cast<long long>(u) + k_cta;  // unique per (unit, CTA) segment
+    float* po = p.part_o + slot * GT * kHeadDim;
+    float* pml = p.part_ml + slot * GT * 2;
+    if constexpr (STREAMS == 1) {
+#pragma unroll
+      for (int gi = 0; gi < GPW; ++gi)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int row = 8 * j + 2 * t + e;
+            float* dst = po + row * kHeadDim + 64 * (dg * GPW + gi) + 8 * g;
+            reinterpret_cast<float4*>(dst)[0] =
+                make_float4(O[gi][0][j][e], O[gi][0][j][e + 2], O[gi][1][j][e], O[gi][1][j][e + 2]);
+            reinterpret_cast<float4*>(dst)[1] =
+                make_float4(O[gi][2][j][e], O[gi][2][j][e + 2], O[gi][3][j][e], O[gi][3][j][e + 2]);
+          }
+      if (dg == 0 && g == 0)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int row = 8 * j + 2 * t + e;
+            pml[row * 2] = msc[j][e];
+            pml[row * 2 + 1] = lrow[j][e];
+          }
+    } else {  // merge the token streams in shared memory first, in stream order
+      if (dg == 0 && g == 0)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) mbuf[stream * GT + 8 * j + 2 * t + e] = msc[j][e];
+      named_bar(1, NCT);
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = 8 * j + 2 * t + e;
+          float M = mbuf[row];
+#pragma unroll
+          for (int s = 1; s < STREAMS; ++s) M = fmaxf(M, mbuf[s * GT + row]);
+          const float a = msc[j][e] == NEG_INF ? 0.f : ex2_approx(msc[j][e] - M);
+          if (dg == 0 && g == 0) lbuf[stream * GT + row] = lrow[j][e] * a;
+#pragma unroll
+          for (int gi = 0; gi < GPW; ++gi) {
+            float* dst = obuf + (stream * GT + row) * kHeadDim + 64 * (dg * GPW + gi) + 8 * g;
+            reinterpret_cast<float4*>(dst)[0] = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a,
+                                                            O[gi][1][j][e] * a, O[gi][1][j][e + 2] * a);
+            reinterpret_cast<float4*>(dst)[1] = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a,
+                                                            O[gi][3][j][e] * a, O[gi][3][j][e + 2] * a);
+          }
+        }
+      named_bar(1, NCT);
+      for (int idx = threadIdx.x; idx < GT * 64; idx += NCT) {
+        const int r = idx >> 6, c4 = idx & 63;
+        float4 a = reinterpret_cast<const float4*>(obuf + r * kHeadDim)[c4];
+#pragma unroll
+        for (int s = 1; s < STREAMS; ++s) {
+          const float4 v = reinterpret_cast<const float4*>(obuf + (s * GT + r) * kHeadDim)[c4];
+          a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        }
+        reinterpret_cast<float4*>(po + r * kHeadDim)[c4] = a;
+      }
+      for (int r = threadIdx.x; r < GT; r += NCT) {
+        float M = mbuf[r], L = lbuf[r];
+#pragma unroll
+        for (int s = 1; s < STREAMS; ++s) {
+          M = fmaxf(M, mbuf[s * GT + r]);
+          L += lbuf[s * GT + r];
+        }
+        pml[r * 2] = M;
+        pml[r * 2 + 1] = L;
+      }
+    }
+
+    // segments of this unit: CTAs k_first .. k_last (partial slots u + k)
+    const long long ustart = p.prefix[u], uend = p.prefix[u + 1];
+    const int k_first = cta_of(ustart, W, G), k_last = cta_of(uend - 1, W, G);
+    const int nseg = k_last - k_first + 1;
+    __threadfence();
     named_bar(1, NCT);
-    for (int idx = threadIdx.x; idx < GT * 64; idx += NCT) {
-      const int r = idx >> 6, c4 = idx & 63;
-      float4 a = reinterpret_cast<const float4*>(obuf + r * kHeadDim)[c4];
+    if (threadIdx.x == 0)
+      *s_flag = atomicAdd(p.counters + p.unit_base + u, 1u) + 1 == static_cast<unsigned>(nseg);
+    named_bar(1, NCT);
+    if (!*s_flag) return;
+    __threadfence();
+
+    // combine: per row, the log-sum-exp weights of the segments
+    const long long slot0 = static_cast<long long>(u) + k_first;
+    for (int r = cw; r < GT; r += CW) {  // a warp per row: max, then normaliser
+      float M = NEG_INF;
+      for (int s = lane; s < nseg; s += 32) M = fmaxf(M, __ldcg(p.part_ml + ((slot0 + s) * GT + r) * 2));
 #pragma unroll
-      for (int s = 1; s < STREAMS; ++s) {
-        const float4 v = reinterpret_cast<const float4*>(obuf + (s * GT + r) * kHeadDim)[c4];
-        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float L = 0.f;
+      for (int s = lane; s < nseg; s += 32) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + (slot0 + s) * GT + r);
+        L = fmaf(ml.x == NEG_INF ? 0.f : ex2_approx(ml.x - M), ml.y, L);
       }
-      reinterpret_cast<float4*>(po + r * kHeadDim)[c4] = a;
-    }
-    for (int r = threadIdx.x; r < GT; r += NCT) {
-      float M = mbuf[r], L = lbuf[r];
 #pragma unroll
-      for (int s = 1; s < STREAMS; ++s) {
-        M = fmaxf(M, mbuf[s * GT + r]);
-        L += lbuf[s * GT + r];
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      if (lane == 0) {
+        mbuf[r] = M;
+        lbuf[r] = L;
       }
-      pml[r * 2] = M;
-      pml[r * 2 + 1] = L;
     }
-  }
-}
-
-// ------------------------------------------------------------------ combine
-
-struct CombineParams {
-  const float* part_o;
-  const float* part_ml;
-  const uint16_t* rot;
-  void* out;
-  unsigned* status;
-  int out_f32;
-  int batch, kv_heads, rep, nq, nqt, gt, chunk_tok, maxc, causal;
-  int lens[IQ_MAX_BATCH];
-};
-
-// One warp per output row (b, query head, query).  Lane l owns dims 8l..8l+7
-// (two rotation blocks).
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
-  const int lane = threadIdx.x & 31;
-  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int hq_total = p.kv_heads * p.rep;
-  const long long rows = static_cast<long long>(p.batch) * hq_total * p.nq;
-  if (w >= rows) return;
-  const int i = static_cast<int>(w % p.nq);
-  const int hq = static_cast<int>((w / p.nq) % hq_total);
-  const int b = static_cast<int>(w / (static_cast<long long>(p.nq) * hq_total));
-  const int kvh = hq / p.rep, hr = hq % p.rep;
-  const int R = i * p.rep + hr, qt = R / p.gt, r = R % p.gt;
-  const int T = p.lens[b];
-  int limit = T;
-  if (p.causal) limit = T - p.nq + min(qt * p.gt + p.gt - 1, p.rep * p.nq - 1) / p.rep + 1;
-  const int nch = (limit + p.chunk_tok - 1) / p.chunk_tok;
-  const long long pbase = ((static_cast<long long>(b) * p.kv_heads + kvh) * p.nqt + qt) * p.maxc;
-
-  float M = NEG_INF;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part_ml[((pbase + c) * p.gt + r) * 2]);
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float L = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const float* ml = p.part_ml + ((pbase + c) * p.gt + r) * 2;
-    const float m = ml[0];
-    const float wgt = m == NEG_INF ? 0.f : ex2_approx((m - M) * LOG2E);
-    L = fmaf(wgt, ml[1], L);
-    const float4* o = reinterpret_cast<const float4*>(p.part_o + ((pbase + c) * p.gt + r) * kHeadDim + 8 * lane);
-    const float4 o0 = o[0], o1 = o[1];
-    acc[0] = fmaf(wgt, o0.x, acc[0]); acc[1] = fmaf(wgt, o0.y, acc[1]);
-    acc[2] = fmaf(wgt, o0.z, acc[2]); acc[3] = fmaf(wgt, o0.w, acc[3]);
-    acc[4] = fmaf(wgt, o1.x, acc[4]); acc[5] = fmaf(wgt, o1.y, acc[5]);
-    acc[6] = fmaf(wgt, o1.z, acc[6]); acc[7] = fmaf(wgt, o1.w, acc[7]);
-  }
-  if (!(L > 0.f) && lane == 0) atomicOr(p.status, 4u);
-  float o[8];
-#pragma unroll
-  for (int d = 0; d < 8; ++d) o[d] = __fdiv_rn(acc[d], L);
-  // inverse rotation: out[4c+i] = sum_j o[4c+j] * M_b[c][i][j]
-  const uint4* r4 = reinterpret_cast<const uint4*>(p.rot) + lane * 4;
-  uint32_t mw[16];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = __ldg(r4 + q);
-    mw[4 * q] = v.x; mw[4 * q + 1] = v.y; mw[4 * q + 2] = v.z; mw[4 * q + 3] = v.w;
-  }
-  float y[8];
-#pragma unroll
-  for (int c = 0; c < 2; ++c)
-#pragma unroll
-    for (int ii = 0; ii < 4; ++ii) {
-      float s = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = c * 16 + ii * 4 + j;
-        const float m = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
-        s = j == 0 ? __fmul_rn(o[4 * c], m) : fmaf(o[4 * c + j], m, s);
+    named_bar(1, NCT);
+    for (int idx = threadIdx.x; idx < GT * 32; idx += NCT) {
+      const int r = idx >> 5, l8 = idx & 31;
+      const int R = qt * GT + r, i = R / p.rep, hr = R % p.rep;
+      if (i >= p.nq) continue;
+      const float M = mbuf[r], L = lbuf[r];
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int s = 0; s < nseg; ++s) {
+        const float m = __ldcg(p.part_ml + ((slot0 + s) * GT + r) * 2);
+        const float wgt = m == NEG_INF ? 0.f : ex2_approx(m - M);
+        const float4* o = reinterpret_cast<const float4*>(p.part_o + ((slot0 + s) * GT + r) * kHeadDim + 8 * l8);
+        const float4 o0 = __ldcg(o), o1 = __ldcg(o + 1);
+        acc[0] = fmaf(wgt, o0.x, acc[0]); acc[1] = fmaf(wgt, o0.y, acc[1]);
+        acc[2] = fmaf(wgt, o0.z, acc[2]); acc[3] = fmaf(wgt, o0.w, acc[3]);
+        acc[4] = fmaf(wgt, o1.x, acc[4]); acc[5] = fmaf(wgt, o1.y, acc[5]);
+        acc[6] = fmaf(wgt, o1.z, acc[6]); acc[7] = fmaf(wgt, o1.w, acc[7]);
       }
-      y[4 * c + ii] = s;
+      if (!(L > 0.f)) atomicOr(p.status, 4u);
+      float o[8];
+#pragma unroll
+      for (int d = 0; d < 8; ++d) o[d] = __fdiv_rn(acc[d], L);
+      // inverse rotation: out[4c+i] = sum_j o[4c+j] * M_b[c][i][j]
+      const uint4* r4 = reinterpret_cast<const uint4*>(p.rot) + l8 * 4;
+      uint32_t mw[16];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 v = __ldg(r4 + q4);
+        mw[4 * q4] = v.x; mw[4 * q4 + 1] = v.y; mw[4 * q4 + 2] = v.z; mw[4 * q4 + 3] = v.w;
+      }
+      float y[8];
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+          float sacc = 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int e = cb * 16 + ii * 4 + jj;
+            const float m = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
+            sacc = jj == 0 ? o[4 * cb] * m : fmaf(o[4 * cb + jj], m, sacc);
+          }
+          y[4 * cb + ii] = sacc;
+        }
+      const int hq = kvh * p.rep + hr;
+      const long long orow = (static_cast<long long>(b) * p.kv_heads * p.rep + hq) * p.nq + i;
+      if (p.out_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHeadDim + 8 * l8);
+        dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+        dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+      } else {
+        uint4 v;
+        v.x = f32_to_bf16_bits(y[0]) | (f32_to_bf16_bits(y[1]) << 16);
+        v.y = f32_to_bf16_bits(y[2]) | (f32_to_bf16_bits(y[3]) << 16);
+        v.z = f32_to_bf16_bits(y[4]) | (f32_to_bf16_bits(y[5]) << 16);
+        v.w = f32_to_bf16_bits(y[6]) | (f32_to_bf16_bits(y[7]) << 16);
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kHeadDim + 8 * l8) = v;
+      }
     }
-  const long long orow = (static_cast<long long>(b) * hq_total + hq) * p.nq + i;
-  if (p.out_f32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHeadDim + 8 * lane);
-    dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-    dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-  } else {
-    uint4 v;
-    v.x = f32_to_bf16_bits(y[0]) | (f32_to_bf16_bits(y[1]) << 16);
-    v.y = f32_to_bf16_bits(y[2]) | (f32_to_bf16_bits(y[3]) << 16);
-    v.z = f32_to_bf16_bits(y[4]) | (f32_to_bf16_bits(y[5]) << 16);
-    v.w = f32_to_bf16_bits(y[6]) | (f32_to_bf16_bits(y[7]) << 16);
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kHeadDim + 8 * lane) = v;
+    if (threadIdx.x == 0) p.counters[p.unit_base + u] = 0;  // ready for the next call
+  };
+
+  // ------------------------------------------------------------ main loop over this CTA's tiles
+  int u = u0;
+  begin_unit(u);
+  long long k = 0;
+  for (long long gt = g0; gt < g1; ++gt, ++k) {
+    if (gt >= p.prefix[u + 1]) {  // crossed into the next unit (units hold >= 1 tile)
+      end_unit(u);
+      ++u;
+      begin_unit(u);
+    }
+    const int st = static_cast<int>(k % NSTAGE);
+    if (!mbar_wait(&full[st], static_cast<uint32_t>(k / NSTAGE) & 1)) {
+      atomicOr(p.status, 2u);
+      break;
+    }
+    const uint32_t sb = smem_u32(smem + st * STAGE);
+    const int tile_tok = static_cast<int>(gt - p.prefix[u]) * TILE;
+    for (int sub = stream; sub < 4; sub += STREAMS) {
+      const int tokbase = tile_tok + sub * 16;
+      if (tokbase >= limit) break;
+      if (tokbase + 16 <= limit && tokbase + 15 <= qmin)
+        subtile(std::true_type{}, sub, tokbase, sb);
+      else
+        subtile(std::false_type{}, sub, tokbase, sb);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
   }
+  end_unit(u);
 }
 
 // ------------------------------------------------------------------ host plan
 
+constexpr int kMaxLaunches = 64;
+
 struct Plan {
-  int nt, gt, nqt, chunk_tiles, maxc;
-  size_t part_count, bytes;
+  int nt, gt, nqt, launches, grid[kMaxLaunches];
+  size_t units, slots, head_bytes, bytes;
 };
 
+// workspace: [status word, padded to 256 B][per-unit segment counters, padded
+// to 256 B][partial O: slots x GT x 256 f32][partial (max, sum): slots x GT x 2 f32]
 constexpr size_t kStatusBytes = 256;
 
 template <int NT, int DS, int STREAMS>
@@ -704,26 +816,50 @@ int blocks_per_sm() {
 #define IQ_DECODE_CFG 1, 1, 4
 #define IQ_MULTI_CFG 4, 4, 1
 
-int make_plan(const iq_cache* c, int q_heads, int nq, Plan* pl) {
+// Tiles of every unit, in unit order: unit u = (b, kv head, query tile).
+void unit_tiles(const iq_cache* c, int rep, int nq, int causal, int gt, int nqt, int* tiles) {
+  for (int b = 0; b < c->batch; ++b)
+    for (int h = 0; h < c->kv_heads; ++h)
+      for (int qt = 0; qt < nqt; ++qt) {
+        const int T = c->lens[b];
+        int limit = T;
+        if (causal) limit = T - nq + std::min(qt * gt + gt - 1, rep * nq - 1) / rep + 1;
+        tiles[(b * c->kv_heads + h) * nqt + qt] = (limit + TILE - 1) / TILE;
+      }
+}
+
+// tiles == nullptr: size an upper bound (every unit as long as the longest sequence)
+int make_plan(const iq_cache* c, int q_heads, int nq, int causal, Plan* pl, const int* tiles) {
   const int rep = q_heads / c->kv_heads;
   const int rows = rep * nq;
   pl->nt = rows <= 8 ? 1 : 4;
   pl->gt = 8 * pl->nt;
   pl->nqt = (rows + pl->gt - 1) / pl->gt;
-  int max_t = 0;
-  for (int b = 0; b < c->batch; ++b) max_t = c->lens[b] > max_t ? c->lens[b] : max_t;
-  const int tiles_max = (max_t + TILE - 1) / TILE;
+  pl->units = static_cast<size_t>(c->batch) * c->kv_heads * pl->nqt;
+  pl->launches = static_cast<int>((pl->units + UNIT_CAP - 1) / UNIT_CAP);
+  if (pl->launches > kMaxLaunches) return fail(IQ_ERR_UNSUPPORTED, "too many query tiles for one call");
   const int bps = pl->nt == 1 ? blocks_per_sm<IQ_DECODE_CFG>() : blocks_per_sm<IQ_MULTI_CFG>();
-  const long long slots = static_cast<long long>(num_sms()) * bps;
-  const long long units = static_cast<long long>(c->batch) * c->kv_heads * pl->nqt;
-  long long nch = (4 * slots + units - 1) / units;
-  if (nch < 1) nch = 1;
-  int ct = static_cast<int>((tiles_max + nch - 1) / nch);
-  if (ct < 4) ct = 4;
-  pl->chunk_tiles = ct;
-  pl->maxc = (tiles_max + ct - 1) / ct;
-  pl->part_count = static_cast<size_t>(units) * pl->maxc;
-  pl->bytes = kStatusBytes + pl->part_count * pl->gt * (kHeadDim + 2) * sizeof(float);
+  const long long slots_hw = static_cast<long long>(num_sms()) * bps;
+  int max_tiles = 0;
+  for (int b = 0; b < c->batch; ++b) max_tiles = std::max(max_tiles, (static_cast<int>(c->lens[b]) + TILE - 1) / TILE);
+  pl->slots = 0;
+  for (int l = 0; l < pl->launches; ++l) {
+    const size_t u0 = static_cast<size_t>(l) * UNIT_CAP;
+    const size_t nu = std::min(pl->units - u0, static_cast<size_t>(UNIT_CAP));
+    long long W = 0;
+    if (tiles) {
+      for (size_t u = 0; u < nu; ++u) W += tiles[u0 + u];
+    } else {
+      W = static_cast<long long>(nu) * max_tiles;
+    }
+    const long long G = std::min(slots_hw, std::max(1LL, W / MIN_TILES_PER_CTA));
+    pl->grid[l] = static_cast<int>(G);
+    pl->slots = std::max(pl->slots, nu + static_cast<size_t>(G));
+  }
+  if (!tiles)  // independent of the tile counts, so it bounds every later plan
+    pl->slots = std::min(pl->units, static_cast<size_t>(UNIT_CAP)) + static_cast<size_t>(slots_hw);
+  pl->head_bytes = kStatusBytes + (pl->units * sizeof(unsigned) + 255) / 256 * 256;
+  pl->bytes = pl->head_bytes + pl->slots * pl->gt * (kHeadDim + 2) * sizeof(float);
   return IQ_OK;
 }
 
@@ -764,7 +900,7 @@ int validate(const iq_cache* c, const uint16_t* q, int q_heads, int nq, int caus
 }
 
 template <int NT, int DS, int STREAMS>
-int launch_attend(const Params& prm, const CUtensorMap& map, dim3 grid, cudaStream_t s) {
+int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStream_t s) {
   using C = Cfg<NT, DS, STREAMS>;
   blocks_per_sm<NT, DS, STREAMS>();  // sets the shared-memory attribute once
   attend_kernel<NT, DS, STREAMS><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
@@ -788,7 +924,8 @@ int iq_attend_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* b
   if (n_queries < 1 || q_heads < 1 || q_heads % c->kv_heads)
     return fail(IQ_ERR_INVALID_ARG, "bad head or query count");
   Plan pl;
-  make_plan(c, q_heads, n_queries, &pl);
+  st = make_plan(c, q_heads, n_queries, 0, &pl, nullptr);
+  if (st != IQ_OK) return st;
   *bytes = pl.bytes;
   return IQ_OK;
 }
@@ -799,10 +936,18 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   clear_error();
   int st = validate(c, q, q_heads, n_queries, causal, rot_bf16, out);
   if (st != IQ_OK) return st;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(IQ_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
+  Plan bound;  // what iq_attend_workspace promised: an upper bound of this call's needs
+  st = make_plan(c, q_heads, n_queries, causal, &bound, nullptr);
+  if (st != IQ_OK) return st;
+  if (workspace_bytes < bound.bytes) return fail(IQ_ERR_WORKSPACE, "workspace smaller than iq_attend_workspace()");
+  static thread_local std::vector<int> tiles;
+  tiles.assign(bound.units, 0);
+  unit_tiles(c, q_heads / c->kv_heads, n_queries, causal, bound.gt, bound.nqt, tiles.data());
   Plan pl;
-  make_plan(c, q_heads, n_queries, &pl);
-  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256) return fail(IQ_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
-  if (workspace_bytes < pl.bytes) return fail(IQ_ERR_WORKSPACE, "workspace smaller than iq_attend_workspace()");
+  st = make_plan(c, q_heads, n_queries, causal, &pl, tiles.data());
+  if (st != IQ_OK) return st;
   auto encode = encode_fn();
   if (!encode) return fail(IQ_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
 
@@ -820,11 +965,14 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   unsigned* status = reinterpret_cast<unsigned*>(ws);
-  float* part_o = reinterpret_cast<float*>(ws + kStatusBytes);
-  float* part_ml = part_o + pl.part_count * pl.gt * kHeadDim;
-  IQ_CUDA(cudaMemsetAsync(status, 0, sizeof(unsigned), s));
+  unsigned* counters = reinterpret_cast<unsigned*>(ws + kStatusBytes);
+  float* part_o = reinterpret_cast<float*>(ws + bound.head_bytes);
+  float* part_ml = part_o + bound.slots * pl.gt * kHeadDim;
+  // status word and segment counters start at zero (the combining CTA resets
+  // its unit's counter too, so this matters only for a fresh workspace)
+  IQ_CUDA(cudaMemsetAsync(ws, 0, pl.head_bytes, s));
 
-  Params prm;
+  static thread_local Params prm;  // ~5 KB: kept off the stack
   std::memset(&prm, 0, sizeof(prm));
   prm.k_codes = c->k_codes;
   prm.k_scales = c->k_scales;
@@ -837,43 +985,31 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   prm.part_o = part_o;
   prm.part_ml = part_ml;
   prm.status = status;
+  prm.counters = counters;
+  prm.out = out;
+  prm.out_f32 = out_f32 ? 1 : 0;
   prm.batch = c->batch;
   prm.kv_heads = c->kv_heads;
   prm.rep = q_heads / c->kv_heads;
   prm.nq = n_queries;
   prm.cap = c->capacity;
   prm.nqt = pl.nqt;
-  prm.chunk_tiles = pl.chunk_tiles;
-  prm.maxc = pl.maxc;
   prm.causal = causal;
   prm.scale = scale;
   for (int b = 0; b < c->batch; ++b) prm.lens[b] = c->lens[b];
-  dim3 grid(pl.maxc, c->kv_heads * pl.nqt, c->batch);
-  st = pl.nt == 1 ? launch_attend<IQ_DECODE_CFG>(prm, map, grid, s) : launch_attend<IQ_MULTI_CFG>(prm, map, grid, s);
-  if (st != IQ_OK) return st;
-
-  CombineParams cp;
-  std::memset(&cp, 0, sizeof(cp));
-  cp.part_o = part_o;
-  cp.part_ml = part_ml;
-  cp.rot = rot_bf16;
-  cp.out = out;
-  cp.status = status;
-  cp.out_f32 = out_f32 ? 1 : 0;
-  cp.batch = c->batch;
-  cp.kv_heads = c->kv_heads;
-  cp.rep = prm.rep;
-  cp.nq = n_queries;
-  cp.nqt = pl.nqt;
-  cp.gt = pl.gt;
-  cp.chunk_tok = pl.chunk_tiles * TILE;
-  cp.maxc = pl.maxc;
-  cp.causal = causal;
-  for (int b = 0; b < c->batch; ++b) cp.lens[b] = c->lens[b];
-  const long long rows = static_cast<long long>(c->batch) * q_heads * n_queries;
-  const long long blocks = (rows * 32 + 255) / 256;
-  combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(cp);
-  IQ_CUDA(cudaGetLastError());
+  // launches run in stream order and reuse the partial slots
+  for (int l = 0; l < pl.launches; ++l) {
+    const int u0 = l * UNIT_CAP;
+    const int nu = static_cast<int>(std::min(pl.units - u0, static_cast<size_t>(UNIT_CAP)));
+    prm.unit_base = u0;
+    prm.num_units = nu;
+    prm.grid = pl.grid[l];
+    prm.prefix[0] = 0;
+    for (int u = 0; u < nu; ++u) prm.prefix[u + 1] = prm.prefix[u] + tiles[u0 + u];
+    st = pl.nt == 1 ? launch_attend<IQ_DECODE_CFG>(prm, map, prm.grid, s)
+                    : launch_attend<IQ_MULTI_CFG>(prm, map, prm.grid, s);
+    if (st != IQ_OK) return st;
+  }
   return IQ_OK;
 }
 
