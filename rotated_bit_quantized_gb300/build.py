@@ -42,6 +42,14 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+    """Compile and link libiqkv.so (skipped when it is newer than every source).
+
+    Extra nvcc flags (e.g. a -D tuning macro) can be passed in the environment
+    variable IQKV_NVCC_FLAGS; setting it forces a rebuild.
+    """
+    extra = os.environ.get("IQKV_NVCC_FLAGS", "").split()
+    if extra:
+        force = True
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
@@ -49,7 +57,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     def compile_one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -21,7 +21,7 @@
 // Inside a CTA:
 //  * a producer warp streams the tiles (packed K codes by a 2-D tensor copy with
 //    128-byte swizzle; packed V codes and the four scale/bias rows by 1-D bulk
-//    copies) into a 4-stage shared-memory ring guarded by mbarriers, running
+//    copies) into a multi-stage shared-memory ring guarded by mbarriers, running
 //    ahead across unit boundaries;
 //  * consumer warps unpack codes to fp16 in registers with bit tricks and run
 //    m16n8k16 tensor-core MMAs: S = K_codes . q (per 64-dim group, fp32
@@ -44,8 +44,7 @@
 namespace iq {
 namespace attn {
 
-constexpr int TILE = 64;     // tokens per pipeline stage
-constexpr int NSTAGE = 4;
+constexpr int TILE = 64;     // tokens per pipeline stage (4 sub-tiles of 16)
 constexpr int OFF_K = 0;                     // 64 rows x 128 B, 128-byte swizzle
 constexpr int OFF_V = 8192;                  // 64 rows x 96 B (+ pad for the field window)
 constexpr int OFF_KS = OFF_V + 6144 + 128;   // 64 x 8 B each
@@ -147,12 +146,12 @@ __device__ __forceinline__ void unpack_v3_pair(uint32_t fa, uint32_t fb, uint32_
   h[7] = dq3<5>(x2);
 }
 
-template <int NT, int DS, int STREAMS>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB>
 struct Cfg {
   static constexpr int GT = 8 * NT;            // query rows per unit
   static constexpr int GPW = 4 / DS;           // 64-dim groups per consumer warp
   static constexpr int CW = DS * STREAMS;      // consumer warps
-  static constexpr int THREADS = (CW + 1) * 32;
+  static constexpr int THREADS = (CW + 1) * 32;  // + one producer warp
   static constexpr int OFF_QS = NSTAGE * STAGE;
   static constexpr int OFF_QSUM = OFF_QS + GT * 512;
   static constexpr int OFF_MBUF = OFF_QSUM + GT * 16;
@@ -160,27 +159,32 @@ struct Cfg {
   static constexpr int OFF_XBUF = OFF_LBUF + STREAMS * GT * 4;
   static constexpr int XBUF_BYTES = DS > 1 ? STREAMS * 2 * DS * NT * 32 * 16 : 0;
   static constexpr int OFF_OBUF = OFF_XBUF + XBUF_BYTES;
-  static constexpr int OBUF_BYTES = STREAMS > 1 ? STREAMS * GT * 256 * 4 : 0;
-  static constexpr int OFF_BAR = OFF_OBUF + OBUF_BYTES;
+  static constexpr int OBUF_BYTES = STREAMS > 1 ? GT * 256 * 4 : 0;  // streams merge in turn
+  static constexpr int OFF_QB = OFF_OBUF + OBUF_BYTES;
+  static constexpr int QB_BYTES = DS * GPW * 4 * NT * 32 * 8;       // q'' MMA B fragments
+  static constexpr int OFF_BAR = OFF_QB + QB_BYTES;
   static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8;
   static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
   static_assert(OFF_XBUF % 16 == 0 && OFF_OBUF % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
-  static_assert(4 % STREAMS == 0 && 4 % DS == 0, "shape");
+  static_assert(4 % DS == 0, "shape");
 };
 
-template <int NT, int DS, int STREAMS>
-__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB>
+__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, MINB)
     attend_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap kmap) {
-  using C = Cfg<NT, DS, STREAMS>;
+  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB>;
   constexpr int GT = C::GT, GPW = C::GPW, CW = C::CW, NCT = CW * 32;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base (128-byte swizzle atom), derived by pointer
+  // arithmetic on the shared array so loads through it stay shared-memory loads
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint16_t* qs = reinterpret_cast<uint16_t*>(smem + C::OFF_QS);
   float* qsum = reinterpret_cast<float*>(smem + C::OFF_QSUM);
   float* mbuf = reinterpret_cast<float*>(smem + C::OFF_MBUF);
   float* lbuf = reinterpret_cast<float*>(smem + C::OFF_LBUF);
   float4* xbuf = reinterpret_cast<float4*>(smem + C::OFF_XBUF);
   float* obuf = reinterpret_cast<float*>(smem + C::OFF_OBUF);
+  uint2* qbs = reinterpret_cast<uint2*>(smem + C::OFF_QB);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + NSTAGE;
   int* s_flag = reinterpret_cast<int*>(smem + C::OFF_FLAG);
@@ -212,6 +216,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
   __syncthreads();
 
   // ------------------------------------------------------------ producer
+  // One warp (lane 0) streams the CTA's tiles through the ring, refilling a
+  // stage as soon as every consumer warp has released it.
   if (warp == CW) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -220,14 +226,14 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
       for (long long gt = g0; gt < g1; ++gt, ++k) {
         while (gt >= p.prefix[u + 1]) ++u;
         const int ug = p.unit_base + u;
-        const int b = ug / (p.kv_heads * p.nqt), kvh = (ug / p.nqt) % p.kv_heads;
+        const int bb = ug / (p.kv_heads * p.nqt), hh = (ug / p.nqt) % p.kv_heads;
         const int st = static_cast<int>(k % NSTAGE);
         if (k >= NSTAGE && !mbar_wait(&empty[st], static_cast<uint32_t>((k / NSTAGE) - 1) & 1)) {
           atomicOr(p.status, 1u);
           break;
         }
         uint8_t* sb = smem + st * STAGE;
-        const long long row0 = (static_cast<long long>(b) * p.kv_heads + kvh) * p.cap +
+        const long long row0 = (static_cast<long long>(bb) * p.kv_heads + hh) * p.cap +
                                (gt - p.prefix[u]) * TILE;
         mbar_arrive_expect_tx(&full[st], STAGE_TX);
         tensor2d_g2s(sb + OFF_K, &kmap, 0, static_cast<int>(row0), &full[st], pol);
@@ -258,7 +264,6 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
   // per-unit state
   int b = 0, kvh = 0, qt = 0, T = 0, limit = 0, qmin = 0;
   int qpos[NT][2];
-  uint32_t qb[GPW][4][NT][2];
   float qsr[GPW][NT][2];
   float O[GPW][4][NT][4];
   float bacc[GPW][NT][2];
@@ -318,28 +323,35 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
       if ((lane & 7) == 0) qsum[r * 4 + (lane >> 3)] = s;
     }
     named_bar(1, NCT);
-    // q'' as fp16 B fragments.  Thread t covers dims 64G+16t .. +15 of group G;
-    // register pair m of its unpacked codes holds dims (m, m+4) for m < 4 and
-    // (m+4, m+8) for m >= 4; k-step s uses pairs 2s (slots 2t,2t+1) and 2s+1.
+    // q'' as fp16 MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].
+    // Thread t covers dims 64G+16t .. +15 of group G; register pair m of its
+    // unpacked codes holds dims (m, m+4) for m < 4 and (m+4, m+8) for m >= 4;
+    // k-step s uses pairs 2s (slots 2t,2t+1) and 2s+1.  Stream 0 writes them.
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
       const int Gr = dg * GPW + gi;
       const int base = 64 * Gr + 16 * t;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        const uint16_t* qrow = qs + (8 * j + g) * kHeadDim + base;
+        if (stream == 0) {
+          const uint16_t* qrow = qs + (8 * j + g) * kHeadDim + base;
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
+          for (int s = 0; s < 4; ++s) {
+            uint32_t h2[2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int m = 2 * s + h;
-            const int lo = m < 4 ? m : m + 4;
-            qb[gi][s][j][h] = pack_f16x2(bf16_to_f32(qrow[lo]), bf16_to_f32(qrow[lo + 4]));
+            for (int h = 0; h < 2; ++h) {
+              const int m = 2 * s + h;
+              const int lo = m < 4 ? m : m + 4;
+              h2[h] = pack_f16x2(bf16_to_f32(qrow[lo]), bf16_to_f32(qrow[lo + 4]));
+            }
+            qbs[((Gr * 4 + s) * NT + j) * 32 + lane] = make_uint2(h2[0], h2[1]);
           }
+        }
         qsr[gi][j][0] = qsum[(8 * j + 2 * t) * 4 + Gr];
         qsr[gi][j][1] = qsum[(8 * j + 2 * t + 1) * 4 + Gr];
       }
     }
+    named_bar(1, NCT);  // fragments visible to every stream
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -392,7 +404,10 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
       for (int s = 0; s < 4; ++s) {
         const uint32_t A[4] = {RA[2 * s], RB[2 * s], RA[2 * s + 1], RB[2 * s + 1]};
 #pragma unroll
-        for (int j = 0; j < NT; ++j) mma_f16(acc[j], A, qb[gi][s][j][0], qb[gi][s][j][1]);
+        for (int j = 0; j < NT; ++j) {
+          const uint2 bq = qbs[((Gr * 4 + s) * NT + j) * 32 + lane];
+          mma_f16(acc[j], A, bq.x, bq.y);
+        }
       }
       const float s0 = pick_bf16(ksc0, Gr), s1 = pick_bf16(ksc1, Gr);
       const float b0 = pick_bf16(kbi0, Gr), b1 = pick_bf16(kbi1, Gr);
@@ -605,13 +620,14 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
             pml[row * 2] = msc[j][e];
             pml[row * 2 + 1] = lrow[j][e];
           }
-    } else {  // merge the token streams in shared memory first, in stream order
+    } else {  // merge the token streams in turn through one shared accumulation buffer
       if (dg == 0 && g == 0)
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
           for (int e = 0; e < 2; ++e) mbuf[stream * GT + 8 * j + 2 * t + e] = msc[j][e];
       named_bar(1, NCT);
+      float a_row[NT][2];
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -620,37 +636,48 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
           float M = mbuf[row];
 #pragma unroll
           for (int s = 1; s < STREAMS; ++s) M = fmaxf(M, mbuf[s * GT + row]);
-          const float a = msc[j][e] == NEG_INF ? 0.f : ex2_approx(msc[j][e] - M);
-          if (dg == 0 && g == 0) lbuf[stream * GT + row] = lrow[j][e] * a;
-#pragma unroll
-          for (int gi = 0; gi < GPW; ++gi) {
-            float* dst = obuf + (stream * GT + row) * kHeadDim + 64 * (dg * GPW + gi) + 8 * g;
-            reinterpret_cast<float4*>(dst)[0] = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a,
-                                                            O[gi][1][j][e] * a, O[gi][1][j][e + 2] * a);
-            reinterpret_cast<float4*>(dst)[1] = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a,
-                                                            O[gi][3][j][e] * a, O[gi][3][j][e + 2] * a);
-          }
+          a_row[j][e] = msc[j][e] == NEG_INF ? 0.f : ex2_approx(msc[j][e] - M);
+          if (dg == 0 && g == 0) lbuf[stream * GT + row] = lrow[j][e] * a_row[j][e];
         }
-      named_bar(1, NCT);
-      for (int idx = threadIdx.x; idx < GT * 64; idx += NCT) {
-        const int r = idx >> 6, c4 = idx & 63;
-        float4 a = reinterpret_cast<const float4*>(obuf + r * kHeadDim)[c4];
+#pragma unroll 1
+      for (int turn = 0; turn < STREAMS; ++turn) {
+        if (stream == turn) {
 #pragma unroll
-        for (int s = 1; s < STREAMS; ++s) {
-          const float4 v = reinterpret_cast<const float4*>(obuf + (s * GT + r) * kHeadDim)[c4];
-          a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-        }
-        reinterpret_cast<float4*>(po + r * kHeadDim)[c4] = a;
-      }
-      for (int r = threadIdx.x; r < GT; r += NCT) {
-        float M = mbuf[r], L = lbuf[r];
+          for (int j = 0; j < NT; ++j)
 #pragma unroll
-        for (int s = 1; s < STREAMS; ++s) {
-          M = fmaxf(M, mbuf[s * GT + r]);
-          L += lbuf[s * GT + r];
+            for (int e = 0; e < 2; ++e) {
+              const int row = 8 * j + 2 * t + e;
+              const float a = a_row[j][e];
+#pragma unroll
+              for (int gi = 0; gi < GPW; ++gi) {
+                const int col = 64 * (dg * GPW + gi) + 8 * g;
+                float4 v0 = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a, O[gi][1][j][e] * a,
+                                        O[gi][1][j][e + 2] * a);
+                float4 v1 = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a, O[gi][3][j][e] * a,
+                                        O[gi][3][j][e + 2] * a);
+                float4* acc = reinterpret_cast<float4*>(obuf + row * kHeadDim + col);
+                if (turn > 0) {
+                  const float4 p0 = acc[0], p1 = acc[1];
+                  v0.x += p0.x; v0.y += p0.y; v0.z += p0.z; v0.w += p0.w;
+                  v1.x += p1.x; v1.y += p1.y; v1.z += p1.z; v1.w += p1.w;
+                }
+                float4* dst = turn == STREAMS - 1 ? reinterpret_cast<float4*>(po + row * kHeadDim + col) : acc;
+                dst[0] = v0;
+                dst[1] = v1;
+              }
+              if (turn == STREAMS - 1 && dg == 0 && g == 0) {
+                float M = mbuf[row], L = lbuf[row];
+#pragma unroll
+                for (int s = 1; s < STREAMS; ++s) {
+                  M = fmaxf(M, mbuf[s * GT + row]);
+                  L += lbuf[s * GT + row];
+                }
+                pml[row * 2] = M;
+                pml[row * 2 + 1] = L;
+              }
+            }
         }
-        pml[r * 2] = M;
-        pml[r * 2 + 1] = L;
+        if (turn < STREAMS - 1) named_bar(1, NCT);
       }
     }
 
@@ -764,7 +791,9 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS>::THREADS, 2)
     }
     const uint32_t sb = smem_u32(smem + st * STAGE);
     const int tile_tok = static_cast<int>(gt - p.prefix[u]) * TILE;
-    for (int sub = stream; sub < 4; sub += STREAMS) {
+    // global sub-tile 4k + sub belongs to stream (4k + sub) % STREAMS
+    const int first = static_cast<int>((stream - (4 * k) % STREAMS + STREAMS) % STREAMS);
+    for (int sub = first; sub < 4; sub += STREAMS) {
       const int tokbase = tile_tok + sub * 16;
       if (tokbase >= limit) break;
       if (tokbase + 16 <= limit && tokbase + 15 <= qmin)
@@ -791,17 +820,19 @@ struct Plan {
 // to 256 B][partial O: slots x GT x 256 f32][partial (max, sum): slots x GT x 2 f32]
 constexpr size_t kStatusBytes = 256;
 
-template <int NT, int DS, int STREAMS>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB>
 int blocks_per_sm() {
   static int cache[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (cache[dev] == 0) {
-    using C = Cfg<NT, DS, STREAMS>;
+    using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB>;
     int n = 0;
-    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS>, C::THREADS, C::SMEM) !=
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         C::SMEM);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB>, C::THREADS,
+                                                      C::SMEM) !=
             cudaSuccess ||
         n <= 0)
       n = 1;
@@ -810,11 +841,23 @@ int blocks_per_sm() {
   return cache[dev];
 }
 
-// Decode (<= 8 query rows per kv head): one warp owns all four groups, four
-// token streams per CTA.  Verify / prefill (more rows): 32-row query tiles, a
-// warp per 64-dim group, one token stream.
-#define IQ_DECODE_CFG 1, 1, 4
-#define IQ_MULTI_CFG 4, 4, 1
+// <query n-tiles, warps per token stream, token streams, ring stages, CTAs per SM>
+// Decode (<= 8 query rows per kv head): one warp owns all four groups; four
+// token streams per CTA, two CTAs per SM (measured best: more streams per CTA
+// make the warps wait on one shared ring; fewer stages starve it).  Verify /
+// prefill (more rows): 32-row query tiles, a warp per 64-dim group, one token
+// stream, two CTAs per SM.
+#ifndef IQ_DECODE_STREAMS
+#define IQ_DECODE_STREAMS 4
+#endif
+#ifndef IQ_DECODE_STAGES
+#define IQ_DECODE_STAGES 4
+#endif
+#ifndef IQ_DECODE_MINB
+#define IQ_DECODE_MINB 2
+#endif
+#define IQ_DECODE_CFG 1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB
+#define IQ_MULTI_CFG 4, 4, 1, 3, 2
 
 // Tiles of every unit, in unit order: unit u = (b, kv head, query tile).
 void unit_tiles(const iq_cache* c, int rep, int nq, int causal, int gt, int nqt, int* tiles) {
@@ -899,11 +942,11 @@ int validate(const iq_cache* c, const uint16_t* q, int q_heads, int nq, int caus
   return IQ_OK;
 }
 
-template <int NT, int DS, int STREAMS>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB>
 int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStream_t s) {
-  using C = Cfg<NT, DS, STREAMS>;
-  blocks_per_sm<NT, DS, STREAMS>();  // sets the shared-memory attribute once
-  attend_kernel<NT, DS, STREAMS><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
+  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB>;
+  blocks_per_sm<NT, DS, STREAMS, NSTAGE, MINB>();  // sets the shared-memory attribute once
+  attend_kernel<NT, DS, STREAMS, NSTAGE, MINB><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
   IQ_CUDA(cudaGetLastError());
   return IQ_OK;
 }

@@ -33,7 +33,7 @@ constexpr int kGroup = 64;
 constexpr int kKWords = 32;   // 256 dims * 4 bits / 32
 constexpr int kVWords = 24;   // 256 dims * 3 bits / 32
 constexpr int kGroups = 4;    // 256 / 64
-constexpr uint32_t kSpinLimit = 1u << 22;  // bounded waits (~seconds), then report
+constexpr uint32_t kSpinLimit = 1u << 17;  // bounded waits (seconds at most), then report
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
@@ -68,21 +68,25 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One potentially blocking test of phase `parity`: the hardware suspends the
+// warp for up to `suspend_ns` while the phase is incomplete, so waiting warps
+// do not spend issue slots polling.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
-// Bounded wait: true when the phase completed, false after kSpinLimit polls.
+// Bounded wait: true when the phase completed, false after kSpinLimit tests
+// (each of which may suspend the warp for up to 20 us).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, 20000u)) return true;
   return false;
 }
 
@@ -114,7 +118,8 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// ---- shared loads
+// ---- shared loads (volatile: measured faster than letting the compiler
+// reorder them, and it keeps every load after the mbarrier wait)
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -155,7 +160,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
 }
 __device__ __forceinline__ float ex2_approx(float x) {
