@@ -23,9 +23,10 @@
 //    128-byte swizzle; packed V codes and the four scale/bias rows by 1-D bulk
 //    copies) into a multi-stage shared-memory ring guarded by mbarriers, running
 //    ahead across unit boundaries;
-//  * consumer warps unpack codes to fp16 in registers with bit tricks and run
-//    m16n8k16 tensor-core MMAs: S = K_codes . q (per 64-dim group, fp32
-//    accumulate), folded with the group scale/bias on CUDA cores; online
+//  * consumer warps unpack codes in registers with bit tricks and run m16n8k16
+//    tensor-core MMAs: S = (128 + K_codes) . q (bf16, per 64-dim group, fp32
+//    accumulate), folded with the group scale and (bias - 128 scale) on CUDA
+//    cores; online
 //    softmax in fp32 with a lazily moving reference max; O^T += (V_codes - 4)^T
 //    . (P * s_v) with P transposed in registers by movmatrix; the value bias
 //    term sum_t p_t (b_t + 4 s_t) on CUDA cores.
@@ -109,16 +110,18 @@ __device__ __forceinline__ float pick_bf16(uint2 v, int G) {
   return bf16_to_f32((G & 1) ? (w >> 16) : (w & 0xFFFFu));
 }
 
-// 4-bit word (8 codes, LSB first) -> fp16x2 pairs (c0,c4) (c1,c5) (c2,c6) (c3,c7)
+// Key codes enter the q.K product as bf16 values 128 + c (the code ORed into
+// the mantissa of 128.0; exact): the 128 * sum(q'') offset is removed in the
+// per-token fold, where it becomes part of the bias (b - 128 s).
+constexpr float KOFFSET = 128.0f;
+
+// 4-bit word (8 codes, LSB first) -> bf16x2 pairs 128+(c0,c4) (c1,c5) (c2,c6) (c3,c7)
 __device__ __forceinline__ void unpack_k4(uint32_t w, uint32_t* r) {
-  constexpr uint32_t MAGIC = 0x64006400u;                       // 1024.0 in each half
-  constexpr uint32_t ONE = 0x3C003C00u, NEG1024 = 0xE400E400u;  // 1, -1024
-  constexpr uint32_t SIXTEENTH = 0x2C002C00u, NEG64 = 0xD400D400u;  // 1/16, -64
-  const uint32_t w8 = w >> 8;
-  r[0] = fma_f16x2(and_or(w, 0x000F000Fu, MAGIC), ONE, NEG1024);
-  r[1] = fma_f16x2(and_or(w, 0x00F000F0u, MAGIC), SIXTEENTH, NEG64);
-  r[2] = fma_f16x2(and_or(w8, 0x000F000Fu, MAGIC), ONE, NEG1024);
-  r[3] = fma_f16x2(and_or(w8, 0x00F000F0u, MAGIC), SIXTEENTH, NEG64);
+  constexpr uint32_t MAGIC = 0x43004300u;  // 128.0 in each half
+  r[0] = and_or(w, 0x000F000Fu, MAGIC);
+  r[1] = and_or(w >> 4, 0x000F000Fu, MAGIC);
+  r[2] = and_or(w >> 8, 0x000F000Fu, MAGIC);
+  r[3] = and_or(w >> 12, 0x000F000Fu, MAGIC);
 }
 
 // 3-bit code at bit `L` (0..7) of each 16-bit half of x -> fp16x2 (code - 4)
@@ -323,7 +326,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, M
       if ((lane & 7) == 0) qsum[r * 4 + (lane >> 3)] = s;
     }
     named_bar(1, NCT);
-    // q'' as fp16 MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].
+    // q'' as bf16 MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].
     // Thread t covers dims 64G+16t .. +15 of group G; register pair m of its
     // unpacked codes holds dims (m, m+4) for m < 4 and (m+4, m+8) for m >= 4;
     // k-step s uses pairs 2s (slots 2t,2t+1) and 2s+1.  Stream 0 writes them.
@@ -342,7 +345,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, M
             for (int h = 0; h < 2; ++h) {
               const int m = 2 * s + h;
               const int lo = m < 4 ? m : m + 4;
-              h2[h] = pack_f16x2(bf16_to_f32(qrow[lo]), bf16_to_f32(qrow[lo + 4]));
+              h2[h] = static_cast<uint32_t>(qrow[lo]) | (static_cast<uint32_t>(qrow[lo + 4]) << 16);
             }
             qbs[((Gr * 4 + s) * NT + j) * 32 + lane] = make_uint2(h2[0], h2[1]);
           }
@@ -383,7 +386,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, M
     const uint2 ksc0 = lds64(sb + OFF_KS + rr0 * 8), ksc1 = lds64(sb + OFF_KS + rr1 * 8);
     const uint2 kbi0 = lds64(sb + OFF_KB + rr0 * 8), kbi1 = lds64(sb + OFF_KB + rr1 * 8);
 
-    // scores: per group, S_G = codes . q'' (fp32), folded with scale/bias
+    // scores: per group, S_G = (128 + codes) . q'' (fp32), folded with scale/bias
     float sc[NT][4];
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
@@ -406,11 +409,12 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, M
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           const uint2 bq = qbs[((Gr * 4 + s) * NT + j) * 32 + lane];
-          mma_f16(acc[j], A, bq.x, bq.y);
+          mma_bf16(acc[j], A, bq.x, bq.y);
         }
       }
       const float s0 = pick_bf16(ksc0, Gr), s1 = pick_bf16(ksc1, Gr);
-      const float b0 = pick_bf16(kbi0, Gr), b1 = pick_bf16(kbi1, Gr);
+      const float b0 = fmaf(-KOFFSET, s0, pick_bf16(kbi0, Gr));
+      const float b1 = fmaf(-KOFFSET, s1, pick_bf16(kbi1, Gr));
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         if constexpr (DS == 1) {
