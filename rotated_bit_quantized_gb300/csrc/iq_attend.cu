@@ -779,36 +779,41 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, M
   };
 
   // ------------------------------------------------------------ main loop over this CTA's tiles
+  // One pass per unit segment, so the per-unit prologue and epilogue each have a
+  // single call site outside the hot per-tile loop.
   int u = u0;
-  begin_unit(u);
-  long long k = 0;
-  for (long long gt = g0; gt < g1; ++gt, ++k) {
-    if (gt >= p.prefix[u + 1]) {  // crossed into the next unit (units hold >= 1 tile)
-      end_unit(u);
-      ++u;
-      begin_unit(u);
+  long long k = 0, gt = g0;
+  bool ok = true;
+  for (;;) {
+    begin_unit(u);
+    const long long seg_end = p.prefix[u + 1] < g1 ? p.prefix[u + 1] : g1;
+    const int tile0 = static_cast<int>(p.prefix[u]);
+    for (; gt < seg_end; ++gt, ++k) {
+      const int st = static_cast<int>(k % NSTAGE);
+      if (!mbar_wait(&full[st], static_cast<uint32_t>(k / NSTAGE) & 1)) {
+        atomicOr(p.status, 2u);
+        ok = false;
+        break;
+      }
+      const uint32_t sb = smem_u32(smem + st * STAGE);
+      const int tile_tok = static_cast<int>(gt - tile0) * TILE;
+      // global sub-tile 4k + sub belongs to stream (4k + sub) % STREAMS
+      const int first = static_cast<int>((stream - (4 * k) % STREAMS + STREAMS) % STREAMS);
+      for (int sub = first; sub < 4; sub += STREAMS) {
+        const int tokbase = tile_tok + sub * 16;
+        if (tokbase >= limit) break;
+        if (tokbase + 16 <= limit && tokbase + 15 <= qmin)
+          subtile(std::true_type{}, sub, tokbase, sb);
+        else
+          subtile(std::false_type{}, sub, tokbase, sb);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
     }
-    const int st = static_cast<int>(k % NSTAGE);
-    if (!mbar_wait(&full[st], static_cast<uint32_t>(k / NSTAGE) & 1)) {
-      atomicOr(p.status, 2u);
-      break;
-    }
-    const uint32_t sb = smem_u32(smem + st * STAGE);
-    const int tile_tok = static_cast<int>(gt - p.prefix[u]) * TILE;
-    // global sub-tile 4k + sub belongs to stream (4k + sub) % STREAMS
-    const int first = static_cast<int>((stream - (4 * k) % STREAMS + STREAMS) % STREAMS);
-    for (int sub = first; sub < 4; sub += STREAMS) {
-      const int tokbase = tile_tok + sub * 16;
-      if (tokbase >= limit) break;
-      if (tokbase + 16 <= limit && tokbase + 15 <= qmin)
-        subtile(std::true_type{}, sub, tokbase, sb);
-      else
-        subtile(std::false_type{}, sub, tokbase, sb);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    end_unit(u);
+    if (!ok || gt >= g1) break;
+    ++u;
   }
-  end_unit(u);
 }
 
 // ------------------------------------------------------------------ host plan

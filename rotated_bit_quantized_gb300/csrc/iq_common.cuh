@@ -82,11 +82,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, ui
       : "memory");
   return ok != 0;
 }
+#ifndef IQ_SUSPEND_NS
+#define IQ_SUSPEND_NS 20000u
+#endif
 // Bounded wait: true when the phase completed, false after kSpinLimit tests
-// (each of which may suspend the warp for up to 20 us).
+// (each of which may suspend the warp for up to IQ_SUSPEND_NS).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity, 20000u)) return true;
+    if (mbar_try_wait(bar, parity, IQ_SUSPEND_NS)) return true;
   return false;
 }
 
