@@ -45,15 +45,25 @@
 namespace iq {
 namespace attn {
 
-constexpr int TILE = 64;     // tokens per pipeline stage (4 sub-tiles of 16)
-constexpr int OFF_K = 0;                     // 64 rows x 128 B, 128-byte swizzle
-constexpr int OFF_V = 8192;                  // 64 rows x 96 B (+ pad for the field window)
-constexpr int OFF_KS = OFF_V + 6144 + 128;   // 64 x 8 B each
-constexpr int OFF_KB = OFF_KS + 512;
-constexpr int OFF_VS = OFF_KB + 512;
-constexpr int OFF_VB = OFF_VS + 512;
-constexpr int STAGE = 17408;                 // multiple of 1024 (swizzle atom)
-constexpr uint32_t STAGE_TX = 8192 + 6144 + 4 * 512;
+// Shared-memory stage of TILE tokens: packed K codes (swizzled), packed V
+// codes (+ pad for the field window) and the four scale/bias rows.
+template <int TILE_>
+struct Tiling {
+  static constexpr int TILE = TILE_;               // tokens per pipeline stage
+  static constexpr int SUBS = TILE / 16;           // 16-token sub-tiles per stage
+  static constexpr int K_BYTES = TILE * 128;       // TILE rows x 128 B, 128-byte swizzle
+  static constexpr int V_BYTES = TILE * 96;        // TILE rows x 96 B
+  static constexpr int SB_BYTES = TILE * 8;        // TILE rows x 4 bf16
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = K_BYTES;
+  static constexpr int OFF_KS = OFF_V + V_BYTES + 128;
+  static constexpr int OFF_KB = OFF_KS + SB_BYTES;
+  static constexpr int OFF_VS = OFF_KB + SB_BYTES;
+  static constexpr int OFF_VB = OFF_VS + SB_BYTES;
+  static constexpr int STAGE = (OFF_VB + SB_BYTES + 1023) / 1024 * 1024;  // multiple of the swizzle atom
+  static constexpr uint32_t STAGE_TX = K_BYTES + V_BYTES + 4 * SB_BYTES;
+  static_assert(TILE % 16 == 0 && TILE <= 256 && 256 % TILE == 0, "tile must divide the capacity granule");
+};
 constexpr int UNIT_CAP = 1024;   // units per launch (their tile prefix travels by value)
 constexpr int MIN_TILES_PER_CTA = 8;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -149,8 +159,9 @@ __device__ __forceinline__ void unpack_v3_pair(uint32_t fa, uint32_t fb, uint32_
   h[7] = dq3<5>(x2);
 }
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB>
-struct Cfg {
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_>
+struct Cfg : Tiling<TILE_> {
+  using Tiling<TILE_>::STAGE;
   static constexpr int GT = 8 * NT;            // query rows per unit
   static constexpr int GPW = 4 / DS;           // 64-dim groups per consumer warp
   static constexpr int CW = DS * STREAMS;      // consumer warps
@@ -172,10 +183,14 @@ struct Cfg {
   static_assert(4 % DS == 0, "shape");
 };
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB>
-__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, MINB)
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_>
+__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THREADS, MINB)
     attend_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap kmap) {
-  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB>;
+  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>;
+  constexpr int TILE = C::TILE, SUBS = C::SUBS, STAGE = C::STAGE;
+  constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_KS = C::OFF_KS, OFF_KB = C::OFF_KB;
+  constexpr int OFF_VS = C::OFF_VS, OFF_VB = C::OFF_VB, V_BYTES = C::V_BYTES, SB_BYTES = C::SB_BYTES;
+  constexpr uint32_t STAGE_TX = C::STAGE_TX;
   constexpr int GT = C::GT, GPW = C::GPW, CW = C::CW, NCT = CW * 32;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base (128-byte swizzle atom), derived by pointer
@@ -240,11 +255,11 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, M
                                (gt - p.prefix[u]) * TILE;
         mbar_arrive_expect_tx(&full[st], STAGE_TX);
         tensor2d_g2s(sb + OFF_K, &kmap, 0, static_cast<int>(row0), &full[st], pol);
-        bulk_g2s(sb + OFF_V, p.v_codes + row0 * kVWords, 6144, &full[st], pol);
-        bulk_g2s(sb + OFF_KS, p.k_scales + row0 * kGroups, 512, &full[st], pol);
-        bulk_g2s(sb + OFF_KB, p.k_biases + row0 * kGroups, 512, &full[st], pol);
-        bulk_g2s(sb + OFF_VS, p.v_scales + row0 * kGroups, 512, &full[st], pol);
-        bulk_g2s(sb + OFF_VB, p.v_biases + row0 * kGroups, 512, &full[st], pol);
+        bulk_g2s(sb + OFF_V, p.v_codes + row0 * kVWords, V_BYTES, &full[st], pol);
+        bulk_g2s(sb + OFF_KS, p.k_scales + row0 * kGroups, SB_BYTES, &full[st], pol);
+        bulk_g2s(sb + OFF_KB, p.k_biases + row0 * kGroups, SB_BYTES, &full[st], pol);
+        bulk_g2s(sb + OFF_VS, p.v_scales + row0 * kGroups, SB_BYTES, &full[st], pol);
+        bulk_g2s(sb + OFF_VB, p.v_biases + row0 * kGroups, SB_BYTES, &full[st], pol);
       }
       // never leave with copies in flight: wait for the last tile issued to each stage
       for (long long s = 0; s < NSTAGE && s < k; ++s) {
@@ -797,9 +812,9 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, M
       }
       const uint32_t sb = smem_u32(smem + st * STAGE);
       const int tile_tok = static_cast<int>(gt - tile0) * TILE;
-      // global sub-tile 4k + sub belongs to stream (4k + sub) % STREAMS
-      const int first = static_cast<int>((stream - (4 * k) % STREAMS + STREAMS) % STREAMS);
-      for (int sub = first; sub < 4; sub += STREAMS) {
+      // global sub-tile SUBS*k + sub belongs to stream (SUBS*k + sub) % STREAMS
+      const int first = static_cast<int>((stream - (SUBS * k) % STREAMS + STREAMS) % STREAMS);
+      for (int sub = first; sub < SUBS; sub += STREAMS) {
         const int tokbase = tile_tok + sub * 16;
         if (tokbase >= limit) break;
         if (tokbase + 16 <= limit && tokbase + 15 <= qmin)
@@ -821,7 +836,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB>::THREADS, M
 constexpr int kMaxLaunches = 64;
 
 struct Plan {
-  int nt, gt, nqt, launches, grid[kMaxLaunches];
+  int nt, gt, nqt, tile, launches, grid[kMaxLaunches];
   size_t units, slots, head_bytes, bytes;
 };
 
@@ -829,19 +844,19 @@ struct Plan {
 // to 256 B][partial O: slots x GT x 256 f32][partial (max, sum): slots x GT x 2 f32]
 constexpr size_t kStatusBytes = 256;
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_>
 int blocks_per_sm() {
   static int cache[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (cache[dev] == 0) {
-    using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB>;
+    using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>;
     int n = 0;
-    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         C::SMEM);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB>, C::THREADS,
-                                                      C::SMEM) !=
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_>,
+                                                      C::THREADS, C::SMEM) !=
             cudaSuccess ||
         n <= 0)
       n = 1;
@@ -850,33 +865,37 @@ int blocks_per_sm() {
   return cache[dev];
 }
 
-// <query n-tiles, warps per token stream, token streams, ring stages, CTAs per SM>
+// <query n-tiles, warps per token stream, token streams, ring stages, CTAs per SM, tile tokens>
 // Decode (<= 8 query rows per kv head): one warp owns all four groups; four
-// token streams per CTA, two CTAs per SM (measured best: more streams per CTA
-// make the warps wait on one shared ring; fewer stages starve it).  Verify /
+// token streams per CTA, two CTAs per SM, two 128-token stages (measured best:
+// more streams per CTA make the warps wait on one shared ring; 64-token stages
+// cost more handshakes per byte).  Verify /
 // prefill (more rows): 32-row query tiles, a warp per 64-dim group, one token
 // stream, two CTAs per SM.
 #ifndef IQ_DECODE_STREAMS
 #define IQ_DECODE_STREAMS 4
 #endif
 #ifndef IQ_DECODE_STAGES
-#define IQ_DECODE_STAGES 4
+#define IQ_DECODE_STAGES 2
+#endif
+#ifndef IQ_DECODE_TILE
+#define IQ_DECODE_TILE 128
 #endif
 #ifndef IQ_DECODE_MINB
 #define IQ_DECODE_MINB 2
 #endif
-#define IQ_DECODE_CFG 1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB
-#define IQ_MULTI_CFG 4, 4, 1, 3, 2
+#define IQ_DECODE_CFG 1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB, IQ_DECODE_TILE
+#define IQ_MULTI_CFG 4, 4, 1, 3, 2, 64
 
 // Tiles of every unit, in unit order: unit u = (b, kv head, query tile).
-void unit_tiles(const iq_cache* c, int rep, int nq, int causal, int gt, int nqt, int* tiles) {
+void unit_tiles(const iq_cache* c, int rep, int nq, int causal, int gt, int nqt, int tile, int* tiles) {
   for (int b = 0; b < c->batch; ++b)
     for (int h = 0; h < c->kv_heads; ++h)
       for (int qt = 0; qt < nqt; ++qt) {
         const int T = c->lens[b];
         int limit = T;
         if (causal) limit = T - nq + std::min(qt * gt + gt - 1, rep * nq - 1) / rep + 1;
-        tiles[(b * c->kv_heads + h) * nqt + qt] = (limit + TILE - 1) / TILE;
+        tiles[(b * c->kv_heads + h) * nqt + qt] = (limit + tile - 1) / tile;
       }
 }
 
@@ -887,13 +906,14 @@ int make_plan(const iq_cache* c, int q_heads, int nq, int causal, Plan* pl, cons
   pl->nt = rows <= 8 ? 1 : 4;
   pl->gt = 8 * pl->nt;
   pl->nqt = (rows + pl->gt - 1) / pl->gt;
+  pl->tile = pl->nt == 1 ? Cfg<IQ_DECODE_CFG>::TILE : Cfg<IQ_MULTI_CFG>::TILE;
   pl->units = static_cast<size_t>(c->batch) * c->kv_heads * pl->nqt;
   pl->launches = static_cast<int>((pl->units + UNIT_CAP - 1) / UNIT_CAP);
   if (pl->launches > kMaxLaunches) return fail(IQ_ERR_UNSUPPORTED, "too many query tiles for one call");
   const int bps = pl->nt == 1 ? blocks_per_sm<IQ_DECODE_CFG>() : blocks_per_sm<IQ_MULTI_CFG>();
   const long long slots_hw = static_cast<long long>(num_sms()) * bps;
   int max_tiles = 0;
-  for (int b = 0; b < c->batch; ++b) max_tiles = std::max(max_tiles, (static_cast<int>(c->lens[b]) + TILE - 1) / TILE);
+  for (int b = 0; b < c->batch; ++b) max_tiles = std::max(max_tiles, (static_cast<int>(c->lens[b]) + pl->tile - 1) / pl->tile);
   pl->slots = 0;
   for (int l = 0; l < pl->launches; ++l) {
     const size_t u0 = static_cast<size_t>(l) * UNIT_CAP;
@@ -951,11 +971,11 @@ int validate(const iq_cache* c, const uint16_t* q, int q_heads, int nq, int caus
   return IQ_OK;
 }
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_>
 int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStream_t s) {
-  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB>;
-  blocks_per_sm<NT, DS, STREAMS, NSTAGE, MINB>();  // sets the shared-memory attribute once
-  attend_kernel<NT, DS, STREAMS, NSTAGE, MINB><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
+  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>;
+  blocks_per_sm<NT, DS, STREAMS, NSTAGE, MINB, TILE_>();  // sets the shared-memory attribute once
+  attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
   IQ_CUDA(cudaGetLastError());
   return IQ_OK;
 }
@@ -996,7 +1016,7 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   if (workspace_bytes < bound.bytes) return fail(IQ_ERR_WORKSPACE, "workspace smaller than iq_attend_workspace()");
   static thread_local std::vector<int> tiles;
   tiles.assign(bound.units, 0);
-  unit_tiles(c, q_heads / c->kv_heads, n_queries, causal, bound.gt, bound.nqt, tiles.data());
+  unit_tiles(c, q_heads / c->kv_heads, n_queries, causal, bound.gt, bound.nqt, bound.tile, tiles.data());
   Plan pl;
   st = make_plan(c, q_heads, n_queries, causal, &pl, tiles.data());
   if (st != IQ_OK) return st;
@@ -1007,7 +1027,7 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kKWords),
                               static_cast<cuuint64_t>(c->batch) * c->kv_heads * c->capacity};
   const cuuint64_t strides[1] = {kKWords * 4};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKWords), static_cast<cuuint32_t>(TILE)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKWords), static_cast<cuuint32_t>(pl.tile)};
   const cuuint32_t estr[2] = {1, 1};
   CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, c->k_codes, dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
