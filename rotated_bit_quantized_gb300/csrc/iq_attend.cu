@@ -431,23 +431,16 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THR
       const float b0 = fmaf(-KOFFSET, s0, pick_bf16(kbi0, Gr));
       const float b1 = fmaf(-KOFFSET, s1, pick_bf16(kbi1, Gr));
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        if constexpr (DS == 1) {
-          if (gi == 0) {
-            sc[j][0] = s0 * acc[j][0]; sc[j][1] = s0 * acc[j][1];
-            sc[j][2] = s1 * acc[j][2]; sc[j][3] = s1 * acc[j][3];
-          } else {
-            sc[j][0] = fmaf(s0, acc[j][0], sc[j][0]); sc[j][1] = fmaf(s0, acc[j][1], sc[j][1]);
-            sc[j][2] = fmaf(s1, acc[j][2], sc[j][2]); sc[j][3] = fmaf(s1, acc[j][3], sc[j][3]);
-          }
-          sc[j][0] = fmaf(b0, qsr[gi][j][0], sc[j][0]); sc[j][1] = fmaf(b0, qsr[gi][j][1], sc[j][1]);
-          sc[j][2] = fmaf(b1, qsr[gi][j][0], sc[j][2]); sc[j][3] = fmaf(b1, qsr[gi][j][1], sc[j][3]);
+      for (int j = 0; j < NT; ++j) {  // this warp's groups, summed in group order
+        if (gi == 0) {
+          sc[j][0] = s0 * acc[j][0]; sc[j][1] = s0 * acc[j][1];
+          sc[j][2] = s1 * acc[j][2]; sc[j][3] = s1 * acc[j][3];
         } else {
-          sc[j][0] = fmaf(s0, acc[j][0], b0 * qsr[gi][j][0]);
-          sc[j][1] = fmaf(s0, acc[j][1], b0 * qsr[gi][j][1]);
-          sc[j][2] = fmaf(s1, acc[j][2], b1 * qsr[gi][j][0]);
-          sc[j][3] = fmaf(s1, acc[j][3], b1 * qsr[gi][j][1]);
+          sc[j][0] = fmaf(s0, acc[j][0], sc[j][0]); sc[j][1] = fmaf(s0, acc[j][1], sc[j][1]);
+          sc[j][2] = fmaf(s1, acc[j][2], sc[j][2]); sc[j][3] = fmaf(s1, acc[j][3], sc[j][3]);
         }
+        sc[j][0] = fmaf(b0, qsr[gi][j][0], sc[j][0]); sc[j][1] = fmaf(b0, qsr[gi][j][1], sc[j][1]);
+        sc[j][2] = fmaf(b1, qsr[gi][j][0], sc[j][2]); sc[j][3] = fmaf(b1, qsr[gi][j][1], sc[j][3]);
       }
     }
     if constexpr (DS > 1) {  // sum the group partials of the DS warps, in group order
@@ -869,9 +862,12 @@ int blocks_per_sm() {
 // Decode (<= 8 query rows per kv head): one warp owns all four groups; four
 // token streams per CTA, two CTAs per SM, two 128-token stages (measured best:
 // more streams per CTA make the warps wait on one shared ring; 64-token stages
-// cost more handshakes per byte).  Verify /
-// prefill (more rows): 32-row query tiles, a warp per 64-dim group, one token
-// stream, two CTAs per SM.
+// cost more handshakes per byte; a consumer warp that issues the refills
+// itself instead of a producer warp was slower).  Verify / prefill (more
+// rows): 16-row query tiles, two warps per token stream (two 64-dim groups
+// each, partial scores summed through shared memory), two streams per CTA, two
+// CTAs per SM, two 128-token stages (measured best among 8/16/32-row tiles and
+// one/two/four warps per stream).
 #ifndef IQ_DECODE_STREAMS
 #define IQ_DECODE_STREAMS 4
 #endif
@@ -885,7 +881,25 @@ int blocks_per_sm() {
 #define IQ_DECODE_MINB 2
 #endif
 #define IQ_DECODE_CFG 1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB, IQ_DECODE_TILE
-#define IQ_MULTI_CFG 4, 4, 1, 3, 2, 64
+#ifndef IQ_MULTI_NT
+#define IQ_MULTI_NT 2
+#endif
+#ifndef IQ_MULTI_DS
+#define IQ_MULTI_DS 2
+#endif
+#ifndef IQ_MULTI_STREAMS
+#define IQ_MULTI_STREAMS 2
+#endif
+#ifndef IQ_MULTI_STAGES
+#define IQ_MULTI_STAGES 2
+#endif
+#ifndef IQ_MULTI_MINB
+#define IQ_MULTI_MINB 2
+#endif
+#ifndef IQ_MULTI_TILE
+#define IQ_MULTI_TILE 128
+#endif
+#define IQ_MULTI_CFG IQ_MULTI_NT, IQ_MULTI_DS, IQ_MULTI_STREAMS, IQ_MULTI_STAGES, IQ_MULTI_MINB, IQ_MULTI_TILE
 
 // Tiles of every unit, in unit order: unit u = (b, kv head, query tile).
 void unit_tiles(const iq_cache* c, int rep, int nq, int causal, int gt, int nqt, int tile, int* tiles) {
@@ -903,7 +917,7 @@ void unit_tiles(const iq_cache* c, int rep, int nq, int causal, int gt, int nqt,
 int make_plan(const iq_cache* c, int q_heads, int nq, int causal, Plan* pl, const int* tiles) {
   const int rep = q_heads / c->kv_heads;
   const int rows = rep * nq;
-  pl->nt = rows <= 8 ? 1 : 4;
+  pl->nt = rows <= 8 ? 1 : IQ_MULTI_NT;
   pl->gt = 8 * pl->nt;
   pl->nqt = (rows + pl->gt - 1) / pl->gt;
   pl->tile = pl->nt == 1 ? Cfg<IQ_DECODE_CFG>::TILE : Cfg<IQ_MULTI_CFG>::TILE;
