@@ -25,8 +25,35 @@ from . import _abi
 from ._abi import IQ_STEP, IQCacheDesc, check, lib
 
 
-def _stream() -> ctypes.c_void_p:
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(device_index: int | None = None) -> ctypes.c_void_p:
+    """The current PyTorch stream of the device (the current device by default)."""
+    if _raw_stream is not None:
+        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device() if device_index is None else device_index))
+    return ctypes.c_void_p(torch.cuda.current_stream(device_index).cuda_stream)
+
+
+class _OnDevice:
+    """Make `index` the current device for a call, switching only when it is not."""
+
+    __slots__ = ("index", "prev")
+
+    def __init__(self, index: int):
+        self.index, self.prev = index, None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.index:
+            self.prev = cur
+            torch.cuda.set_device(self.index)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+            self.prev = None
 
 
 def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
@@ -78,8 +105,12 @@ class IQCache:
         self.batch, self.kv_heads, self.head_dim = batch, kv_heads, head_dim
         self.group_size, self.k_bits, self.v_bits = group_size, k_bits, v_bits
         self.device = torch.device(device or "cuda")
+        if self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        self._on = _OnDevice(self.device.index)
         self.lens = np.zeros(batch, dtype=np.int32)
         self._workspace = None
+        self._ws_need = {}
         self._alloc(capacity)
 
     # ---------------------------------------------------------------- storage
@@ -100,13 +131,22 @@ class IQCache:
         for name, n in zip(self.BUFFERS, sizes):
             assert getattr(self, name).numel() * getattr(self, name).element_size() == n
         self.capacity = capacity
+        self._desc, self._desc_lens = None, None
+        self._ws_need = {}
 
     def desc(self) -> IQCacheDesc:
-        d = IQCacheDesc(self.batch, self.kv_heads, self.head_dim, self.group_size, self.k_bits,
-                        self.v_bits, self.capacity)
-        for name in self.BUFFERS:
-            setattr(d, name, getattr(self, name).data_ptr())
-        d.lens = self.lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        """The C descriptor of this cache (built once per allocation and lengths array;
+        the library updates `lens` through it)."""
+        d = self._desc
+        if d is None or self._desc_lens is not self.lens:
+            d = IQCacheDesc(self.batch, self.kv_heads, self.head_dim, self.group_size, self.k_bits,
+                            self.v_bits, self.capacity)
+            for name in self.BUFFERS:
+                setattr(d, name, getattr(self, name).data_ptr())
+            if self.lens.dtype != np.int32 or not self.lens.flags["C_CONTIGUOUS"]:
+                raise ValueError("lens must be a contiguous int32 array")
+            d.lens = self.lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+            self._desc, self._desc_lens = d, self.lens
         return d
 
     @property
@@ -132,9 +172,10 @@ class IQCache:
     def _gather_from(self, src: "IQCache", src_of) -> None:
         m = np.ascontiguousarray(src_of, dtype=np.int32)
         ds, dd = src.desc(), self.desc()
-        with torch.cuda.device(self.device):
+        with self._on:
             check(lib().iq_cache_gather(ctypes.byref(ds), ctypes.byref(dd),
-                                        m.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _stream()),
+                                        m.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                        _stream(self.device.index)),
                   "iq_cache_gather")
         self.lens[:] = np.ctypeslib.as_array(dd.lens, shape=(self.batch,))
 
@@ -164,9 +205,10 @@ class IQCache:
         if need > self.capacity:  # grow by ceil(n/256)*256 like the page, or more if needed
             self.reserve(max(need, self.capacity + int(math.ceil(n / IQ_STEP)) * IQ_STEP))
         d = self.desc()
-        with torch.cuda.device(self.device):
+        with self._on:
             check(lib().iq_cache_append(ctypes.byref(d), _ptr(keys), _ptr(values), n,
-                                        _ptr(rotation.blocks_bf16), _stream()), "iq_cache_append")
+                                        _ptr(rotation.blocks_bf16), _stream(self.device.index)),
+                  "iq_cache_append")
 
     def trim(self, n) -> np.ndarray:
         """Drop up to n tokens from each sequence; returns the counts dropped (page `trim`)."""
@@ -178,11 +220,17 @@ class IQCache:
         return out
 
     def workspace_bytes(self, q_heads: int, n_queries: int) -> int:
-        nb = ctypes.c_size_t()
-        d = self.desc()
-        check(lib().iq_attend_workspace(ctypes.byref(d), q_heads, n_queries, ctypes.byref(nb)),
-              "iq_attend_workspace")
-        return nb.value
+        """Workspace bytes iq_attend needs for this cache's batch (independent of the lengths)."""
+        key = (self.batch, self.kv_heads, q_heads, n_queries)
+        nb = self._ws_need.get(key)
+        if nb is None:
+            c = ctypes.c_size_t()
+            d = self.desc()
+            with self._on:
+                check(lib().iq_attend_workspace(ctypes.byref(d), q_heads, n_queries, ctypes.byref(c)),
+                      "iq_attend_workspace")
+            nb = self._ws_need[key] = c.value
+        return nb
 
     def attend(self, q: torch.Tensor, rotation: Rotation, causal: bool = False, scale: float | None = None,
                out: torch.Tensor | None = None, out_dtype=torch.bfloat16) -> torch.Tensor:
@@ -205,10 +253,10 @@ class IQCache:
         if self._workspace is None or self._workspace.numel() < need:
             self._workspace = torch.empty(max(need, 1 << 20), dtype=torch.uint8, device=self.device)
         d = self.desc()
-        with torch.cuda.device(self.device):
+        with self._on:
             check(lib().iq_attend(ctypes.byref(d), _ptr(q), Hq, L, float(scale), 1 if causal else 0,
                                   _ptr(rotation.blocks_bf16), _ptr(out), out_f32, _ptr(self._workspace),
-                                  self._workspace.numel(), _stream()), "iq_attend")
+                                  self._workspace.numel(), _stream(self.device.index)), "iq_attend")
         return out
 
     def device_status(self) -> int:
@@ -216,7 +264,8 @@ class IQCache:
         if self._workspace is None:
             return 0
         st = ctypes.c_int()
-        code = lib().iq_read_status(_ptr(self._workspace), _stream(), ctypes.byref(st))
+        with self._on:
+            code = lib().iq_read_status(_ptr(self._workspace), _stream(self.device.index), ctypes.byref(st))
         if code not in (_abi.IQ_OK, _abi.IQ_ERR_DEVICE):
             check(code, "iq_read_status")
         return st.value

@@ -48,6 +48,14 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
 
 __device__ __forceinline__ float round_bf16(float x) { return bf16_to_f32(f32_to_bf16_bits(x)); }
 
+// The same rounding by the conversion instruction (finite inputs; NaN comes
+// back as the canonical bf16 NaN).
+__device__ __forceinline__ float round_bf16_rn(float x) {
+  unsigned short h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
