@@ -22,16 +22,18 @@
 //  * a producer warp streams the tiles (packed K codes by a 2-D tensor copy with
 //    128-byte swizzle; packed V codes and the four scale/bias rows by 1-D bulk
 //    copies) into a multi-stage shared-memory ring guarded by mbarriers, running
-//    ahead across unit boundaries;
+//    ahead across unit boundaries; its warpgroup hands most of its registers
+//    to the consumer warps;
 //  * consumer warps unpack codes in registers with bit tricks and run m16n8k16
-//    tensor-core MMAs: S = (128 + K_codes) . q (bf16, per 64-dim group, fp32
-//    accumulate), folded with the group scale and (bias - 128 scale) on CUDA
+//    tensor-core MMAs: S = (64 + K_codes) . q (fp16, per 64-dim group, fp32
+//    accumulate), folded with the group scale and (bias - 64 scale) on CUDA
 //    cores; online
 //    softmax in fp32 with a lazily moving reference max; O^T += (V_codes - 4)^T
 //    . (P * s_v) with P transposed in registers by movmatrix; the value bias
 //    term sum_t p_t (b_t + 4 s_t) on CUDA cores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -45,8 +47,11 @@
 namespace iq {
 namespace attn {
 
-// Shared-memory stage of TILE tokens: packed K codes (swizzled), packed V
-// codes (+ pad for the field window) and the four scale/bias rows.
+// Shared-memory stage of TILE tokens: the four scale/bias rows, packed K
+// codes (128-byte swizzled, 1024-byte aligned) and packed V codes, 256 bytes
+// per token with no padding.  The value-field window reads at most 4 bytes
+// past a stage's V rows, which land in the next stage or in the area that
+// follows the ring.
 template <int TILE_>
 struct Tiling {
   static constexpr int TILE = TILE_;               // tokens per pipeline stage
@@ -54,15 +59,16 @@ struct Tiling {
   static constexpr int K_BYTES = TILE * 128;       // TILE rows x 128 B, 128-byte swizzle
   static constexpr int V_BYTES = TILE * 96;        // TILE rows x 96 B
   static constexpr int SB_BYTES = TILE * 8;        // TILE rows x 4 bf16
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = K_BYTES;
-  static constexpr int OFF_KS = OFF_V + V_BYTES + 128;
+  static constexpr int OFF_KS = 0;
   static constexpr int OFF_KB = OFF_KS + SB_BYTES;
   static constexpr int OFF_VS = OFF_KB + SB_BYTES;
   static constexpr int OFF_VB = OFF_VS + SB_BYTES;
-  static constexpr int STAGE = (OFF_VB + SB_BYTES + 1023) / 1024 * 1024;  // multiple of the swizzle atom
+  static constexpr int OFF_K = OFF_VB + SB_BYTES;
+  static constexpr int OFF_V = OFF_K + K_BYTES;
+  static constexpr int STAGE = OFF_V + V_BYTES;
+  static_assert(OFF_K % 1024 == 0 && STAGE % 1024 == 0, "swizzle atom alignment");
   static constexpr uint32_t STAGE_TX = K_BYTES + V_BYTES + 4 * SB_BYTES;
-  static_assert(TILE % 16 == 0 && TILE <= 256 && 256 % TILE == 0, "tile must divide the capacity granule");
+  static_assert(TILE % 32 == 0 && TILE <= 256 && 256 % TILE == 0, "tile must divide the capacity granule");
 };
 constexpr int UNIT_CAP = 1024;   // units per launch (their tile prefix travels by value)
 constexpr int MIN_TILES_PER_CTA = 8;
@@ -120,18 +126,43 @@ __device__ __forceinline__ float pick_bf16(uint2 v, int G) {
   return bf16_to_f32((G & 1) ? (w >> 16) : (w & 0xFFFFu));
 }
 
-// Key codes enter the q.K product as bf16 values 128 + c (the code ORed into
-// the mantissa of 128.0; exact): the 128 * sum(q'') offset is removed in the
-// per-token fold, where it becomes part of the bias (b - 128 s).
-constexpr float KOFFSET = 128.0f;
+// Key codes enter the q.K product as fp16 values 64 + c: a nibble ORed into
+// bits 4..7 of the half 0x5400 (64.0, mantissa step 1 from bit 4 up) is
+// exactly 64 + c.  The 64 * sum(q'') offset is removed in the per-token fold,
+// where it becomes part of the bias (b - 64 s).  The query operand is q''
+// converted to fp16 (exact for 2^-14 <= |q''| < 65504).
+constexpr float KOFFSET = 64.0f;
 
-// 4-bit word (8 codes, LSB first) -> bf16x2 pairs 128+(c0,c4) (c1,c5) (c2,c6) (c3,c7)
-__device__ __forceinline__ void unpack_k4(uint32_t w, uint32_t* r) {
-  constexpr uint32_t MAGIC = 0x43004300u;  // 128.0 in each half
-  r[0] = and_or(w, 0x000F000Fu, MAGIC);
-  r[1] = and_or(w >> 4, 0x000F000Fu, MAGIC);
-  r[2] = and_or(w >> 8, 0x000F000Fu, MAGIC);
-  r[3] = and_or(w >> 12, 0x000F000Fu, MAGIC);
+// The 16 codes of two consecutive words (dims 0..7 in w0, 8..15 in w1) ->
+// eight fp16x2 registers 64 + (c_a, c_b); register m holds the dims
+// k_pair(m, 0..1).  Two byte permutes bring the third and fourth nibbles of each
+// byte pair down; four shifts by 4 (multiplies, off the logic pipe) lift the
+// low nibbles to bits 4..7.
+__host__ __device__ constexpr int k_pair(int m, int h) {
+  // {0,4} {1,5} {8,12} {9,13} {2,10} {3,11} {6,14} {7,15}
+  return h == 0 ? (m < 4 ? (m & 1) + 8 * (m >> 1) : (m == 4 ? 2 : m == 5 ? 3 : m)) : k_pair(m, 0) + (m < 4 ? 4 : 8);
+}
+static_assert(k_pair(0, 1) == 4 && k_pair(3, 0) == 9 && k_pair(3, 1) == 13 && k_pair(4, 1) == 10 &&
+                  k_pair(6, 0) == 6 && k_pair(7, 1) == 15 && k_pair(2, 0) == 8,
+              "register -> dim map");
+__device__ __forceinline__ void unpack_k16(uint32_t w0, uint32_t w1, uint32_t* r) {
+  constexpr uint32_t MAGIC = 0x54005400u;  // 64.0 in each half
+  constexpr uint32_t MASK = 0x00F000F0u;
+  const uint32_t x = __byte_perm(w0, w1, 0x0501);  // bytes w0.b1 (nibbles 2, 3), w1.b1
+  const uint32_t y = __byte_perm(w0, w1, 0x0703);  // bytes w0.b3 (nibbles 6, 7), w1.b3
+  r[0] = and_or(w0 * 16u, MASK, MAGIC);  // (0, 4)
+  r[1] = and_or(w0, MASK, MAGIC);        // (1, 5)
+  r[2] = and_or(w1 * 16u, MASK, MAGIC);  // (8, 12)
+  r[3] = and_or(w1, MASK, MAGIC);        // (9, 13)
+  r[4] = and_or(x * 16u, MASK, MAGIC);   // (2, 10)
+  r[5] = and_or(x, MASK, MAGIC);         // (3, 11)
+  r[6] = and_or(y * 16u, MASK, MAGIC);   // (6, 14)
+  r[7] = and_or(y, MASK, MAGIC);         // (7, 15)
+}
+
+// bf16 bits -> fp16 bits (round to nearest; exact for normal fp16 values)
+__device__ __forceinline__ uint32_t bf16_to_f16_bits(uint32_t bits16) {
+  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(bf16_to_f32(bits16))));
 }
 
 // 3-bit code at bit `L` (0..7) of each 16-bit half of x -> fp16x2 (code - 4)
@@ -159,22 +190,36 @@ __device__ __forceinline__ void unpack_v3_pair(uint32_t fa, uint32_t fb, uint32_
   h[7] = dq3<5>(x2);
 }
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
 struct Cfg : Tiling<TILE_> {
   using Tiling<TILE_>::STAGE;
   static constexpr int GT = 8 * NT;            // query rows per unit
   static constexpr int GPW = 4 / DS;           // 64-dim groups per consumer warp
   static constexpr int CW = DS * STREAMS;      // consumer warps
-  static constexpr int THREADS = (CW + 1) * 32;  // + one producer warp
+  // CW consumer warps (a multiple of 4: whole warpgroups), then one producer
+  // warpgroup whose first warp streams the tiles; registers move from the
+  // producer warpgroup to the consumers (setmaxnreg)
+  static constexpr int THREADS = (CW + 4) * 32;
+  static constexpr int LAUNCH_REGS = (65536 / (MINB * THREADS)) / 8 * 8;
+  static constexpr int PRODUCER_REGS = 24;
+  static constexpr int CONSUMER_REGS =
+      ((65536 / MINB - 128 * PRODUCER_REGS) / (CW * 32)) / 8 * 8 > 248
+          ? 248
+          : ((65536 / MINB - 128 * PRODUCER_REGS) / (CW * 32)) / 8 * 8;
+  static_assert(CW % 4 == 0, "consumer warps form whole warpgroups");
+  static_assert(CONSUMER_REGS >= LAUNCH_REGS && PRODUCER_REGS <= LAUNCH_REGS, "register split");
+  static_assert(MINB * (CW * 32 * CONSUMER_REGS + 128 * PRODUCER_REGS) <= 65536, "register file");
+  // the rotated queries (unit start) and the stream-merge buffer (unit end) share one area
+  static constexpr int OBUF_BYTES = STREAMS > 1 ? GT * 256 * 4 : 0;
+  static constexpr int QS_BYTES = GT * 512 > OBUF_BYTES ? GT * 512 : OBUF_BYTES;
   static constexpr int OFF_QS = NSTAGE * STAGE;
-  static constexpr int OFF_QSUM = OFF_QS + GT * 512;
+  static constexpr int OFF_OBUF = OFF_QS;
+  static constexpr int OFF_QSUM = OFF_QS + QS_BYTES;
   static constexpr int OFF_MBUF = OFF_QSUM + GT * 16;
   static constexpr int OFF_LBUF = OFF_MBUF + STREAMS * GT * 4;
   static constexpr int OFF_XBUF = OFF_LBUF + STREAMS * GT * 4;
-  static constexpr int XBUF_BYTES = DS > 1 ? STREAMS * 2 * DS * NT * 32 * 16 : 0;
-  static constexpr int OFF_OBUF = OFF_XBUF + XBUF_BYTES;
-  static constexpr int OBUF_BYTES = STREAMS > 1 ? GT * 256 * 4 : 0;  // streams merge in turn
-  static constexpr int OFF_QB = OFF_OBUF + OBUF_BYTES;
+  static constexpr int XBUF_BYTES = DS > 1 ? STREAMS * 2 * 2 * DS * NT * 32 * 16 : 0;  // x2 parities x2 sub-tiles
+  static constexpr int OFF_QB = OFF_XBUF + XBUF_BYTES;
   static constexpr int QB_BYTES = DS * GPW * 4 * NT * 32 * 8;       // q'' MMA B fragments
   static constexpr int OFF_BAR = OFF_QB + QB_BYTES;
   static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8;
@@ -183,10 +228,10 @@ struct Cfg : Tiling<TILE_> {
   static_assert(4 % DS == 0, "shape");
 };
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_>
-__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THREADS, MINB)
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
+__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>::THREADS, MINB)
     attend_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap kmap) {
-  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>;
+  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>;
   constexpr int TILE = C::TILE, SUBS = C::SUBS, STAGE = C::STAGE;
   constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_KS = C::OFF_KS, OFF_KB = C::OFF_KB;
   constexpr int OFF_VS = C::OFF_VS, OFF_VB = C::OFF_VB, V_BYTES = C::V_BYTES, SB_BYTES = C::SB_BYTES;
@@ -234,10 +279,14 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THR
   __syncthreads();
 
   // ------------------------------------------------------------ producer
-  // One warp (lane 0) streams the CTA's tiles through the ring, refilling a
-  // stage as soon as every consumer warp has released it.
-  if (warp == CW) {
-    if (lane == 0) {
+  // One lane streams the CTA's tiles through the ring, refilling a stage as
+  // soon as every consumer warp has released it: packed K codes by a 2-D
+  // tensor copy (128-byte swizzle), packed V codes and the four scale/bias rows
+  // by 1-D bulk copies, all counted on the stage's full barrier; L2
+  // evict-first (the cache is read once).
+  if (warp >= CW) {
+    setmaxnreg_dec<C::PRODUCER_REGS>();
+    if (warp == CW && lane == 0) {
       const uint64_t pol = policy_evict_first();
       int u = u0;
       long long k = 0;
@@ -250,16 +299,15 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THR
           atomicOr(p.status, 1u);
           break;
         }
-        uint8_t* sb = smem + st * STAGE;
-        const long long row0 = (static_cast<long long>(bb) * p.kv_heads + hh) * p.cap +
-                               (gt - p.prefix[u]) * TILE;
+        uint8_t* sbp = smem + st * STAGE;
+        const long long row0 = (static_cast<long long>(bb) * p.kv_heads + hh) * p.cap + (gt - p.prefix[u]) * TILE;
         mbar_arrive_expect_tx(&full[st], STAGE_TX);
-        tensor2d_g2s(sb + OFF_K, &kmap, 0, static_cast<int>(row0), &full[st], pol);
-        bulk_g2s(sb + OFF_V, p.v_codes + row0 * kVWords, V_BYTES, &full[st], pol);
-        bulk_g2s(sb + OFF_KS, p.k_scales + row0 * kGroups, SB_BYTES, &full[st], pol);
-        bulk_g2s(sb + OFF_KB, p.k_biases + row0 * kGroups, SB_BYTES, &full[st], pol);
-        bulk_g2s(sb + OFF_VS, p.v_scales + row0 * kGroups, SB_BYTES, &full[st], pol);
-        bulk_g2s(sb + OFF_VB, p.v_biases + row0 * kGroups, SB_BYTES, &full[st], pol);
+        tensor2d_g2s(sbp + OFF_K, &kmap, 0, static_cast<int>(row0), &full[st], pol);
+        bulk_g2s(sbp + OFF_V, p.v_codes + row0 * kVWords, V_BYTES, &full[st], pol);
+        bulk_g2s(sbp + OFF_KS, p.k_scales + row0 * kGroups, SB_BYTES, &full[st], pol);
+        bulk_g2s(sbp + OFF_KB, p.k_biases + row0 * kGroups, SB_BYTES, &full[st], pol);
+        bulk_g2s(sbp + OFF_VS, p.v_scales + row0 * kGroups, SB_BYTES, &full[st], pol);
+        bulk_g2s(sbp + OFF_VB, p.v_biases + row0 * kGroups, SB_BYTES, &full[st], pol);
       }
       // never leave with copies in flight: wait for the last tile issued to each stage
       for (long long s = 0; s < NSTAGE && s < k; ++s) {
@@ -269,6 +317,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THR
     }
     return;
   }
+  setmaxnreg_inc<C::CONSUMER_REGS>();
 
   // ------------------------------------------------------------ consumers
   const int cw = warp, stream = cw / DS, dg = cw % DS;
@@ -335,16 +384,18 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THR
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       float s = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s += bf16_to_f32(w[e] & 0xFFFFu) + bf16_to_f32(w[e] >> 16);
+      for (int e = 0; e < 4; ++e)  // sum of the fp16 operand values (the offset the fold removes)
+        s += __half2float(__ushort_as_half(static_cast<unsigned short>(bf16_to_f16_bits(w[e] & 0xFFFFu)))) +
+             __half2float(__ushort_as_half(static_cast<unsigned short>(bf16_to_f16_bits(w[e] >> 16))));
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       if ((lane & 7) == 0) qsum[r * 4 + (lane >> 3)] = s;
     }
     named_bar(1, NCT);
-    // q'' as bf16 MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].
-    // Thread t covers dims 64G+16t .. +15 of group G; register pair m of its
-    // unpacked codes holds dims (m, m+4) for m < 4 and (m+4, m+8) for m >= 4;
-    // k-step s uses pairs 2s (slots 2t,2t+1) and 2s+1.  Stream 0 writes them.
+    // q'' as fp16 MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].
+    // Thread t covers dims 64G+16t .. +15 of group G; register m of its
+    // unpacked codes holds the dims k_pair(m, 0), k_pair(m, 1); k-step s uses registers 2s
+    // (slots 2t,2t+1) and 2s+1.  Stream 0 writes them.
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
       const int Gr = dg * GPW + gi;
@@ -359,8 +410,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THR
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int m = 2 * s + h;
-              const int lo = m < 4 ? m : m + 4;
-              h2[h] = static_cast<uint32_t>(qrow[lo]) | (static_cast<uint32_t>(qrow[lo + 4]) << 16);
+              h2[h] = bf16_to_f16_bits(qrow[k_pair(m, 0)]) | (bf16_to_f16_bits(qrow[k_pair(m, 1)]) << 16);
             }
             qbs[((Gr * 4 + s) * NT + j) * 32 + lane] = make_uint2(h2[0], h2[1]);
           }
@@ -393,108 +443,140 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THR
     }
   };
 
-  // ---- one 16-token sub-tile.  FULL: every token is inside the unit's range
-  // and visible to every row (no masking work at all).
-  auto subtile = [&](auto full_tag, int sub, int tokbase, uint32_t sb) {
+  // ---- N (1 or 2) of this warp's 16-token sub-tiles of one stage, processed
+  // together: both score products, one softmax step, both value products (two
+  // independent chains per phase, one vote and one query-fragment load per
+  // k-step for both).  FULL: every token of the N sub-tiles is inside the
+  // unit's range and visible to every row (no masking work at all).
+  auto subtiles = [&](auto n_tag, auto full_tag, const int (&subs)[2], const int (&tokbase)[2], uint32_t sb) {
+    constexpr int N = decltype(n_tag)::value;
     constexpr bool FULL = decltype(full_tag)::value;
-    const int rr0 = sub * 16 + rS0, rr1 = rr0 + 8;
-    const uint2 ksc0 = lds64(sb + OFF_KS + rr0 * 8), ksc1 = lds64(sb + OFF_KS + rr1 * 8);
-    const uint2 kbi0 = lds64(sb + OFF_KB + rr0 * 8), kbi1 = lds64(sb + OFF_KB + rr1 * 8);
+    int rr0[N], rr1[N];
+    uint2 ksc0[N], ksc1[N], kbi0[N], kbi1[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      rr0[n] = subs[n] * 16 + rS0;
+      rr1[n] = rr0[n] + 8;
+      ksc0[n] = lds64(sb + OFF_KS + rr0[n] * 8);
+      ksc1[n] = lds64(sb + OFF_KS + rr1[n] * 8);
+      kbi0[n] = lds64(sb + OFF_KB + rr0[n] * 8);
+      kbi1[n] = lds64(sb + OFF_KB + rr1[n] * 8);
+    }
 
-    // scores: per group, S_G = (128 + codes) . q'' (fp32), folded with scale/bias
-    float sc[NT][4];
+    // scores: per group, S_G = (64 + codes) . q'' (fp32), folded with scale/bias
+    float sc[N][NT][4];
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
       const int Gr = dg * GPW + gi;
       const uint32_t chunk16 = 2 * Gr + (t >> 1);
-      const uint32_t a0 = sb + OFF_K + rr0 * 128 + ((chunk16 ^ (rr0 & 7)) << 4) + kswz;
-      const uint32_t a1 = sb + OFF_K + rr1 * 128 + ((chunk16 ^ (rr1 & 7)) << 4) + kswz;
-      const uint2 w0 = lds64(a0), w1 = lds64(a1);
-      uint32_t RA[8], RB[8];
-      unpack_k4(w0.x, RA);
-      unpack_k4(w0.y, RA + 4);
-      unpack_k4(w1.x, RB);
-      unpack_k4(w1.y, RB + 4);
-      float acc[NT][4];
+      uint32_t RA[N][8], RB[N][8];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+      for (int n = 0; n < N; ++n) {
+        const uint32_t a0 = sb + OFF_K + rr0[n] * 128 + ((chunk16 ^ (rr0[n] & 7)) << 4) + kswz;
+        const uint32_t a1 = sb + OFF_K + rr1[n] * 128 + ((chunk16 ^ (rr1[n] & 7)) << 4) + kswz;
+        const uint2 w0 = lds64(a0), w1 = lds64(a1);
+        unpack_k16(w0.x, w0.y, RA[n]);
+        unpack_k16(w1.x, w1.y, RB[n]);
+      }
+      float acc[N][NT][4];
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint32_t A[4] = {RA[2 * s], RB[2 * s], RA[2 * s + 1], RB[2 * s + 1]};
+      for (int n = 0; n < N; ++n)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) acc[n][j][0] = acc[n][j][1] = acc[n][j][2] = acc[n][j][3] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           const uint2 bq = qbs[((Gr * 4 + s) * NT + j) * 32 + lane];
-          mma_bf16(acc[j], A, bq.x, bq.y);
-        }
-      }
-      const float s0 = pick_bf16(ksc0, Gr), s1 = pick_bf16(ksc1, Gr);
-      const float b0 = fmaf(-KOFFSET, s0, pick_bf16(kbi0, Gr));
-      const float b1 = fmaf(-KOFFSET, s1, pick_bf16(kbi1, Gr));
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {  // this warp's groups, summed in group order
-        if (gi == 0) {
-          sc[j][0] = s0 * acc[j][0]; sc[j][1] = s0 * acc[j][1];
-          sc[j][2] = s1 * acc[j][2]; sc[j][3] = s1 * acc[j][3];
-        } else {
-          sc[j][0] = fmaf(s0, acc[j][0], sc[j][0]); sc[j][1] = fmaf(s0, acc[j][1], sc[j][1]);
-          sc[j][2] = fmaf(s1, acc[j][2], sc[j][2]); sc[j][3] = fmaf(s1, acc[j][3], sc[j][3]);
+          for (int n = 0; n < N; ++n) {
+            const uint32_t A[4] = {RA[n][2 * s], RB[n][2 * s], RA[n][2 * s + 1], RB[n][2 * s + 1]};
+            mma_f16(acc[n][j], A, bq.x, bq.y);
+          }
         }
-        sc[j][0] = fmaf(b0, qsr[gi][j][0], sc[j][0]); sc[j][1] = fmaf(b0, qsr[gi][j][1], sc[j][1]);
-        sc[j][2] = fmaf(b1, qsr[gi][j][0], sc[j][2]); sc[j][3] = fmaf(b1, qsr[gi][j][1], sc[j][3]);
+#pragma unroll
+      for (int n = 0; n < N; ++n) {
+        const float s0 = pick_bf16(ksc0[n], Gr), s1 = pick_bf16(ksc1[n], Gr);
+        const float b0 = fmaf(-KOFFSET, s0, pick_bf16(kbi0[n], Gr));
+        const float b1 = fmaf(-KOFFSET, s1, pick_bf16(kbi1[n], Gr));
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {  // this warp's groups, summed in group order
+          float* c = sc[n][j];
+          const float* a = acc[n][j];
+          if (gi == 0) {
+            c[0] = s0 * a[0]; c[1] = s0 * a[1]; c[2] = s1 * a[2]; c[3] = s1 * a[3];
+          } else {
+            c[0] = fmaf(s0, a[0], c[0]); c[1] = fmaf(s0, a[1], c[1]);
+            c[2] = fmaf(s1, a[2], c[2]); c[3] = fmaf(s1, a[3], c[3]);
+          }
+          c[0] = fmaf(b0, qsr[gi][j][0], c[0]); c[1] = fmaf(b0, qsr[gi][j][1], c[1]);
+          c[2] = fmaf(b1, qsr[gi][j][0], c[2]); c[3] = fmaf(b1, qsr[gi][j][1], c[3]);
+        }
       }
     }
     if constexpr (DS > 1) {  // sum the group partials of the DS warps, in group order
-      float4* xb = xbuf + (stream * 2 + xpar) * DS * NT * 32;
+      float4* xb = xbuf + (stream * 2 + xpar) * 2 * DS * NT * 32;
 #pragma unroll
-      for (int j = 0; j < NT; ++j)
-        xb[(dg * NT + j) * 32 + lane] = make_float4(sc[j][0], sc[j][1], sc[j][2], sc[j][3]);
+      for (int n = 0; n < N; ++n)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+          xb[((n * DS + dg) * NT + j) * 32 + lane] = make_float4(sc[n][j][0], sc[n][j][1], sc[n][j][2], sc[n][j][3]);
       named_bar(2 + stream, DS * 32);
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        float4 a = xb[j * 32 + lane];
+      for (int n = 0; n < N; ++n)
 #pragma unroll
-        for (int d = 1; d < DS; ++d) {
-          const float4 v = xb[(d * NT + j) * 32 + lane];
-          a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        for (int j = 0; j < NT; ++j) {
+          float4 a = xb[(n * DS * NT + j) * 32 + lane];
+#pragma unroll
+          for (int d = 1; d < DS; ++d) {
+            const float4 v = xb[((n * DS + d) * NT + j) * 32 + lane];
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+          }
+          sc[n][j][0] = a.x; sc[n][j][1] = a.y; sc[n][j][2] = a.z; sc[n][j][3] = a.w;
         }
-        sc[j][0] = a.x; sc[j][1] = a.y; sc[j][2] = a.z; sc[j][3] = a.w;
-      }
       xpar ^= 1;
     }
 
     // mask (ragged tail, causal): only on sub-tiles that need it
-    bool valid[NT][4];
+    bool valid[N][NT][4];
     if constexpr (!FULL) {
-      const int tok0 = tokbase + rS0, tok1 = tok0 + 8;
-      const bool in0 = tok0 < limit, in1 = tok1 < limit;
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        valid[j][0] = in0 && tok0 <= qpos[j][0];
-        valid[j][1] = in0 && tok0 <= qpos[j][1];
-        valid[j][2] = in1 && tok1 <= qpos[j][0];
-        valid[j][3] = in1 && tok1 <= qpos[j][1];
+      for (int n = 0; n < N; ++n) {
+        const int tok0 = tokbase[n] + rS0, tok1 = tok0 + 8;
+        const bool in0 = tok0 < limit, in1 = tok1 < limit;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[j][e] = valid[j][e] ? sc[j][e] : NEG_INF;
+        for (int j = 0; j < NT; ++j) {
+          valid[n][j][0] = in0 && tok0 <= qpos[j][0];
+          valid[n][j][1] = in0 && tok0 <= qpos[j][1];
+          valid[n][j][2] = in1 && tok1 <= qpos[j][0];
+          valid[n][j][3] = in1 && tok1 <= qpos[j][1];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[n][j][e] = valid[n][j][e] ? sc[n][j][e] : NEG_INF;
+        }
       }
     }
 
-    // online softmax with a lazily moving reference max
-    float x[NT][4];
+    // online softmax with a lazily moving reference max (one vote for the N sub-tiles)
+    float x[N][NT][4];
     bool trig = false;
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
+    for (int n = 0; n < N; ++n)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[j][e] = fmaf(sc[j][e], LOG2E, -msc[j][e & 1]);
-        trig |= !(x[j][e] <= TAU);
-      }
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          x[n][j][e] = fmaf(sc[n][j][e], LOG2E, -msc[j][e & 1]);
+          trig |= !(x[n][j][e] <= TAU);
+        }
     if (__any_sync(0xffffffffu, trig)) {
       float alpha[NT][2];
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          float mx = fmaxf(sc[j][e], sc[j][e + 2]);
+          float mx = fmaxf(sc[0][j][e], sc[0][j][e + 2]);
+#pragma unroll
+          for (int n = 1; n < N; ++n) mx = fmaxf(mx, fmaxf(sc[n][j][e], sc[n][j][e + 2]));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -519,65 +601,81 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THR
           }
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float m = msc[j][e & 1];
-          x[j][e] = fmaf(sc[j][e], LOG2E, m == NEG_INF ? 0.f : -m);
-        }
+        for (int n = 0; n < N; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float m = msc[j][e & 1];
+            x[n][j][e] = fmaf(sc[n][j][e], LOG2E, m == NEG_INF ? 0.f : -m);
+          }
       }
     }
-    float pr[NT][4];
+    float pr[N][NT][4];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
+    for (int n = 0; n < N; ++n)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pr[j][e] = ex2_approx(x[j][e]);
-      lrow[j][0] += pr[j][0] + pr[j][2];
-      lrow[j][1] += pr[j][1] + pr[j][3];
-    }
+      for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pr[n][j][e] = ex2_approx(x[n][j][e]);
+        lrow[j][0] += pr[n][j][0] + pr[n][j][2];
+        lrow[j][1] += pr[n][j][1] + pr[n][j][3];
+      }
 
     // values: O^T += (V_codes - 4)^T . (P * s_v); bias term on CUDA cores
-    const uint2 vsc0 = lds64(sb + OFF_VS + rr0 * 8), vsc1 = lds64(sb + OFF_VS + rr1 * 8);
-    const uint2 vbi0 = lds64(sb + OFF_VB + rr0 * 8), vbi1 = lds64(sb + OFF_VB + rr1 * 8);
-    const uint32_t vrow0 = sb + OFF_V + (sub * 16 + rV0) * 96;
-    const uint32_t vrow1 = sb + OFF_V + (sub * 16 + rV1) * 96;
-    const uint32_t vrow2 = vrow0 + 8 * 96;
-    const uint32_t vrow3 = vrow1 + 8 * 96;
+    uint2 vsc0[N], vsc1[N], vbi0[N], vbi1[N];
+    uint32_t vrow[N][4];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      vsc0[n] = lds64(sb + OFF_VS + rr0[n] * 8);
+      vsc1[n] = lds64(sb + OFF_VS + rr1[n] * 8);
+      vbi0[n] = lds64(sb + OFF_VB + rr0[n] * 8);
+      vbi1[n] = lds64(sb + OFF_VB + rr1[n] * 8);
+      vrow[n][0] = sb + OFF_V + (subs[n] * 16 + rV0) * 96;
+      vrow[n][1] = sb + OFF_V + (subs[n] * 16 + rV1) * 96;
+      vrow[n][2] = vrow[n][0] + 8 * 96;
+      vrow[n][3] = vrow[n][1] + 8 * 96;
+    }
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
       const int Gr = dg * GPW + gi;
-      const float vs0 = pick_bf16(vsc0, Gr), vs1 = pick_bf16(vsc1, Gr);
-      const float vb0 = fmaf(VCENTRE, vs0, pick_bf16(vbi0, Gr));
-      const float vb1 = fmaf(VCENTRE, vs1, pick_bf16(vbi1, Gr));
-      uint32_t bp[NT][2];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        float q0 = pr[j][0] * vs0, q1 = pr[j][1] * vs0, q2 = pr[j][2] * vs1, q3 = pr[j][3] * vs1;
-        if constexpr (FULL) {
-          bacc[gi][j][0] = fmaf(pr[j][0], vb0, fmaf(pr[j][2], vb1, bacc[gi][j][0]));
-          bacc[gi][j][1] = fmaf(pr[j][1], vb0, fmaf(pr[j][3], vb1, bacc[gi][j][1]));
-        } else {  // masked tokens may hold stale (even NaN) scales: select, never multiply
-          q0 = valid[j][0] ? q0 : 0.f;
-          q1 = valid[j][1] ? q1 : 0.f;
-          q2 = valid[j][2] ? q2 : 0.f;
-          q3 = valid[j][3] ? q3 : 0.f;
-          bacc[gi][j][0] += (valid[j][0] ? pr[j][0] * vb0 : 0.f) + (valid[j][2] ? pr[j][2] * vb1 : 0.f);
-          bacc[gi][j][1] += (valid[j][1] ? pr[j][1] * vb0 : 0.f) + (valid[j][3] ? pr[j][3] * vb1 : 0.f);
-        }
-        bp[j][0] = movmatrix_trans(pack_f16x2(q0, q1));
-        bp[j][1] = movmatrix_trans(pack_f16x2(q2, q3));
-      }
       const uint32_t wofs = (6 * Gr + vword) * 4;
-      const uint32_t f0 = __funnelshift_r(lds32(vrow0 + wofs), lds32(vrow0 + wofs + 4), vshift);
-      const uint32_t f1 = __funnelshift_r(lds32(vrow1 + wofs), lds32(vrow1 + wofs + 4), vshift);
-      const uint32_t f2 = __funnelshift_r(lds32(vrow2 + wofs), lds32(vrow2 + wofs + 4), vshift);
-      const uint32_t f3 = __funnelshift_r(lds32(vrow3 + wofs), lds32(vrow3 + wofs + 4), vshift);
-      uint32_t h01[8], h23[8];
-      unpack_v3_pair(f0, f1, h01);
-      unpack_v3_pair(f2, f3, h23);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t A[4] = {h01[2 * i], h01[2 * i + 1], h23[2 * i], h23[2 * i + 1]};
+      for (int n = 0; n < N; ++n) {
+        const float vs0 = pick_bf16(vsc0[n], Gr), vs1 = pick_bf16(vsc1[n], Gr);
+        const float vb0 = fmaf(VCENTRE, vs0, pick_bf16(vbi0[n], Gr));
+        const float vb1 = fmaf(VCENTRE, vs1, pick_bf16(vbi1[n], Gr));
+        uint32_t bp[NT][2];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) mma_f16(O[gi][i][j], A, bp[j][0], bp[j][1]);
+        for (int j = 0; j < NT; ++j) {
+          const float* p = pr[n][j];
+          float q0 = p[0] * vs0, q1 = p[1] * vs0, q2 = p[2] * vs1, q3 = p[3] * vs1;
+          if constexpr (FULL) {
+            bacc[gi][j][0] = fmaf(p[0], vb0, fmaf(p[2], vb1, bacc[gi][j][0]));
+            bacc[gi][j][1] = fmaf(p[1], vb0, fmaf(p[3], vb1, bacc[gi][j][1]));
+          } else {  // masked tokens may hold stale (even NaN) scales: select, never multiply
+            const bool* v = valid[n][j];
+            q0 = v[0] ? q0 : 0.f;
+            q1 = v[1] ? q1 : 0.f;
+            q2 = v[2] ? q2 : 0.f;
+            q3 = v[3] ? q3 : 0.f;
+            bacc[gi][j][0] += (v[0] ? p[0] * vb0 : 0.f) + (v[2] ? p[2] * vb1 : 0.f);
+            bacc[gi][j][1] += (v[1] ? p[1] * vb0 : 0.f) + (v[3] ? p[3] * vb1 : 0.f);
+          }
+          bp[j][0] = movmatrix_trans(pack_f16x2(q0, q1));
+          bp[j][1] = movmatrix_trans(pack_f16x2(q2, q3));
+        }
+        uint32_t f[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          f[r] = __funnelshift_r(lds32(vrow[n][r] + wofs), lds32(vrow[n][r] + wofs + 4), vshift);
+        uint32_t h01[8], h23[8];
+        unpack_v3_pair(f[0], f[1], h01);
+        unpack_v3_pair(f[2], f[3], h23);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t A[4] = {h01[2 * i], h01[2 * i + 1], h23[2 * i], h23[2 * i + 1]};
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma_f16(O[gi][i][j], A, bp[j][0], bp[j][1]);
+        }
       }
     }
   };
@@ -805,15 +903,24 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>::THR
       }
       const uint32_t sb = smem_u32(smem + st * STAGE);
       const int tile_tok = static_cast<int>(gt - tile0) * TILE;
-      // global sub-tile SUBS*k + sub belongs to stream (SUBS*k + sub) % STREAMS
+      // global sub-tile SUBS*k + sub belongs to stream (SUBS*k + sub) % STREAMS;
+      // a stream takes its sub-tiles of the stage PAIR at a time
       const int first = static_cast<int>((stream - (SUBS * k) % STREAMS + STREAMS) % STREAMS);
-      for (int sub = first; sub < SUBS; sub += STREAMS) {
-        const int tokbase = tile_tok + sub * 16;
-        if (tokbase >= limit) break;
-        if (tokbase + 16 <= limit && tokbase + 15 <= qmin)
-          subtile(std::true_type{}, sub, tokbase, sb);
-        else
-          subtile(std::false_type{}, sub, tokbase, sb);
+      for (int sub = first; sub < SUBS; sub += PAIR * STREAMS) {
+        const int subs[2] = {sub, sub + STREAMS};
+        const int tb[2] = {tile_tok + sub * 16, tile_tok + (sub + STREAMS) * 16};
+        if (tb[0] >= limit) break;
+        if (PAIR == 2 && subs[1] < SUBS && tb[1] < limit) {
+          if (tb[1] + 16 <= limit && tb[1] + 15 <= qmin)
+            subtiles(std::integral_constant<int, 2>{}, std::true_type{}, subs, tb, sb);
+          else
+            subtiles(std::integral_constant<int, 2>{}, std::false_type{}, subs, tb, sb);
+        } else {
+          if (tb[0] + 16 <= limit && tb[0] + 15 <= qmin)
+            subtiles(std::integral_constant<int, 1>{}, std::true_type{}, subs, tb, sb);
+          else
+            subtiles(std::integral_constant<int, 1>{}, std::false_type{}, subs, tb, sb);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
@@ -837,18 +944,18 @@ struct Plan {
 // to 256 B][partial O: slots x GT x 256 f32][partial (max, sum): slots x GT x 2 f32]
 constexpr size_t kStatusBytes = 256;
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
 int blocks_per_sm() {
   static int cache[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (cache[dev] == 0) {
-    using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>;
+    using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>;
     int n = 0;
-    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_>,
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>,
                                                       C::THREADS, C::SMEM) !=
             cudaSuccess ||
         n <= 0)
@@ -880,7 +987,10 @@ int blocks_per_sm() {
 #ifndef IQ_DECODE_MINB
 #define IQ_DECODE_MINB 2
 #endif
-#define IQ_DECODE_CFG 1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB, IQ_DECODE_TILE
+#ifndef IQ_DECODE_PAIR
+#define IQ_DECODE_PAIR 2
+#endif
+#define IQ_DECODE_CFG 1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB, IQ_DECODE_TILE, IQ_DECODE_PAIR
 #ifndef IQ_MULTI_NT
 #define IQ_MULTI_NT 2
 #endif
@@ -888,18 +998,21 @@ int blocks_per_sm() {
 #define IQ_MULTI_DS 2
 #endif
 #ifndef IQ_MULTI_STREAMS
-#define IQ_MULTI_STREAMS 2
+#define IQ_MULTI_STREAMS 4
 #endif
 #ifndef IQ_MULTI_STAGES
-#define IQ_MULTI_STAGES 2
+#define IQ_MULTI_STAGES 4
 #endif
 #ifndef IQ_MULTI_MINB
-#define IQ_MULTI_MINB 2
+#define IQ_MULTI_MINB 1
 #endif
 #ifndef IQ_MULTI_TILE
 #define IQ_MULTI_TILE 128
 #endif
-#define IQ_MULTI_CFG IQ_MULTI_NT, IQ_MULTI_DS, IQ_MULTI_STREAMS, IQ_MULTI_STAGES, IQ_MULTI_MINB, IQ_MULTI_TILE
+#ifndef IQ_MULTI_PAIR
+#define IQ_MULTI_PAIR 1
+#endif
+#define IQ_MULTI_CFG IQ_MULTI_NT, IQ_MULTI_DS, IQ_MULTI_STREAMS, IQ_MULTI_STAGES, IQ_MULTI_MINB, IQ_MULTI_TILE, IQ_MULTI_PAIR
 
 // Tiles of every unit, in unit order: unit u = (b, kv head, query tile).
 void unit_tiles(const iq_cache* c, int rep, int nq, int causal, int gt, int nqt, int tile, int* tiles) {
@@ -985,11 +1098,22 @@ int validate(const iq_cache* c, const uint16_t* q, int q_heads, int nq, int caus
   return IQ_OK;
 }
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
 int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStream_t s) {
-  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_>;
-  blocks_per_sm<NT, DS, STREAMS, NSTAGE, MINB, TILE_>();  // sets the shared-memory attribute once
-  attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
+  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>;
+  blocks_per_sm<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>();  // sets the shared-memory attribute once
+  // The warpgroups move registers between them (setmaxnreg); that split adds
+  // up to the block's launch allocation only at the register count it was
+  // designed for, so any other build of the kernel is refused, never launched.
+  static int launch_regs = -1;
+  if (launch_regs < 0) {
+    cudaFuncAttributes fa;
+    IQ_CUDA(cudaFuncGetAttributes(&fa, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>));
+    launch_regs = fa.numRegs;
+  }
+  if (launch_regs != C::LAUNCH_REGS)
+    return fail(IQ_ERR_UNSUPPORTED, "attention kernel built with an unexpected register count");
+  attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
   IQ_CUDA(cudaGetLastError());
   return IQ_OK;
 }

@@ -124,6 +124,17 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// ---- register reallocation between warpgroups (every warp of a warpgroup
+// executes it; the counts are per thread, multiples of 8 in [24, 256])
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---- named barrier among a subset of warps
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
