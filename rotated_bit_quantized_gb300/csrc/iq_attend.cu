@@ -209,12 +209,9 @@ struct Cfg : Tiling<TILE_> {
   static_assert(CW % 4 == 0, "consumer warps form whole warpgroups");
   static_assert(CONSUMER_REGS >= LAUNCH_REGS && PRODUCER_REGS <= LAUNCH_REGS, "register split");
   static_assert(MINB * (CW * 32 * CONSUMER_REGS + 128 * PRODUCER_REGS) <= 65536, "register file");
-  // the rotated queries (unit start) and the stream-merge buffer (unit end) share one area
-  static constexpr int OBUF_BYTES = STREAMS > 1 ? GT * 256 * 4 : 0;
-  static constexpr int QS_BYTES = GT * 512 > OBUF_BYTES ? GT * 512 : OBUF_BYTES;
-  static constexpr int OFF_QS = NSTAGE * STAGE;
-  static constexpr int OFF_OBUF = OFF_QS;
-  static constexpr int OFF_QSUM = OFF_QS + QS_BYTES;
+  static constexpr int OBUF_BYTES = GT * 256 * 4;  // the CTA's merged O of a unit
+  static constexpr int OFF_OBUF = NSTAGE * STAGE;
+  static constexpr int OFF_QSUM = OFF_OBUF + OBUF_BYTES;
   static constexpr int OFF_MBUF = OFF_QSUM + GT * 16;
   static constexpr int OFF_LBUF = OFF_MBUF + STREAMS * GT * 4;
   static constexpr int OFF_XBUF = OFF_LBUF + STREAMS * GT * 4;
@@ -241,7 +238,6 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   // 1024-byte aligned base (128-byte swizzle atom), derived by pointer
   // arithmetic on the shared array so loads through it stay shared-memory loads
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + C::OFF_QS);
   float* qsum = reinterpret_cast<float*>(smem + C::OFF_QSUM);
   float* mbuf = reinterpret_cast<float*>(smem + C::OFF_MBUF);
   float* lbuf = reinterpret_cast<float*>(smem + C::OFF_LBUF);
@@ -346,80 +342,83 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     T = p.lens[b];
     limit = tile_limit(p, T, qt, GT);
     qmin = p.causal ? T - p.nq + (qt * GT) / p.rep : T - 1;
-    named_bar(1, NCT);  // every consumer is done with the previous unit's qs / qsum
-    // q' = bf16(q @ M_b), q'' = bf16(q' * scale); rows r <-> (query R/rep, head R%rep)
-    for (int idx = threadIdx.x; idx < GT * 64; idx += NCT) {
-      const int r = idx >> 6, blk = idx & 63;
-      const int R = qt * GT + r, i = R / p.rep, hr = R % p.rep;
-      uint32_t o01 = 0, o23 = 0;
+    named_bar(1, NCT);  // every consumer is done with the previous unit's fragments and sums
+    // q' = bf16(q @ M_b), q'' = bf16(q' * scale), written straight into the fp16
+    // MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].  Item
+    // (n-tile j, group G) goes to one warp; its thread (g, t) rotates row 8j+g,
+    // dims 64G+16t .. +15 (rotation blocks 16G+4t .. +3), whose register m
+    // holds the dims k_pair(m, 0..1); k-step s uses registers 2s (slots 2t,
+    // 2t+1) and 2s+1.  An item's global loads are issued together.  Rows
+    // r <-> (query R/rep, head R%rep); rows past the queries are zero.
+    for (int item = cw; item < NT * 4; item += CW) {
+      const int j = item >> 2, G = item & 3;
+      const int R = qt * GT + 8 * j + g, i = R / p.rep, hr = R % p.rep;
+      uint32_t yb[16];  // q'' (bf16 bits) of the thread's 16 dims
       if (i < p.nq) {
         const long long qrow =
             (static_cast<long long>(b) * p.kv_heads * p.rep + kvh * p.rep + hr) * p.nq + i;
-        const uint2 raw = *reinterpret_cast<const uint2*>(p.q + qrow * kHeadDim + blk * 4);
-        const float x[4] = {bf16_to_f32(raw.x & 0xFFFFu), bf16_to_f32(raw.x >> 16),
-                            bf16_to_f32(raw.y & 0xFFFFu), bf16_to_f32(raw.y >> 16)};
-        const uint4* r4 = reinterpret_cast<const uint4*>(p.rot + blk * 16);
-        const uint4 m01 = __ldg(r4), m23 = __ldg(r4 + 1);
-        const uint32_t mw[8] = {m01.x, m01.y, m01.z, m01.w, m23.x, m23.y, m23.z, m23.w};
-        uint32_t yb[4];
+        const uint4* qv = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim + 64 * G + 16 * t);
+        const uint4* rv = reinterpret_cast<const uint4*>(p.rot + (16 * G + 4 * t) * 16);
+        uint4 qw4[2], mw4[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float acc = 0.f;
+        for (int c = 0; c < 2; ++c) qw4[c] = __ldg(qv + c);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int e = k * 4 + j;
-            const float mkj = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
-            acc = k == 0 ? __fmul_rn(x[0], mkj) : __fadd_rn(acc, __fmul_rn(x[k], mkj));
+        for (int c = 0; c < 8; ++c) mw4[c] = __ldg(rv + c);
+        const uint32_t qw[8] = {qw4[0].x, qw4[0].y, qw4[0].z, qw4[0].w, qw4[1].x, qw4[1].y, qw4[1].z, qw4[1].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // rotation block 16G + 4t + c: dims 4c .. 4c+3 of the thread
+          const uint32_t mw[8] = {mw4[2 * c].x, mw4[2 * c].y, mw4[2 * c].z, mw4[2 * c].w,
+                                  mw4[2 * c + 1].x, mw4[2 * c + 1].y, mw4[2 * c + 1].z, mw4[2 * c + 1].w};
+          float x[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t w = qw[(4 * c + e) >> 1];
+            x[e] = bf16_to_f32((e & 1) ? (w >> 16) : (w & 0xFFFFu));
           }
-          yb[j] = f32_to_bf16_bits(__fmul_rn(round_bf16(acc), p.scale));
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {  // y[jj] = sum_k x[k] * M_b[k][jj], f32 in order k = 0..3
+            float acc = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int e = kk * 4 + jj;
+              const float mkj = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
+              acc = kk == 0 ? __fmul_rn(x[0], mkj) : __fadd_rn(acc, __fmul_rn(x[kk], mkj));
+            }
+            yb[4 * c + jj] = f32_to_bf16_bits(__fmul_rn(round_bf16(acc), p.scale));
+          }
         }
-        o01 = yb[0] | (yb[1] << 16);
-        o23 = yb[2] | (yb[3] << 16);
+      } else {
+#pragma unroll
+        for (int d = 0; d < 16; ++d) yb[d] = 0u;
       }
-      *reinterpret_cast<uint2*>(qs + r * kHeadDim + blk * 4) = make_uint2(o01, o23);
-    }
-    named_bar(1, NCT);
-    for (int r = cw; r < GT; r += CW) {
-      const uint4 v = *reinterpret_cast<const uint4*>(qs + r * kHeadDim + lane * 8);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      float s = 0.f;
+      float qpart = 0.f;  // sum of the fp16 operand values (the offset the fold removes)
 #pragma unroll
-      for (int e = 0; e < 4; ++e)  // sum of the fp16 operand values (the offset the fold removes)
-        s += __half2float(__ushort_as_half(static_cast<unsigned short>(bf16_to_f16_bits(w[e] & 0xFFFFu)))) +
-             __half2float(__ushort_as_half(static_cast<unsigned short>(bf16_to_f16_bits(w[e] >> 16))));
+      for (int d = 0; d < 16; ++d)
+        qpart += __half2float(__ushort_as_half(static_cast<unsigned short>(bf16_to_f16_bits(yb[d]))));
 #pragma unroll
-      for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if ((lane & 7) == 0) qsum[r * 4 + (lane >> 3)] = s;
+      for (int s = 0; s < 4; ++s) {
+        uint32_t h2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int m = 2 * s + h;
+          h2[h] = bf16_to_f16_bits(yb[k_pair(m, 0)]) | (bf16_to_f16_bits(yb[k_pair(m, 1)]) << 16);
+        }
+        qbs[((G * 4 + s) * NT + j) * 32 + lane] = make_uint2(h2[0], h2[1]);
+      }
+      qpart += __shfl_xor_sync(0xffffffffu, qpart, 1);
+      qpart += __shfl_xor_sync(0xffffffffu, qpart, 2);
+      if (t == 0) qsum[(8 * j + g) * 4 + G] = qpart;
     }
-    named_bar(1, NCT);
-    // q'' as fp16 MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].
-    // Thread t covers dims 64G+16t .. +15 of group G; register m of its
-    // unpacked codes holds the dims k_pair(m, 0), k_pair(m, 1); k-step s uses registers 2s
-    // (slots 2t,2t+1) and 2s+1.  Stream 0 writes them.
+    named_bar(1, NCT);  // fragments and sums visible to every warp
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
       const int Gr = dg * GPW + gi;
-      const int base = 64 * Gr + 16 * t;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        if (stream == 0) {
-          const uint16_t* qrow = qs + (8 * j + g) * kHeadDim + base;
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            uint32_t h2[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int m = 2 * s + h;
-              h2[h] = bf16_to_f16_bits(qrow[k_pair(m, 0)]) | (bf16_to_f16_bits(qrow[k_pair(m, 1)]) << 16);
-            }
-            qbs[((Gr * 4 + s) * NT + j) * 32 + lane] = make_uint2(h2[0], h2[1]);
-          }
-        }
         qsr[gi][j][0] = qsum[(8 * j + 2 * t) * 4 + Gr];
         qsr[gi][j][1] = qsum[(8 * j + 2 * t + 1) * 4 + Gr];
       }
     }
-    named_bar(1, NCT);  // fragments visible to every stream
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -680,7 +679,63 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     }
   };
 
-  // ---- finish unit u's segment: partial store; the unit's last segment combines
+  // ---- output of one (row, 8-dim chunk): normalise, undo the rotation
+  // (out[4c+i] = sum_j o[4c+j] * M_b[c][i][j]) and store bf16 or fp32.  `mw`
+  // holds the two rotation blocks of the chunk, loaded by the caller early.
+  auto store_out = [&](int ub, int r, int l8, const float (&acc)[8], float L, const uint32_t (&mw)[16]) {
+    const int R = (ub % p.nqt) * GT + r, i = R / p.rep, hr = R % p.rep;
+    const int bb = ub / (p.kv_heads * p.nqt), hh = (ub / p.nqt) % p.kv_heads;
+    if (!(L > 0.f)) atomicOr(p.status, 4u);
+    float o[8];
+#pragma unroll
+    for (int d = 0; d < 8; ++d) o[d] = __fdiv_rn(acc[d], L);
+    float y[8];
+#pragma unroll
+    for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        float sacc = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int e = cb * 16 + ii * 4 + jj;
+          const float m = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
+          sacc = jj == 0 ? o[4 * cb] * m : fmaf(o[4 * cb + jj], m, sacc);
+        }
+        y[4 * cb + ii] = sacc;
+      }
+    const int hq = hh * p.rep + hr;
+    const long long orow = (static_cast<long long>(bb) * p.kv_heads * p.rep + hq) * p.nq + i;
+    if (p.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHeadDim + 8 * l8);
+      dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+      dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+    } else {
+      uint4 v;
+      v.x = f32_to_bf16_bits(y[0]) | (f32_to_bf16_bits(y[1]) << 16);
+      v.y = f32_to_bf16_bits(y[2]) | (f32_to_bf16_bits(y[3]) << 16);
+      v.z = f32_to_bf16_bits(y[4]) | (f32_to_bf16_bits(y[5]) << 16);
+      v.w = f32_to_bf16_bits(y[6]) | (f32_to_bf16_bits(y[7]) << 16);
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kHeadDim + 8 * l8) = v;
+    }
+  };
+  auto load_rot = [&](int l8, uint32_t (&mw)[16]) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(p.rot) + l8 * 4;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const uint4 v = __ldg(r4 + q4);
+      mw[4 * q4] = v.x; mw[4 * q4 + 1] = v.y; mw[4 * q4 + 2] = v.z; mw[4 * q4 + 3] = v.w;
+    }
+  };
+  // segments of unit u: CTAs k_first .. k_last (partial slots u + k)
+  auto seg_range = [&](int u, int& k_first, int& nseg) {
+    k_first = cta_of(p.prefix[u], W, G);
+    nseg = cta_of(p.prefix[u + 1] - 1, W, G) - k_first + 1;
+  };
+
+  // ---- finish this CTA's segment of unit u: fold the value-bias sums into O
+  // and merge the token streams (log-sum-exp) into obuf; a unit held by this
+  // CTA alone is finalised at once, a shared one leaves a partial (O, running
+  // max in log2 units, running sum) for the combine.
   auto end_unit = [&](int u) {
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -704,184 +759,135 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
           }
         }
       }
-    const long long slot = static_cast<long long>(u) + k_cta;  // unique per (unit, CTA) segment
-    float* po = p.part_o + slot * GT * kHeadDim;
-    float* pml = p.part_ml + slot * GT * 2;
-    if constexpr (STREAMS == 1) {
-#pragma unroll
-      for (int gi = 0; gi < GPW; ++gi)
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int row = 8 * j + 2 * t + e;
-            float* dst = po + row * kHeadDim + 64 * (dg * GPW + gi) + 8 * g;
-            reinterpret_cast<float4*>(dst)[0] =
-                make_float4(O[gi][0][j][e], O[gi][0][j][e + 2], O[gi][1][j][e], O[gi][1][j][e + 2]);
-            reinterpret_cast<float4*>(dst)[1] =
-                make_float4(O[gi][2][j][e], O[gi][2][j][e + 2], O[gi][3][j][e], O[gi][3][j][e + 2]);
-          }
-      if (dg == 0 && g == 0)
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int row = 8 * j + 2 * t + e;
-            pml[row * 2] = msc[j][e];
-            pml[row * 2 + 1] = lrow[j][e];
-          }
-    } else {  // merge the token streams in turn through one shared accumulation buffer
-      if (dg == 0 && g == 0)
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) mbuf[stream * GT + 8 * j + 2 * t + e] = msc[j][e];
-      named_bar(1, NCT);
-      float a_row[NT][2];
+    // merge the token streams in turn through obuf
+    if (dg == 0 && g == 0)
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = 8 * j + 2 * t + e;
-          float M = mbuf[row];
+        for (int e = 0; e < 2; ++e) mbuf[stream * GT + 8 * j + 2 * t + e] = msc[j][e];
+    named_bar(1, NCT);
+    float a_row[NT][2];
 #pragma unroll
-          for (int s = 1; s < STREAMS; ++s) M = fmaxf(M, mbuf[s * GT + row]);
-          a_row[j][e] = msc[j][e] == NEG_INF ? 0.f : ex2_approx(msc[j][e] - M);
-          if (dg == 0 && g == 0) lbuf[stream * GT + row] = lrow[j][e] * a_row[j][e];
-        }
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int row = 8 * j + 2 * t + e;
+        float M = mbuf[row];
+#pragma unroll
+        for (int s = 1; s < STREAMS; ++s) M = fmaxf(M, mbuf[s * GT + row]);
+        a_row[j][e] = msc[j][e] == NEG_INF ? 0.f : ex2_approx(msc[j][e] - M);
+        if (dg == 0 && g == 0) lbuf[stream * GT + row] = lrow[j][e] * a_row[j][e];
+      }
 #pragma unroll 1
-      for (int turn = 0; turn < STREAMS; ++turn) {
-        if (stream == turn) {
+    for (int turn = 0; turn < STREAMS; ++turn) {
+      if (stream == turn) {
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
+        for (int j = 0; j < NT; ++j)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int row = 8 * j + 2 * t + e;
-              const float a = a_row[j][e];
+          for (int e = 0; e < 2; ++e) {
+            const int row = 8 * j + 2 * t + e;
+            const float a = a_row[j][e];
 #pragma unroll
-              for (int gi = 0; gi < GPW; ++gi) {
-                const int col = 64 * (dg * GPW + gi) + 8 * g;
-                float4 v0 = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a, O[gi][1][j][e] * a,
-                                        O[gi][1][j][e + 2] * a);
-                float4 v1 = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a, O[gi][3][j][e] * a,
-                                        O[gi][3][j][e + 2] * a);
-                float4* acc = reinterpret_cast<float4*>(obuf + row * kHeadDim + col);
-                if (turn > 0) {
-                  const float4 p0 = acc[0], p1 = acc[1];
-                  v0.x += p0.x; v0.y += p0.y; v0.z += p0.z; v0.w += p0.w;
-                  v1.x += p1.x; v1.y += p1.y; v1.z += p1.z; v1.w += p1.w;
-                }
-                float4* dst = turn == STREAMS - 1 ? reinterpret_cast<float4*>(po + row * kHeadDim + col) : acc;
-                dst[0] = v0;
-                dst[1] = v1;
+            for (int gi = 0; gi < GPW; ++gi) {
+              const int col = 64 * (dg * GPW + gi) + 8 * g;
+              float4 v0 = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a, O[gi][1][j][e] * a,
+                                      O[gi][1][j][e + 2] * a);
+              float4 v1 = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a, O[gi][3][j][e] * a,
+                                      O[gi][3][j][e + 2] * a);
+              float4* acc = reinterpret_cast<float4*>(obuf + row * kHeadDim + col);
+              if (turn > 0) {
+                const float4 p0 = acc[0], p1 = acc[1];
+                v0.x += p0.x; v0.y += p0.y; v0.z += p0.z; v0.w += p0.w;
+                v1.x += p1.x; v1.y += p1.y; v1.z += p1.z; v1.w += p1.w;
               }
-              if (turn == STREAMS - 1 && dg == 0 && g == 0) {
-                float M = mbuf[row], L = lbuf[row];
-#pragma unroll
-                for (int s = 1; s < STREAMS; ++s) {
-                  M = fmaxf(M, mbuf[s * GT + row]);
-                  L += lbuf[s * GT + row];
-                }
-                pml[row * 2] = M;
-                pml[row * 2 + 1] = L;
-              }
+              acc[0] = v0;
+              acc[1] = v1;
             }
+          }
+      }
+      named_bar(1, NCT);
+    }
+    // obuf holds the CTA's O for the unit; per row M = max and L = sum over the streams
+    int k_first, nseg;
+    seg_range(u, k_first, nseg);
+    const int ub = p.unit_base + u;
+    if (nseg == 1) {  // the whole unit is here: finalise
+      for (int idx = threadIdx.x; idx < GT * 32; idx += NCT) {
+        const int r = idx >> 5, l8 = idx & 31;
+        if ((qt * GT + r) / p.rep >= p.nq) continue;
+        uint32_t mw[16];
+        load_rot(l8, mw);
+        float L = lbuf[r];
+#pragma unroll
+        for (int s = 1; s < STREAMS; ++s) L += lbuf[s * GT + r];
+        const float4 o0 = reinterpret_cast<const float4*>(obuf + r * kHeadDim + 8 * l8)[0];
+        const float4 o1 = reinterpret_cast<const float4*>(obuf + r * kHeadDim + 8 * l8)[1];
+        const float acc[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+        store_out(ub, r, l8, acc, L, mw);
+      }
+    } else {  // partial for the combine: slot u + k_cta
+      const long long slot = static_cast<long long>(u) + k_cta;
+      float4* po = reinterpret_cast<float4*>(p.part_o + slot * GT * kHeadDim);
+      for (int idx = threadIdx.x; idx < GT * kHeadDim / 4; idx += NCT)
+        po[idx] = reinterpret_cast<const float4*>(obuf)[idx];
+      for (int r = threadIdx.x; r < GT; r += NCT) {
+        float M = mbuf[r], L = lbuf[r];
+#pragma unroll
+        for (int s = 1; s < STREAMS; ++s) {
+          M = fmaxf(M, mbuf[s * GT + r]);
+          L += lbuf[s * GT + r];
         }
-        if (turn < STREAMS - 1) named_bar(1, NCT);
+        reinterpret_cast<float2*>(p.part_ml)[slot * GT + r] = make_float2(M, L);
       }
     }
+  };
 
-    // segments of this unit: CTAs k_first .. k_last (partial slots u + k)
-    const long long ustart = p.prefix[u], uend = p.prefix[u + 1];
-    const int k_first = cta_of(ustart, W, G), k_last = cta_of(uend - 1, W, G);
-    const int nseg = k_last - k_first + 1;
-    __threadfence();
-    named_bar(1, NCT);
-    if (threadIdx.x == 0)
-      *s_flag = atomicAdd(p.counters + p.unit_base + u, 1u) + 1 == static_cast<unsigned>(nseg);
-    named_bar(1, NCT);
-    if (!*s_flag) return;
-    __threadfence();
-
-    // combine: per row, the log-sum-exp weights of the segments
+  // ---- combine unit u from its segments' partials (log-sum-exp, online over
+  // the segments, eight segments' loads in flight), then finalise
+  auto combine = [&](int u) {
+    int k_first, nseg;
+    seg_range(u, k_first, nseg);
     const long long slot0 = static_cast<long long>(u) + k_first;
-    for (int r = cw; r < GT; r += CW) {  // a warp per row: max, then normaliser
-      float M = NEG_INF;
-      for (int s = lane; s < nseg; s += 32) M = fmaxf(M, __ldcg(p.part_ml + ((slot0 + s) * GT + r) * 2));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float L = 0.f;
-      for (int s = lane; s < nseg; s += 32) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + (slot0 + s) * GT + r);
-        L = fmaf(ml.x == NEG_INF ? 0.f : ex2_approx(ml.x - M), ml.y, L);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      if (lane == 0) {
-        mbuf[r] = M;
-        lbuf[r] = L;
-      }
-    }
-    named_bar(1, NCT);
+    const int ub = p.unit_base + u;
     for (int idx = threadIdx.x; idx < GT * 32; idx += NCT) {
       const int r = idx >> 5, l8 = idx & 31;
-      const int R = qt * GT + r, i = R / p.rep, hr = R % p.rep;
-      if (i >= p.nq) continue;
-      const float M = mbuf[r], L = lbuf[r];
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int s = 0; s < nseg; ++s) {
-        const float m = __ldcg(p.part_ml + ((slot0 + s) * GT + r) * 2);
-        const float wgt = m == NEG_INF ? 0.f : ex2_approx(m - M);
-        const float4* o = reinterpret_cast<const float4*>(p.part_o + ((slot0 + s) * GT + r) * kHeadDim + 8 * l8);
-        const float4 o0 = __ldcg(o), o1 = __ldcg(o + 1);
-        acc[0] = fmaf(wgt, o0.x, acc[0]); acc[1] = fmaf(wgt, o0.y, acc[1]);
-        acc[2] = fmaf(wgt, o0.z, acc[2]); acc[3] = fmaf(wgt, o0.w, acc[3]);
-        acc[4] = fmaf(wgt, o1.x, acc[4]); acc[5] = fmaf(wgt, o1.y, acc[5]);
-        acc[6] = fmaf(wgt, o1.z, acc[6]); acc[7] = fmaf(wgt, o1.w, acc[7]);
-      }
-      if (!(L > 0.f)) atomicOr(p.status, 4u);
-      float o[8];
-#pragma unroll
-      for (int d = 0; d < 8; ++d) o[d] = __fdiv_rn(acc[d], L);
-      // inverse rotation: out[4c+i] = sum_j o[4c+j] * M_b[c][i][j]
-      const uint4* r4 = reinterpret_cast<const uint4*>(p.rot) + l8 * 4;
+      if (((ub % p.nqt) * GT + r) / p.rep >= p.nq) continue;
       uint32_t mw[16];
+      load_rot(l8, mw);
+      float M = NEG_INF, L = 0.f;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int s0 = 0; s0 < nseg; s0 += 8) {
+        float2 ml[8];
+        float4 oa[8], ob[8];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint4 v = __ldg(r4 + q4);
-        mw[4 * q4] = v.x; mw[4 * q4 + 1] = v.y; mw[4 * q4 + 2] = v.z; mw[4 * q4 + 3] = v.w;
-      }
-      float y[8];
-#pragma unroll
-      for (int cb = 0; cb < 2; ++cb)
-#pragma unroll
-        for (int ii = 0; ii < 4; ++ii) {
-          float sacc = 0.f;
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int e = cb * 16 + ii * 4 + jj;
-            const float m = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
-            sacc = jj == 0 ? o[4 * cb] * m : fmaf(o[4 * cb + jj], m, sacc);
+        for (int q8 = 0; q8 < 8; ++q8) {
+          if (s0 + q8 < nseg) {
+            const long long sl = slot0 + s0 + q8;
+            ml[q8] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl * GT + r);
+            const float4* o = reinterpret_cast<const float4*>(p.part_o + (sl * GT + r) * kHeadDim + 8 * l8);
+            oa[q8] = __ldcg(o);
+            ob[q8] = __ldcg(o + 1);
+          } else {
+            ml[q8] = make_float2(NEG_INF, 0.f);
+            oa[q8] = ob[q8] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          y[4 * cb + ii] = sacc;
         }
-      const int hq = kvh * p.rep + hr;
-      const long long orow = (static_cast<long long>(b) * p.kv_heads * p.rep + hq) * p.nq + i;
-      if (p.out_f32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHeadDim + 8 * l8);
-        dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-        dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-      } else {
-        uint4 v;
-        v.x = f32_to_bf16_bits(y[0]) | (f32_to_bf16_bits(y[1]) << 16);
-        v.y = f32_to_bf16_bits(y[2]) | (f32_to_bf16_bits(y[3]) << 16);
-        v.z = f32_to_bf16_bits(y[4]) | (f32_to_bf16_bits(y[5]) << 16);
-        v.w = f32_to_bf16_bits(y[6]) | (f32_to_bf16_bits(y[7]) << 16);
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kHeadDim + 8 * l8) = v;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          if (ml[q8].x == NEG_INF) continue;  // empty segment
+          const float Mn = fmaxf(M, ml[q8].x);
+          const float so = M == NEG_INF ? 0.f : ex2_approx(M - Mn);
+          const float w = ex2_approx(ml[q8].x - Mn);
+          const float v[8] = {oa[q8].x, oa[q8].y, oa[q8].z, oa[q8].w, ob[q8].x, ob[q8].y, ob[q8].z, ob[q8].w};
+#pragma unroll
+          for (int d = 0; d < 8; ++d) acc[d] = fmaf(w, v[d], acc[d] * so);
+          L = fmaf(w, ml[q8].y, L * so);
+          M = Mn;
+        }
       }
+      store_out(ub, r, l8, acc, L, mw);
     }
-    if (threadIdx.x == 0) p.counters[p.unit_base + u] = 0;  // ready for the next call
+    if (threadIdx.x == 0) p.counters[ub] = 0;  // ready for the next call
   };
 
   // ------------------------------------------------------------ main loop over this CTA's tiles
@@ -928,6 +934,25 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     end_unit(u);
     if (!ok || gt >= g1) break;
     ++u;
+  }
+  // arrivals for the shared units this CTA touched (only its first and last
+  // can be shared), deferred to here so no mid-range unit boundary waits on a
+  // fence or an atomic; the last CTA to arrive at a unit combines it
+  {
+    int kf, ns0, ns1;
+    seg_range(u0, kf, ns0);
+    seg_range(u, kf, ns1);
+    __threadfence();  // partials visible before the arrivals
+    named_bar(1, NCT);
+    if (threadIdx.x == 0) {
+      s_flag[0] = ns0 > 1 && atomicAdd(p.counters + p.unit_base + u0, 1u) + 1 == static_cast<unsigned>(ns0);
+      s_flag[1] = u != u0 && ns1 > 1 && atomicAdd(p.counters + p.unit_base + u, 1u) + 1 == static_cast<unsigned>(ns1);
+    }
+    named_bar(1, NCT);
+    const int f0 = s_flag[0], f1 = s_flag[1];
+    if (f0 || f1) __threadfence();
+    if (f0) combine(u0);
+    if (f1) combine(u);
   }
 }
 
