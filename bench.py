@@ -279,7 +279,7 @@ def run_ours(args):
                          "avg_launch_us": attn_avg_s * 1e6},
             "e2e": {"value": e_tokens_all / (e_ms_max / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * K,  # append_kernel + attend_kernel per step
+            "gpu_launches": 3 * K,  # append_kernel + attend_kernel + combine_kernel per step
             "clocks": clk.summary(),
             "device_status": status,
             "cpu_baseline": cpu,

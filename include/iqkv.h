@@ -156,9 +156,9 @@ int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of,
                     iq_stream_t stream);
 
 /*
- * iq_attend_workspace — device scratch bytes iq_attend needs for these
- * lengths and shapes (status word, per-unit chunk counters and the split-KV
- * partial results).
+ * iq_attend_workspace — device scratch bytes iq_attend needs for this batch
+ * and these shapes (status word and the split-KV partial results); the size
+ * does not depend on the lengths.
  */
 int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_t* bytes);
 
@@ -176,13 +176,17 @@ int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_
  * out: device [B][Hq][n_queries][head_dim], bf16 (out_f32 == 0) or float32
  *    (out_f32 == 1), in unrotated space: out = bf16(o @ M_b^T).
  * workspace: device buffer of at least iq_attend_workspace() bytes,
- *    256-byte aligned; its contents on entry do not matter.
+ *    256-byte aligned.  Its first 4 bytes are the status word, which must be
+ *    zero before the first call (e.g. a zero-filled allocation); kernels only
+ *    ever set bits in it and iq_read_status clears it.  The rest needs no
+ *    initialisation.  Two kernels run per 1024 query tiles: the attention
+ *    grid and, as its programmatic dependent, the split combine.
  * Scores, softmax and P.V accumulate in float32 on tensor cores; dequantised
  * key codes enter the products exactly; P times the value scale enters as fp16.
  * Errors: INVALID_ARG (null, bad causal flag, empty sequence, lens[b] <
  * n_queries when causal), WORKSPACE, UNSUPPORTED, CUDA.  A kernel-side failure
- * (a pipeline wait that timed out) is recorded in the workspace status word and
- * reported by iq_read_status.
+ * (a pipeline wait that timed out, an empty softmax row) sets a bit in the
+ * workspace status word, reported by iq_read_status.
  */
 int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
               float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
@@ -205,8 +209,8 @@ int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queri
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.
  * Sharing: every call uses the same array and it keeps the last call's
- * contents (the status word is cleared by each call; the partials are written
- * before they are read).  Calls that can run at the same time on the GPU
+ * contents (the partials are written before they are read; the status word,
+ * zero at load, only ever gains bits).  Calls that can run at the same time on the GPU
  * (different streams without ordering) race on the array: serialise them.
  * Errors: as iq_attend, plus WORKSPACE when the call needs more scratch than
  * IQ_NOALLOC_SCRATCH_BYTES (use iq_attend with a caller workspace then).
@@ -219,9 +223,10 @@ int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q_heads, int
                       iq_stream_t stream);
 
 /*
- * iq_read_status — synchronise `stream`, read the status word that the last
- * iq_attend on this workspace left, and clear it.  *device_status is 0 when
- * every kernel completed normally.  Blocks the calling thread.
+ * iq_read_status — synchronise `stream`, read the status word that the
+ * iq_attend calls on this workspace since the last read left, and clear it.
+ * *device_status is 0 when every kernel completed normally.  Blocks the
+ * calling thread.
  */
 int iq_read_status(void* workspace, iq_stream_t stream, int* device_status);
 

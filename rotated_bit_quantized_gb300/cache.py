@@ -251,7 +251,8 @@ class IQCache:
             raise ValueError("out must be a contiguous bf16 or f32 tensor")
         need = self.workspace_bytes(Hq, L)
         if self._workspace is None or self._workspace.numel() < need:
-            self._workspace = torch.empty(max(need, 1 << 20), dtype=torch.uint8, device=self.device)
+            # zeroed once: the status word at its head starts clear (iq_read_status clears it again)
+            self._workspace = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=self.device)
         d = self.desc()
         with self._on:
             check(lib().iq_attend(ctypes.byref(d), _ptr(q), Hq, L, float(scale), 1 if causal else 0,

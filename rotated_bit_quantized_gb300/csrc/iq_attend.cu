@@ -99,7 +99,6 @@ struct Params {
   float* part_o;       // [slots][GT][256]
   float* part_ml;      // [slots][GT][2] (running max in log2 units, running sum)
   unsigned* status;
-  unsigned* counters;  // [units]: finished segments per unit
   void* out;
   int out_f32;
   int batch, kv_heads, rep, nq, cap, nqt, causal;
@@ -119,6 +118,71 @@ __device__ __forceinline__ int tile_limit(const Params& p, int T, int qt, int gt
 __device__ __forceinline__ int cta_of(long long x, long long W, int G) {
   return static_cast<int>(((x + 1) * G - 1) / W);
 }
+
+// segments of unit u of this launch: CTAs k_first .. k_first + nseg - 1
+// (partial slots u + k)
+__device__ __forceinline__ void seg_range(const Params& p, int u, int& k_first, int& nseg) {
+  const long long W = p.prefix[p.num_units];
+  k_first = cta_of(p.prefix[u], W, p.grid);
+  nseg = cta_of(p.prefix[u + 1] - 1, W, p.grid) - k_first + 1;
+}
+
+// The two M_b blocks of output dims 8*l8 .. 8*l8+7 (32 bf16).
+__device__ __forceinline__ void load_rot(const Params& p, int l8, uint32_t (&mw)[16]) {
+  const uint4* r4 = reinterpret_cast<const uint4*>(p.rot) + l8 * 4;
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const uint4 v = __ldg(r4 + q4);
+    mw[4 * q4] = v.x; mw[4 * q4 + 1] = v.y; mw[4 * q4 + 2] = v.z; mw[4 * q4 + 3] = v.w;
+  }
+}
+
+// Output of one (row r of unit ub, 8-dim chunk l8): normalise by L, undo the
+// rotation (out[4c+i] = sum_j o[4c+j] * M_b[c][i][j]) and store bf16 or fp32.
+template <int GT>
+__device__ __forceinline__ void store_out(const Params& p, int ub, int r, int l8, const float (&acc)[8], float L,
+                                          const uint32_t (&mw)[16]) {
+  const int R = (ub % p.nqt) * GT + r, i = R / p.rep, hr = R % p.rep;
+  const int bb = ub / (p.kv_heads * p.nqt), hh = (ub / p.nqt) % p.kv_heads;
+  if (!(L > 0.f)) atomicOr(p.status, 4u);
+  float o[8];
+#pragma unroll
+  for (int d = 0; d < 8; ++d) o[d] = __fdiv_rn(acc[d], L);
+  float y[8];
+#pragma unroll
+  for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      float sacc = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int e = cb * 16 + ii * 4 + jj;
+        const float m = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
+        sacc = jj == 0 ? o[4 * cb] * m : fmaf(o[4 * cb + jj], m, sacc);
+      }
+      y[4 * cb + ii] = sacc;
+    }
+  const int hq = hh * p.rep + hr;
+  const long long orow = (static_cast<long long>(bb) * p.kv_heads * p.rep + hq) * p.nq + i;
+  if (p.out_f32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHeadDim + 8 * l8);
+    dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+    dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+  } else {
+    uint4 v;
+    v.x = f32_to_bf16_bits(y[0]) | (f32_to_bf16_bits(y[1]) << 16);
+    v.y = f32_to_bf16_bits(y[2]) | (f32_to_bf16_bits(y[3]) << 16);
+    v.z = f32_to_bf16_bits(y[4]) | (f32_to_bf16_bits(y[5]) << 16);
+    v.w = f32_to_bf16_bits(y[6]) | (f32_to_bf16_bits(y[7]) << 16);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kHeadDim + 8 * l8) = v;
+  }
+}
+
+// Programmatic dependent launch: the attention grid lets the combine grid be
+// scheduled early; the combine waits for the attention grid's completion
+// (and the visibility of its writes) before reading the partials.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // group G's bf16 from a packed row of 4 bf16 (uint2)
 __device__ __forceinline__ float pick_bf16(uint2 v, int G) {
@@ -253,6 +317,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   const long long W = p.prefix[p.num_units];
   const int k_cta = blockIdx.x;
   const long long g0 = W * k_cta / G, g1 = W * (k_cta + 1) / G;
+  pdl_launch_dependents();
   if (g0 >= g1) return;
   int u0 = 0;  // unit holding tile g0: last u with prefix[u] <= g0
   {
@@ -679,59 +744,6 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     }
   };
 
-  // ---- output of one (row, 8-dim chunk): normalise, undo the rotation
-  // (out[4c+i] = sum_j o[4c+j] * M_b[c][i][j]) and store bf16 or fp32.  `mw`
-  // holds the two rotation blocks of the chunk, loaded by the caller early.
-  auto store_out = [&](int ub, int r, int l8, const float (&acc)[8], float L, const uint32_t (&mw)[16]) {
-    const int R = (ub % p.nqt) * GT + r, i = R / p.rep, hr = R % p.rep;
-    const int bb = ub / (p.kv_heads * p.nqt), hh = (ub / p.nqt) % p.kv_heads;
-    if (!(L > 0.f)) atomicOr(p.status, 4u);
-    float o[8];
-#pragma unroll
-    for (int d = 0; d < 8; ++d) o[d] = __fdiv_rn(acc[d], L);
-    float y[8];
-#pragma unroll
-    for (int cb = 0; cb < 2; ++cb)
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii) {
-        float sacc = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int e = cb * 16 + ii * 4 + jj;
-          const float m = bf16_to_f32((e & 1) ? (mw[e >> 1] >> 16) : (mw[e >> 1] & 0xFFFFu));
-          sacc = jj == 0 ? o[4 * cb] * m : fmaf(o[4 * cb + jj], m, sacc);
-        }
-        y[4 * cb + ii] = sacc;
-      }
-    const int hq = hh * p.rep + hr;
-    const long long orow = (static_cast<long long>(bb) * p.kv_heads * p.rep + hq) * p.nq + i;
-    if (p.out_f32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHeadDim + 8 * l8);
-      dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-      dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-    } else {
-      uint4 v;
-      v.x = f32_to_bf16_bits(y[0]) | (f32_to_bf16_bits(y[1]) << 16);
-      v.y = f32_to_bf16_bits(y[2]) | (f32_to_bf16_bits(y[3]) << 16);
-      v.z = f32_to_bf16_bits(y[4]) | (f32_to_bf16_bits(y[5]) << 16);
-      v.w = f32_to_bf16_bits(y[6]) | (f32_to_bf16_bits(y[7]) << 16);
-      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kHeadDim + 8 * l8) = v;
-    }
-  };
-  auto load_rot = [&](int l8, uint32_t (&mw)[16]) {
-    const uint4* r4 = reinterpret_cast<const uint4*>(p.rot) + l8 * 4;
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const uint4 v = __ldg(r4 + q4);
-      mw[4 * q4] = v.x; mw[4 * q4 + 1] = v.y; mw[4 * q4 + 2] = v.z; mw[4 * q4 + 3] = v.w;
-    }
-  };
-  // segments of unit u: CTAs k_first .. k_last (partial slots u + k)
-  auto seg_range = [&](int u, int& k_first, int& nseg) {
-    k_first = cta_of(p.prefix[u], W, G);
-    nseg = cta_of(p.prefix[u + 1] - 1, W, G) - k_first + 1;
-  };
-
   // ---- finish this CTA's segment of unit u: fold the value-bias sums into O
   // and merge the token streams (log-sum-exp) into obuf; a unit held by this
   // CTA alone is finalised at once, a shared one leaves a partial (O, running
@@ -809,21 +821,21 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     }
     // obuf holds the CTA's O for the unit; per row M = max and L = sum over the streams
     int k_first, nseg;
-    seg_range(u, k_first, nseg);
+    seg_range(p, u, k_first, nseg);
     const int ub = p.unit_base + u;
     if (nseg == 1) {  // the whole unit is here: finalise
       for (int idx = threadIdx.x; idx < GT * 32; idx += NCT) {
         const int r = idx >> 5, l8 = idx & 31;
         if ((qt * GT + r) / p.rep >= p.nq) continue;
         uint32_t mw[16];
-        load_rot(l8, mw);
+        load_rot(p, l8, mw);
         float L = lbuf[r];
 #pragma unroll
         for (int s = 1; s < STREAMS; ++s) L += lbuf[s * GT + r];
         const float4 o0 = reinterpret_cast<const float4*>(obuf + r * kHeadDim + 8 * l8)[0];
         const float4 o1 = reinterpret_cast<const float4*>(obuf + r * kHeadDim + 8 * l8)[1];
         const float acc[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-        store_out(ub, r, l8, acc, L, mw);
+        store_out<GT>(p, ub, r, l8, acc, L, mw);
       }
     } else {  // partial for the combine: slot u + k_cta
       const long long slot = static_cast<long long>(u) + k_cta;
@@ -840,54 +852,6 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         reinterpret_cast<float2*>(p.part_ml)[slot * GT + r] = make_float2(M, L);
       }
     }
-  };
-
-  // ---- combine unit u from its segments' partials (log-sum-exp, online over
-  // the segments, eight segments' loads in flight), then finalise
-  auto combine = [&](int u) {
-    int k_first, nseg;
-    seg_range(u, k_first, nseg);
-    const long long slot0 = static_cast<long long>(u) + k_first;
-    const int ub = p.unit_base + u;
-    for (int idx = threadIdx.x; idx < GT * 32; idx += NCT) {
-      const int r = idx >> 5, l8 = idx & 31;
-      if (((ub % p.nqt) * GT + r) / p.rep >= p.nq) continue;
-      uint32_t mw[16];
-      load_rot(l8, mw);
-      float M = NEG_INF, L = 0.f;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int s0 = 0; s0 < nseg; s0 += 8) {
-        float2 ml[8];
-        float4 oa[8], ob[8];
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-          if (s0 + q8 < nseg) {
-            const long long sl = slot0 + s0 + q8;
-            ml[q8] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl * GT + r);
-            const float4* o = reinterpret_cast<const float4*>(p.part_o + (sl * GT + r) * kHeadDim + 8 * l8);
-            oa[q8] = __ldcg(o);
-            ob[q8] = __ldcg(o + 1);
-          } else {
-            ml[q8] = make_float2(NEG_INF, 0.f);
-            oa[q8] = ob[q8] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-          if (ml[q8].x == NEG_INF) continue;  // empty segment
-          const float Mn = fmaxf(M, ml[q8].x);
-          const float so = M == NEG_INF ? 0.f : ex2_approx(M - Mn);
-          const float w = ex2_approx(ml[q8].x - Mn);
-          const float v[8] = {oa[q8].x, oa[q8].y, oa[q8].z, oa[q8].w, ob[q8].x, ob[q8].y, ob[q8].z, ob[q8].w};
-#pragma unroll
-          for (int d = 0; d < 8; ++d) acc[d] = fmaf(w, v[d], acc[d] * so);
-          L = fmaf(w, ml[q8].y, L * so);
-          M = Mn;
-        }
-      }
-      store_out(ub, r, l8, acc, L, mw);
-    }
-    if (threadIdx.x == 0) p.counters[ub] = 0;  // ready for the next call
   };
 
   // ------------------------------------------------------------ main loop over this CTA's tiles
@@ -935,24 +899,61 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     if (!ok || gt >= g1) break;
     ++u;
   }
-  // arrivals for the shared units this CTA touched (only its first and last
-  // can be shared), deferred to here so no mid-range unit boundary waits on a
-  // fence or an atomic; the last CTA to arrive at a unit combines it
-  {
-    int kf, ns0, ns1;
-    seg_range(u0, kf, ns0);
-    seg_range(u, kf, ns1);
-    __threadfence();  // partials visible before the arrivals
-    named_bar(1, NCT);
-    if (threadIdx.x == 0) {
-      s_flag[0] = ns0 > 1 && atomicAdd(p.counters + p.unit_base + u0, 1u) + 1 == static_cast<unsigned>(ns0);
-      s_flag[1] = u != u0 && ns1 > 1 && atomicAdd(p.counters + p.unit_base + u, 1u) + 1 == static_cast<unsigned>(ns1);
+}
+
+
+// ------------------------------------------------------------------ combine
+// One CTA per unit of the launch; units held by a single CTA were finalised by
+// it and are skipped.  Each thread merges one (row, 8-dim chunk) over the
+// unit's segments (log-sum-exp, online over the segments, eight segments'
+// loads in flight), then normalises, undoes the rotation and stores.
+template <int GT>
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Params p) {
+  pdl_wait();  // the attention grid has finished and its partials are visible
+  const int u = blockIdx.x;
+  if (u >= p.num_units) return;
+  int k_first, nseg;
+  seg_range(p, u, k_first, nseg);
+  if (nseg == 1) return;
+  const long long slot0 = static_cast<long long>(u) + k_first;
+  const int ub = p.unit_base + u;
+  for (int idx = threadIdx.x; idx < GT * 32; idx += blockDim.x) {
+    const int r = idx >> 5, l8 = idx & 31;
+    if (((ub % p.nqt) * GT + r) / p.rep >= p.nq) continue;
+    uint32_t mw[16];
+    load_rot(p, l8, mw);
+    float M = NEG_INF, L = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < nseg; s0 += 8) {
+      float2 ml[8];
+      float4 oa[8], ob[8];
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        if (s0 + q8 < nseg) {
+          const long long sl = slot0 + s0 + q8;
+          ml[q8] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl * GT + r);
+          const float4* o = reinterpret_cast<const float4*>(p.part_o + (sl * GT + r) * kHeadDim + 8 * l8);
+          oa[q8] = __ldcg(o);
+          ob[q8] = __ldcg(o + 1);
+        } else {
+          ml[q8] = make_float2(NEG_INF, 0.f);
+          oa[q8] = ob[q8] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        if (ml[q8].x == NEG_INF) continue;  // empty segment
+        const float Mn = fmaxf(M, ml[q8].x);
+        const float so = M == NEG_INF ? 0.f : ex2_approx(M - Mn);
+        const float w = ex2_approx(ml[q8].x - Mn);
+        const float v[8] = {oa[q8].x, oa[q8].y, oa[q8].z, oa[q8].w, ob[q8].x, ob[q8].y, ob[q8].z, ob[q8].w};
+#pragma unroll
+        for (int d = 0; d < 8; ++d) acc[d] = fmaf(w, v[d], acc[d] * so);
+        L = fmaf(w, ml[q8].y, L * so);
+        M = Mn;
+      }
     }
-    named_bar(1, NCT);
-    const int f0 = s_flag[0], f1 = s_flag[1];
-    if (f0 || f1) __threadfence();
-    if (f0) combine(u0);
-    if (f1) combine(u);
+    store_out<GT>(p, ub, r, l8, acc, L, mw);
   }
 }
 
@@ -965,8 +966,10 @@ struct Plan {
   size_t units, slots, head_bytes, bytes;
 };
 
-// workspace: [status word, padded to 256 B][per-unit segment counters, padded
-// to 256 B][partial O: slots x GT x 256 f32][partial (max, sum): slots x GT x 2 f32]
+// workspace: [status word, padded to 256 B][partial O: slots x GT x 256 f32]
+// [partial (max, sum): slots x GT x 2 f32].  The status word accumulates
+// failure bits until iq_read_status reads and clears it; nothing else needs
+// initialising (partials are written before the combine reads them).
 constexpr size_t kStatusBytes = 256;
 
 template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
@@ -1082,7 +1085,7 @@ int make_plan(const iq_cache* c, int q_heads, int nq, int causal, Plan* pl, cons
   }
   if (!tiles)  // independent of the tile counts, so it bounds every later plan
     pl->slots = std::min(pl->units, static_cast<size_t>(UNIT_CAP)) + static_cast<size_t>(slots_hw);
-  pl->head_bytes = kStatusBytes + (pl->units * sizeof(unsigned) + 255) / 256 * 256;
+  pl->head_bytes = kStatusBytes;
   pl->bytes = pl->head_bytes + pl->slots * pl->gt * (kHeadDim + 2) * sizeof(float);
   return IQ_OK;
 }
@@ -1140,6 +1143,18 @@ int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStrea
     return fail(IQ_ERR_UNSUPPORTED, "attention kernel built with an unexpected register count");
   attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
   IQ_CUDA(cudaGetLastError());
+  // the split combine, launched as a programmatic dependent of the attention grid
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(prm.num_units));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  IQ_CUDA(cudaLaunchKernelEx(&cfg, combine_kernel<C::GT>, prm));
   return IQ_OK;
 }
 
@@ -1200,12 +1215,8 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   unsigned* status = reinterpret_cast<unsigned*>(ws);
-  unsigned* counters = reinterpret_cast<unsigned*>(ws + kStatusBytes);
   float* part_o = reinterpret_cast<float*>(ws + bound.head_bytes);
   float* part_ml = part_o + bound.slots * pl.gt * kHeadDim;
-  // status word and segment counters start at zero (the combining CTA resets
-  // its unit's counter too, so this matters only for a fresh workspace)
-  IQ_CUDA(cudaMemsetAsync(ws, 0, pl.head_bytes, s));
 
   static thread_local Params prm;  // ~5 KB: kept off the stack
   std::memset(&prm, 0, sizeof(prm));
@@ -1220,7 +1231,6 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   prm.part_o = part_o;
   prm.part_ml = part_ml;
   prm.status = status;
-  prm.counters = counters;
   prm.out = out;
   prm.out_f32 = out_f32 ? 1 : 0;
   prm.batch = c->batch;

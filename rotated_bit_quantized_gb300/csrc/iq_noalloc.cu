@@ -66,8 +66,8 @@ extern "C" int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q
   void* scratch = nullptr;
   st = iq::scratch_address(&scratch);
   if (st != IQ_OK) return st;
-  // iq_attend clears the status word at the start of every call; the split
-  // partials are written before they are read, so nothing else needs zeroing.
+  // The array is zero when the library loads, so its status word starts
+  // clear; the split partials are written before they are read.
   return iq_attend(cache, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, scratch,
                    IQ_NOALLOC_SCRATCH_BYTES, stream);
 }
