@@ -71,6 +71,7 @@ struct Tiling {
   static_assert(TILE % 32 == 0 && TILE <= 256 && 256 % TILE == 0, "tile must divide the capacity granule");
 };
 constexpr int UNIT_CAP = 1024;   // units per launch (their tile prefix travels by value)
+constexpr int GRID_CAP = 1024;   // CTAs per launch (their tile ranges travel by value)
 constexpr int MIN_TILES_PER_CTA = 8;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float NEG_INF = -__builtin_huge_valf();
@@ -106,6 +107,7 @@ struct Params {
   float scale;
   int lens[IQ_MAX_BATCH];
   int prefix[UNIT_CAP + 1];  // tile prefix over this launch's units
+  int cstart[GRID_CAP + 1];  // CTA k streams tiles [cstart[k], cstart[k+1]) (maybe none)
 };
 
 __device__ __forceinline__ int tile_limit(const Params& p, int T, int qt, int gt) {
@@ -114,17 +116,22 @@ __device__ __forceinline__ int tile_limit(const Params& p, int T, int qt, int gt
   return T - p.nq + rmax / p.rep + 1;
 }
 
-// CTA that owns global tile x when W tiles are split evenly over G CTAs
-__device__ __forceinline__ int cta_of(long long x, long long W, int G) {
-  return static_cast<int>(((x + 1) * G - 1) / W);
+// The CTA that streams tile x: the last k with cstart[k] <= x (never one with
+// an empty range).
+__device__ __forceinline__ int cta_of(const Params& p, long long x) {
+  int lo = 0, hi = p.grid - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cstart[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
-// segments of unit u of this launch: CTAs k_first .. k_first + nseg - 1
-// (partial slots u + k)
-__device__ __forceinline__ void seg_range(const Params& p, int u, int& k_first, int& nseg) {
-  const long long W = p.prefix[p.num_units];
-  k_first = cta_of(p.prefix[u], W, p.grid);
-  nseg = cta_of(p.prefix[u + 1] - 1, W, p.grid) - k_first + 1;
+// CTAs holding tiles of unit u of this launch: k_first .. k_last (partial
+// slots u + k; CTAs in between with empty ranges hold no partial)
+__device__ __forceinline__ void seg_range(const Params& p, int u, int& k_first, int& k_last) {
+  k_first = cta_of(p, p.prefix[u]);
+  k_last = cta_of(p, p.prefix[u + 1] - 1);
 }
 
 // The two M_b blocks of output dims 8*l8 .. 8*l8+7 (32 bf16).
@@ -313,10 +320,11 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   int* s_flag = reinterpret_cast<int*>(smem + C::OFF_FLAG);
 
   // ---- this CTA's even share of the launch's tiles
-  const int G = p.grid;
-  const long long W = p.prefix[p.num_units];
   const int k_cta = blockIdx.x;
-  const long long g0 = W * k_cta / G, g1 = W * (k_cta + 1) / G;
+  const long long g0 = p.cstart[k_cta], g1 = p.cstart[k_cta + 1];
+  // launched as a programmatic dependent of the previous kernel in the stream:
+  // wait for it (and its writes) before touching any memory it may produce
+  pdl_wait();
   pdl_launch_dependents();
   if (g0 >= g1) return;
   int u0 = 0;  // unit holding tile g0: last u with prefix[u] <= g0
@@ -820,10 +828,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       named_bar(1, NCT);
     }
     // obuf holds the CTA's O for the unit; per row M = max and L = sum over the streams
-    int k_first, nseg;
-    seg_range(p, u, k_first, nseg);
     const int ub = p.unit_base + u;
-    if (nseg == 1) {  // the whole unit is here: finalise
+    if (p.prefix[u] >= g0 && p.prefix[u + 1] <= g1) {  // the whole unit is here: finalise
       for (int idx = threadIdx.x; idx < GT * 32; idx += NCT) {
         const int r = idx >> 5, l8 = idx & 31;
         if ((qt * GT + r) / p.rep >= p.nq) continue;
@@ -912,9 +918,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Pa
   pdl_wait();  // the attention grid has finished and its partials are visible
   const int u = blockIdx.x;
   if (u >= p.num_units) return;
-  int k_first, nseg;
-  seg_range(p, u, k_first, nseg);
-  if (nseg == 1) return;
+  int k_first, k_last;
+  seg_range(p, u, k_first, k_last);
+  if (k_first == k_last) return;
+  const int nseg = k_last - k_first + 1;
   const long long slot0 = static_cast<long long>(u) + k_first;
   const int ub = p.unit_base + u;
   for (int idx = threadIdx.x; idx < GT * 32; idx += blockDim.x) {
@@ -929,7 +936,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Pa
       float4 oa[8], ob[8];
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
-        if (s0 + q8 < nseg) {
+        const int kk = k_first + s0 + q8;
+        if (s0 + q8 < nseg && p.cstart[kk] < p.cstart[kk + 1]) {
           const long long sl = slot0 + s0 + q8;
           ml[q8] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl * GT + r);
           const float4* o = reinterpret_cast<const float4*>(p.part_o + (sl * GT + r) * kHeadDim + 8 * l8);
@@ -942,7 +950,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Pa
       }
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
-        if (ml[q8].x == NEG_INF) continue;  // empty segment
+        if (ml[q8].x == NEG_INF) continue;  // empty segment or CTA without tiles
         const float Mn = fmaxf(M, ml[q8].x);
         const float so = M == NEG_INF ? 0.f : ex2_approx(M - Mn);
         const float w = ex2_approx(ml[q8].x - Mn);
@@ -1018,6 +1026,9 @@ int blocks_per_sm() {
 #ifndef IQ_DECODE_PAIR
 #define IQ_DECODE_PAIR 2
 #endif
+#ifndef IQ_DECODE_BOUNDARY
+#define IQ_DECODE_BOUNDARY 3
+#endif
 #define IQ_DECODE_CFG 1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB, IQ_DECODE_TILE, IQ_DECODE_PAIR
 #ifndef IQ_MULTI_NT
 #define IQ_MULTI_NT 2
@@ -1039,6 +1050,9 @@ int blocks_per_sm() {
 #endif
 #ifndef IQ_MULTI_PAIR
 #define IQ_MULTI_PAIR 1
+#endif
+#ifndef IQ_MULTI_BOUNDARY
+#define IQ_MULTI_BOUNDARY 3
 #endif
 #define IQ_MULTI_CFG IQ_MULTI_NT, IQ_MULTI_DS, IQ_MULTI_STREAMS, IQ_MULTI_STAGES, IQ_MULTI_MINB, IQ_MULTI_TILE, IQ_MULTI_PAIR
 
@@ -1079,15 +1093,37 @@ int make_plan(const iq_cache* c, int q_heads, int nq, int causal, Plan* pl, cons
     } else {
       W = static_cast<long long>(nu) * max_tiles;
     }
-    const long long G = std::min(slots_hw, std::max(1LL, W / MIN_TILES_PER_CTA));
+    const long long G = std::min(std::min(slots_hw, static_cast<long long>(GRID_CAP)),
+                                 std::max(1LL, W / MIN_TILES_PER_CTA));
     pl->grid[l] = static_cast<int>(G);
     pl->slots = std::max(pl->slots, nu + static_cast<size_t>(G));
   }
   if (!tiles)  // independent of the tile counts, so it bounds every later plan
-    pl->slots = std::min(pl->units, static_cast<size_t>(UNIT_CAP)) + static_cast<size_t>(slots_hw);
+    pl->slots = std::min(pl->units, static_cast<size_t>(UNIT_CAP)) +
+                static_cast<size_t>(std::min(slots_hw, static_cast<long long>(GRID_CAP)));
   pl->head_bytes = kStatusBytes;
   pl->bytes = pl->head_bytes + pl->slots * pl->gt * (kHeadDim + 2) * sizeof(float);
   return IQ_OK;
+}
+
+// Tile ranges of the G CTAs of a launch.  Starting a unit costs a CTA about
+// `boundary` tiles' worth of time (finishing the previous unit's segment and
+// rotating the new queries), so the ranges split evenly a virtual line on
+// which every unit after the first is preceded by that many virtual tiles: a
+// CTA that crosses unit starts streams correspondingly fewer real tiles.
+void split_ranges(const int* prefix, int nu, int G, int boundary, int* cstart) {
+  const long long W = prefix[nu];
+  const long long V = W + static_cast<long long>(boundary) * (nu - 1);
+  int u = 0;
+  cstart[0] = 0;
+  for (int k = 1; k < G; ++k) {
+    const long long v = V * k / G;
+    // unit u's real tiles sit at virtual [prefix[u] + boundary*u, prefix[u+1] + boundary*u)
+    while (u < nu - 1 && v >= prefix[u + 1] + static_cast<long long>(boundary) * u) ++u;
+    const long long vs = prefix[u] + static_cast<long long>(boundary) * u;
+    cstart[k] = static_cast<int>(v < vs ? prefix[u] : std::min<long long>(v - static_cast<long long>(boundary) * u, prefix[u + 1]));
+  }
+  cstart[G] = static_cast<int>(W);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1141,19 +1177,24 @@ int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStrea
   }
   if (launch_regs != C::LAUNCH_REGS)
     return fail(IQ_ERR_UNSUPPORTED, "attention kernel built with an unexpected register count");
-  attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR><<<grid, C::THREADS, C::SMEM, s>>>(prm, map);
-  IQ_CUDA(cudaGetLastError());
-  // the split combine, launched as a programmatic dependent of the attention grid
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(prm.num_units));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
+  // Both kernels are programmatic dependents of their predecessor in the
+  // stream: their launch overlaps its tail, and each waits for it
+  // (griddepcontrol.wait) before reading anything.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  IQ_CUDA(cudaLaunchKernelEx(&cfg, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>, prm, map));
+  // the split combine, after the attention grid
+  cfg.gridDim = dim3(static_cast<unsigned>(prm.num_units));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
   IQ_CUDA(cudaLaunchKernelEx(&cfg, combine_kernel<C::GT>, prm));
   return IQ_OK;
 }
@@ -1251,6 +1292,7 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
     prm.grid = pl.grid[l];
     prm.prefix[0] = 0;
     for (int u = 0; u < nu; ++u) prm.prefix[u + 1] = prm.prefix[u] + tiles[u0 + u];
+    split_ranges(prm.prefix, nu, prm.grid, pl.nt == 1 ? IQ_DECODE_BOUNDARY : IQ_MULTI_BOUNDARY, prm.cstart);
     st = pl.nt == 1 ? launch_attend<IQ_DECODE_CFG>(prm, map, prm.grid, s)
                     : launch_attend<IQ_MULTI_CFG>(prm, map, prm.grid, s);
     if (st != IQ_OK) return st;

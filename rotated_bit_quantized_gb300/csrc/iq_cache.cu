@@ -210,6 +210,9 @@ __device__ __forceinline__ void encode_row(const uint4 raw, const float (&m)[2][
 #define IQ_APPEND_MINB 3
 #endif
 __global__ void __launch_bounds__(256, IQ_APPEND_MINB) append_kernel(const __grid_constant__ AppendParams p) {
+  // the next kernel in the stream (attention) may launch now; it waits for
+  // this grid's completion before it reads the cache
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int gwarp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);  // within this (b, h)
   const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
