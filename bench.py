@@ -37,6 +37,24 @@ METRIC = "quantized-KV decode attention: KV tokens/s and HBM GB/s vs ~8 TB/s roo
 UNIT = "KV tokens/s"
 K_ROW, V_ROW = 144, 112  # algorithmic bytes per token-head: codes + bf16 scales/biases
 
+# DRAM bytes (read + write) per iq_attend call on the default workload, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of attend_kernel and
+# combine_kernel; profiles/attend_kernel_batched_decode_32x32k.md).  Reported
+# only while the attention source is the one that was measured.
+TRAFFIC = {"source": "rotated_bit_quantized_gb300/csrc/iq_attend.cu", "sha256": None, "bytes": None}
+
+
+def measured_traffic():
+    import hashlib
+    if not TRAFFIC["sha256"]:
+        return None
+    try:
+        with open(os.path.join(ROOT, TRAFFIC["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return TRAFFIC["bytes"] if digest == TRAFFIC["sha256"] else None
+
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -272,9 +290,10 @@ def run_ours(args):
                        "parallelism": f"replicas x{ws}",
                        "l2": f"no flush: the cache read per step ({token_heads * (K_ROW + V_ROW) / 1e6:.0f} MB) "
                              f"{'exceeds' if token_heads * (K_ROW + V_ROW) > 129e6 else 'is below'} the 129 MB L2"},
-            "roofline": {"bound": "hbm", "kernel": "attend_kernel (iq_attend: split-KV attention with fused combine)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "iq_attend: attend_kernel (split-KV attention) + combine_kernel (split merge)",
                          "achieved": achieved, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": None,
+                         "frac": achieved / hbm, "traffic": measured_traffic(),
                          "bytes_per_token_head": K_ROW + V_ROW, "token_heads_per_launch": token_heads,
                          "avg_launch_us": attn_avg_s * 1e6},
             "e2e": {"value": e_tokens_all / (e_ms_max / 1e3), "unit": UNIT,

@@ -25,9 +25,9 @@
 //    ahead across unit boundaries; its warpgroup hands most of its registers
 //    to the consumer warps;
 //  * consumer warps unpack codes in registers with bit tricks and run m16n8k16
-//    tensor-core MMAs: S = (64 + K_codes) . q (fp16, per 64-dim group, fp32
-//    accumulate), folded with the group scale and (bias - 64 scale) on CUDA
-//    cores; online
+//    tensor-core MMAs: S = (64 + K_codes) . q - 64 sum(q) (fp16, per 64-dim
+//    group, fp32 accumulate from -64 sum(q)), folded with the group scale and
+//    bias on CUDA cores; online
 //    softmax in fp32 with a lazily moving reference max; O^T += (V_codes - 4)^T
 //    . (P * s_v) with P transposed in registers by movmatrix; the value bias
 //    term sum_t p_t (b_t + 4 s_t) on CUDA cores.
@@ -152,9 +152,10 @@ __device__ __forceinline__ void store_out(const Params& p, int ub, int r, int l8
   const int R = (ub % p.nqt) * GT + r, i = R / p.rep, hr = R % p.rep;
   const int bb = ub / (p.kv_heads * p.nqt), hh = (ub / p.nqt) % p.kv_heads;
   if (!(L > 0.f)) atomicOr(p.status, 4u);
+  const float inv = __frcp_rn(L);
   float o[8];
 #pragma unroll
-  for (int d = 0; d < 8; ++d) o[d] = __fdiv_rn(acc[d], L);
+  for (int d = 0; d < 8; ++d) o[d] = acc[d] * inv;
   float y[8];
 #pragma unroll
   for (int cb = 0; cb < 2; ++cb)
@@ -199,9 +200,9 @@ __device__ __forceinline__ float pick_bf16(uint2 v, int G) {
 
 // Key codes enter the q.K product as fp16 values 64 + c: a nibble ORed into
 // bits 4..7 of the half 0x5400 (64.0, mantissa step 1 from bit 4 up) is
-// exactly 64 + c.  The 64 * sum(q'') offset is removed in the per-token fold,
-// where it becomes part of the bias (b - 64 s).  The query operand is q''
-// converted to fp16 (exact for 2^-14 <= |q''| < 65504).
+// exactly 64 + c.  The 64 * sum(q'') offset is removed by starting the
+// accumulator at -64 * sum(q'').  The query operand is q'' converted to fp16
+// (exact for 2^-14 <= |q''| < 65504).
 constexpr float KOFFSET = 64.0f;
 
 // The 16 codes of two consecutive words (dims 0..7 in w0, 8..15 in w1) ->
@@ -400,7 +401,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   // per-unit state
   int b = 0, kvh = 0, qt = 0, T = 0, limit = 0, qmin = 0;
   int qpos[NT][2];
-  float qsr[GPW][NT][2];
+  float qsr[GPW][NT][2];   // per group: sum of q'' over the group's dims (rows 2t, 2t+1 of each n-tile)
+  float qoff[GPW][NT][2];  // -64 * qsr: the score accumulators start there, cancelling the code offset
   float O[GPW][4][NT][4];
   float bacc[GPW][NT][2];
   float msc[NT][2], lrow[NT][2];  // reference max (log2 units), partial row sum
@@ -490,6 +492,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       for (int j = 0; j < NT; ++j) {
         qsr[gi][j][0] = qsum[(8 * j + 2 * t) * 4 + Gr];
         qsr[gi][j][1] = qsum[(8 * j + 2 * t + 1) * 4 + Gr];
+        qoff[gi][j][0] = -KOFFSET * qsr[gi][j][0];
+        qoff[gi][j][1] = -KOFFSET * qsr[gi][j][1];
       }
     }
 #pragma unroll
@@ -535,15 +539,16 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       kbi1[n] = lds64(sb + OFF_KB + rr1[n] * 8);
     }
 
-    // scores: per group, S_G = (64 + codes) . q'' (fp32), folded with scale/bias
+    // scores: per group, S_G = (64 + codes) . q'' - 64 sum(q'') = codes . q''
+    // (fp32; the accumulator starts at -64 sum(q'')), folded with scale/bias
     float sc[N][NT][4];
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
       const int Gr = dg * GPW + gi;
-      const uint32_t chunk16 = 2 * Gr + (t >> 1);
       uint32_t RA[N][8], RB[N][8];
 #pragma unroll
       for (int n = 0; n < N; ++n) {
+        const uint32_t chunk16 = 2 * Gr + (t >> 1);
         const uint32_t a0 = sb + OFF_K + rr0[n] * 128 + ((chunk16 ^ (rr0[n] & 7)) << 4) + kswz;
         const uint32_t a1 = sb + OFF_K + rr1[n] * 128 + ((chunk16 ^ (rr1[n] & 7)) << 4) + kswz;
         const uint2 w0 = lds64(a0), w1 = lds64(a1);
@@ -554,7 +559,10 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
       for (int n = 0; n < N; ++n)
 #pragma unroll
-        for (int j = 0; j < NT; ++j) acc[n][j][0] = acc[n][j][1] = acc[n][j][2] = acc[n][j][3] = 0.f;
+        for (int j = 0; j < NT; ++j) {
+          acc[n][j][0] = acc[n][j][2] = qoff[gi][j][0];
+          acc[n][j][1] = acc[n][j][3] = qoff[gi][j][1];
+        }
 #pragma unroll
       for (int s = 0; s < 4; ++s)
 #pragma unroll
@@ -569,8 +577,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
       for (int n = 0; n < N; ++n) {
         const float s0 = pick_bf16(ksc0[n], Gr), s1 = pick_bf16(ksc1[n], Gr);
-        const float b0 = fmaf(-KOFFSET, s0, pick_bf16(kbi0[n], Gr));
-        const float b1 = fmaf(-KOFFSET, s1, pick_bf16(kbi1[n], Gr));
+        const float b0 = pick_bf16(kbi0[n], Gr), b1 = pick_bf16(kbi1[n], Gr);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {  // this warp's groups, summed in group order
           float* c = sc[n][j];
@@ -911,8 +918,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 // ------------------------------------------------------------------ combine
 // One CTA per unit of the launch; units held by a single CTA were finalised by
 // it and are skipped.  Each thread merges one (row, 8-dim chunk) over the
-// unit's segments (log-sum-exp, online over the segments, eight segments'
-// loads in flight), then normalises, undoes the rotation and stores.
+// unit's segments (log-sum-exp over batches of eight segments whose loads are
+// in flight together), then normalises, undoes the rotation and stores.
 template <int GT>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Params p) {
   pdl_wait();  // the attention grid has finished and its partials are visible
@@ -948,18 +955,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Pa
           oa[q8] = ob[q8] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
+      // merge the batch: its max first, then independent weights (empty
+      // segments and CTAs without tiles carry a max of -inf and weigh 0)
+      float Mb = M;
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) Mb = fmaxf(Mb, ml[q8].x);
+      if (Mb == NEG_INF) continue;
+      const float so = M == NEG_INF ? 0.f : ex2_approx(M - Mb);
+#pragma unroll
+      for (int d = 0; d < 8; ++d) acc[d] *= so;
+      L *= so;
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
-        if (ml[q8].x == NEG_INF) continue;  // empty segment or CTA without tiles
-        const float Mn = fmaxf(M, ml[q8].x);
-        const float so = M == NEG_INF ? 0.f : ex2_approx(M - Mn);
-        const float w = ex2_approx(ml[q8].x - Mn);
+        const float w = ml[q8].x == NEG_INF ? 0.f : ex2_approx(ml[q8].x - Mb);
         const float v[8] = {oa[q8].x, oa[q8].y, oa[q8].z, oa[q8].w, ob[q8].x, ob[q8].y, ob[q8].z, ob[q8].w};
 #pragma unroll
-        for (int d = 0; d < 8; ++d) acc[d] = fmaf(w, v[d], acc[d] * so);
-        L = fmaf(w, ml[q8].y, L * so);
-        M = Mn;
+        for (int d = 0; d < 8; ++d) acc[d] = fmaf(w, v[d], acc[d]);
+        L = fmaf(w, ml[q8].y, L);
       }
+      M = Mb;
     }
     store_out<GT>(p, ub, r, l8, acc, L, mw);
   }
@@ -1049,7 +1063,7 @@ int blocks_per_sm() {
 #define IQ_MULTI_TILE 128
 #endif
 #ifndef IQ_MULTI_PAIR
-#define IQ_MULTI_PAIR 1
+#define IQ_MULTI_PAIR 2
 #endif
 #ifndef IQ_MULTI_BOUNDARY
 #define IQ_MULTI_BOUNDARY 3
