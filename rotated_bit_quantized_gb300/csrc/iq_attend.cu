@@ -1,5 +1,5 @@
-// libiqkv: GQA attention over the packed K4/V3 cache (persistent stream-K
-// kernel with the split combine and the inverse rotation fused in).
+// libiqkv: GQA attention over the packed K4/V3 cache (persistent split-KV
+// kernel with the inverse rotation fused in, and the split combine kernel).
 //
 // Method source: page "sparkle mlx_streaming/core/cache/quant_kv.py",
 // `asym_quantized_sdpa` (scale the queries, GQA reshape so query head h reads
@@ -9,14 +9,14 @@
 // rotation; `rotate_last` gives the query rotation.
 //
 // Work decomposition.  A "unit" is (sequence, kv head, tile of 8*NT query
-// rows); its keys form a run of 64-token tiles.  All units' tiles are laid
-// end to end and split evenly over a persistent grid (at most one CTA per
-// resident slot), so every CTA streams the same number of tiles; a CTA whose
-// range crosses unit boundaries finishes one unit segment and starts the
-// next.  Each segment writes an un-normalised partial (O, running max in log2
-// units, running sum); the CTA that finishes a unit's last segment (an atomic
-// counter per unit) merges the unit's partials (log-sum-exp), divides,
-// applies M_b^T and stores bf16 or fp32.
+// rows); its keys form a run of TILE-token tiles.  All units' tiles are laid
+// end to end and split over a persistent grid (at most one CTA per resident
+// slot); the host gives each CTA an explicit tile range, balanced so that a CTA
+// crossing unit starts streams fewer tiles.  A CTA whose range holds a whole
+// unit finishes it (normalise, inverse rotation, store); a unit shared by
+// several CTAs gets an un-normalised partial (O, running max in log2 units,
+// running sum) from each, merged afterwards by combine_kernel, a programmatic
+// dependent launch.
 //
 // Inside a CTA:
 //  * a producer warp streams the tiles (packed K codes by a 2-D tensor copy with
@@ -27,8 +27,8 @@
 //  * consumer warps unpack codes in registers with bit tricks and run m16n8k16
 //    tensor-core MMAs: S = (64 + K_codes) . q - 64 sum(q) (fp16, per 64-dim
 //    group, fp32 accumulate from -64 sum(q)), folded with the group scale and
-//    bias on CUDA cores; online
-//    softmax in fp32 with a lazily moving reference max; O^T += (V_codes - 4)^T
+//    bias on CUDA cores; online softmax in fp32 with a lazily moving
+//    reference max; O^T += (V_codes - 4)^T
 //    . (P * s_v) with P transposed in registers by movmatrix; the value bias
 //    term sum_t p_t (b_t + 4 s_t) on CUDA cores.
 #include <cuda.h>
