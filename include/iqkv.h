@@ -160,6 +160,7 @@ int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of,
  * and these shapes (status word and the split-KV partial results); the size
  * does not depend on the lengths.
  */
+#define IQ_WORKSPACE_HEAD_BYTES 4352u
 int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_t* bytes);
 
 /*
@@ -176,11 +177,14 @@ int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_
  * out: device [B][Hq][n_queries][head_dim], bf16 (out_f32 == 0) or float32
  *    (out_f32 == 1), in unrotated space: out = bf16(o @ M_b^T).
  * workspace: device buffer of at least iq_attend_workspace() bytes,
- *    256-byte aligned.  Its first 4 bytes are the status word, which must be
- *    zero before the first call (e.g. a zero-filled allocation); kernels only
- *    ever set bits in it and iq_read_status clears it.  The rest needs no
- *    initialisation.  Two kernels run per 1024 query tiles: the attention
- *    grid and, as its programmatic dependent, the split combine.
+ *    256-byte aligned.  Its first IQ_WORKSPACE_HEAD_BYTES (the status word
+ *    and per-unit partial counters) must be zero before the first call (e.g.
+ *    a zero-filled allocation); the kernels return the counters to zero and
+ *    only ever set bits in the status word, which iq_read_status clears.  The
+ *    rest needs no initialisation.  Two kernels run per 1024 query tiles: the
+ *    attention grid and, as its programmatic dependent, the split combine,
+ *    which merges each split unit as soon as its partials are stored and
+ *    completes after the attention grid.
  * Scores, softmax and P.V accumulate in float32 on tensor cores; dequantised
  * key codes enter the products exactly; P times the value scale enters as fp16.
  * Errors: INVALID_ARG (null, bad causal flag, empty sequence, lens[b] <
@@ -209,8 +213,9 @@ int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queri
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.
  * Sharing: every call uses the same array and it keeps the last call's
- * contents (the partials are written before they are read; the status word,
- * zero at load, only ever gains bits).  Calls that can run at the same time on the GPU
+ * contents (the partials are written before they are read; the head, zero at
+ * load, keeps its counters at zero between calls and its status word only
+ * gains bits).  Calls that can run at the same time on the GPU
  * (different streams without ordering) race on the array: serialise them.
  * Errors: as iq_attend, plus WORKSPACE when the call needs more scratch than
  * IQ_NOALLOC_SCRATCH_BYTES (use iq_attend with a caller workspace then).
@@ -224,9 +229,9 @@ int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q_heads, int
 
 /*
  * iq_read_status — synchronise `stream`, read the status word that the
- * iq_attend calls on this workspace since the last read left, and clear it.
- * *device_status is 0 when every kernel completed normally.  Blocks the
- * calling thread.
+ * iq_attend calls on this workspace since the last read left, and clear it
+ * (after a failure, the whole workspace head).  *device_status is 0 when
+ * every kernel completed normally.  Blocks the calling thread.
  */
 int iq_read_status(void* workspace, iq_stream_t stream, int* device_status);
 

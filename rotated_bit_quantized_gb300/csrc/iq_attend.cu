@@ -70,8 +70,8 @@ struct Tiling {
   static constexpr uint32_t STAGE_TX = K_BYTES + V_BYTES + 4 * SB_BYTES;
   static_assert(TILE % 32 == 0 && TILE <= 256 && 256 % TILE == 0, "tile must divide the capacity granule");
 };
-constexpr int UNIT_CAP = 1024;   // units per launch (their tile prefix travels by value)
-constexpr int GRID_CAP = 1024;   // CTAs per launch (their tile ranges travel by value)
+constexpr int UNIT_CAP = 1024;  // units per launch (their tile prefix travels by value)
+constexpr int GRID_CAP = 1024;  // CTAs per launch (their tile ranges travel by value)
 constexpr int MIN_TILES_PER_CTA = 8;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float NEG_INF = -__builtin_huge_valf();
@@ -100,6 +100,7 @@ struct Params {
   float* part_o;       // [slots][GT][256]
   float* part_ml;      // [slots][GT][2] (running max in log2 units, running sum)
   unsigned* status;
+  unsigned* counters;  // [UNIT_CAP]: partials stored per unit of this launch (the combine resets them)
   void* out;
   int out_f32;
   int batch, kv_heads, rep, nq, cap, nqt, causal;
@@ -186,9 +187,22 @@ __device__ __forceinline__ void store_out(const Params& p, int ub, int r, int l8
   }
 }
 
-// Programmatic dependent launch: the attention grid lets the combine grid be
-// scheduled early; the combine waits for the attention grid's completion
-// (and the visibility of its writes) before reading the partials.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* ptr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+constexpr unsigned long long kCombineWaitNs = 4000000000ull;  // 4 s: far above any attention grid
+
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start once every CTA of its predecessor has executed
+// launch_dependents (or exited); griddepcontrol.wait then blocks until the
+// predecessor has completed and its writes are visible.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -864,6 +878,11 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         }
         reinterpret_cast<float2*>(p.part_ml)[slot * GT + r] = make_float2(M, L);
       }
+      named_bar(1, NCT);  // every thread's partial stores precede the arrival
+      if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(p.counters + u, 1u);
+      }
     }
   };
 
@@ -921,14 +940,32 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 // unit's segments (log-sum-exp over batches of eight segments whose loads are
 // in flight together), then normalises, undoes the rotation and stores.
 template <int GT>
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Params p) {
-  pdl_wait();  // the attention grid has finished and its partials are visible
-  const int u = blockIdx.x;
-  if (u >= p.num_units) return;
+__device__ __forceinline__ void combine_unit(const Params& p, int u) {
+  __shared__ int s_ready;
   int k_first, k_last;
   seg_range(p, u, k_first, k_last);
-  if (k_first == k_last) return;
+  if (k_first == k_last) return;  // finished by the CTA that held the whole unit
   const int nseg = k_last - k_first + 1;
+  // Wait (bounded, in time) until every CTA holding tiles of the unit has
+  // stored its partial, so units are merged while the attention grid still
+  // runs; every attention CTA started before this grid was launched.
+  if (threadIdx.x == 0) {
+    unsigned expect = 0;
+    for (int k = k_first; k <= k_last; ++k) expect += p.cstart[k] < p.cstart[k + 1];
+    const unsigned long long t0 = global_ns();
+    int ready = 0;
+    for (;;) {
+      if (ld_acquire_gpu(p.counters + u) >= expect) { ready = 1; break; }
+      if (global_ns() - t0 > kCombineWaitNs) break;
+      __nanosleep(256);
+    }
+    s_ready = ready;
+  }
+  __syncthreads();
+  if (!s_ready) {
+    if (threadIdx.x == 0) atomicOr(p.status, 8u);
+    return;
+  }
   const long long slot0 = static_cast<long long>(u) + k_first;
   const int ub = p.unit_base + u;
   for (int idx = threadIdx.x; idx < GT * 32; idx += blockDim.x) {
@@ -977,6 +1014,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Pa
     }
     store_out<GT>(p, ub, r, l8, acc, L, mw);
   }
+  __syncthreads();
+  if (threadIdx.x == 0) p.counters[u] = 0;  // ready for the next call
+}
+
+
+template <int GT>
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Params p) {
+  const int u = blockIdx.x;
+  if (u < p.num_units) combine_unit<GT>(p, u);
+  // This grid may run ahead of the attention grid it depends on; it completes
+  // only after that grid has completed, so work behind it in the stream (a copy
+  // of the output) sees both grids' stores.
+  pdl_wait();
 }
 
 // ------------------------------------------------------------------ host plan
@@ -988,11 +1038,15 @@ struct Plan {
   size_t units, slots, head_bytes, bytes;
 };
 
-// workspace: [status word, padded to 256 B][partial O: slots x GT x 256 f32]
-// [partial (max, sum): slots x GT x 2 f32].  The status word accumulates
-// failure bits until iq_read_status reads and clears it; nothing else needs
-// initialising (partials are written before the combine reads them).
+// workspace: [status word, padded to 256 B][per-unit partial counters:
+// UNIT_CAP x u32][partial O: slots x GT x 256 f32][partial (max, sum): slots x
+// GT x 2 f32].  The head (status word and counters) starts zeroed; the status
+// word accumulates failure bits until iq_read_status reads it, and the combine
+// returns each counter to zero (iq_read_status re-zeroes the whole head after a
+// failure).  Partials are written before they are read.
 constexpr size_t kStatusBytes = 256;
+constexpr size_t kHeadBytes = kStatusBytes + UNIT_CAP * sizeof(unsigned);  // status word + unit counters
+static_assert(kHeadBytes == IQ_WORKSPACE_HEAD_BYTES, "workspace head size in iqkv.h");
 
 template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
 int blocks_per_sm() {
@@ -1115,7 +1169,7 @@ int make_plan(const iq_cache* c, int q_heads, int nq, int causal, Plan* pl, cons
   if (!tiles)  // independent of the tile counts, so it bounds every later plan
     pl->slots = std::min(pl->units, static_cast<size_t>(UNIT_CAP)) +
                 static_cast<size_t>(std::min(slots_hw, static_cast<long long>(GRID_CAP)));
-  pl->head_bytes = kStatusBytes;
+  pl->head_bytes = kHeadBytes;
   pl->bytes = pl->head_bytes + pl->slots * pl->gt * (kHeadDim + 2) * sizeof(float);
   return IQ_OK;
 }
@@ -1270,6 +1324,7 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   unsigned* status = reinterpret_cast<unsigned*>(ws);
+  unsigned* counters = reinterpret_cast<unsigned*>(ws + kStatusBytes);
   float* part_o = reinterpret_cast<float*>(ws + bound.head_bytes);
   float* part_ml = part_o + bound.slots * pl.gt * kHeadDim;
 
@@ -1286,6 +1341,7 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   prm.part_o = part_o;
   prm.part_ml = part_ml;
   prm.status = status;
+  prm.counters = counters;
   prm.out = out;
   prm.out_f32 = out_f32 ? 1 : 0;
   prm.batch = c->batch;
@@ -1321,7 +1377,8 @@ int iq_read_status(void* workspace, iq_stream_t stream, int* device_status) {
   unsigned v = 0;
   IQ_CUDA(cudaStreamSynchronize(s));
   IQ_CUDA(cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost));
-  IQ_CUDA(cudaMemset(workspace, 0, sizeof(unsigned)));
+  // after a failure the unit counters may be stale too: clear the whole head
+  IQ_CUDA(cudaMemset(workspace, 0, v ? kHeadBytes : sizeof(unsigned)));
   *device_status = static_cast<int>(v);
   return v ? fail(IQ_ERR_DEVICE, "a kernel reported a failure (status bits set)") : IQ_OK;
 }
