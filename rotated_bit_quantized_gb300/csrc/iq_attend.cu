@@ -1021,6 +1021,7 @@ __device__ __forceinline__ void combine_unit(const Params& p, int u) {
 
 template <int GT>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Params p) {
+  pdl_launch_dependents();  // the next kernel may launch; it waits for this grid before reading
   const int u = blockIdx.x;
   if (u < p.num_units) combine_unit<GT>(p, u);
   // This grid may run ahead of the attention grid it depends on; it completes

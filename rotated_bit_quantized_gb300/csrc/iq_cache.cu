@@ -210,8 +210,11 @@ __device__ __forceinline__ void encode_row(const uint4 raw, const float (&m)[2][
 #define IQ_APPEND_MINB 3
 #endif
 __global__ void __launch_bounds__(256, IQ_APPEND_MINB) append_kernel(const __grid_constant__ AppendParams p) {
-  // the next kernel in the stream (attention) may launch now; it waits for
-  // this grid's completion before it reads the cache
+  // Launched as a programmatic dependent of the previous kernel in the
+  // stream: wait for it (and its writes) before touching memory.  The next
+  // kernel (attention) may launch now; it waits for this grid's completion
+  // before it reads the cache.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int gwarp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);  // within this (b, h)
@@ -400,9 +403,17 @@ int iq_cache_append(iq_cache* c, const uint16_t* keys, const uint16_t* values, i
   long long gx = (static_cast<long long>(n) + 7) / 8;
   const long long cap_x = std::max(1LL, static_cast<long long>(num_sms()) * 8 / bh);
   if (gx > cap_x) gx = cap_x;
-  append_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(bh)), 256, 0,
-                  static_cast<cudaStream_t>(stream)>>>(p);
-  IQ_CUDA(cudaGetLastError());
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(bh));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  IQ_CUDA(cudaLaunchKernelEx(&cfg, append_kernel, p));
   for (int b = 0; b < c->batch; ++b) c->lens[b] += n;
   return IQ_OK;
 }
