@@ -197,6 +197,24 @@ int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queri
               void* workspace, size_t workspace_bytes, iq_stream_t stream);
 
 /*
+ * iq_cache_append_attend — iq_cache_append(keys, values, n) followed by
+ * iq_attend(q, ...), the page's decode step (quant_kv.py: `update_and_fetch`,
+ * then `asym_quantized_sdpa` over the updated cache), with the same results
+ * as the two calls.  When every (sequence, kv head) holds at most 8 query
+ * rows (q_heads / kv_heads * n_queries <= 8) and each sequence's n new rows
+ * fall in one 128-token tile, it is one attention launch whose CTAs encode the
+ * new rows themselves before streaming the tiles that hold them; otherwise it
+ * is the append launch followed by the attention.
+ * Arguments, layouts and workspace as iq_cache_append and iq_attend; lens[b]
+ * grows by n on success (the causal mask and the scanned length use the
+ * grown lengths).  Errors: as both (nothing is launched on an error).
+ */
+int iq_cache_append_attend(iq_cache* cache, const uint16_t* keys, const uint16_t* values, int n,
+                           const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
+                           const uint16_t* rot_bf16, void* out, int out_f32, void* workspace,
+                           size_t workspace_bytes, iq_stream_t stream);
+
+/*
  * iq_attend_noalloc — iq_attend for callers that cannot allocate device
  * memory.  (The source pages have no counterpart: this is a library service.)
  *

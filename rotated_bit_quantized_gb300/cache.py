@@ -260,6 +260,42 @@ class IQCache:
                                   self._workspace.numel(), _stream(self.device.index)), "iq_attend")
         return out
 
+    def append_attend(self, keys: torch.Tensor, values: torch.Tensor, q: torch.Tensor, rotation: Rotation,
+                      causal: bool = False, scale: float | None = None, out: torch.Tensor | None = None,
+                      out_dtype=torch.bfloat16) -> torch.Tensor:
+        """`append(keys, values)` then `attend(q)` in one library call (the page's
+        `update_and_fetch` followed by `asym_quantized_sdpa`): one kernel launch
+        for decode-shaped steps, the same results as the two calls."""
+        keys = _need_cuda(keys, torch.bfloat16, "keys")
+        values = _need_cuda(values, torch.bfloat16, "values")
+        q = _need_cuda(q, torch.bfloat16, "q")
+        n = keys.shape[2]
+        if tuple(keys.shape) != (self.batch, self.kv_heads, n, self.head_dim) or values.shape != keys.shape:
+            raise ValueError("keys/values must be [B, Hkv, n, D]")
+        B, Hq, L, D = q.shape
+        if B != self.batch or D != self.head_dim:
+            raise ValueError("q must be [B, Hq, L, D] matching the cache")
+        need = int(self.lens.max()) + n
+        if need > self.capacity:
+            self.reserve(max(need, self.capacity + int(math.ceil(n / IQ_STEP)) * IQ_STEP))
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        if out is None:
+            out = torch.empty((B, Hq, L, D), dtype=out_dtype, device=q.device)
+        if out.dtype not in (torch.float32, torch.bfloat16) or not out.is_contiguous():
+            raise ValueError("out must be a contiguous bf16 or f32 tensor")
+        out_f32 = 1 if out.dtype == torch.float32 else 0
+        need_ws = self.workspace_bytes(Hq, L)
+        if self._workspace is None or self._workspace.numel() < need_ws:
+            self._workspace = torch.zeros(max(need_ws, 1 << 20), dtype=torch.uint8, device=self.device)
+        d = self.desc()
+        with self._on:
+            check(lib().iq_cache_append_attend(ctypes.byref(d), _ptr(keys), _ptr(values), n, _ptr(q), Hq, L,
+                                               float(scale), 1 if causal else 0, _ptr(rotation.blocks_bf16),
+                                               _ptr(out), out_f32, _ptr(self._workspace), self._workspace.numel(),
+                                               _stream(self.device.index)), "iq_cache_append_attend")
+        return out
+
     def device_status(self) -> int:
         """Synchronise and return the kernels' status word (0 = all normal)."""
         if self._workspace is None:

@@ -43,6 +43,7 @@
 #include <vector>
 
 #include "iq_common.cuh"
+#include "iq_encode.cuh"
 
 namespace iq {
 namespace attn {
@@ -101,6 +102,12 @@ struct Params {
   float* part_ml;      // [slots][GT][2] (running max in log2 units, running sum)
   unsigned* status;
   unsigned* counters;  // [UNIT_CAP]: partials stored per unit of this launch (the combine resets them)
+  // fused append (n_new > 0): the new rows [lens[b] - n_new, lens[b]) of every
+  // (sequence, kv head) are encoded from these bf16 [B][Hkv][n_new][256] rows
+  // by the CTA that streams the unit's last tile, which holds them all
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int n_new;
   void* out;
   int out_f32;
   int batch, kv_heads, rep, nq, cap, nqt, causal;
@@ -305,7 +312,7 @@ struct Cfg : Tiling<TILE_> {
   static constexpr int OFF_QB = OFF_XBUF + XBUF_BYTES;
   static constexpr int QB_BYTES = DS * GPW * 4 * NT * 32 * 8;       // q'' MMA B fragments
   static constexpr int OFF_BAR = OFF_QB + QB_BYTES;
-  static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8;
+  static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8 + 8;  // + the fused-append barrier
   static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
   static_assert(OFF_XBUF % 16 == 0 && OFF_OBUF % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
   static_assert(4 % DS == 0, "shape");
@@ -332,6 +339,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   uint2* qbs = reinterpret_cast<uint2*>(smem + C::OFF_QB);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + NSTAGE;
+  uint64_t* encoded = empty + NSTAGE;  // fused append: every consumer warp has stored its new rows
   int* s_flag = reinterpret_cast<int*>(smem + C::OFF_FLAG);
 
   // ---- this CTA's even share of the launch's tiles
@@ -351,6 +359,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     }
     u0 = lo;
   }
+  int u1 = u0;  // unit holding tile g1 - 1
+  while (g1 > p.prefix[u1 + 1]) ++u1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -358,6 +368,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], CW);
     }
+    mbar_init(encoded, CW);
     mbar_fence_init();
   }
   __syncthreads();
@@ -374,8 +385,16 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       const uint64_t pol = policy_evict_first();
       int u = u0;
       long long k = 0;
+      bool enc_seen = p.n_new == 0;
       for (long long gt = g0; gt < g1; ++gt, ++k) {
         while (gt >= p.prefix[u + 1]) ++u;
+        if (!enc_seen && gt == p.prefix[u + 1] - 1) {  // a last tile: its new rows must be stored first
+          if (!mbar_wait(encoded, 0)) {
+            atomicOr(p.status, 1u);
+            break;
+          }
+          enc_seen = true;
+        }
         const int ug = p.unit_base + u;
         const int bb = ug / (p.kv_heads * p.nqt), hh = (ug / p.nqt) % p.kv_heads;
         const int st = static_cast<int>(k % NSTAGE);
@@ -886,6 +905,36 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     }
   };
 
+  // ------------------------------------------------------------ fused append
+  // This CTA holds the last tile of units u0 .. u1 - 1, and of u1 when its
+  // range reaches u1's end; it encodes their new rows (a warp per token row,
+  // its K and V), makes the stores visible to the tensor copies and tells the
+  // producer.  One unit per (sequence, kv head) here (a single query tile).
+  if (p.n_new > 0) {
+    const int ulast = p.prefix[u1 + 1] <= g1 ? u1 : u1 - 1;
+    const int rows = (ulast - u0 + 1) * p.n_new;
+    if (rows > 0) {
+      float m[2][4][4];
+      load_row_rotation(p.rot, lane, m);
+      for (int item = cw; item < rows; item += CW) {
+        const int ue = u0 + item / p.n_new, i = item % p.n_new;
+        const int ug = p.unit_base + ue;
+        const int bb = ug / p.kv_heads, hh = ug % p.kv_heads;
+        const long long src = ((static_cast<long long>(bb) * p.kv_heads + hh) * p.n_new + i) * kHeadDim + lane * 8;
+        const uint4 rk = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
+        const uint4 rv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
+        const long long dst = (static_cast<long long>(bb) * p.kv_heads + hh) * p.cap + p.lens[bb] - p.n_new + i;
+        encode_row<4>(rk, m, lane, dst, const_cast<uint32_t*>(p.k_codes), const_cast<uint16_t*>(p.k_scales),
+                      const_cast<uint16_t*>(p.k_biases));
+        encode_row<3>(rv, m, lane, dst, const_cast<uint32_t*>(p.v_codes), const_cast<uint16_t*>(p.v_scales),
+                      const_cast<uint16_t*>(p.v_biases));
+      }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");  // generic stores before the async-proxy reads
+    __syncwarp();
+    if (lane == 0) mbar_arrive(encoded);
+  }
+
   // ------------------------------------------------------------ main loop over this CTA's tiles
   // One pass per unit segment, so the per-unit prologue and epilogue each have a
   // single call site outside the hot per-tile loop.
@@ -1290,10 +1339,17 @@ int iq_attend_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* b
   return IQ_OK;
 }
 
-int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
-              const uint16_t* rot_bf16, void* out, int out_f32, void* workspace, size_t workspace_bytes,
-              iq_stream_t stream) {
-  clear_error();
+}  // extern "C"
+
+namespace iq {
+namespace attn {
+
+// Attention over the cache; with n_new > 0 the last n_new rows of every
+// sequence (already counted in c->lens) are first encoded from k_new / v_new
+// inside the same kernel (see the fused append in attend_kernel).
+int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
+                const uint16_t* rot_bf16, void* out, int out_f32, void* workspace, size_t workspace_bytes,
+                iq_stream_t stream, const uint16_t* k_new, const uint16_t* v_new, int n_new) {
   int st = validate(c, q, q_heads, n_queries, causal, rot_bf16, out);
   if (st != IQ_OK) return st;
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
@@ -1343,6 +1399,9 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
   prm.part_ml = part_ml;
   prm.status = status;
   prm.counters = counters;
+  prm.k_new = k_new;
+  prm.v_new = v_new;
+  prm.n_new = n_new;
   prm.out = out;
   prm.out_f32 = out_f32 ? 1 : 0;
   prm.batch = c->batch;
@@ -1369,6 +1428,54 @@ int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, 
     if (st != IQ_OK) return st;
   }
   return IQ_OK;
+}
+
+}  // namespace attn
+}  // namespace iq
+
+extern "C" {
+
+int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
+              const uint16_t* rot_bf16, void* out, int out_f32, void* workspace, size_t workspace_bytes,
+              iq_stream_t stream) {
+  clear_error();
+  return attend_impl(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
+                     stream, nullptr, nullptr, 0);
+}
+
+int iq_cache_append_attend(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n, const uint16_t* q,
+                           int q_heads, int n_queries, float scale, int causal, const uint16_t* rot_bf16,
+                           void* out, int out_f32, void* workspace, size_t workspace_bytes, iq_stream_t stream) {
+  clear_error();
+  int st = iq_cache_check(c);
+  if (st != IQ_OK) return st;
+  if (n < 1) return fail(IQ_ERR_INVALID_ARG, "append_attend needs n >= 1 new tokens");
+  if (!keys || !values || !rot_bf16) return fail(IQ_ERR_INVALID_ARG, "null keys/values/rotation");
+  if (reinterpret_cast<uintptr_t>(keys) % 16 || reinterpret_cast<uintptr_t>(values) % 16)
+    return fail(IQ_ERR_INVALID_ARG, "keys/values not 16-byte aligned");
+  for (int b = 0; b < c->batch; ++b)
+    if (static_cast<long long>(c->lens[b]) + n > c->capacity)
+      return fail(IQ_ERR_CAPACITY, "append past capacity (grow the cache first)");
+  // One kernel when every (sequence, kv head) is one query tile and the new
+  // rows of each sequence sit in one key tile; otherwise the append, then the
+  // attention.
+  const int tile = Cfg<IQ_DECODE_CFG>::TILE;
+  bool fused = q_heads >= c->kv_heads && q_heads % c->kv_heads == 0 &&
+               static_cast<long long>(q_heads / c->kv_heads) * n_queries <= 8;
+  for (int b = 0; b < c->batch && fused; ++b)
+    fused = c->lens[b] / tile == (c->lens[b] + n - 1) / tile;
+  if (!fused) {
+    st = iq_cache_append(c, keys, values, n, rot_bf16, stream);
+    if (st != IQ_OK) return st;
+    return iq_attend(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
+                     stream);
+  }
+  for (int b = 0; b < c->batch; ++b) c->lens[b] += n;
+  st = attend_impl(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
+                   stream, keys, values, n);
+  if (st != IQ_OK)
+    for (int b = 0; b < c->batch; ++b) c->lens[b] -= n;  // nothing was launched
+  return st;
 }
 
 int iq_read_status(void* workspace, iq_stream_t stream, int* device_status) {
