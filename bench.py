@@ -42,8 +42,8 @@ K_ROW, V_ROW = 144, 112  # algorithmic bytes per token-head: codes + bf16 scales
 # combine_kernel; profiles/attend_kernel_batched_decode_32x32k.md).  Reported
 # only while the attention source is the one that was measured.
 TRAFFIC = {"source": "rotated_bit_quantized_gb300/csrc/iq_attend.cu",
-           "sha256": "6e8c269844b3002e1be98ddfe168da69fc3dc6bf3fe9a75328c5f7343c419612",
-           "bytes": (539.33 + 3.21 + 2.92) * 1e6}
+           "sha256": "c3028c4e608184b68f1b59e4694cd09f6210566c3acdef3c448c5dc98c307be6",
+           "bytes": (539.41 + 3.26 + 2.93) * 1e6}
 
 
 def measured_traffic():
