@@ -297,6 +297,7 @@ def run_ours(args):
         h2d = (dsteps[0][0].numel() + dsteps[0][1].numel() + dsteps[0][2].numel()) * 2
         d2h = out.numel() * 2
         cpu = None if args.no_cpu_baseline else cpu_baseline_sample(args.workload, budget_s=args.cpu_seconds)
+        append = append_throughput(dev, rot)
         rec = {
             "metric": METRIC, "value": tokens_all / (ms_max / 1e3), "unit": UNIT, "n_gpus": ws,
             "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
@@ -323,11 +324,46 @@ def run_ours(args):
             "clocks": clk.summary(),
             "device_status": status,
             "cpu_baseline": cpu,
+            "append": append,
         }
         print(json.dumps(rec), flush=True)
     if ws > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
+
+
+def append_throughput(dev, rot, reps: int = 10):
+    """Appended tokens/s of the append kernel (rotate + quantise + pack + store)
+    on two shapes: the batched-decode prefill chunks (32 sequences x 2 kv heads x
+    4096 tokens per call) and one chunked-prefill chunk (1 sequence x 2 kv heads
+    x 2048 tokens).  CUDA events around `reps` calls; each call is undone by a
+    host-side trim, so every call writes the same rows."""
+    from rotated_bit_quantized_gb300 import IQCache
+    stream = torch.cuda.current_stream(dev)
+    res = []
+    for wid, B, n in ((4, 32, 4096), (3, 1, 2048)):
+        w = si.WORKLOADS[wid]
+        cache = IQCache(B, w["Hkv"], device=dev, capacity=n + 256)
+        k, v = si.kv_tokens(w["seed"], B, w["Hkv"], n, outliers=w["outliers"])
+        k, v = k.to(dev), v.to(dev)
+        for _ in range(3):
+            cache.append(k, v, rot)
+            cache.trim(n)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            cache.append(k, v, rot)
+            cache.trim(n)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        sec = e0.elapsed_time(e1) / 1e3 / reps
+        th = B * w["Hkv"] * n
+        res.append({"workload": f"{w['name']} append: B={B} x {w['Hkv']} kv heads x {n} tokens per call",
+                    "appended_tokens_per_s": B * n / sec, "token_heads_per_s": th / sec,
+                    "gbs": th * (4 * 256 + K_ROW + V_ROW) / sec / 1e9, "us_per_call": sec * 1e6,
+                    "bytes_per_token_head": 4 * 256 + K_ROW + V_ROW})
+    return res
 
 
 def _oracle_sequence(wid: int, b: int):

@@ -18,9 +18,16 @@ Readings:
   bfloat16).  The page's MLX kernels would round intermediates to the query
   dtype; the method's accuracy target (bf16 I/O, fp32 accumulation) is read as
   "no intermediate rounding".
-* Masked scores are -inf (the page uses the dtype's most negative finite
-  value; with at least one unmasked key per row the two give the same
+* Causally masked scores are -inf (the page uses the dtype's most negative
+  finite value; with at least one unmasked key per row the two give the same
   softmax).
+* Explicit masks (page: a bool mask selects `where(mask, scores, finfo.min)`,
+  a float mask is added to the scores) are read per sequence and query,
+  shared by every head: mask [B, L, S] with S >= the sequence length.  A bool
+  mask's masked scores become bfloat16's most negative finite value, so a row
+  with every key masked averages all values uniformly, as the page's softmax
+  would; an additive mask may hold -inf, and a row that is -inf everywhere
+  gives NaN, as the page's softmax would.
 """
 from __future__ import annotations
 
@@ -47,11 +54,15 @@ def softmax_rows(s) -> np.ndarray:
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def attend_slice(q_rows, k_hat, v_hat, blocks_b, scale, causal, q_pos=None):
+BF16_MIN = -3.3895313892515355e38  # most negative finite bfloat16: (2 - 2^-7) * 2^127
+
+
+def attend_slice(q_rows, k_hat, v_hat, blocks_b, scale, causal, q_pos=None, mask_rows=None):
     """Attention for query rows of one kv head.
 
     q_rows float32 [R, D] (bfloat16 values, unrotated); k_hat, v_hat float64 [T, D];
-    q_pos int [R]: absolute position of each row's query (causal limit t <= q_pos).
+    q_pos int [R]: absolute position of each row's query (causal limit t <= q_pos);
+    mask_rows [R, T] bool (keep where True) or float (added to the scores).
     Returns float64 [R, D] in unrotated space.
     """
     qr = codec.rotate(q_rows, blocks_b) * np.float32(scale)
@@ -60,18 +71,28 @@ def attend_slice(q_rows, k_hat, v_hat, blocks_b, scale, causal, q_pos=None):
     if causal:
         t = np.arange(k_hat.shape[0])
         s = np.where(t[None, :] <= np.asarray(q_pos)[:, None], s, -np.inf)
+    if mask_rows is not None:
+        mask_rows = np.asarray(mask_rows)
+        if mask_rows.dtype == np.bool_:
+            s = np.where(mask_rows, s, BF16_MIN)
+        else:
+            s = s + mask_rows.astype(np.float64)
     p = softmax_rows(s)
     return inverse_rotate(p @ v_hat, blocks_b)
 
 
 def attend(q, cache, blocks_b, scale=None, causal=False, heads=None, batches=None,
-           query_index=None):
+           query_index=None, mask=None):
     """Full oracle attention.
 
     q float32 [B, Hq, L, D]; cache an `OracleCache` already holding the queries'
-    own keys/values when causal.  Returns float64 [B, Hq, L, D] (entries of
-    skipped rows left as NaN when `heads` / `batches` / `query_index` subsample).
+    own keys/values when causal; mask None or [B, L, S] (bool: keep where True;
+    float: added to the scores), S >= every length, shared by the heads.
+    Returns float64 [B, Hq, L, D] (entries of skipped rows left as NaN when
+    `heads` / `batches` / `query_index` subsample).
     """
+    if mask is not None and causal:
+        raise ValueError("give either causal or an explicit mask")
     q = np.asarray(q, dtype=np.float32)
     B, Hq, L, D = q.shape
     rep = Hq // cache.kv_heads
@@ -92,7 +113,8 @@ def attend(q, cache, blocks_b, scale=None, causal=False, heads=None, batches=Non
             kh, vh = cache.dequantized(b, kvh)
             rows = q[b, hl][:, qi].reshape(-1, D)
             pos = np.tile(T - L + qi, len(hl))
-            o = attend_slice(rows, kh, vh, blocks_b, scale, causal, pos)
+            mrows = None if mask is None else np.tile(np.asarray(mask[b])[qi, :T], (len(hl), 1))
+            o = attend_slice(rows, kh, vh, blocks_b, scale, causal, pos, mrows)
             o = o.reshape(len(hl), len(qi), D)
             for j, h in enumerate(hl):
                 out[b, h, qi] = o[j]

@@ -219,3 +219,69 @@ def test_codec_bypass_rotation_cancels(mb):
     rot = attention.attend_slice(q, kr, vr, mb, 1 / 16, False)
     plain = dense_attention_f32(q, k, v, 1 / 16)
     np.testing.assert_allclose(rot, plain, atol=3e-2)
+
+
+# ---------------------------------------------------------------- explicit masks
+
+def dense_masked_f32(q, k, v, scale, keep=None, add=None):
+    """Second formulation with an explicit mask: float32, masked scores dropped
+    from the normaliser by index (keep) or added (add), exp-normalise."""
+    s = (q.astype(np.float32) * np.float32(scale)) @ k.astype(np.float32).T
+    if add is not None:
+        s = s + add.astype(np.float32)
+    out = np.zeros((q.shape[0], v.shape[1]), np.float32)
+    for r in range(q.shape[0]):
+        idx = np.arange(k.shape[0]) if keep is None else np.nonzero(keep[r])[0]
+        if idx.size == 0:  # nothing kept: every score equal, a uniform average
+            idx = np.arange(k.shape[0])
+            w = np.ones(idx.size, np.float32)
+        else:
+            w = np.exp(s[r, idx] - s[r, idx].max())
+        out[r] = (w @ v[idx].astype(np.float32)) / w.sum()
+    return out
+
+
+def test_masks_match_dense_brute_force(mb):
+    c = build(mb, 1, 2, 45)
+    q = f32(si.queries(21, 1, 16, 3))
+    rng = np.random.default_rng(22)
+    keep = rng.random((1, 3, 64)) < 0.6
+    keep[0, 1, :] = False  # one row with every key masked
+    add = rng.standard_normal((1, 3, 64)).astype(np.float32)
+    add[0, 2, ::3] = -np.inf
+    out_keep = attention.attend(q, c, mb, mask=keep)
+    out_add = attention.attend(q, c, mb, mask=add)
+    m = rotation.dense(mb)
+    for h in (0, 5, 9, 15):
+        kh, vh = c.dequantized(0, h // 8)
+        qr = codec.rotate(q[0, h], mb)
+        o = dense_masked_f32(qr, kh, vh, 1 / 16, keep=keep[0, :, :45])
+        np.testing.assert_allclose(out_keep[0, h], o.astype(np.float64) @ m.T, atol=1e-5)
+        o = dense_masked_f32(qr, kh, vh, 1 / 16, add=add[0, :, :45])
+        np.testing.assert_allclose(out_add[0, h], o.astype(np.float64) @ m.T, atol=1e-5)
+
+
+def test_mask_special_cases(mb):
+    c = build(mb, 2, 2, 40)
+    q = f32(si.queries(23, 2, 16, 4))
+    plain = attention.attend(q, c, mb)
+    # all-True bool mask, all-zero and constant additive masks: no mask
+    np.testing.assert_array_equal(attention.attend(q, c, mb, mask=np.ones((2, 4, 48), bool)), plain)
+    np.testing.assert_array_equal(attention.attend(q, c, mb, mask=np.zeros((2, 4, 48), np.float32)), plain)
+    np.testing.assert_allclose(attention.attend(q, c, mb, mask=np.full((2, 4, 48), 3.5, np.float32)), plain,
+                               atol=1e-12)
+    # the causal pattern as a bool mask, and as -inf added: causal
+    causal = attention.attend(q, c, mb, causal=True)
+    keep = np.arange(48)[None, None, :] <= (40 - 4 + np.arange(4))[None, :, None]
+    keep = np.broadcast_to(keep, (2, 4, 48))
+    np.testing.assert_array_equal(attention.attend(q, c, mb, mask=keep), causal)
+    np.testing.assert_array_equal(attention.attend(q, c, mb, mask=np.where(keep, 0.0, -np.inf)), causal)
+    # every key masked: the uniform mean of the values
+    none = np.zeros((2, 4, 48), bool)
+    out = attention.attend(q, c, mb, mask=none)
+    for b in range(2):
+        for h in (0, 8):
+            _, vh = c.dequantized(b, h // 8)
+            np.testing.assert_allclose(out[b, h, 2], vh.mean(0) @ rotation.dense(mb).T, atol=1e-12)
+    with pytest.raises(ValueError):
+        attention.attend(q, c, mb, causal=True, mask=keep)
