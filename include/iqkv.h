@@ -197,6 +197,32 @@ int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queri
               void* workspace, size_t workspace_bytes, iq_stream_t stream);
 
 /*
+ * iq_attend_mask — iq_attend with the page's general masks (quant_kv.py,
+ * `asym_quantized_sdpa`: a bool mask keeps a score where true and replaces it
+ * by the dtype's most negative value elsewhere; a float mask is added to the
+ * scores).
+ * mask_kind: IQ_MASK_NONE, IQ_MASK_CAUSAL (as iq_attend's causal flag),
+ *    IQ_MASK_ADD_F32 (device float32, may hold -inf) or IQ_MASK_BOOL_U8
+ *    (device uint8, 0 = masked).
+ * mask: [B][n_queries][mask_stride] elements, row (b, i) covering keys
+ *    0 .. lens[b]-1 (mask_stride >= every lens[b]); shared by every query head.
+ * A row whose keys are all masked by a bool mask averages the values
+ * uniformly, as the page's softmax does; a float-mask row that is -inf
+ * everywhere has no softmax (NaN output, status bit 4).  Scores are float32:
+ * a float mask should use -inf (not huge finite values) to exclude keys, and
+ * scaled scores are taken to stay above -1e5 (bool-masked keys score -1e6).
+ * Other arguments as iq_attend.  Errors: as iq_attend, plus INVALID_ARG for a
+ * bad kind, a null or misaligned mask, or a mask row shorter than a sequence.
+ */
+#define IQ_MASK_NONE 0
+#define IQ_MASK_CAUSAL 1
+#define IQ_MASK_ADD_F32 2
+#define IQ_MASK_BOOL_U8 3
+int iq_attend_mask(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries, float scale,
+                   int mask_kind, const void* mask, long long mask_stride, const uint16_t* rot_bf16,
+                   void* out, int out_f32, void* workspace, size_t workspace_bytes, iq_stream_t stream);
+
+/*
  * iq_cache_append_attend — iq_cache_append(keys, values, n) followed by
  * iq_attend(q, ...), the page's decode step (quant_kv.py: `update_and_fetch`,
  * then `asym_quantized_sdpa` over the updated cache), with the same results

@@ -233,11 +233,17 @@ class IQCache:
         return nb
 
     def attend(self, q: torch.Tensor, rotation: Rotation, causal: bool = False, scale: float | None = None,
-               out: torch.Tensor | None = None, out_dtype=torch.bfloat16) -> torch.Tensor:
+               out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+               mask: torch.Tensor | None = None) -> torch.Tensor:
         """Attention of q [B, Hq, L, D] (bf16, unrotated) over the cache (page `asym_quantized_sdpa`).
 
-        Returns [B, Hq, L, D] in unrotated space (the inverse rotation applied).
+        mask: optional CUDA tensor [B, L, S] (S >= every length), shared by the
+        heads: bool (keep where True) or float32 (added to the scores); not
+        together with causal.  Returns [B, Hq, L, D] in unrotated space (the
+        inverse rotation applied).
         """
+        if mask is not None:
+            return self._attend_mask(q, rotation, mask, causal, scale, out, out_dtype)
         q = _need_cuda(q, torch.bfloat16, "q")
         B, Hq, L, D = q.shape
         if B != self.batch or D != self.head_dim:
@@ -258,6 +264,38 @@ class IQCache:
             check(lib().iq_attend(ctypes.byref(d), _ptr(q), Hq, L, float(scale), 1 if causal else 0,
                                   _ptr(rotation.blocks_bf16), _ptr(out), out_f32, _ptr(self._workspace),
                                   self._workspace.numel(), _stream(self.device.index)), "iq_attend")
+        return out
+
+    def _attend_mask(self, q, rotation, mask, causal, scale, out, out_dtype):
+        if causal:
+            raise ValueError("give either causal or an explicit mask")
+        q = _need_cuda(q, torch.bfloat16, "q")
+        B, Hq, L, D = q.shape
+        if B != self.batch or D != self.head_dim:
+            raise ValueError("q must be [B, Hq, L, D] matching the cache")
+        if not mask.is_cuda or mask.dim() != 3 or mask.shape[0] != B or mask.shape[1] != L:
+            raise ValueError("mask must be a CUDA tensor [B, L, S]")
+        if mask.dtype == torch.bool:
+            mask, kind = mask.contiguous().view(torch.uint8), _abi.IQ_MASK_BOOL_U8
+        elif mask.dtype == torch.float32:
+            mask, kind = mask.contiguous(), _abi.IQ_MASK_ADD_F32
+        else:
+            raise ValueError("mask must be bool or float32")
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        if out is None:
+            out = torch.empty((B, Hq, L, D), dtype=out_dtype, device=q.device)
+        if out.dtype not in (torch.float32, torch.bfloat16) or not out.is_contiguous():
+            raise ValueError("out must be a contiguous bf16 or f32 tensor")
+        need = self.workspace_bytes(Hq, L)
+        if self._workspace is None or self._workspace.numel() < need:
+            self._workspace = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=self.device)
+        d = self.desc()
+        with self._on:
+            check(lib().iq_attend_mask(ctypes.byref(d), _ptr(q), Hq, L, float(scale), kind, _ptr(mask),
+                                       mask.shape[2], _ptr(rotation.blocks_bf16), _ptr(out),
+                                       1 if out.dtype == torch.float32 else 0, _ptr(self._workspace),
+                                       self._workspace.numel(), _stream(self.device.index)), "iq_attend_mask")
         return out
 
     def append_attend(self, keys: torch.Tensor, values: torch.Tensor, q: torch.Tensor, rotation: Rotation,

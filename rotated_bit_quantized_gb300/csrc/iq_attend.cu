@@ -76,6 +76,12 @@ constexpr int GRID_CAP = 1024;  // CTAs per launch (their tile ranges travel by 
 constexpr int MIN_TILES_PER_CTA = 8;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float NEG_INF = -__builtin_huge_valf();
+// Score of a key a bool mask hides: far below any real score (|q.k| * scale
+// stays well under 1e5), so it weighs exactly 0 next to one; finite and equal
+// for every hidden key, so a row whose keys are all hidden averages them
+// uniformly, like the page's where(mask, s, finfo.min) softmax; and small
+// enough that its log2 and the running max agree to a fraction of a unit.
+constexpr float MASKED_SCORE = -1e6f;
 // Lazy running max: the reference max of a row moves only when a score exceeds
 // it by more than 2^TAU (log2 units), so p = 2^(s - m) stays below 2^TAU and
 // p * s_v stays inside fp16 for value scales below 2^(16 - TAU).
@@ -108,6 +114,11 @@ struct Params {
   const uint16_t* k_new;
   const uint16_t* v_new;
   int n_new;
+  // explicit mask (mask_kind 2: float32 added to the scores; 3: uint8, 0 =
+  // masked): [B][nq][mask_stride] over the keys, shared by every head
+  int mask_kind;
+  const void* mask;
+  long long mask_stride;
   void* out;
   int out_f32;
   int batch, kv_heads, rep, nq, cap, nqt, causal;
@@ -434,6 +445,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   // per-unit state
   int b = 0, kvh = 0, qt = 0, T = 0, limit = 0, qmin = 0;
   int qpos[NT][2];
+  int qrow[NT][2];  // query index of rows 2t, 2t+1 of each n-tile (explicit masks)
   float qsr[GPW][NT][2];   // per group: sum of q'' over the group's dims (rows 2t, 2t+1 of each n-tile)
   float qoff[GPW][NT][2];  // -64 * qsr: the score accumulators start there, cancelling the code offset
   float O[GPW][4][NT][4];
@@ -449,7 +461,9 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     qt = ug % p.nqt;
     T = p.lens[b];
     limit = tile_limit(p, T, qt, GT);
-    qmin = p.causal ? T - p.nq + (qt * GT) / p.rep : T - 1;
+    // the first key some row of the unit cannot see (no sub-tile at or past it
+    // takes the unmasked path); an explicit mask reads every sub-tile
+    qmin = p.mask_kind >= 2 ? -1 : p.causal ? T - p.nq + (qt * GT) / p.rep : T - 1;
     named_bar(1, NCT);  // every consumer is done with the previous unit's fragments and sums
     // q' = bf16(q @ M_b), q'' = bf16(q' * scale), written straight into the fp16
     // MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].  Item
@@ -536,6 +550,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         const int R = qt * GT + 8 * j + 2 * t + e;
         const int i = min(R / p.rep, p.nq - 1);
         qpos[j][e] = p.causal ? T - p.nq + i : T - 1;
+        qrow[j][e] = i;
       }
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi)
@@ -662,6 +677,18 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
           valid[n][j][1] = in0 && tok0 <= qpos[j][1];
           valid[n][j][2] = in1 && tok1 <= qpos[j][0];
           valid[n][j][3] = in1 && tok1 <= qpos[j][1];
+          if (p.mask_kind >= 2) {  // explicit mask: added, or a masked score made most negative
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (!valid[n][j][e]) continue;
+              const long long mi = (static_cast<long long>(b) * p.nq + qrow[j][e & 1]) * p.mask_stride +
+                                   (e < 2 ? tok0 : tok1);
+              if (p.mask_kind == 2)
+                sc[n][j][e] += __ldg(static_cast<const float*>(p.mask) + mi);
+              else if (__ldg(static_cast<const unsigned char*>(p.mask) + mi) == 0)
+                sc[n][j][e] = MASKED_SCORE;
+            }
+          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[n][j][e] = valid[n][j][e] ? sc[n][j][e] : NEG_INF;
         }
@@ -1349,7 +1376,8 @@ namespace attn {
 // inside the same kernel (see the fused append in attend_kernel).
 int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
                 const uint16_t* rot_bf16, void* out, int out_f32, void* workspace, size_t workspace_bytes,
-                iq_stream_t stream, const uint16_t* k_new, const uint16_t* v_new, int n_new) {
+                iq_stream_t stream, const uint16_t* k_new, const uint16_t* v_new, int n_new, int mask_kind = 0,
+                const void* mask = nullptr, long long mask_stride = 0) {
   int st = validate(c, q, q_heads, n_queries, causal, rot_bf16, out);
   if (st != IQ_OK) return st;
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
@@ -1402,6 +1430,9 @@ int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries
   prm.k_new = k_new;
   prm.v_new = v_new;
   prm.n_new = n_new;
+  prm.mask_kind = mask_kind;
+  prm.mask = mask;
+  prm.mask_stride = mask_stride;
   prm.out = out;
   prm.out_f32 = out_f32 ? 1 : 0;
   prm.batch = c->batch;
@@ -1476,6 +1507,26 @@ int iq_cache_append_attend(iq_cache* c, const uint16_t* keys, const uint16_t* va
   if (st != IQ_OK)
     for (int b = 0; b < c->batch; ++b) c->lens[b] -= n;  // nothing was launched
   return st;
+}
+
+int iq_attend_mask(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int mask_kind,
+                   const void* mask, long long mask_stride, const uint16_t* rot_bf16, void* out, int out_f32,
+                   void* workspace, size_t workspace_bytes, iq_stream_t stream) {
+  clear_error();
+  if (mask_kind == IQ_MASK_NONE || mask_kind == IQ_MASK_CAUSAL)
+    return attend_impl(c, q, q_heads, n_queries, scale, mask_kind, rot_bf16, out, out_f32, workspace,
+                       workspace_bytes, stream, nullptr, nullptr, 0);
+  if (mask_kind != IQ_MASK_ADD_F32 && mask_kind != IQ_MASK_BOOL_U8)
+    return fail(IQ_ERR_INVALID_ARG, "unknown mask kind");
+  int st = iq_cache_check(c);
+  if (st != IQ_OK) return st;
+  if (!mask) return fail(IQ_ERR_INVALID_ARG, "null mask");
+  if (mask_kind == IQ_MASK_ADD_F32 && reinterpret_cast<uintptr_t>(mask) % 4)
+    return fail(IQ_ERR_INVALID_ARG, "float mask not 4-byte aligned");
+  for (int b = 0; b < c->batch; ++b)
+    if (mask_stride < c->lens[b]) return fail(IQ_ERR_INVALID_ARG, "mask row shorter than a sequence");
+  return attend_impl(c, q, q_heads, n_queries, scale, 0, rot_bf16, out, out_f32, workspace, workspace_bytes,
+                     stream, nullptr, nullptr, 0, mask_kind, mask, mask_stride);
 }
 
 int iq_read_status(void* workspace, iq_stream_t stream, int* device_status) {
