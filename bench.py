@@ -205,16 +205,30 @@ def run_ours(args):
               if "accept_seed" in w else None)
     # attend_kernel + combine_kernel, plus append_kernel when the step does not fuse
     # (more than 8 query rows per kv head)
-    launches_per_step = 2 if Hq // Hkv * L <= 8 else 3
+    launches_per_step = 2 if Hq // Hkv * L <= 8 and args.mask == "none" else 3
+
+    mask = None
+    if args.mask != "none":  # an explicit mask instead of the causal one: [B, L, S], ~90% of keys kept
+        S = cache.capacity
+        g = torch.Generator(device="cpu").manual_seed(w["seed"])
+        keep = torch.rand((B, L, S), generator=g) < 0.9
+        keep[:, :, :] |= torch.arange(S)[None, None, :] >= S - 256  # never a fully masked row
+        mask = (keep if args.mask == "bool" else torch.where(keep, 0.0, float("-inf")).float()).to(dev)
 
     def step(i, ev=None):
         # append the step's new tokens, then attend (one library call: a single
         # attention launch that also encodes the new rows for decode-shaped
         # steps, the append launch then the attention otherwise)
         k, v, q = dsteps[i]
-        if ev is not None:
+        if ev is not None and mask is None:
             ev[0].record(stream)
-        cache.append_attend(k, v, q, rot, causal=w["causal"], out=out)
+        if mask is None:
+            cache.append_attend(k, v, q, rot, causal=w["causal"], out=out)
+        else:
+            cache.append(k, v, rot)
+            if ev is not None:
+                ev[0].record(stream)
+            cache.attend(q, rot, mask=mask, out=out)
         if ev is not None:
             ev[1].record(stream)
         if accept is not None:  # speculative verify: keep the accepted prefix only
@@ -276,7 +290,11 @@ def run_ours(args):
         dk.copy_(k, non_blocking=True)
         dv.copy_(v, non_blocking=True)
         dq.copy_(q, non_blocking=True)
-        cache.append_attend(dk, dv, dq, rot, causal=w["causal"], out=out)
+        if mask is None:
+            cache.append_attend(dk, dv, dq, rot, causal=w["causal"], out=out)
+        else:
+            cache.append(dk, dv, rot)
+            cache.attend(dq, rot, mask=mask, out=out)
         host_out.copy_(out, non_blocking=True)
         e_tokens += int(cache.lens.sum())
         if accept is not None:
@@ -293,6 +311,8 @@ def run_ours(args):
         # per call: the cache scanned (256 B per token-head) plus the append
         # (1024 B of bf16 K/V read and 256 B written per new token-head)
         call_bytes = token_heads * (K_ROW + V_ROW) + B * Hkv * w["append"] * (4 * 256 + K_ROW + V_ROW)
+        if mask is not None:  # the mask entries of the scanned keys; the append runs outside the bracket
+            call_bytes = token_heads * (K_ROW + V_ROW) + token_heads / Hkv * L * mask.element_size()
         achieved = call_bytes / attn_avg_s / 1e9
         h2d = (dsteps[0][0].numel() + dsteps[0][1].numel() + dsteps[0][2].numel()) * 2
         d2h = out.numel() * 2
@@ -305,7 +325,8 @@ def run_ours(args):
             "data": "synthetic (seeded N(0,1); keys with x20 outlier channels)",
             "config": {"workload": f"{w['name']}: B={B} seqs, Hq={Hq}/Hkv={Hkv}, head_dim=256, "
                                    f"{w['prefill']}-token K4/V3 cache, append {w['append']} + attend "
-                                   f"{L} query per step",
+                                   f"{L} query per step"
+                                   + ("" if mask is None else f", explicit {args.mask} mask [B, L, {mask.shape[2]}]"),
                        "parallelism": f"replicas x{ws}",
                        "l2": f"no flush: the cache read per step ({token_heads * (K_ROW + V_ROW) / 1e6:.0f} MB) "
                              f"{'exceeds' if token_heads * (K_ROW + V_ROW) > 129e6 else 'is below'} the 129 MB L2"},
@@ -448,6 +469,8 @@ def main():
     ap.add_argument("--workload", type=int, default=4, choices=[2, 4, 5])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mask", default="none", choices=["none", "bool", "add"],
+                    help="attend with an explicit bool / additive mask [B, L, S] instead of the causal one")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per step instead of the workload's own count (smaller profiling cases)")
     args = ap.parse_args()
