@@ -25,9 +25,10 @@
 //    ahead across unit boundaries; its warpgroup hands most of its registers
 //    to the consumer warps;
 //  * consumer warps unpack codes in registers with bit tricks and run m16n8k16
-//    tensor-core MMAs: S = (64 + K_codes) . q - 64 sum(q) (fp16, per 64-dim
-//    group, fp32 accumulate from -64 sum(q)), folded with the group scale and
-//    bias on CUDA cores; online softmax in fp32 with a lazily moving
+//    tensor-core MMAs: S_G = (64 + K_codes) . q (fp16, per 64-dim group, fp32
+//    accumulate) scaled by the group scale on CUDA cores, plus the per-token
+//    bias sum_G (b_G - 64 s_G) sum(q_G) from two bf16 MMAs over the raw
+//    scale/bias words; online softmax in fp32 with a lazily moving
 //    reference max; O^T += (V_codes - 4)^T
 //    . (P * s_v) with P transposed in registers by movmatrix; the value bias
 //    term sum_t p_t (b_t + 4 s_t) on CUDA cores.
@@ -232,9 +233,9 @@ __device__ __forceinline__ float pick_bf16(uint2 v, int G) {
 
 // Key codes enter the q.K product as fp16 values 64 + c: a nibble ORed into
 // bits 4..7 of the half 0x5400 (64.0, mantissa step 1 from bit 4 up) is
-// exactly 64 + c.  The 64 * sum(q'') offset is removed by starting the
-// accumulator at -64 * sum(q'').  The query operand is q'' converted to fp16
-// (exact for 2^-14 <= |q''| < 65504).
+// exactly 64 + c.  The 64 * sum(q'') offset is cancelled inside the per-token
+// bias product (-64 s_G sum(q''_G)).  The query operand is q'' converted to
+// fp16 (exact for 2^-14 <= |q''| < 65504).
 constexpr float KOFFSET = 64.0f;
 
 // The 16 codes of two consecutive words (dims 0..7 in w0, 8..15 in w1) ->
@@ -446,8 +447,11 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   int b = 0, kvh = 0, qt = 0, T = 0, limit = 0, qmin = 0;
   int qpos[NT][2];
   int qrow[NT][2];  // query index of rows 2t, 2t+1 of each n-tile (explicit masks)
-  float qsr[GPW][NT][2];   // per group: sum of q'' over the group's dims (rows 2t, 2t+1 of each n-tile)
-  float qoff[GPW][NT][2];  // -64 * qsr: the score accumulators start there, cancelling the code offset
+  // B fragments of the per-token bias product (two bf16 MMAs per n-tile):
+  // k-slots [b_0..b_3, s_0..s_3, b_0..b_3, s_0..s_3] of a key row against
+  // [S_hi, -64 S_hi, S_mid, -64 S_mid] and [S_lo, -64 S_lo, 0, 0], S_G = sum of
+  // q'' over group G for this lane's query row, S = S_hi + S_mid + S_lo exactly
+  uint32_t kbq[NT][2][2];
   float O[GPW][4][NT][4];
   float bacc[GPW][NT][2];
   float msc[NT][2], lrow[NT][2];  // reference max (log2 units), partial row sum
@@ -532,16 +536,28 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       if (t == 0) qsum[(8 * j + g) * 4 + G] = qpart;
     }
     named_bar(1, NCT);  // fragments and sums visible to every warp
+    // this lane's k-slots: 2t, 2t+1 (and 2t+8, 2t+9) = groups 2(t&1), 2(t&1)+1
+    // of b (t < 2) or of s (t >= 2, coefficient -64); groups another warp of the
+    // stream owns contribute there instead
 #pragma unroll
-    for (int gi = 0; gi < GPW; ++gi) {
-      const int Gr = dg * GPW + gi;
+    for (int j = 0; j < NT; ++j) {
+      uint32_t parts[3] = {0u, 0u, 0u};  // bf16x2 of (group 2(t&1), group 2(t&1)+1) per part
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        qsr[gi][j][0] = qsum[(8 * j + 2 * t) * 4 + Gr];
-        qsr[gi][j][1] = qsum[(8 * j + 2 * t + 1) * 4 + Gr];
-        qoff[gi][j][0] = -KOFFSET * qsr[gi][j][0];
-        qoff[gi][j][1] = -KOFFSET * qsr[gi][j][1];
+      for (int h = 0; h < 2; ++h) {
+        const int G = 2 * (t & 1) + h;
+        const bool mine = G >= dg * GPW && G < dg * GPW + GPW;
+        float x = mine ? qsum[(8 * j + g) * 4 + G] * (t < 2 ? 1.0f : -KOFFSET) : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {  // x = hi + mid + lo exactly (each a bf16)
+          const uint32_t bits = f32_to_bf16_bits(x);
+          parts[k] |= bits << (16 * h);
+          x -= bf16_to_f32(bits);
+        }
       }
+      kbq[j][0][0] = parts[0];
+      kbq[j][0][1] = parts[1];
+      kbq[j][1][0] = parts[2];
+      kbq[j][1][1] = 0u;
     }
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -576,20 +592,28 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     constexpr int N = decltype(n_tag)::value;
     constexpr bool FULL = decltype(full_tag)::value;
     int rr0[N], rr1[N];
-    uint2 ksc0[N], ksc1[N], kbi0[N], kbi1[N];
+    uint2 ksc0[N], ksc1[N];
+    float sc[N][NT][4];
+    // per-token bias: sum_G (b_G - 64 s_G) sum(q''_G), by two bf16 MMAs whose A
+    // operand is the raw bias/scale words of the two token rows
+    const uint32_t bs_off = (t < 2 ? OFF_KB : OFF_KS) + (t & 1) * 4;
 #pragma unroll
     for (int n = 0; n < N; ++n) {
       rr0[n] = subs[n] * 16 + rS0;
       rr1[n] = rr0[n] + 8;
       ksc0[n] = lds64(sb + OFF_KS + rr0[n] * 8);
       ksc1[n] = lds64(sb + OFF_KS + rr1[n] * 8);
-      kbi0[n] = lds64(sb + OFF_KB + rr0[n] * 8);
-      kbi1[n] = lds64(sb + OFF_KB + rr1[n] * 8);
+      const uint32_t w0 = lds32(sb + bs_off + rr0[n] * 8), w1 = lds32(sb + bs_off + rr1[n] * 8);
+      const uint32_t A[4] = {w0, w1, w0, w1};
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        sc[n][j][0] = sc[n][j][1] = sc[n][j][2] = sc[n][j][3] = 0.f;
+        mma_bf16(sc[n][j], A, kbq[j][0][0], kbq[j][0][1]);
+        mma_bf16(sc[n][j], A, kbq[j][1][0], kbq[j][1][1]);
+      }
     }
 
-    // scores: per group, S_G = (64 + codes) . q'' - 64 sum(q'') = codes . q''
-    // (fp32; the accumulator starts at -64 sum(q'')), folded with scale/bias
-    float sc[N][NT][4];
+    // scores: per group, S_G = (64 + codes) . q'' (fp32), added as s_G * S_G
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
       const int Gr = dg * GPW + gi;
@@ -607,10 +631,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
       for (int n = 0; n < N; ++n)
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          acc[n][j][0] = acc[n][j][2] = qoff[gi][j][0];
-          acc[n][j][1] = acc[n][j][3] = qoff[gi][j][1];
-        }
+        for (int j = 0; j < NT; ++j) acc[n][j][0] = acc[n][j][1] = acc[n][j][2] = acc[n][j][3] = 0.f;
 #pragma unroll
       for (int s = 0; s < 4; ++s)
 #pragma unroll
@@ -625,19 +646,12 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
       for (int n = 0; n < N; ++n) {
         const float s0 = pick_bf16(ksc0[n], Gr), s1 = pick_bf16(ksc1[n], Gr);
-        const float b0 = pick_bf16(kbi0[n], Gr), b1 = pick_bf16(kbi1[n], Gr);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {  // this warp's groups, summed in group order
+        for (int j = 0; j < NT; ++j) {  // this warp's groups, in group order
           float* c = sc[n][j];
           const float* a = acc[n][j];
-          if (gi == 0) {
-            c[0] = s0 * a[0]; c[1] = s0 * a[1]; c[2] = s1 * a[2]; c[3] = s1 * a[3];
-          } else {
-            c[0] = fmaf(s0, a[0], c[0]); c[1] = fmaf(s0, a[1], c[1]);
-            c[2] = fmaf(s1, a[2], c[2]); c[3] = fmaf(s1, a[3], c[3]);
-          }
-          c[0] = fmaf(b0, qsr[gi][j][0], c[0]); c[1] = fmaf(b0, qsr[gi][j][1], c[1]);
-          c[2] = fmaf(b1, qsr[gi][j][0], c[2]); c[3] = fmaf(b1, qsr[gi][j][1], c[3]);
+          c[0] = fmaf(s0, a[0], c[0]); c[1] = fmaf(s0, a[1], c[1]);
+          c[2] = fmaf(s1, a[2], c[2]); c[3] = fmaf(s1, a[3], c[3]);
         }
       }
     }
