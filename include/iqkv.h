@@ -205,7 +205,9 @@ int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queri
  *    IQ_MASK_ADD_F32 (device float32, may hold -inf) or IQ_MASK_BOOL_U8
  *    (device uint8, 0 = masked).
  * mask: [B][n_queries][mask_stride] elements, row (b, i) covering keys
- *    0 .. lens[b]-1 (mask_stride >= every lens[b]); shared by every query head.
+ *    0 .. lens[b]-1 (mask_stride >= every lens[b], a multiple of 128; the base
+ *    16-byte aligned); shared by every query head.  The attention streams the
+ *    rows in 128-key pieces with the cache tiles.
  * A row whose keys are all masked by a bool mask averages the values
  * uniformly, as the page's softmax does; a float-mask row that is -inf
  * everywhere has no softmax (NaN output, status bit 4).  Scores are float32:

@@ -276,11 +276,18 @@ class IQCache:
         if not mask.is_cuda or mask.dim() != 3 or mask.shape[0] != B or mask.shape[1] != L:
             raise ValueError("mask must be a CUDA tensor [B, L, S]")
         if mask.dtype == torch.bool:
-            mask, kind = mask.contiguous().view(torch.uint8), _abi.IQ_MASK_BOOL_U8
+            kind = _abi.IQ_MASK_BOOL_U8
         elif mask.dtype == torch.float32:
-            mask, kind = mask.contiguous(), _abi.IQ_MASK_ADD_F32
+            kind = _abi.IQ_MASK_ADD_F32
         else:
             raise ValueError("mask must be bool or float32")
+        S = mask.shape[2]
+        if S % 128 or not mask.is_contiguous():  # the library streams mask rows in 128-key pieces
+            padded = torch.zeros((B, L, (S + 127) // 128 * 128), dtype=mask.dtype, device=mask.device)
+            padded[:, :, :S] = mask
+            mask = padded
+        if kind == _abi.IQ_MASK_BOOL_U8:
+            mask = mask.view(torch.uint8)
         if scale is None:
             scale = 1.0 / math.sqrt(D)
         if out is None:

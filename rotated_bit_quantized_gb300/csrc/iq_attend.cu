@@ -325,12 +325,17 @@ struct Cfg : Tiling<TILE_> {
   static constexpr int QB_BYTES = DS * GPW * 4 * NT * 32 * 8;       // q'' MMA B fragments
   static constexpr int OFF_BAR = OFF_QB + QB_BYTES;
   static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8 + 8;  // + the fused-append barrier
-  static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
+  // explicit-mask rows of a stage (the unit's queries, at most GT, x TILE keys,
+  // 4-byte elements at most): the last area, part of the launch only with a mask
+  static constexpr int MSK_STAGE = GT * TILE_ * 4;
+  static constexpr int OFF_MSK = (OFF_FLAG + 16 + 127) / 128 * 128;
+  static constexpr int SMEM = OFF_MSK + 1024;                          // + alignment slack
+  static constexpr int SMEM_MASK = OFF_MSK + NSTAGE * MSK_STAGE + 1024;
   static_assert(OFF_XBUF % 16 == 0 && OFF_OBUF % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
   static_assert(4 % DS == 0, "shape");
 };
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, bool MASKED>
 __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>::THREADS, MINB)
     attend_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap kmap) {
   using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>;
@@ -416,7 +421,20 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         }
         uint8_t* sbp = smem + st * STAGE;
         const long long row0 = (static_cast<long long>(bb) * p.kv_heads + hh) * p.cap + (gt - p.prefix[u]) * TILE;
-        mbar_arrive_expect_tx(&full[st], STAGE_TX);
+        if constexpr (MASKED) {  // the unit's mask rows for this tile's keys (one copy per query)
+          const int qt = ug % p.nqt, elem = p.mask_kind == 2 ? 4 : 1;
+          const int i_lo = qt * C::GT / p.rep, i_hi = min((qt * C::GT + C::GT - 1) / p.rep, p.nq - 1);
+          const uint32_t bytes = TILE * elem;
+          mbar_arrive_expect_tx(&full[st], STAGE_TX + (i_hi - i_lo + 1) * bytes);
+          for (int i = i_lo; i <= i_hi; ++i)
+            bulk_g2s_plain(smem + C::OFF_MSK + st * C::MSK_STAGE + (i - i_lo) * bytes,
+                           static_cast<const uint8_t*>(p.mask) +
+                               ((static_cast<long long>(bb) * p.nq + i) * p.mask_stride + (gt - p.prefix[u]) * TILE) *
+                                   elem,
+                           bytes, &full[st]);
+        } else {
+          mbar_arrive_expect_tx(&full[st], STAGE_TX);
+        }
         tensor2d_g2s(sbp + OFF_K, &kmap, 0, static_cast<int>(row0), &full[st], pol);
         bulk_g2s(sbp + OFF_V, p.v_codes + row0 * kVWords, V_BYTES, &full[st], pol);
         bulk_g2s(sbp + OFF_KS, p.k_scales + row0 * kGroups, SB_BYTES, &full[st], pol);
@@ -447,6 +465,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   int b = 0, kvh = 0, qt = 0, T = 0, limit = 0, qmin = 0;
   int qpos[NT][2];
   int qrow[NT][2];  // query index of rows 2t, 2t+1 of each n-tile (explicit masks)
+  int qlo = 0;      // the unit's first query (its mask row is the stage's first)
   // B fragments of the per-token bias product (two bf16 MMAs per n-tile):
   // k-slots [b_0..b_3, s_0..s_3, b_0..b_3, s_0..s_3] of a key row against
   // [S_hi, -64 S_hi, S_mid, -64 S_mid] and [S_lo, -64 S_lo, 0, 0], S_G = sum of
@@ -467,7 +486,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     limit = tile_limit(p, T, qt, GT);
     // the first key some row of the unit cannot see (no sub-tile at or past it
     // takes the unmasked path); an explicit mask reads every sub-tile
-    qmin = p.mask_kind >= 2 ? -1 : p.causal ? T - p.nq + (qt * GT) / p.rep : T - 1;
+    qmin = MASKED ? -1 : p.causal ? T - p.nq + (qt * GT) / p.rep : T - 1;
+    qlo = (qt * GT) / p.rep;
     named_bar(1, NCT);  // every consumer is done with the previous unit's fragments and sums
     // q' = bf16(q @ M_b), q'' = bf16(q' * scale), written straight into the fp16
     // MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].  Item
@@ -588,7 +608,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   // independent chains per phase, one vote and one query-fragment load per
   // k-step for both).  FULL: every token of the N sub-tiles is inside the
   // unit's range and visible to every row (no masking work at all).
-  auto subtiles = [&](auto n_tag, auto full_tag, const int (&subs)[2], const int (&tokbase)[2], uint32_t sb) {
+  auto subtiles = [&](auto n_tag, auto full_tag, const int (&subs)[2], const int (&tokbase)[2], uint32_t sb,
+                      uint32_t msk) {
     constexpr int N = decltype(n_tag)::value;
     constexpr bool FULL = decltype(full_tag)::value;
     int rr0[N], rr1[N];
@@ -691,15 +712,14 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
           valid[n][j][1] = in0 && tok0 <= qpos[j][1];
           valid[n][j][2] = in1 && tok1 <= qpos[j][0];
           valid[n][j][3] = in1 && tok1 <= qpos[j][1];
-          if (p.mask_kind >= 2) {  // explicit mask: added, or a masked score made most negative
+          if constexpr (MASKED) {  // explicit mask (staged with the tile): added, or masked
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               if (!valid[n][j][e]) continue;
-              const long long mi = (static_cast<long long>(b) * p.nq + qrow[j][e & 1]) * p.mask_stride +
-                                   (e < 2 ? tok0 : tok1);
+              const int mi = (qrow[j][e & 1] - qlo) * TILE + subs[n] * 16 + rS0 + (e < 2 ? 0 : 8);
               if (p.mask_kind == 2)
-                sc[n][j][e] += __ldg(static_cast<const float*>(p.mask) + mi);
-              else if (__ldg(static_cast<const unsigned char*>(p.mask) + mi) == 0)
+                sc[n][j][e] += __uint_as_float(lds32(msk + mi * 4));
+              else if (lds8(msk + mi) == 0)
                 sc[n][j][e] = MASKED_SCORE;
             }
           }
@@ -994,6 +1014,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         break;
       }
       const uint32_t sb = smem_u32(smem + st * STAGE);
+      const uint32_t msk = smem_u32(smem + C::OFF_MSK + st * C::MSK_STAGE);
       const int tile_tok = static_cast<int>(gt - tile0) * TILE;
       // global sub-tile SUBS*k + sub belongs to stream (SUBS*k + sub) % STREAMS;
       // a stream takes its sub-tiles of the stage PAIR at a time
@@ -1004,14 +1025,14 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         if (tb[0] >= limit) break;
         if (PAIR == 2 && subs[1] < SUBS && tb[1] < limit) {
           if (tb[1] + 16 <= limit && tb[1] + 15 <= qmin)
-            subtiles(std::integral_constant<int, 2>{}, std::true_type{}, subs, tb, sb);
+            subtiles(std::integral_constant<int, 2>{}, std::true_type{}, subs, tb, sb, msk);
           else
-            subtiles(std::integral_constant<int, 2>{}, std::false_type{}, subs, tb, sb);
+            subtiles(std::integral_constant<int, 2>{}, std::false_type{}, subs, tb, sb, msk);
         } else {
           if (tb[0] + 16 <= limit && tb[0] + 15 <= qmin)
-            subtiles(std::integral_constant<int, 1>{}, std::true_type{}, subs, tb, sb);
+            subtiles(std::integral_constant<int, 1>{}, std::true_type{}, subs, tb, sb, msk);
           else
-            subtiles(std::integral_constant<int, 1>{}, std::false_type{}, subs, tb, sb);
+            subtiles(std::integral_constant<int, 1>{}, std::false_type{}, subs, tb, sb, msk);
         }
       }
       __syncwarp();
@@ -1148,9 +1169,11 @@ int blocks_per_sm() {
   if (cache[dev] == 0) {
     using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>;
     int n = 0;
-    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>,
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, false>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>,
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, true>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_MASK);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, false>,
                                                       C::THREADS, C::SMEM) !=
             cudaSuccess ||
         n <= 0)
@@ -1328,13 +1351,15 @@ int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStrea
   // The warpgroups move registers between them (setmaxnreg); that split adds
   // up to the block's launch allocation only at the register count it was
   // designed for, so any other build of the kernel is refused, never launched.
-  static int launch_regs = -1;
-  if (launch_regs < 0) {
+  const bool masked = prm.mask_kind >= 2;
+  static int launch_regs[2] = {-1, -1};
+  if (launch_regs[masked] < 0) {
     cudaFuncAttributes fa;
-    IQ_CUDA(cudaFuncGetAttributes(&fa, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>));
-    launch_regs = fa.numRegs;
+    IQ_CUDA(cudaFuncGetAttributes(&fa, masked ? attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, true>
+                                              : attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, false>));
+    launch_regs[masked] = fa.numRegs;
   }
-  if (launch_regs != C::LAUNCH_REGS)
+  if (launch_regs[masked] != C::LAUNCH_REGS)
     return fail(IQ_ERR_UNSUPPORTED, "attention kernel built with an unexpected register count");
   // Both kernels are programmatic dependents of their predecessor in the
   // stream: their launch overlaps its tail, and each waits for it
@@ -1345,11 +1370,14 @@ int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStrea
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.dynamicSmemBytes = prm.mask_kind >= 2 ? C::SMEM_MASK : C::SMEM;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  IQ_CUDA(cudaLaunchKernelEx(&cfg, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>, prm, map));
+  if (masked)
+    IQ_CUDA(cudaLaunchKernelEx(&cfg, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, true>, prm, map));
+  else
+    IQ_CUDA(cudaLaunchKernelEx(&cfg, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, false>, prm, map));
   // the split combine, after the attention grid
   cfg.gridDim = dim3(static_cast<unsigned>(prm.num_units));
   cfg.blockDim = dim3(256);
@@ -1537,6 +1565,8 @@ int iq_attend_mask(const iq_cache* c, const uint16_t* q, int q_heads, int n_quer
   if (!mask) return fail(IQ_ERR_INVALID_ARG, "null mask");
   if (mask_kind == IQ_MASK_ADD_F32 && reinterpret_cast<uintptr_t>(mask) % 4)
     return fail(IQ_ERR_INVALID_ARG, "float mask not 4-byte aligned");
+  if (reinterpret_cast<uintptr_t>(mask) % 16 || mask_stride % 128)
+    return fail(IQ_ERR_INVALID_ARG, "mask not 16-byte aligned or its row stride not a multiple of 128");
   for (int b = 0; b < c->batch; ++b)
     if (mask_stride < c->lens[b]) return fail(IQ_ERR_INVALID_ARG, "mask row shorter than a sequence");
   return attend_impl(c, q, q_heads, n_queries, scale, 0, rot_bf16, out, out_f32, workspace, workspace_bytes,
