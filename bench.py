@@ -42,8 +42,8 @@ K_ROW, V_ROW = 144, 112  # algorithmic bytes per token-head: codes + bf16 scales
 # combine_kernel; profiles/attend_kernel_batched_decode_32x32k.md).  Reported
 # only while the attention source is the one that was measured.
 TRAFFIC = {"source": "rotated_bit_quantized_gb300/csrc/iq_attend.cu",
-           "sha256": "c3028c4e608184b68f1b59e4694cd09f6210566c3acdef3c448c5dc98c307be6",
-           "bytes": (539.41 + 3.26 + 2.93) * 1e6}
+           "sha256": "b4d7924876908c4f2fc16a58cfcb0a8063d72cdc56c674bac6e76c3bc6372f54",
+           "bytes": ((539.39 + 3.16 + 2.93) + (539.44 + 0.46 + 2.93)) / 2 * 1e6}
 
 
 def measured_traffic():
