@@ -25,9 +25,10 @@
 //    ahead across unit boundaries; its warpgroup hands most of its registers
 //    to the consumer warps;
 //  * consumer warps unpack codes in registers with bit tricks and run m16n8k16
-//    tensor-core MMAs: S_G = (64 + K_codes) . q (fp16, per 64-dim group, fp32
-//    accumulate) scaled by the group scale on CUDA cores, plus the per-token
-//    bias sum_G (b_G - 64 s_G) sum(q_G) from two bf16 MMAs over the raw
+//    tensor-core MMAs: S_G = (off + K_codes) . q (even dims bf16 with off =
+//    128, odd dims fp16 with off = 64, per 64-dim group, fp32 accumulate)
+//    scaled by the group scale on CUDA cores, plus the per-token bias
+//    sum_G b_G sum(q_G) - s_G sum(off q_G) from two bf16 MMAs over the raw
 //    scale/bias words; online softmax in fp32 with a lazily moving
 //    reference max; O^T += (V_codes - 4)^T
 //    . (P * s_v) with P transposed in registers by movmatrix; the value bias
@@ -231,18 +232,23 @@ __device__ __forceinline__ float pick_bf16(uint2 v, int G) {
   return bf16_to_f32((G & 1) ? (w >> 16) : (w & 0xFFFFu));
 }
 
-// Key codes enter the q.K product as fp16 values 64 + c: a nibble ORed into
-// bits 4..7 of the half 0x5400 (64.0, mantissa step 1 from bit 4 up) is
-// exactly 64 + c.  The 64 * sum(q'') offset is cancelled inside the per-token
-// bias product (-64 s_G sum(q''_G)).  The query operand is q'' converted to
-// fp16 (exact for 2^-14 <= |q''| < 65504).
-constexpr float KOFFSET = 64.0f;
+// Key codes enter the q.K product without any shift: the code in the low
+// nibble of a byte (an even dim) becomes the bf16 value 128 + c (the nibble
+// ORed into the mantissa of 0x4300, whose unit step is bit 0) and the code in
+// the high nibble (an odd dim) becomes the fp16 value 64 + c (the nibble in
+// bits 4..7 of 0x5400, whose unit step is bit 4).  Even dims therefore meet
+// q'' in bf16 MMAs (q'' is a bf16 value: exact) and odd dims in fp16 MMAs
+// (q'' converted to fp16, exact for 2^-14 <= |q''| < 65504); both accumulate
+// into the same fp32 scores.  The offsets 128 sum(q''_even) + 64 sum(q''_odd)
+// are cancelled inside the per-token bias product.
+constexpr float KOFF_EVEN = 128.0f;
+constexpr float KOFF_ODD = 64.0f;
 
 // The 16 codes of two consecutive words (dims 0..7 in w0, 8..15 in w1) ->
-// eight fp16x2 registers 64 + (c_a, c_b); register m holds the dims
-// k_pair(m, 0..1).  Two byte permutes bring the third and fourth nibbles of each
-// byte pair down; four shifts by 4 (multiplies, off the logic pipe) lift the
-// low nibbles to bits 4..7.
+// eight registers; register m holds the dims k_pair(m, 0..1): even m as bf16x2
+// 128 + (c_a, c_b) (even dims), odd m as fp16x2 64 + (c_a, c_b) (odd dims).
+// Two byte permutes bring the nibbles of bytes 1 and 3 down; every register is
+// then one AND-OR.
 __host__ __device__ constexpr int k_pair(int m, int h) {
   // {0,4} {1,5} {8,12} {9,13} {2,10} {3,11} {6,14} {7,15}
   return h == 0 ? (m < 4 ? (m & 1) + 8 * (m >> 1) : (m == 4 ? 2 : m == 5 ? 3 : m)) : k_pair(m, 0) + (m < 4 ? 4 : 8);
@@ -250,19 +256,27 @@ __host__ __device__ constexpr int k_pair(int m, int h) {
 static_assert(k_pair(0, 1) == 4 && k_pair(3, 0) == 9 && k_pair(3, 1) == 13 && k_pair(4, 1) == 10 &&
                   k_pair(6, 0) == 6 && k_pair(7, 1) == 15 && k_pair(2, 0) == 8,
               "register -> dim map");
+// Registers of k-step s of a 16-dim chunk: steps 0, 1 are the bf16 (even-dim)
+// MMAs over registers (0, 2) and (4, 6), steps 2, 3 the fp16 (odd-dim) MMAs
+// over (1, 3) and (5, 7); h = 0 feeds k-slots 2t, 2t+1, h = 1 slots 2t+8, 2t+9.
+__host__ __device__ constexpr int kreg(int s, int h) { return s < 2 ? 4 * s + 2 * h : 4 * (s - 2) + 2 * h + 1; }
+static_assert(k_pair(kreg(0, 0), 0) % 2 == 0 && k_pair(kreg(1, 1), 1) % 2 == 0 && k_pair(kreg(2, 0), 0) % 2 == 1 &&
+                  k_pair(kreg(3, 1), 1) % 2 == 1,
+              "bf16 steps hold even dims, fp16 steps odd dims");
 __device__ __forceinline__ void unpack_k16(uint32_t w0, uint32_t w1, uint32_t* r) {
-  constexpr uint32_t MAGIC = 0x54005400u;  // 64.0 in each half
-  constexpr uint32_t MASK = 0x00F000F0u;
+  constexpr uint32_t LO_MAGIC = 0x43004300u;  // bf16 128.0 in each half
+  constexpr uint32_t HI_MAGIC = 0x54005400u;  // fp16 64.0 in each half
+  constexpr uint32_t LO = 0x000F000Fu, HI = 0x00F000F0u;
   const uint32_t x = __byte_perm(w0, w1, 0x0501);  // bytes w0.b1 (nibbles 2, 3), w1.b1
   const uint32_t y = __byte_perm(w0, w1, 0x0703);  // bytes w0.b3 (nibbles 6, 7), w1.b3
-  r[0] = and_or(w0 * 16u, MASK, MAGIC);  // (0, 4)
-  r[1] = and_or(w0, MASK, MAGIC);        // (1, 5)
-  r[2] = and_or(w1 * 16u, MASK, MAGIC);  // (8, 12)
-  r[3] = and_or(w1, MASK, MAGIC);        // (9, 13)
-  r[4] = and_or(x * 16u, MASK, MAGIC);   // (2, 10)
-  r[5] = and_or(x, MASK, MAGIC);         // (3, 11)
-  r[6] = and_or(y * 16u, MASK, MAGIC);   // (6, 14)
-  r[7] = and_or(y, MASK, MAGIC);         // (7, 15)
+  r[0] = and_or(w0, LO, LO_MAGIC);  // (0, 4)
+  r[1] = and_or(w0, HI, HI_MAGIC);  // (1, 5)
+  r[2] = and_or(w1, LO, LO_MAGIC);  // (8, 12)
+  r[3] = and_or(w1, HI, HI_MAGIC);  // (9, 13)
+  r[4] = and_or(x, LO, LO_MAGIC);   // (2, 10)
+  r[5] = and_or(x, HI, HI_MAGIC);   // (3, 11)
+  r[6] = and_or(y, LO, LO_MAGIC);   // (6, 14)
+  r[7] = and_or(y, HI, HI_MAGIC);   // (7, 15)
 }
 
 // bf16 bits -> fp16 bits (round to nearest; exact for normal fp16 values)
@@ -317,7 +331,7 @@ struct Cfg : Tiling<TILE_> {
   static constexpr int OBUF_BYTES = GT * 256 * 4;  // the CTA's merged O of a unit
   static constexpr int OFF_OBUF = NSTAGE * STAGE;
   static constexpr int OFF_QSUM = OFF_OBUF + OBUF_BYTES;
-  static constexpr int OFF_MBUF = OFF_QSUM + GT * 16;
+  static constexpr int OFF_MBUF = OFF_QSUM + GT * 32;
   static constexpr int OFF_LBUF = OFF_MBUF + STREAMS * GT * 4;
   static constexpr int OFF_XBUF = OFF_LBUF + STREAMS * GT * 4;
   static constexpr int XBUF_BYTES = DS > 1 ? STREAMS * 2 * 2 * DS * NT * 32 * 16 : 0;  // x2 parities x2 sub-tiles
@@ -468,8 +482,10 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   int qlo = 0;      // the unit's first query (its mask row is the stage's first)
   // B fragments of the per-token bias product (two bf16 MMAs per n-tile):
   // k-slots [b_0..b_3, s_0..s_3, b_0..b_3, s_0..s_3] of a key row against
-  // [S_hi, -64 S_hi, S_mid, -64 S_mid] and [S_lo, -64 S_lo, 0, 0], S_G = sum of
-  // q'' over group G for this lane's query row, S = S_hi + S_mid + S_lo exactly
+  // [S_hi, -F_hi, S_mid, -F_mid] and [S_lo, -F_lo, 0, 0], S_G = sum of q''
+  // over group G for this lane's query row and F_G = sum of off * q'' (the
+  // code offsets' share), each split into three bf16 parts that add up to it
+  // exactly
   uint32_t kbq[NT][2][2];
   float O[GPW][4][NT][4];
   float bacc[GPW][NT][2];
@@ -537,27 +553,38 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
         for (int d = 0; d < 16; ++d) yb[d] = 0u;
       }
-      float qpart = 0.f;  // sum of the fp16 operand values (the offset the fold removes)
+      // sums of the operand values the MMAs multiply: even dims as bf16 (q''
+      // itself), odd dims as fp16
+      float qe = 0.f, qo = 0.f;
 #pragma unroll
-      for (int d = 0; d < 16; ++d)
-        qpart += __half2float(__ushort_as_half(static_cast<unsigned short>(bf16_to_f16_bits(yb[d]))));
+      for (int d = 0; d < 16; d += 2) {
+        qe += bf16_to_f32(yb[d]);
+        qo += __half2float(__ushort_as_half(static_cast<unsigned short>(bf16_to_f16_bits(yb[d + 1]))));
+      }
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         uint32_t h2[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int m = 2 * s + h;
-          h2[h] = bf16_to_f16_bits(yb[k_pair(m, 0)]) | (bf16_to_f16_bits(yb[k_pair(m, 1)]) << 16);
+          const int m = kreg(s, h);
+          h2[h] = s < 2 ? (yb[k_pair(m, 0)] | (yb[k_pair(m, 1)] << 16))
+                        : (bf16_to_f16_bits(yb[k_pair(m, 0)]) | (bf16_to_f16_bits(yb[k_pair(m, 1)]) << 16));
         }
         qbs[((G * 4 + s) * NT + j) * 32 + lane] = make_uint2(h2[0], h2[1]);
       }
-      qpart += __shfl_xor_sync(0xffffffffu, qpart, 1);
-      qpart += __shfl_xor_sync(0xffffffffu, qpart, 2);
-      if (t == 0) qsum[(8 * j + g) * 4 + G] = qpart;
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        qe += __shfl_xor_sync(0xffffffffu, qe, o);
+        qo += __shfl_xor_sync(0xffffffffu, qo, o);
+      }
+      if (t == 0) {  // sum(q''_G) for the bias, and the code offsets' share
+        qsum[((8 * j + g) * 4 + G) * 2] = qe + qo;
+        qsum[((8 * j + g) * 4 + G) * 2 + 1] = fmaf(KOFF_EVEN, qe, KOFF_ODD * qo);
+      }
     }
     named_bar(1, NCT);  // fragments and sums visible to every warp
     // this lane's k-slots: 2t, 2t+1 (and 2t+8, 2t+9) = groups 2(t&1), 2(t&1)+1
-    // of b (t < 2) or of s (t >= 2, coefficient -64); groups another warp of the
+    // of b (t < 2, against S_G) or of s (t >= 2, against -F_G); groups another warp of the
     // stream owns contribute there instead
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -566,7 +593,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       for (int h = 0; h < 2; ++h) {
         const int G = 2 * (t & 1) + h;
         const bool mine = G >= dg * GPW && G < dg * GPW + GPW;
-        float x = mine ? qsum[(8 * j + g) * 4 + G] * (t < 2 ? 1.0f : -KOFFSET) : 0.0f;
+        float x = mine ? (t < 2 ? qsum[((8 * j + g) * 4 + G) * 2] : -qsum[((8 * j + g) * 4 + G) * 2 + 1]) : 0.0f;
 #pragma unroll
         for (int k = 0; k < 3; ++k) {  // x = hi + mid + lo exactly (each a bf16)
           const uint32_t bits = f32_to_bf16_bits(x);
@@ -634,7 +661,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       }
     }
 
-    // scores: per group, S_G = (64 + codes) . q'' (fp32), added as s_G * S_G
+    // scores: per group, S_G = (off + codes) . q'' (fp32), added as s_G * S_G
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
       const int Gr = dg * GPW + gi;
@@ -660,8 +687,11 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
           const uint2 bq = qbs[((Gr * 4 + s) * NT + j) * 32 + lane];
 #pragma unroll
           for (int n = 0; n < N; ++n) {
-            const uint32_t A[4] = {RA[n][2 * s], RB[n][2 * s], RA[n][2 * s + 1], RB[n][2 * s + 1]};
-            mma_f16(acc[n][j], A, bq.x, bq.y);
+            const uint32_t A[4] = {RA[n][kreg(s, 0)], RB[n][kreg(s, 0)], RA[n][kreg(s, 1)], RB[n][kreg(s, 1)]};
+            if (s < 2)
+              mma_bf16(acc[n][j], A, bq.x, bq.y);
+            else
+              mma_f16(acc[n][j], A, bq.x, bq.y);
           }
         }
 #pragma unroll
