@@ -309,25 +309,31 @@ __device__ __forceinline__ void unpack_v3_pair(uint32_t fa, uint32_t fb, uint32_
   h[7] = dq3<5>(x2);
 }
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES>
 struct Cfg : Tiling<TILE_> {
   using Tiling<TILE_>::STAGE;
   static constexpr int GT = 8 * NT;            // query rows per unit
   static constexpr int GPW = 4 / DS;           // 64-dim groups per consumer warp
-  static constexpr int CW = DS * STREAMS;      // consumer warps
-  // CW consumer warps (a multiple of 4: whole warpgroups), then one producer
-  // warpgroup whose first warp streams the tiles; registers move from the
-  // producer warpgroup to the consumers (setmaxnreg)
-  static constexpr int THREADS = (CW + 4) * 32;
+  static constexpr int CW = DS * STREAMS;      // consumer warps of a half
+  // HALVES independent halves (each its own tile range, ring, producer lane
+  // and CW consumer warps, a multiple of 4), then one producer warpgroup whose
+  // warp h streams the tiles of half h; registers move from the producer
+  // warpgroup to the consumers (setmaxnreg).  Two halves share an SM as two
+  // CTAs would, but their consumer warps alternate over the four warp
+  // schedulers, so neither half is served first (two CTAs on one SM are not:
+  // the scheduler favours the older one, which finishes ~12% earlier).
+  static constexpr int THREADS = (HALVES * CW + 4) * 32;
   static constexpr int LAUNCH_REGS = (65536 / (MINB * THREADS)) / 8 * 8;
   static constexpr int PRODUCER_REGS = 24;
   static constexpr int CONSUMER_REGS =
-      ((65536 / MINB - 128 * PRODUCER_REGS) / (CW * 32)) / 8 * 8 > 248
+      ((65536 / MINB - 128 * PRODUCER_REGS) / (HALVES * CW * 32)) / 8 * 8 > 248
           ? 248
-          : ((65536 / MINB - 128 * PRODUCER_REGS) / (CW * 32)) / 8 * 8;
+          : ((65536 / MINB - 128 * PRODUCER_REGS) / (HALVES * CW * 32)) / 8 * 8;
   static_assert(CW % 4 == 0, "consumer warps form whole warpgroups");
+  static_assert(HALVES == 1 || (HALVES == 2 && CW == 4), "two halves of one consumer warpgroup each");
   static_assert(CONSUMER_REGS >= LAUNCH_REGS && PRODUCER_REGS <= LAUNCH_REGS, "register split");
-  static_assert(MINB * (CW * 32 * CONSUMER_REGS + 128 * PRODUCER_REGS) <= 65536, "register file");
+  static_assert(HALVES * CW * 32 * CONSUMER_REGS + 128 * PRODUCER_REGS <= LAUNCH_REGS * THREADS,
+                "the split fits the block's launch allocation");
   static constexpr int OBUF_BYTES = GT * 256 * 4;  // the CTA's merged O of a unit
   static constexpr int OFF_OBUF = NSTAGE * STAGE;
   static constexpr int OFF_QSUM = OFF_OBUF + OBUF_BYTES;
@@ -343,25 +349,49 @@ struct Cfg : Tiling<TILE_> {
   // 4-byte elements at most): the last area, part of the launch only with a mask
   static constexpr int MSK_STAGE = GT * TILE_ * 4;
   static constexpr int OFF_MSK = (OFF_FLAG + 16 + 127) / 128 * 128;
-  static constexpr int SMEM = OFF_MSK + 1024;                          // + alignment slack
-  static constexpr int SMEM_MASK = OFF_MSK + NSTAGE * MSK_STAGE + 1024;
+  // one half's area, a multiple of the 1024-byte swizzle atom
+  static constexpr int HALF_PLAIN = (OFF_MSK + 1023) / 1024 * 1024;
+  static constexpr int HALF_MASK = (OFF_MSK + NSTAGE * MSK_STAGE + 1023) / 1024 * 1024;
+  static constexpr int SMEM = HALVES * HALF_PLAIN + 1024;  // + alignment slack
+  static constexpr int SMEM_MASK = HALVES * HALF_MASK + 1024;
   static_assert(OFF_XBUF % 16 == 0 && OFF_OBUF % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
   static_assert(4 % DS == 0, "shape");
+  // the masked variant's producer also copies mask rows: it takes 8 registers
+  // per consumer thread from the consumers
+  static constexpr int CONSUMER_REGS_MASK = CONSUMER_REGS - 8;
+  static constexpr int PRODUCER_REGS_MASK =
+      (LAUNCH_REGS * THREADS - HALVES * CW * 32 * CONSUMER_REGS_MASK) / 128 / 8 * 8 > 248
+          ? 248
+          : (LAUNCH_REGS * THREADS - HALVES * CW * 32 * CONSUMER_REGS_MASK) / 128 / 8 * 8;
+  static_assert(CONSUMER_REGS_MASK >= LAUNCH_REGS && PRODUCER_REGS_MASK >= PRODUCER_REGS, "masked register split");
+  static_assert(HALVES * CW * 32 * CONSUMER_REGS_MASK + 128 * PRODUCER_REGS_MASK <= LAUNCH_REGS * THREADS,
+                "the masked split fits the block's launch allocation");
 };
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, bool MASKED>
-__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>::THREADS, MINB)
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES, bool MASKED>
+__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>::THREADS, MINB)
     attend_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap kmap) {
-  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>;
+  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>;
   constexpr int TILE = C::TILE, SUBS = C::SUBS, STAGE = C::STAGE;
   constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_KS = C::OFF_KS, OFF_KB = C::OFF_KB;
   constexpr int OFF_VS = C::OFF_VS, OFF_VB = C::OFF_VB, V_BYTES = C::V_BYTES, SB_BYTES = C::SB_BYTES;
   constexpr uint32_t STAGE_TX = C::STAGE_TX;
   constexpr int GT = C::GT, GPW = C::GPW, CW = C::CW, NCT = CW * 32;
+  constexpr int HALF_BYTES = MASKED ? C::HALF_MASK : C::HALF_PLAIN;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base (128-byte swizzle atom), derived by pointer
   // arithmetic on the shared array so loads through it stay shared-memory loads
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* const smem0 = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+  // ---- roles: the half a warp serves and its index among the half's consumers
+  // (two halves: half ((w >> 2) ^ w) & 1, index (w >> 1) & 3, so each warp
+  // scheduler w % 4 holds one consumer warp of each half); producer warpgroup
+  // warp HALVES*CW + h streams for half h, its other warps idle
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool consumer = warp < HALVES * CW;
+  const int half = consumer ? (HALVES == 2 ? ((warp >> 2) ^ warp) & 1 : 0) : warp - HALVES * CW;
+  const int cw = consumer ? (HALVES == 2 ? (warp >> 1) & 3 : warp) : 0;
+  uint8_t* const smem = smem0 + (half < HALVES ? half : 0) * HALF_BYTES;
   float* qsum = reinterpret_cast<float*>(smem + C::OFF_QSUM);
   float* mbuf = reinterpret_cast<float*>(smem + C::OFF_MBUF);
   float* lbuf = reinterpret_cast<float*>(smem + C::OFF_LBUF);
@@ -371,16 +401,29 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + NSTAGE;
   uint64_t* encoded = empty + NSTAGE;  // fused append: every consumer warp has stored its new rows
-  int* s_flag = reinterpret_cast<int*>(smem + C::OFF_FLAG);
+  // named barriers of this half: every consumer warp, and (DS > 1) one per token stream
+  const int bar_all = 1 + half * (1 + STREAMS);
 
-  // ---- this CTA's even share of the launch's tiles
-  const int k_cta = blockIdx.x;
-  const long long g0 = p.cstart[k_cta], g1 = p.cstart[k_cta + 1];
   // launched as a programmatic dependent of the previous kernel in the stream:
   // wait for it (and its writes) before touching any memory it may produce
   pdl_wait();
   pdl_launch_dependents();
-  if (g0 >= g1) return;
+  if (threadIdx.x == 0) {
+    for (int h = 0; h < HALVES; ++h) {
+      uint64_t* f = reinterpret_cast<uint64_t*>(smem0 + h * HALF_BYTES + C::OFF_BAR);
+      for (int s = 0; s < NSTAGE; ++s) {
+        mbar_init(&f[s], 1);
+        mbar_init(&f[NSTAGE + s], CW);
+      }
+      mbar_init(&f[2 * NSTAGE], CW);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  // ---- this half's share of the launch's tiles
+  const int k_cta = blockIdx.x * HALVES + (half < HALVES ? half : 0);
+  const long long g0 = p.cstart[k_cta], g1 = p.cstart[k_cta + 1];
   int u0 = 0;  // unit holding tile g0: last u with prefix[u] <= g0
   {
     int lo = 0, hi = p.num_units - 1;
@@ -393,26 +436,15 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   int u1 = u0;  // unit holding tile g1 - 1
   while (g1 > p.prefix[u1 + 1]) ++u1;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CW);
-    }
-    mbar_init(encoded, CW);
-    mbar_fence_init();
-  }
-  __syncthreads();
-
   // ------------------------------------------------------------ producer
   // One lane streams the CTA's tiles through the ring, refilling a stage as
   // soon as every consumer warp has released it: packed K codes by a 2-D
   // tensor copy (128-byte swizzle), packed V codes and the four scale/bias rows
   // by 1-D bulk copies, all counted on the stage's full barrier; L2
   // evict-first (the cache is read once).
-  if (warp >= CW) {
-    setmaxnreg_dec<C::PRODUCER_REGS>();
-    if (warp == CW && lane == 0) {
+  if (!consumer) {
+    setmaxnreg_dec<MASKED ? C::PRODUCER_REGS_MASK : C::PRODUCER_REGS>();
+    if (half < HALVES && lane == 0 && g0 < g1) {
       const uint64_t pol = policy_evict_first();
       int u = u0;
       long long k = 0;
@@ -464,10 +496,12 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     }
     return;
   }
-  setmaxnreg_inc<C::CONSUMER_REGS>();
+  setmaxnreg_inc<MASKED ? C::CONSUMER_REGS_MASK : C::CONSUMER_REGS>();
+  if (g0 >= g1) return;  // a half without tiles
 
   // ------------------------------------------------------------ consumers
-  const int cw = warp, stream = cw / DS, dg = cw % DS;
+  const int stream = cw / DS, dg = cw % DS;
+  const int ctid = cw * 32 + lane;  // thread index among the half's consumers
   const int g = lane >> 2, t = lane & 3;
   const int rS0 = (MU_PACK >> (4 * g)) & 15;      // token slot g
   const int rV0 = (MU_PACK >> (8 * t)) & 15;      // slot 2t
@@ -504,7 +538,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     // takes the unmasked path); an explicit mask reads every sub-tile
     qmin = MASKED ? -1 : p.causal ? T - p.nq + (qt * GT) / p.rep : T - 1;
     qlo = (qt * GT) / p.rep;
-    named_bar(1, NCT);  // every consumer is done with the previous unit's fragments and sums
+    named_bar(bar_all, NCT);  // every consumer is done with the previous unit's fragments and sums
     // q' = bf16(q @ M_b), q'' = bf16(q' * scale), written straight into the fp16
     // MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].  Item
     // (n-tile j, group G) goes to one warp; its thread (g, t) rotates row 8j+g,
@@ -582,7 +616,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         qsum[((8 * j + g) * 4 + G) * 2 + 1] = fmaf(KOFF_EVEN, qe, KOFF_ODD * qo);
       }
     }
-    named_bar(1, NCT);  // fragments and sums visible to every warp
+    named_bar(bar_all, NCT);  // fragments and sums visible to every warp
     // this lane's k-slots: 2t, 2t+1 (and 2t+8, 2t+9) = groups 2(t&1), 2(t&1)+1
     // of b (t < 2, against S_G) or of s (t >= 2, against -F_G); groups another warp of the
     // stream owns contribute there instead
@@ -713,7 +747,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
         for (int j = 0; j < NT; ++j)
           xb[((n * DS + dg) * NT + j) * 32 + lane] = make_float4(sc[n][j][0], sc[n][j][1], sc[n][j][2], sc[n][j][3]);
-      named_bar(2 + stream, DS * 32);
+      named_bar(bar_all + 1 + stream, DS * 32);
 #pragma unroll
       for (int n = 0; n < N; ++n)
 #pragma unroll
@@ -916,7 +950,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) mbuf[stream * GT + 8 * j + 2 * t + e] = msc[j][e];
-    named_bar(1, NCT);
+    named_bar(bar_all, NCT);
     float a_row[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -956,12 +990,12 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
             }
           }
       }
-      named_bar(1, NCT);
+      named_bar(bar_all, NCT);
     }
     // obuf holds the CTA's O for the unit; per row M = max and L = sum over the streams
     const int ub = p.unit_base + u;
     if (p.prefix[u] >= g0 && p.prefix[u + 1] <= g1) {  // the whole unit is here: finalise
-      for (int idx = threadIdx.x; idx < GT * 32; idx += NCT) {
+      for (int idx = ctid; idx < GT * 32; idx += NCT) {
         const int r = idx >> 5, l8 = idx & 31;
         if ((qt * GT + r) / p.rep >= p.nq) continue;
         uint32_t mw[16];
@@ -977,9 +1011,9 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     } else {  // partial for the combine: slot u + k_cta
       const long long slot = static_cast<long long>(u) + k_cta;
       float4* po = reinterpret_cast<float4*>(p.part_o + slot * GT * kHeadDim);
-      for (int idx = threadIdx.x; idx < GT * kHeadDim / 4; idx += NCT)
+      for (int idx = ctid; idx < GT * kHeadDim / 4; idx += NCT)
         po[idx] = reinterpret_cast<const float4*>(obuf)[idx];
-      for (int r = threadIdx.x; r < GT; r += NCT) {
+      for (int r = ctid; r < GT; r += NCT) {
         float M = mbuf[r], L = lbuf[r];
 #pragma unroll
         for (int s = 1; s < STREAMS; ++s) {
@@ -988,8 +1022,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         }
         reinterpret_cast<float2*>(p.part_ml)[slot * GT + r] = make_float2(M, L);
       }
-      named_bar(1, NCT);  // every thread's partial stores precede the arrival
-      if (threadIdx.x == 0) {
+      named_bar(bar_all, NCT);  // every thread's partial stores precede the arrival
+      if (ctid == 0) {
         __threadfence();
         atomicAdd(p.counters + u, 1u);
       }
@@ -1190,20 +1224,20 @@ constexpr size_t kStatusBytes = 256;
 constexpr size_t kHeadBytes = kStatusBytes + UNIT_CAP * sizeof(unsigned);  // status word + unit counters
 static_assert(kHeadBytes == IQ_WORKSPACE_HEAD_BYTES, "workspace head size in iqkv.h");
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES>
 int blocks_per_sm() {
   static int cache[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (cache[dev] == 0) {
-    using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>;
+    using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>;
     int n = 0;
-    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, false>,
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, false>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, true>,
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, true>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_MASK);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, false>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, false>,
                                                       C::THREADS, C::SMEM) !=
             cudaSuccess ||
         n <= 0)
@@ -1233,7 +1267,10 @@ int blocks_per_sm() {
 #define IQ_DECODE_TILE 128
 #endif
 #ifndef IQ_DECODE_MINB
-#define IQ_DECODE_MINB 2
+#define IQ_DECODE_MINB 1
+#endif
+#ifndef IQ_DECODE_HALVES
+#define IQ_DECODE_HALVES 2
 #endif
 #ifndef IQ_DECODE_PAIR
 #define IQ_DECODE_PAIR 2
@@ -1241,7 +1278,8 @@ int blocks_per_sm() {
 #ifndef IQ_DECODE_BOUNDARY
 #define IQ_DECODE_BOUNDARY 3
 #endif
-#define IQ_DECODE_CFG 1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB, IQ_DECODE_TILE, IQ_DECODE_PAIR
+#define IQ_DECODE_CFG \
+  1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB, IQ_DECODE_TILE, IQ_DECODE_PAIR, IQ_DECODE_HALVES
 #ifndef IQ_MULTI_NT
 #define IQ_MULTI_NT 2
 #endif
@@ -1266,7 +1304,8 @@ int blocks_per_sm() {
 #ifndef IQ_MULTI_BOUNDARY
 #define IQ_MULTI_BOUNDARY 3
 #endif
-#define IQ_MULTI_CFG IQ_MULTI_NT, IQ_MULTI_DS, IQ_MULTI_STREAMS, IQ_MULTI_STAGES, IQ_MULTI_MINB, IQ_MULTI_TILE, IQ_MULTI_PAIR
+#define IQ_MULTI_CFG \
+  IQ_MULTI_NT, IQ_MULTI_DS, IQ_MULTI_STREAMS, IQ_MULTI_STAGES, IQ_MULTI_MINB, IQ_MULTI_TILE, IQ_MULTI_PAIR, 1
 
 // Tiles of every unit, in unit order: unit u = (b, kv head, query tile).
 void unit_tiles(const iq_cache* c, int rep, int nq, int causal, int gt, int nqt, int tile, int* tiles) {
@@ -1291,8 +1330,10 @@ int make_plan(const iq_cache* c, int q_heads, int nq, int causal, Plan* pl, cons
   pl->units = static_cast<size_t>(c->batch) * c->kv_heads * pl->nqt;
   pl->launches = static_cast<int>((pl->units + UNIT_CAP - 1) / UNIT_CAP);
   if (pl->launches > kMaxLaunches) return fail(IQ_ERR_UNSUPPORTED, "too many query tiles for one call");
+  // virtual CTAs (tile ranges): CTAs per SM x the halves of a CTA
+  const int halves = pl->nt == 1 ? IQ_DECODE_HALVES : 1;
   const int bps = pl->nt == 1 ? blocks_per_sm<IQ_DECODE_CFG>() : blocks_per_sm<IQ_MULTI_CFG>();
-  const long long slots_hw = static_cast<long long>(num_sms()) * bps;
+  const long long slots_hw = static_cast<long long>(num_sms()) * bps * halves;
   int max_tiles = 0;
   for (int b = 0; b < c->batch; ++b) max_tiles = std::max(max_tiles, (static_cast<int>(c->lens[b]) + pl->tile - 1) / pl->tile);
   pl->slots = 0;
@@ -1305,8 +1346,9 @@ int make_plan(const iq_cache* c, int q_heads, int nq, int causal, Plan* pl, cons
     } else {
       W = static_cast<long long>(nu) * max_tiles;
     }
-    const long long G = std::min(std::min(slots_hw, static_cast<long long>(GRID_CAP)),
-                                 std::max(1LL, W / MIN_TILES_PER_CTA));
+    long long G = std::min(std::min(slots_hw, static_cast<long long>(GRID_CAP)),
+                           std::max(1LL, W / MIN_TILES_PER_CTA));
+    G = std::max<long long>(halves, G / halves * halves);  // whole CTAs
     pl->grid[l] = static_cast<int>(G);
     pl->slots = std::max(pl->slots, nu + static_cast<size_t>(G));
   }
@@ -1374,10 +1416,10 @@ int validate(const iq_cache* c, const uint16_t* q, int q_heads, int nq, int caus
   return IQ_OK;
 }
 
-template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR>
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES>
 int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStream_t s) {
-  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>;
-  blocks_per_sm<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR>();  // sets the shared-memory attribute once
+  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>;
+  blocks_per_sm<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>();  // sets the shared-memory attribute once
   // The warpgroups move registers between them (setmaxnreg); that split adds
   // up to the block's launch allocation only at the register count it was
   // designed for, so any other build of the kernel is refused, never launched.
@@ -1385,8 +1427,8 @@ int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStrea
   static int launch_regs[2] = {-1, -1};
   if (launch_regs[masked] < 0) {
     cudaFuncAttributes fa;
-    IQ_CUDA(cudaFuncGetAttributes(&fa, masked ? attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, true>
-                                              : attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, false>));
+    IQ_CUDA(cudaFuncGetAttributes(&fa, masked ? attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, true>
+                                              : attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, false>));
     launch_regs[masked] = fa.numRegs;
   }
   if (launch_regs[masked] != C::LAUNCH_REGS)
@@ -1398,16 +1440,16 @@ int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStrea
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid / HALVES));  // `grid` counts tile ranges: HALVES per CTA
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = prm.mask_kind >= 2 ? C::SMEM_MASK : C::SMEM;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (masked)
-    IQ_CUDA(cudaLaunchKernelEx(&cfg, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, true>, prm, map));
+    IQ_CUDA(cudaLaunchKernelEx(&cfg, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, true>, prm, map));
   else
-    IQ_CUDA(cudaLaunchKernelEx(&cfg, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, false>, prm, map));
+    IQ_CUDA(cudaLaunchKernelEx(&cfg, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, false>, prm, map));
   // the split combine, after the attention grid
   cfg.gridDim = dim3(static_cast<unsigned>(prm.num_units));
   cfg.blockDim = dim3(256);
