@@ -1121,6 +1121,10 @@ __device__ __forceinline__ void combine_unit(const Params& p, int u) {
   seg_range(p, u, k_first, k_last);
   if (k_first == k_last) return;  // finished by the CTA that held the whole unit
   const int nseg = k_last - k_first + 1;
+  // every item of this thread has the same 8-dim chunk (blockDim is a multiple
+  // of 32): its two rotation blocks load while the unit is awaited
+  uint32_t mw[16];
+  load_rot(p, threadIdx.x & 31, mw);
   // Wait (bounded, in time) until every CTA holding tiles of the unit has
   // stored its partial, so units are merged while the attention grid still
   // runs; every attention CTA started before this grid was launched.
@@ -1132,7 +1136,7 @@ __device__ __forceinline__ void combine_unit(const Params& p, int u) {
     for (;;) {
       if (ld_acquire_gpu(p.counters + u) >= expect) { ready = 1; break; }
       if (global_ns() - t0 > kCombineWaitNs) break;
-      __nanosleep(256);
+      __nanosleep(32);
     }
     s_ready = ready;
   }
@@ -1146,8 +1150,6 @@ __device__ __forceinline__ void combine_unit(const Params& p, int u) {
   for (int idx = threadIdx.x; idx < GT * 32; idx += blockDim.x) {
     const int r = idx >> 5, l8 = idx & 31;
     if (((ub % p.nqt) * GT + r) / p.rep >= p.nq) continue;
-    uint32_t mw[16];
-    load_rot(p, l8, mw);
     float M = NEG_INF, L = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int s0 = 0; s0 < nseg; s0 += 8) {
