@@ -42,8 +42,8 @@ K_ROW, V_ROW = 144, 112  # algorithmic bytes per token-head: codes + bf16 scales
 # combine_kernel; profiles/attend_kernel_batched_decode_32x32k.md).  Reported
 # only while the attention source is the one that was measured.
 TRAFFIC = {"source": "rotated_bit_quantized_gb300/csrc/iq_attend.cu",
-           "sha256": "b4d7924876908c4f2fc16a58cfcb0a8063d72cdc56c674bac6e76c3bc6372f54",
-           "bytes": ((539.39 + 3.16 + 2.93) + (539.44 + 0.46 + 2.93)) / 2 * 1e6}
+           "sha256": "698ae370a3d8e02116cee296e04ab8a4c4ef2cb08d9678eb3ce41157d8c36b47",
+           "bytes": ((539.383552 + 3.211264 + 2.929664) + (539.406592 + 0.400128 + 2.929408)) / 2 * 1e6}
 
 
 def measured_traffic():
