@@ -95,15 +95,28 @@ struct AppendParams {
   uint16_t* v_biases;
   const uint16_t* rot;
   int batch, heads, n, cap;
+  // row r < 2^31 -> (r / n, r % n): r / n = umulhi(r, n_mul) >> n_shift
+  uint32_t n_mul;
+  int n_shift;
   int lens[IQ_MAX_BATCH];
 };
 
 // One warp per token row (sequence b, kv head h, token i): its K and V rows
-// are encoded together, and the warp's next row's K and V are loaded meanwhile.
+// are encoded together.  The rows of every (b, h) are laid end to end (the
+// input is [B][Hkv][n][256], so flat row r is at r * 256) and a persistent
+// grid strides over them (no second wave of blocks for a small append); each
+// warp keeps the bf16 K and V of its next IQ_APPEND_DEPTH rows in flight while
+// it encodes the current one.  The encoding is bound by instruction issue, so
+// occupancy beats depth: one row ahead at three blocks per SM measured best
+// (two or four rows ahead at two or one block per SM were slower).
 #ifndef IQ_APPEND_MINB
 #define IQ_APPEND_MINB 3
 #endif
+#ifndef IQ_APPEND_DEPTH
+#define IQ_APPEND_DEPTH 1
+#endif
 __global__ void __launch_bounds__(256, IQ_APPEND_MINB) append_kernel(const __grid_constant__ AppendParams p) {
+  constexpr int D = IQ_APPEND_DEPTH;
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: wait for it (and its writes) before touching memory.  The next
   // kernel (attention) may launch now; it waits for this grid's completion
@@ -111,32 +124,46 @@ __global__ void __launch_bounds__(256, IQ_APPEND_MINB) append_kernel(const __gri
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int gwarp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);  // within this (b, h)
+  // every row index fits in 31 bits (the host refuses caches of 2^31 rows or more)
+  const int gwarp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+  const int total = p.batch * p.heads * p.n;
 
   float m[2][4][4];
   load_row_rotation(p.rot, lane, m);
 
-  // blockIdx.y = sequence * heads + head; the warps of the x-blocks stride over tokens
-  const int bh = blockIdx.y;
-  const long long src0 = static_cast<long long>(bh) * p.n;
-  const long long dst0 = static_cast<long long>(bh) * p.cap + p.lens[bh / p.heads];
-  auto load = [&](const uint16_t* base, int i) {
-    return __ldg(reinterpret_cast<const uint4*>(base + (src0 + i) * kHeadDim + lane * 8));
+  // streamed once: keep the inputs out of L1
+  auto load = [&](const uint16_t* base, int r) {
+    return __ldcs(reinterpret_cast<const uint4*>(base + static_cast<long long>(r) * kHeadDim + lane * 8));
   };
-  uint4 nk = make_uint4(0, 0, 0, 0), nv = nk;
-  if (gwarp < p.n) {
-    nk = load(p.keys, gwarp);
-    nv = load(p.values, gwarp);
-  }
-  for (int i = gwarp; i < p.n; i += nwarps) {
-    const uint4 rk = nk, rv = nv;
-    if (i + nwarps < p.n) {
-      nk = load(p.keys, i + nwarps);
-      nv = load(p.values, i + nwarps);
+  uint4 kb[D], vb[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    const int r = gwarp + d * nwarps;
+    kb[d] = vb[d] = make_uint4(0, 0, 0, 0);
+    if (r < total) {
+      kb[d] = load(p.keys, r);
+      vb[d] = load(p.values, r);
     }
-    encode_row<4>(rk, m, lane, dst0 + i, p.k_codes, p.k_scales, p.k_biases);
-    encode_row<3>(rv, m, lane, dst0 + i, p.v_codes, p.v_scales, p.v_biases);
+  }
+  for (int r0 = gwarp; r0 < total; r0 += D * nwarps) {
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const int r = r0 + d * nwarps;
+      if (r >= total) break;
+      const uint4 rk = kb[d], rv = vb[d];
+      const int nx = r + D * nwarps;
+      if (nx < total) {
+        kb[d] = load(p.keys, nx);
+        vb[d] = load(p.values, nx);
+      }
+      const uint32_t r32 = static_cast<uint32_t>(r);
+      const int bh = static_cast<int>(p.n_mul ? __umulhi(r32, p.n_mul) >> p.n_shift : r32 >> p.n_shift);
+      const int i = static_cast<int>(r32 - static_cast<uint32_t>(bh) * static_cast<uint32_t>(p.n));
+      const long long dst = static_cast<long long>(bh) * p.cap + p.lens[bh / p.heads] + i;
+      encode_row<4>(rk, m, lane, dst, p.k_codes, p.k_scales, p.k_biases);
+      encode_row<3>(rv, m, lane, dst, p.v_codes, p.v_scales, p.v_biases);
+    }
   }
 }
 
@@ -247,6 +274,22 @@ size_t iq_cache_nbytes(const iq_cache* c) {
   return t;
 }
 
+namespace {
+// resident 256-thread append blocks per SM (cached per device)
+int append_blocks_per_sm() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, iq::append_kernel, 256, 0) != cudaSuccess || n <= 0) n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+}  // namespace
+
 int iq_cache_append(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n,
                     const uint16_t* rot_bf16, iq_stream_t stream) {
   int st = iq_cache_check(c);
@@ -277,17 +320,29 @@ int iq_cache_append(iq_cache* c, const uint16_t* keys, const uint16_t* values, i
   p.heads = c->kv_heads;
   p.n = n;
   p.cap = c->capacity;
+  // division by n for row indices below 2^31: n = 2^s is a shift; otherwise
+  // with s = floor(log2 n) and mul = ceil(2^(32+s) / n) < 2^32, umulhi(r, mul)
+  // >> s is floor(r / n) exactly (its error is below r / 2^(32+s) < 1 / n)
+  {
+    int sh = 0;
+    while ((2LL << sh) <= n) ++sh;  // floor(log2 n)
+    p.n_shift = sh;
+    p.n_mul = (n & (n - 1)) == 0 ? 0u
+                                 : static_cast<uint32_t>(((static_cast<unsigned long long>(1) << (32 + sh)) + n - 1) /
+                                                         static_cast<unsigned long long>(n));
+  }
   for (int b = 0; b < c->batch; ++b) p.lens[b] = c->lens[b];
-  // grid.y = sequence x head; grid.x: enough 8-warp blocks for about eight per SM in all
-  const int bh = c->batch * c->kv_heads;
-  long long gx = (static_cast<long long>(n) + 7) / 8;
-  const long long cap_x = std::max(1LL, static_cast<long long>(num_sms()) * 8 / bh);
+  // a persistent grid: as many 8-warp blocks as fit at once (one row per warp
+  // at most), striding over every (sequence, head, token) row
+  const long long rows = static_cast<long long>(c->batch) * c->kv_heads * n;
+  long long gx = (rows + 7) / 8;
+  const long long cap_x = static_cast<long long>(num_sms()) * append_blocks_per_sm();
   if (gx > cap_x) gx = cap_x;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(bh));
+  cfg.gridDim = dim3(static_cast<unsigned>(gx));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
