@@ -42,6 +42,7 @@
 #include <cstring>
 #include <mutex>
 #include <type_traits>
+#include <unordered_map>
 #include <vector>
 
 #include "iq_common.cuh"
@@ -76,6 +77,8 @@ struct Tiling {
 constexpr int UNIT_CAP = 1024;  // units per launch (their tile prefix travels by value)
 constexpr int GRID_CAP = 1024;  // CTAs per launch (their tile ranges travel by value)
 constexpr int MIN_TILES_PER_CTA = 8;
+// Rows a fused append writes at most (its new rows sit in one decode tile).
+constexpr int kFreshRows = 128;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float NEG_INF = -__builtin_huge_valf();
 // Score of a key a bool mask hides: far below any real score (|q.k| * scale
@@ -116,6 +119,7 @@ struct Params {
   const uint16_t* k_new;
   const uint16_t* v_new;
   int n_new;
+  int encode_wait;  // 1: the previous attention on this cache may still read rows the new rows overwrite
   // explicit mask (mask_kind 2: float32 added to the scores; 3: uint8, 0 =
   // masked): [B][nq][mask_stride] over the keys, shared by every head
   int mask_kind;
@@ -404,10 +408,18 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   // named barriers of this half: every consumer warp, and (DS > 1) one per token stream
   const int bar_all = 1 + half * (1 + STREAMS);
 
-  // launched as a programmatic dependent of the previous kernel in the stream:
-  // wait for it (and its writes) before touching any memory it may produce
-  pdl_wait();
-  pdl_launch_dependents();
+  // Launched as a programmatic dependent of the previous kernel in the stream,
+  // this grid may start while that kernel (the previous call's combine) and
+  // the attention before it still run.  Of the memory it touches, only these
+  // may still be written by them: the output, the partials and counters (every
+  // write of this grid to them comes after griddepcontrol.wait, in end_unit),
+  // and the cache rows of the previous call's fused append, all among the last
+  // kFreshRows + n_new rows of a sequence (the producer waits before a tile
+  // that reaches them).  The append kernel releases its dependents only when it
+  // completes, and the combine writes no cache rows, so every other cache tile,
+  // the queries and the rotation can be streamed before the wait.  The fused
+  // append's own writes wait too when the host saw a trim since the previous
+  // attention on this cache (that attention may still read those rows).
   if (threadIdx.x == 0) {
     for (int h = 0; h < HALVES; ++h) {
       uint64_t* f = reinterpret_cast<uint64_t*>(smem0 + h * HALF_BYTES + C::OFF_BAR);
@@ -449,6 +461,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       int u = u0;
       long long k = 0;
       bool enc_seen = p.n_new == 0;
+      bool waited = false;  // griddepcontrol.wait done
       for (long long gt = g0; gt < g1; ++gt, ++k) {
         while (gt >= p.prefix[u + 1]) ++u;
         if (!enc_seen && gt == p.prefix[u + 1] - 1) {  // a last tile: its new rows must be stored first
@@ -467,6 +480,10 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         }
         uint8_t* sbp = smem + st * STAGE;
         const long long row0 = (static_cast<long long>(bb) * p.kv_heads + hh) * p.cap + (gt - p.prefix[u]) * TILE;
+        if (!waited && (gt - p.prefix[u] + 1) * TILE > p.lens[bb] - p.n_new - kFreshRows) {
+          pdl_wait();  // the tile may hold rows the previous call's fused append wrote
+          waited = true;
+        }
         if constexpr (MASKED) {  // the unit's mask rows for this tile's keys (one copy per query)
           const int qt = ug % p.nqt, elem = p.mask_kind == 2 ? 4 : 1;
           const int i_lo = qt * C::GT / p.rep, i_hi = min((qt * C::GT + C::GT - 1) / p.rep, p.nq - 1);
@@ -922,6 +939,10 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   // CTA alone is finalised at once, a shared one leaves a partial (O, running
   // max in log2 units, running sum) for the combine.
   auto end_unit = [&](int u) {
+    // the previous grids' writes of the output, partials and counters are done
+    // (the first call waits, later ones return at once); the next grid may launch
+    pdl_wait();
+    pdl_launch_dependents();
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -1039,6 +1060,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     const int ulast = p.prefix[u1 + 1] <= g1 ? u1 : u1 - 1;
     const int rows = (ulast - u0 + 1) * p.n_new;
     if (rows > 0) {
+      if (p.encode_wait) pdl_wait();
       float m[2][4][4];
       load_row_rotation(p.rot, lane, m);
       for (int item = cw; item < rows; item += CW) {
@@ -1487,13 +1509,47 @@ int iq_attend_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* b
 namespace iq {
 namespace attn {
 
+// Rows [0, hi[b]) that the latest attention launched on a cache (keyed by its
+// key-code buffer) reads.  An attention grid may still run while the next call's
+// grid starts (see attend_kernel); a fused append may write its new rows at
+// once only when none of them lies below that mark, i.e. when no trim since the
+// latest attention moved the append point back into rows it reads.  No record
+// (first call, or the table was reset) counts as a trim.
+class ReadMarks {
+ public:
+  void record(const iq_cache* c) {
+    std::lock_guard<std::mutex> lk(mu_);
+    if (marks_.size() >= 256) marks_.clear();  // bounded; a lost record only makes an append wait
+    auto& v = marks_[c->k_codes];
+    v.assign(c->lens, c->lens + c->batch);
+  }
+  // true when rows [lens[b], ...) of every sequence are at or above the mark
+  bool append_clear(const iq_cache* c) {
+    std::lock_guard<std::mutex> lk(mu_);
+    auto it = marks_.find(c->k_codes);
+    if (it == marks_.end() || static_cast<int>(it->second.size()) != c->batch) return false;
+    for (int b = 0; b < c->batch; ++b)
+      if (c->lens[b] < it->second[b]) return false;
+    return true;
+  }
+
+ private:
+  std::mutex mu_;
+  std::unordered_map<const void*, std::vector<int>> marks_;
+};
+ReadMarks& read_marks() {
+  static ReadMarks m;
+  return m;
+}
+
 // Attention over the cache; with n_new > 0 the last n_new rows of every
 // sequence (already counted in c->lens) are first encoded from k_new / v_new
-// inside the same kernel (see the fused append in attend_kernel).
+// inside the same kernel (see the fused append in attend_kernel); encode_wait
+// makes those writes wait for the previous grids.
 int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
                 const uint16_t* rot_bf16, void* out, int out_f32, void* workspace, size_t workspace_bytes,
                 iq_stream_t stream, const uint16_t* k_new, const uint16_t* v_new, int n_new, int mask_kind = 0,
-                const void* mask = nullptr, long long mask_stride = 0) {
+                const void* mask = nullptr, long long mask_stride = 0, int encode_wait = 1) {
   int st = validate(c, q, q_heads, n_queries, causal, rot_bf16, out);
   if (st != IQ_OK) return st;
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
@@ -1546,6 +1602,7 @@ int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries
   prm.k_new = k_new;
   prm.v_new = v_new;
   prm.n_new = n_new;
+  prm.encode_wait = encode_wait ? 1 : 0;
   prm.mask_kind = mask_kind;
   prm.mask = mask;
   prm.mask_stride = mask_stride;
@@ -1574,6 +1631,7 @@ int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries
                     : launch_attend<IQ_MULTI_CFG>(prm, map, prm.grid, s);
     if (st != IQ_OK) return st;
   }
+  read_marks().record(c);
   return IQ_OK;
 }
 
@@ -1617,9 +1675,11 @@ int iq_cache_append_attend(iq_cache* c, const uint16_t* keys, const uint16_t* va
     return iq_attend(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
                      stream);
   }
+  static_assert(Cfg<IQ_DECODE_CFG>::TILE <= kFreshRows, "a fused append writes at most kFreshRows rows");
+  const int encode_wait = read_marks().append_clear(c) ? 0 : 1;
   for (int b = 0; b < c->batch; ++b) c->lens[b] += n;
   st = attend_impl(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
-                   stream, keys, values, n);
+                   stream, keys, values, n, 0, nullptr, 0, encode_wait);
   if (st != IQ_OK)
     for (int b = 0; b < c->batch; ++b) c->lens[b] -= n;  // nothing was launched
   return st;

@@ -118,11 +118,11 @@ struct AppendParams {
 __global__ void __launch_bounds__(256, IQ_APPEND_MINB) append_kernel(const __grid_constant__ AppendParams p) {
   constexpr int D = IQ_APPEND_DEPTH;
   // Launched as a programmatic dependent of the previous kernel in the
-  // stream: wait for it (and its writes) before touching memory.  The next
-  // kernel (attention) may launch now; it waits for this grid's completion
-  // before it reads the cache.
+  // stream: wait for it (and its writes) before touching memory.  It never
+  // releases its dependents early: an attention launched after it streams
+  // cache tiles before its own wait, so it must start after these rows are
+  // written.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   // every row index fits in 31 bits (the host refuses caches of 2^31 rows or more)
   const int gwarp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
