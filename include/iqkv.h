@@ -236,6 +236,12 @@ int iq_attend_mask(const iq_cache* cache, const uint16_t* q, int q_heads, int n_
  * Arguments, layouts and workspace as iq_cache_append and iq_attend; lens[b]
  * grows by n on success (the causal mask and the scanned length use the
  * grown lengths).  Errors: as both (nothing is launched on an error).
+ * Overlap: an attention grid starts streaming cache tiles while the previous
+ * call's grids finish (only its stores wait for them).  The library remembers,
+ * per key-code buffer, the rows the latest attention on it reads; when a trim
+ * since then puts the new rows below that mark, the fused encode also waits.
+ * Writing the cache by other means (outside this library's calls) while a call
+ * on the same stream is in flight is not supported.
  */
 int iq_cache_append_attend(iq_cache* cache, const uint16_t* keys, const uint16_t* values, int n,
                            const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
