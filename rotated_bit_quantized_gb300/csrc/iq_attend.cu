@@ -1497,6 +1497,7 @@ int iq_attend_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* b
   if (!bytes) return fail(IQ_ERR_INVALID_ARG, "null bytes");
   if (n_queries < 1 || q_heads < 1 || q_heads % c->kv_heads)
     return fail(IQ_ERR_INVALID_ARG, "bad head or query count");
+  if (!tuned_format(c)) return attend_any_workspace(c, q_heads, n_queries, bytes);
   Plan pl;
   st = make_plan(c, q_heads, n_queries, 0, &pl, nullptr);
   if (st != IQ_OK) return st;
@@ -1552,6 +1553,11 @@ int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries
                 const void* mask = nullptr, long long mask_stride = 0, int encode_wait = 1) {
   int st = validate(c, q, q_heads, n_queries, causal, rot_bf16, out);
   if (st != IQ_OK) return st;
+  if (!tuned_format(c)) {
+    if (n_new > 0) return fail(IQ_ERR_UNSUPPORTED, "fused append for this cache format");
+    return attend_any(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
+                      stream, mask_kind, mask, mask_stride);
+  }
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
     return fail(IQ_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
   Plan bound;  // what iq_attend_workspace promised: an upper bound of this call's needs
@@ -1665,7 +1671,7 @@ int iq_cache_append_attend(iq_cache* c, const uint16_t* keys, const uint16_t* va
   // rows of each sequence sit in one key tile; otherwise the append, then the
   // attention.
   const int tile = Cfg<IQ_DECODE_CFG>::TILE;
-  bool fused = q_heads >= c->kv_heads && q_heads % c->kv_heads == 0 &&
+  bool fused = tuned_format(c) && q_heads >= c->kv_heads && q_heads % c->kv_heads == 0 &&
                static_cast<long long>(q_heads / c->kv_heads) * n_queries <= 8;
   for (int b = 0; b < c->batch && fused; ++b)
     fused = c->lens[b] / tile == (c->lens[b] + n - 1) / tile;

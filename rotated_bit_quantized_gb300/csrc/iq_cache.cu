@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(256, IQ_APPEND_MINB) append_kernel(const __gri
 struct GatherParams {
   const void* src[6];
   void* dst[6];
-  int row_units[6];  // 8-byte units per row of each buffer
+  int row_units[6];  // 4-byte units per row of each buffer
   int dst_batch, heads, src_cap, dst_cap;
   int src_of[IQ_MAX_BATCH];
   int len[IQ_MAX_BATCH];
@@ -182,10 +182,10 @@ struct GatherParams {
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherParams p) {
   const int seq = blockIdx.y / p.heads, h = blockIdx.y % p.heads, buf = blockIdx.z;
   const long long units = static_cast<long long>(p.len[seq]) * p.row_units[buf];
-  const uint2* s = static_cast<const uint2*>(p.src[buf]) +
-                   (static_cast<long long>(p.src_of[seq]) * p.heads + h) * p.src_cap * p.row_units[buf];
-  uint2* d = static_cast<uint2*>(p.dst[buf]) +
-             (static_cast<long long>(seq) * p.heads + h) * p.dst_cap * p.row_units[buf];
+  const uint32_t* s = static_cast<const uint32_t*>(p.src[buf]) +
+                      (static_cast<long long>(p.src_of[seq]) * p.heads + h) * p.src_cap * p.row_units[buf];
+  uint32_t* d = static_cast<uint32_t*>(p.dst[buf]) +
+                (static_cast<long long>(seq) * p.heads + h) * p.dst_cap * p.row_units[buf];
   for (long long u = blockIdx.x * 256LL + threadIdx.x; u < units; u += 256LL * gridDim.x) d[u] = s[u];
 }
 
@@ -234,8 +234,9 @@ int iq_cache_bytes(int batch, int kv_heads, int head_dim, int group_size, int k_
   if (!out_bytes) return fail(IQ_ERR_INVALID_ARG, "null out_bytes");
   if (batch <= 0 || kv_heads <= 0 || capacity <= 0 || capacity % IQ_STEP)
     return fail(IQ_ERR_INVALID_ARG, "batch, kv_heads > 0 and capacity a positive multiple of 256 required");
-  if (head_dim != kHeadDim || group_size != kGroup || k_bits != 4 || v_bits != 3)
-    return fail(IQ_ERR_UNSUPPORTED, "only head_dim 256, group 64, k_bits 4, v_bits 3 are built");
+  if (!format_supported(head_dim, group_size, k_bits, v_bits))
+    return fail(IQ_ERR_UNSUPPORTED,
+                "built formats: head_dim 256, group 32/64/128, k_bits and v_bits 2/3/4/5/6/8");
   if (batch > IQ_MAX_BATCH) return fail(IQ_ERR_UNSUPPORTED, "batch above IQ_MAX_BATCH");
   const size_t rows = static_cast<size_t>(batch) * kv_heads * capacity;
   const size_t ng = head_dim / group_size;
@@ -305,6 +306,12 @@ int iq_cache_append(iq_cache* c, const uint16_t* keys, const uint16_t* values, i
       return fail(IQ_ERR_CAPACITY, "append past capacity (grow the cache first)");
   if (static_cast<long long>(c->batch) * c->kv_heads * c->capacity >= (1LL << 31))
     return fail(IQ_ERR_UNSUPPORTED, "cache rows exceed 2^31");
+  if (!tuned_format(c)) {
+    st = append_any(c, keys, values, n, rot_bf16, stream);
+    if (st != IQ_OK) return st;
+    for (int b = 0; b < c->batch; ++b) c->lens[b] += n;
+    return IQ_OK;
+  }
   AppendParams p;
   std::memset(&p, 0, sizeof(p));
   p.keys = keys;
@@ -388,7 +395,8 @@ int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of, i
   }
   const void* sp[6] = {src->k_codes, src->k_scales, src->k_biases, src->v_codes, src->v_scales, src->v_biases};
   void* dp[6] = {dst->k_codes, dst->k_scales, dst->k_biases, dst->v_codes, dst->v_scales, dst->v_biases};
-  const int units[6] = {kKWords / 2, 1, 1, kVWords / 2, 1, 1};
+  const int ngw = dst->head_dim / dst->group_size / 2;  // bf16 scales (or biases) per row, in 4-byte words
+  const int units[6] = {dst->head_dim * dst->k_bits / 32, ngw, ngw, dst->head_dim * dst->v_bits / 32, ngw, ngw};
   for (int i = 0; i < 6; ++i) {
     if (sp[i] == dp[i]) return fail(IQ_ERR_INVALID_ARG, "src and dst share a buffer");
     p.src[i] = sp[i];
@@ -400,7 +408,7 @@ int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of, i
   p.src_cap = src->capacity;
   p.dst_cap = dst->capacity;
   if (max_len > 0) {
-    int gx = (max_len * 16 + 255) / 256;
+    int gx = (max_len * 32 + 255) / 256;
     if (gx > 64) gx = 64;
     dim3 grid(gx, dst->batch * dst->kv_heads, 6);
     gather_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);

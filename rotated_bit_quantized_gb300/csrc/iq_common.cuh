@@ -26,6 +26,17 @@ void clear_error();
 
 int num_sms();  // multiprocessor count of the current device (cached per device)
 
+// Cache formats (iq_generic.cu): the tuned one (k 4 bits, v 3 bits, 64-dim
+// groups) runs the tuned kernels, every other supported one the generic path.
+bool tuned_format(const iq_cache* c);
+bool format_supported(int head_dim, int group_size, int k_bits, int v_bits);
+int append_any(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n, const uint16_t* rot,
+               iq_stream_t stream);
+int attend_any_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* bytes);
+int attend_any(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
+               const uint16_t* rot, void* out, int out_f32, void* workspace, size_t workspace_bytes,
+               iq_stream_t stream, int mask_kind, const void* mask, long long mask_stride);
+
 // ------------------------------------------------------------------ device side
 
 constexpr int kHeadDim = 256;

@@ -29,13 +29,11 @@ __device__ __forceinline__ void load_row_rotation(const uint16_t* rot, int lane,
   }
 }
 
-// Rotate, quantise and pack one K (BITS = 4) or V (BITS = 3) row held by a
-// warp: lane l owns dims 8l..8l+7 (rotation blocks 2l, 2l+1); the 64-dim group
-// g is lanes 8g..8g+7.
-template <int BITS>
-__device__ __forceinline__ void encode_row(const uint4 raw, const float (&m)[2][4][4], int lane, long long dst,
-                                           uint32_t* codes_out, uint16_t* scales_out, uint16_t* biases_out) {
-  constexpr int levels = (1 << BITS) - 1;
+// The lane's 8 dims of a bf16 row (raw) rotated by its two M_b blocks and
+// rounded to bf16: y[4c+j] = bf16( sum_{i=0..3} x[4c+i] * M_b[c][i][j] ), f32
+// sum in order.  A bf16 x bf16 product is exact in f32, so each fused
+// multiply-add rounds exactly like the separate product and sum.
+__device__ __forceinline__ void rotate_row_bf16(const uint4 raw, const float (&m)[2][4][4], float (&y)[8]) {
   const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
   float x[8];
 #pragma unroll
@@ -43,9 +41,6 @@ __device__ __forceinline__ void encode_row(const uint4 raw, const float (&m)[2][
     x[2 * e] = bf16_to_f32(rw[e] & 0xFFFFu);
     x[2 * e + 1] = bf16_to_f32(rw[e] >> 16);
   }
-  // rotate: y[4c+j] = bf16( sum_{i=0..3} x[4c+i] * M_b[c][i][j] ), f32 sum in
-  // order.  A bf16 x bf16 product is exact in f32, so each fused multiply-add
-  // rounds exactly like the separate product and sum.
   float acc[8];
 #pragma unroll
   for (int c = 0; c < 2; ++c)
@@ -56,14 +51,24 @@ __device__ __forceinline__ void encode_row(const uint4 raw, const float (&m)[2][
       for (int k = 1; k < 4; ++k) a = __fmaf_rn(x[4 * c + k], m[c][k][j], a);
       acc[4 * c + j] = a;
     }
-  float y[8];  // round to bf16 in pairs (one conversion per two outputs)
 #pragma unroll
-  for (int e = 0; e < 8; e += 2) {
+  for (int e = 0; e < 8; e += 2) {  // round to bf16 in pairs (one conversion per two outputs)
     uint32_t pr;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(pr) : "f"(acc[e + 1]), "f"(acc[e]));
     y[e] = __uint_as_float(pr << 16);
     y[e + 1] = __uint_as_float(pr & 0xFFFF0000u);
   }
+}
+
+// Rotate, quantise and pack one K (BITS = 4) or V (BITS = 3) row held by a
+// warp: lane l owns dims 8l..8l+7 (rotation blocks 2l, 2l+1); the 64-dim group
+// g is lanes 8g..8g+7.
+template <int BITS>
+__device__ __forceinline__ void encode_row(const uint4 raw, const float (&m)[2][4][4], int lane, long long dst,
+                                           uint32_t* codes_out, uint16_t* scales_out, uint16_t* biases_out) {
+  constexpr int levels = (1 << BITS) - 1;
+  float y[8];
+  rotate_row_bf16(raw, m, y);
   float mn = y[0], mx = y[0];
 #pragma unroll
   for (int e = 1; e < 8; ++e) {

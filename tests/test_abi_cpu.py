@@ -45,9 +45,22 @@ def test_cache_bytes(L):
     assert list(out) == [rows * 128, rows * 8, rows * 8, rows * 96, rows * 8, rows * 8]
     assert L.iq_cache_bytes(2, 3, 256, 64, 4, 3, 500, out) == 1        # not a multiple of 256
     assert L.iq_cache_bytes(2, 3, 128, 64, 4, 3, 512, out) == 4        # other head_dim
-    assert L.iq_cache_bytes(2, 3, 256, 64, 2, 3, 512, out) == 4        # other bits
+    assert L.iq_cache_bytes(2, 3, 256, 64, 7, 3, 512, out) == 4        # a width the page does not list
+    assert L.iq_cache_bytes(2, 3, 256, 16, 4, 3, 512, out) == 4        # group size not built
     assert L.iq_cache_bytes(300, 3, 256, 64, 4, 3, 512, out) == 4      # batch above maximum
     assert b"256" in L.iq_last_error() or L.iq_last_error()
+
+
+@pytest.mark.parametrize("kb,vb,gs", [(2, 2, 32), (3, 5, 128), (5, 6, 64), (8, 8, 128), (6, 3, 32)])
+def test_cache_bytes_other_formats(L, kb, vb, gs):
+    # page `_packed_words`: dim * bits / 32 words per row; one bf16 scale and
+    # bias per group
+    out = (ctypes.c_size_t * 6)()
+    assert L.iq_cache_bytes(1, 2, 256, gs, kb, vb, 256, out) == 0
+    rows = 2 * 256
+    ng = 256 // gs
+    assert list(out) == [rows * 8 * kb * 4, rows * ng * 2, rows * ng * 2, rows * 8 * vb * 4, rows * ng * 2,
+                         rows * ng * 2]
 
 
 def fake_desc(batch=2, cap=256, lens=(3, 4), align=0):
