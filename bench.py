@@ -37,6 +37,11 @@ METRIC = "quantized-KV decode attention: KV tokens/s and HBM GB/s vs ~8 TB/s roo
 UNIT = "KV tokens/s"
 K_ROW, V_ROW = 144, 112  # algorithmic bytes per token-head: codes + bf16 scales/biases
 
+
+def row_bytes(bits: int, group_size: int) -> int:
+    """Bytes of one packed row: 256 * bits / 8 of codes + a bf16 scale and bias per group."""
+    return 256 * bits // 8 + 2 * 2 * (256 // group_size)
+
 # DRAM bytes (read + write) per iq_attend call on the default workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of attend_kernel and
 # combine_kernel; profiles/attend_kernel_batched_decode_32x32k.md).  Reported
@@ -157,7 +162,7 @@ def dist_env():
     return ws, rank, local
 
 
-def make_workload(wid: int, steps_total: int, dev, batch: int | None = None):
+def make_workload(wid: int, steps_total: int, dev, batch: int | None = None, fmt=(4, 3, 64)):
     """Device-resident cache holding the prefill, plus per-step inputs (host and device).
 
     `batch` replaces the workload's sequence count (smaller cases for profiling)."""
@@ -167,7 +172,7 @@ def make_workload(wid: int, steps_total: int, dev, batch: int | None = None):
         w["B"] = batch
     B, Hkv, Hq = w["B"], w["Hkv"], w["Hq"]
     rot = Rotation(0, 256, dev)
-    cache = IQCache(B, Hkv, device=dev, capacity=256)
+    cache = IQCache(B, Hkv, device=dev, capacity=256, k_bits=fmt[0], v_bits=fmt[1], group_size=fmt[2])
     cache.reserve(w["prefill"] + w["append"] * steps_total + 256)
     full_k, full_v = si.kv_tokens(w["seed"], B, Hkv, w["prefill"], outliers=w["outliers"])
     chunk = 4096
@@ -194,7 +199,9 @@ def run_ours(args):
     from rotated_bit_quantized_gb300 import build as b
     b.build()
     W, K = args.warmup, args.steps
-    w, rot, cache, steps = make_workload(args.workload, W + K, dev, args.batch)
+    fmt = tuple(int(x) for x in args.kv_format.split(","))
+    w, rot, cache, steps = make_workload(args.workload, W + K, dev, args.batch, fmt)
+    k_row, v_row = row_bytes(fmt[0], fmt[2]), row_bytes(fmt[1], fmt[2])
     B, Hkv, Hq, L = w["B"], w["Hkv"], w["Hq"], w["queries"]
     base_len = cache.lens.copy()
     dsteps = [(k.to(dev), v.to(dev), q.to(dev)) for k, v, q in steps]
@@ -206,6 +213,8 @@ def run_ours(args):
     # attend_kernel + combine_kernel, plus append_kernel when the step does not fuse
     # (more than 8 query rows per kv head)
     launches_per_step = 2 if Hq // Hkv * L <= 8 and args.mask == "none" else 3
+    if fmt != (4, 3, 64):  # the generic path: append, attention over the splits, split merge
+        launches_per_step = 3
 
     mask = None
     if args.mask != "none":  # an explicit mask instead of the causal one: [B, L, S], ~90% of keys kept
@@ -314,9 +323,9 @@ def run_ours(args):
         attn_avg_s = statistics.mean(attn_ms) / 1e3
         # per call: the cache scanned (256 B per token-head) plus the append
         # (1024 B of bf16 K/V read and 256 B written per new token-head)
-        call_bytes = token_heads * (K_ROW + V_ROW) + B * Hkv * w["append"] * (4 * 256 + K_ROW + V_ROW)
+        call_bytes = token_heads * (k_row + v_row) + B * Hkv * w["append"] * (4 * 256 + k_row + v_row)
         if mask is not None:  # the mask entries of the scanned keys; the append runs outside the bracket
-            call_bytes = token_heads * (K_ROW + V_ROW) + token_heads / Hkv * L * mask.element_size()
+            call_bytes = token_heads * (k_row + v_row) + token_heads / Hkv * L * mask.element_size()
         achieved = call_bytes / call_s / 1e9
         h2d = (dsteps[0][0].numel() + dsteps[0][1].numel() + dsteps[0][2].numel()) * 2
         d2h = out.numel() * 2
@@ -328,18 +337,21 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded N(0,1); keys with x20 outlier channels)",
             "config": {"workload": f"{w['name']}: B={B} seqs, Hq={Hq}/Hkv={Hkv}, head_dim=256, "
-                                   f"{w['prefill']}-token K4/V3 cache, append {w['append']} + attend "
+                                   f"{w['prefill']}-token K{fmt[0]}/V{fmt[1]} cache (groups of {fmt[2]}), "
+                                   f"append {w['append']} + attend "
                                    f"{L} query per step"
                                    + ("" if mask is None else f", explicit {args.mask} mask [B, L, {mask.shape[2]}]"),
                        "parallelism": f"replicas x{ws}",
-                       "l2": f"no flush: the cache read per step ({token_heads * (K_ROW + V_ROW) / 1e6:.0f} MB) "
-                             f"{'exceeds' if token_heads * (K_ROW + V_ROW) > 129e6 else 'is below'} the 129 MB L2"},
+                       "l2": f"no flush: the cache read per step ({token_heads * (k_row + v_row) / 1e6:.0f} MB) "
+                             f"{'exceeds' if token_heads * (k_row + v_row) > 129e6 else 'is below'} the 129 MB L2"},
             "roofline": {"bound": "hbm",
-                         "kernel": "iq_cache_append_attend: attend_kernel (split-KV attention, new rows encoded "
+                         "kernel": ("iq_cache_append_attend (generic format: append_any_kernel, attend_any_kernel, "
+                                    "merge_any_kernel)") if fmt != (4, 3, 64) else
+                                   "iq_cache_append_attend: attend_kernel (split-KV attention, new rows encoded "
                                    "in-kernel for decode steps) + combine_kernel (split merge)",
                          "achieved": achieved, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": measured_traffic(),
-                         "bytes_per_token_head": K_ROW + V_ROW, "token_heads_per_launch": token_heads,
+                         "frac": achieved / hbm, "traffic": measured_traffic() if fmt == (4, 3, 64) else None,
+                         "bytes_per_token_head": k_row + v_row, "token_heads_per_launch": token_heads,
                          "bytes_per_call": call_bytes, "avg_launch_us": call_s * 1e6,
                          "timing": "CUDA events at the two ends of the timed region over its K calls (each "
                                    "call's attention grid starts streaming while the previous call's grids "
@@ -469,17 +481,89 @@ def run_reference(args):
     print(json.dumps(rec), flush=True)
 
 
+def prefill_flops(chunk: int, chunks: int, q_heads: int, head_dim: int = 256) -> float:
+    """Attention FLOPs of a causal chunked prefill: per query head and visible
+    (query, key) pair, 2 * D for q.k and 2 * D for p.v."""
+    pairs = 0
+    for c in range(chunks):
+        pairs += chunk * chunk * c + chunk * (chunk + 1) // 2
+    return float(pairs) * q_heads * 4 * head_dim
+
+
+def run_prefill(args):
+    """Chunked prefill (workload 3): 16 chunks of 2048 tokens, each appended and
+    then attended by its own 2048 queries (causal) over the cache so far.  A
+    step is one chunk; the timed region covers K chunks after W warm-up chunks,
+    from an empty cache.  Reported against the bf16 tensor peak (the attention
+    is a dense contraction; the append is HBM-bound and small)."""
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from rotated_bit_quantized_gb300 import build as b
+    b.build()
+    from rotated_bit_quantized_gb300 import IQCache, Rotation
+    w = si.WORKLOADS[3]
+    B, Hkv, Hq, n = w["B"], w["Hkv"], w["Hq"], w["append"]
+    K = min(args.steps, w["steps"])
+    W = args.warmup
+    rot = Rotation(0, 256, dev)
+    cache = IQCache(B, Hkv, device=dev, capacity=256)
+    cache.reserve(n * w["steps"] + 256)
+    chunks = []
+    for s_ in range(w["steps"]):
+        k, v = si.kv_tokens(w["seed"], B, Hkv, n, outliers=w["outliers"], step=s_)
+        q = si.queries(w["seed"], B, Hq, n, step=s_)
+        chunks.append((k.to(dev), v.to(dev), q.to(dev)))
+    out = torch.empty((B, Hq, n, 256), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(W):
+        cache.append_attend(*chunks[i % len(chunks)], rot, causal=True, out=out)
+    torch.cuda.synchronize(dev)
+    cache.trim(cache.lens)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(physical_gpu(local)) as clk:
+        time.sleep(0.25)
+        e0.record(stream)
+        for i in range(K):
+            cache.append_attend(*chunks[i], rot, causal=True, out=out)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    flops = prefill_flops(n, K, Hq)
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops_sustained"]), "measured (sustained)"
+    except Exception:
+        peak, kind = 1700.0, "fallback (sustained)"
+    tflops = flops / (ms / 1e3) / 1e12
+    rec = {"metric": "chunked prefill: attention TFLOP/s", "value": tflops, "unit": "TFLOP/s", "n_gpus": 1,
+           "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f16/bf16 MMA, f32 accumulate", "data": "synthetic",
+           "config": {"workload": f"chunked_prefill: B={B}, Hq={Hq}/Hkv={Hkv}, head_dim=256, {K} chunks of {n} "
+                                  f"tokens, each appended then attended by its {n} queries (causal)"},
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "peak_kind": kind,
+                        "unit": "TFLOP/s", "frac": tflops / peak, "flops": flops,
+                        "tokens_per_s": B * n * K / (ms / 1e3)},
+           "clocks": clk.summary(), "device_status": cache.device_status()}
+    print(json.dumps(rec), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=4, choices=[2, 4, 5])
+    ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4, 5])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mask", default="none", choices=["none", "bool", "add"],
                     help="attend with an explicit bool / additive mask [B, L, S] instead of the causal one")
+    ap.add_argument("--kv-format", default="4,3,64",
+                    help="k_bits,v_bits,group_size of the cache (4,3,64 runs the tuned kernels)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per step instead of the workload's own count (smaller profiling cases)")
     args = ap.parse_args()
@@ -487,6 +571,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == 3:
+        run_prefill(args)
     else:
         run_ours(args)
 

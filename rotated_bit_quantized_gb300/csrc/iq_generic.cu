@@ -161,7 +161,7 @@ struct AttendArgs {
   const uint16_t* rot;
   void* out;
   float* part_o;   // [B*Hkv][rtiles][nch][8][256]
-  float* part_ml;  // [B*Hkv][rtiles][nch][8][2]: max and sum (natural-log units)
+  float* part_ml;  // [B*Hkv][rtiles][nch][8][2]: max (log2 units) and sum
   unsigned* status;
   const void* mask;  // mask_kind 2: float added; 3: uint8, 0 = masked; [B][nq][mask_stride]
   long long mask_stride;
@@ -171,128 +171,218 @@ struct AttendArgs {
   int lens[IQ_MAX_BATCH];
 };
 
-// The lane's 8 codes of a packed row: stream bits [8*bits*lane, 8*bits*(lane+1)).
-__device__ __forceinline__ unsigned long long lane_codes(const uint32_t* row, int bits, int lane) {
-  const int words = 8 * bits;
-  const int s = 8 * bits * lane, w0 = s >> 5, sh = s & 31;
-  const unsigned long long lo = __ldg(row + w0);
-  const unsigned long long hi = w0 + 1 < words ? __ldg(row + w0 + 1) : 0ull;
-  unsigned long long v = (lo | hi << 32) >> sh;
-  if (sh && w0 + 2 < words) v |= static_cast<unsigned long long>(__ldg(row + w0 + 2)) << (64 - sh);
-  return v;
+// Where the lane's 8 codes of a row start: stream bit 8*bits*lane = word w0,
+// bit sh (constant per lane and width).
+struct LaneBits {
+  int w0, sh, g;
+};
+__device__ __forceinline__ LaneBits lane_bits(int bits, int gs, int lane) {
+  const int s = 8 * bits * lane;
+  return LaneBits{s >> 5, s & 31, 8 * lane / gs};
 }
 
-// Dequantised dims 8*lane .. 8*lane+7 of a row: s * c + b, one rounding each.
-__device__ __forceinline__ void dequant_lane(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
-                                             long long row, int bits, int gs, int lane, float (&x)[8]) {
-  const int ng = kHeadDim / gs, g = 8 * lane / gs;
-  const unsigned long long v = lane_codes(codes + row * 8 * bits, bits, lane);
-  const float s = bf16_to_f32(__ldg(scales + row * ng + g)), b = bf16_to_f32(__ldg(biases + row * ng + g));
-  const unsigned long long mask = (1ull << bits) - 1;
+// Dequantised dims 8*lane .. 8*lane+7 of row r of a staged tile, BITS-bit
+// codes: s * c + b with one rounding each (c < 2^23 becomes a float exactly by
+// the 2^23 magic number).  The lane's window is at most 64 bits, so two words
+// hold it.
+template <int BITS>
+__device__ __forceinline__ void dequant_bits(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                                             int r, int ng, LaneBits lb, float (&x)[8]) {
+  constexpr int WORDS = 8 * BITS;
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+  const uint32_t* row = codes + r * WORDS;
+  const uint32_t a = row[lb.w0];
+  const uint32_t b = lb.w0 + 1 < WORDS ? row[lb.w0 + 1] : 0u;
+  const uint32_t lo = __funnelshift_r(a, b, lb.sh), hi = __funnelshift_r(b, 0u, lb.sh);
+  const float s = bf16_to_f32(scales[r * ng + lb.g]), bb = bf16_to_f32(biases[r * ng + lb.g]);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) x[e] = fmaf(s, static_cast<float>((v >> (bits * e)) & mask), b);
+  for (int e = 0; e < 8; ++e) {
+    const int off = BITS * e;
+    uint32_t c;
+    if (off + BITS <= 32)
+      c = (lo >> off) & MASK;
+    else if (off >= 32)
+      c = (hi >> (off - 32)) & MASK;
+    else
+      c = __funnelshift_r(lo, hi, off) & MASK;
+    x[e] = fmaf(s, __uint_as_float(0x4B000000u | c) - 8388608.0f, bb);
+  }
 }
+
+__device__ __forceinline__ void dequant_lane(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                                             int r, int bits, int ng, LaneBits lb, float (&x)[8]) {
+  switch (bits) {  // uniform over the grid
+    case 2: dequant_bits<2>(codes, scales, biases, r, ng, lb, x); break;
+    case 3: dequant_bits<3>(codes, scales, biases, r, ng, lb, x); break;
+    case 4: dequant_bits<4>(codes, scales, biases, r, ng, lb, x); break;
+    case 5: dequant_bits<5>(codes, scales, biases, r, ng, lb, x); break;
+    case 6: dequant_bits<6>(codes, scales, biases, r, ng, lb, x); break;
+    default: dequant_bits<8>(codes, scales, biases, r, ng, lb, x); break;
+  }
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+constexpr int kTileKeys = 32;                                // keys per staged tile
+constexpr int kTileCodeBytes = kTileKeys * kHeadDim;         // 32 rows x 256 B (8-bit codes at most)
+constexpr int kTileMetaBytes = kTileKeys * (kHeadDim / 32) * 2;  // 32 rows x 8 groups x bf16 at most
+
+struct Stage {
+  uint32_t kc[kTileCodeBytes / 4];
+  uint32_t vc[kTileCodeBytes / 4];
+  uint16_t ks[kTileMetaBytes / 2], kb[kTileMetaBytes / 2], vs[kTileMetaBytes / 2], vb[kTileMetaBytes / 2];
+};
 
 // grid (nch, B*Hkv, rtiles), 128 threads.  CTA (x, bh, z): the 8 query rows of
-// tile z over key split x; its 4 warps take every 4th key, then merge.
+// tile z over key split x (a multiple of 32 keys).  The split's keys pass
+// through shared memory in 32-key tiles, two in flight (cp.async, 16-byte
+// pieces: every row and every tile's scale block starts 16-byte aligned); warp
+// w owns rows 2w and 2w+1 over every key, lane l dims 8l .. 8l+7.  Softmax
+// state in log2 units.
 __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__ AttendArgs p) {
-  __shared__ float s_ml[4][8][2];
-  __shared__ float s_o[4][8][kHeadDim];
+  constexpr float LOG2E = 1.4426950408889634f;
+  constexpr float NEG = -__builtin_huge_valf();
+  __shared__ __align__(16) Stage st[2];
   const int x = blockIdx.x, bh = blockIdx.y, z = blockIdx.z;
   const int b = bh / p.kv_heads, h = bh % p.kv_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.lens[b];
-  const int per = (T + p.nch - 1) / p.nch;
-  const int c0 = x * per, c1 = min(T, c0 + per);
+  const int per = ((T + p.nch - 1) / p.nch + kTileKeys - 1) / kTileKeys * kTileKeys;
+  const int c0 = x * per;
 
   float m[2][4][4];
   load_row_rotation(p.rot, lane, m);
-  // q'' = bf16(bf16(q @ M_b) * scale) of the tile's rows, the lane's 8 dims
-  float qq[8][8];
-  int qpos[8], qidx[8];
-  bool rv[8];
+  // q'' = bf16(bf16(q @ M_b) * scale) of the warp's two rows, the lane's 8 dims
+  float qq[2][8];
+  int qpos[2], qidx[2];
+  int cmax = -1;  // the last key some row of the tile may see
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int R = 8 * z + r, i = R / p.rep, hr = R % p.rep;
-    rv[r] = R < p.rows;
-    qidx[r] = min(i, p.nq - 1);
-    qpos[r] = p.causal ? T - p.nq + i : T - 1;
+  for (int j = 0; j < 2; ++j) {
+    const int R = 8 * z + 2 * warp + j, i = R / p.rep, hr = R % p.rep;
+    const bool rv = R < p.rows;
+    qidx[j] = min(i, p.nq - 1);
+    qpos[j] = rv ? (p.causal ? T - p.nq + i : T - 1) : -1;
     uint4 raw = make_uint4(0, 0, 0, 0);
-    if (rv[r]) {
+    if (rv) {
       const long long qrow = (static_cast<long long>(b) * p.kv_heads * p.rep + h * p.rep + hr) * p.nq + i;
       raw = __ldg(reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim + 8 * lane));
     }
     float y[8];
     rotate_row_bf16(raw, m, y);
 #pragma unroll
-    for (int d = 0; d < 8; ++d) qq[r][d] = round_bf16(__fmul_rn(y[d], p.scale));
+    for (int d = 0; d < 8; ++d) qq[j][d] = round_bf16(__fmul_rn(y[d], p.scale));
   }
+  {
+    const int R = min(8 * z + 7, p.rows - 1), i = R / p.rep;
+    cmax = p.causal ? T - p.nq + i : T - 1;
+  }
+  const int c1 = min(min(T, c0 + per), cmax + 1);  // keys [c0, c1) of the split matter to the tile
 
-  float mrow[8], lrow[8], o[8][8];
+  // staging of tile [t, t + 32): codes rows, then the scale and bias blocks
+  const int kbytes = kTileKeys * 32 * p.kbits, vbytes = kTileKeys * 32 * p.vbits;
+  const int ng = kHeadDim / p.gs, mbytes = kTileKeys * ng * 2;
+  const LaneBits klb = lane_bits(p.kbits, p.gs, lane), vlb = lane_bits(p.vbits, p.gs, lane);
+  const long long row0 = static_cast<long long>(bh) * p.cap;
+  auto stage = [&](int s, int t) {
+    const uint8_t* kc = reinterpret_cast<const uint8_t*>(p.k_codes) + (row0 + t) * 32 * p.kbits;
+    const uint8_t* vc = reinterpret_cast<const uint8_t*>(p.v_codes) + (row0 + t) * 32 * p.vbits;
+    for (int o = threadIdx.x * 16; o < kbytes; o += blockDim.x * 16)
+      cp_async16(reinterpret_cast<uint8_t*>(st[s].kc) + o, kc + o);
+    for (int o = threadIdx.x * 16; o < vbytes; o += blockDim.x * 16)
+      cp_async16(reinterpret_cast<uint8_t*>(st[s].vc) + o, vc + o);
+    const long long mo = (row0 + t) * ng * 2;
+    for (int o = threadIdx.x * 16; o < 4 * mbytes; o += blockDim.x * 16) {
+      const int which = o / mbytes, oo = o % mbytes;
+      const uint16_t* src = which == 0 ? p.k_scales : which == 1 ? p.k_biases : which == 2 ? p.v_scales : p.v_biases;
+      uint16_t* dst = which == 0 ? st[s].ks : which == 1 ? st[s].kb : which == 2 ? st[s].vs : st[s].vb;
+      cp_async16(reinterpret_cast<uint8_t*>(dst) + oo, reinterpret_cast<const uint8_t*>(src) + mo + oo);
+    }
+  };
+
+  float mrow[2] = {NEG, NEG}, lrow[2] = {0.f, 0.f}, o[2][8];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    mrow[r] = -__builtin_huge_valf();
-    lrow[r] = 0.f;
+  for (int j = 0; j < 2; ++j)
 #pragma unroll
-    for (int d = 0; d < 8; ++d) o[r][d] = 0.f;
-  }
-  const long long rowbase = static_cast<long long>(bh) * p.cap;
-  for (int t = c0 + warp; t < c1; t += 4) {
-    float k[8], v[8];
-    dequant_lane(p.k_codes, p.k_scales, p.k_biases, rowbase + t, p.kbits, p.gs, lane, k);
-    dequant_lane(p.v_codes, p.v_scales, p.v_biases, rowbase + t, p.vbits, p.gs, lane, v);
+    for (int d = 0; d < 8; ++d) o[j][d] = 0.f;
+
+  const int ntiles = c1 > c0 ? (c1 - c0 + kTileKeys - 1) / kTileKeys : 0;
+  if (ntiles > 0) stage(0, c0);
+  cp_async_commit();
+  for (int it = 0; it < ntiles; ++it) {
+    if (it + 1 < ntiles) stage((it + 1) & 1, c0 + (it + 1) * kTileKeys);
+    cp_async_commit();
+    cp_async_wait_1();  // tile it has landed (the next one may still be in flight)
+    __syncthreads();
+    const Stage& S = st[it & 1];
+    const int tbase = c0 + it * kTileKeys;
+    const int nk = min(kTileKeys, c1 - tbase);
+    for (int r0 = 0; r0 < nk; r0 += 2) {
+      float k[2][8], v[2][8], sc[2][2];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      float s = 0.f;
-#pragma unroll
-      for (int d = 0; d < 8; ++d) s = fmaf(qq[r][d], k[d], s);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (!rv[r] || t > qpos[r]) continue;  // warp-uniform
-      if (p.mask_kind == 2) {
-        s += __ldg(static_cast<const float*>(p.mask) + (static_cast<long long>(b) * p.nq + qidx[r]) * p.mask_stride + t);
-      } else if (p.mask_kind == 3) {
-        if (__ldg(static_cast<const uint8_t*>(p.mask) + (static_cast<long long>(b) * p.nq + qidx[r]) * p.mask_stride +
-                  t) == 0)
-          s = kMaskedScore;
+      for (int u = 0; u < 2; ++u) {
+        const int r = min(r0 + u, nk - 1);  // a second key past the end repeats the first (masked below)
+        dequant_lane(S.kc, S.ks, S.kb, r, p.kbits, ng, klb, k[u]);
+        dequant_lane(S.vc, S.vs, S.vb, r, p.vbits, ng, vlb, v[u]);
       }
-      const float mn = fmaxf(mrow[r], s);
-      const float a = mrow[r] == -__builtin_huge_valf() ? 0.f : expf(mrow[r] - mn);
-      const float pr = s == -__builtin_huge_valf() ? 0.f : expf(s - mn);
-      lrow[r] = fmaf(lrow[r], a, pr);
 #pragma unroll
-      for (int d = 0; d < 8; ++d) o[r][d] = fmaf(o[r][d], a, pr * v[d]);
-      mrow[r] = mn;
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float s = 0.f;
+#pragma unroll
+          for (int d = 0; d < 8; ++d) s = fmaf(qq[j][d], k[u][d], s);
+          sc[u][j] = s;
+        }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) sc[u][j] += __shfl_xor_sync(0xffffffffu, sc[u][j], off);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int t = tbase + r0 + u;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float s = sc[u][j] * LOG2E;
+          if (r0 + u >= nk || t > qpos[j]) s = NEG;  // warp-uniform
+          if (s != NEG && p.mask_kind == 2) {
+            s = fmaf(__ldg(static_cast<const float*>(p.mask) +
+                           (static_cast<long long>(b) * p.nq + qidx[j]) * p.mask_stride + t),
+                     LOG2E, s);
+          } else if (s != NEG && p.mask_kind == 3) {
+            if (__ldg(static_cast<const uint8_t*>(p.mask) + (static_cast<long long>(b) * p.nq + qidx[j]) *
+                                                                p.mask_stride + t) == 0)
+              s = kMaskedScore * LOG2E;
+          }
+          if (s == NEG) continue;
+          const float mn = fmaxf(mrow[j], s);
+          const float a = mrow[j] == NEG ? 0.f : ex2_approx(mrow[j] - mn);
+          const float pr = ex2_approx(s - mn);
+          lrow[j] = fmaf(lrow[j], a, pr);
+#pragma unroll
+          for (int d = 0; d < 8; ++d) o[j][d] = fmaf(o[j][d], a, pr * v[u][d]);
+          mrow[j] = mn;
+        }
+      }
     }
+    __syncthreads();  // every warp is done with this stage before it is refilled
   }
-  // merge the 4 warps, store the split's partial
-#pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    if (lane == 0) {
-      s_ml[warp][r][0] = mrow[r];
-      s_ml[warp][r][1] = lrow[r];
-    }
-#pragma unroll
-    for (int d = 0; d < 8; ++d) s_o[warp][r][8 * lane + d] = o[r][d];
-  }
-  __syncthreads();
+  // the split's partial of the warp's rows
   const long long slot = (static_cast<long long>(bh) * p.rtiles + z) * p.nch + x;
-  for (int it = threadIdx.x; it < 8 * kHeadDim; it += blockDim.x) {
-    const int r = it / kHeadDim, d = it % kHeadDim;
-    float M = s_ml[0][r][0];
-    for (int w = 1; w < 4; ++w) M = fmaxf(M, s_ml[w][r][0]);
-    float L = 0.f, acc = 0.f;
-    if (M != -__builtin_huge_valf())
-      for (int w = 0; w < 4; ++w) {
-        if (s_ml[w][r][0] == -__builtin_huge_valf()) continue;
-        const float wt = expf(s_ml[w][r][0] - M);
-        L = fmaf(s_ml[w][r][1], wt, L);
-        acc = fmaf(s_o[w][r][d], wt, acc);
-      }
-    p.part_o[(slot * 8 + r) * kHeadDim + d] = acc;
-    if (d == 0) {
-      p.part_ml[(slot * 8 + r) * 2] = M;
-      p.part_ml[(slot * 8 + r) * 2 + 1] = L;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const long long r = slot * 8 + 2 * warp + j;
+    float4* dst = reinterpret_cast<float4*>(p.part_o + r * kHeadDim + 8 * lane);
+    dst[0] = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
+    dst[1] = make_float4(o[j][4], o[j][5], o[j][6], o[j][7]);
+    if (lane == 0) {
+      p.part_ml[r * 2] = mrow[j];
+      p.part_ml[r * 2 + 1] = lrow[j];
     }
   }
 }
@@ -312,7 +402,7 @@ __global__ void __launch_bounds__(256) merge_any_kernel(const __grid_constant__ 
     const float mx = p.part_ml[slot * 2], lx = p.part_ml[slot * 2 + 1];
     if (mx == -__builtin_huge_valf()) continue;
     const float Mn = fmaxf(M, mx);
-    const float a = M == -__builtin_huge_valf() ? 0.f : expf(M - Mn), w = expf(mx - Mn);
+    const float a = M == -__builtin_huge_valf() ? 0.f : ex2_approx(M - Mn), w = ex2_approx(mx - Mn);
     const float4* ox = reinterpret_cast<const float4*>(p.part_o + slot * kHeadDim + 8 * lane);
     const float4 u0 = ox[0], u1 = ox[1];
     const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
