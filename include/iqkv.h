@@ -18,10 +18,15 @@
  *  - Functions return an `iq_status`; nothing is thrown across the ABI.  On an
  *    error nothing is enqueued and nothing the caller owns is modified, and
  *    `iq_last_error()` holds a one-line explanation (per host thread).
- *  - Supported shapes: head_dim 256, group_size 64, k_bits 4, v_bits 3,
+ *  - Supported shapes: head_dim 256; k_bits and v_bits 2, 3, 4, 5, 6 or 8 (the
+ *    widths the page's `_packed_words` lists); group_size 32, 64 or 128;
  *    1 <= batch <= IQ_MAX_BATCH, kv heads >= 1, query heads a multiple of kv
  *    heads with at most 8 query heads per kv head and 8 % rep == 0.  Anything
- *    else returns IQ_ERR_UNSUPPORTED.
+ *    else returns IQ_ERR_UNSUPPORTED.  k_bits 4, v_bits 3, group 64 runs the
+ *    tuned kernels; every other format runs a generic path (same arithmetic,
+ *    float32 attention over shared-memory tiles) that serves at most 64 query
+ *    rows (query heads per kv head x n_queries) per call and never fuses the
+ *    append into the attention.
  */
 #ifndef IQKV_H
 #define IQKV_H
