@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libiqkv.so")
-SOURCES = ["iq_cache.cu", "iq_attend.cu", "iq_noalloc.cu", "iq_generic.cu"]
+SOURCES = ["iq_cache.cu", "iq_attend.cu", "iq_noalloc.cu", "iq_generic.cu", "iq_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE]

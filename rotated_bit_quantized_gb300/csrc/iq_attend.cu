@@ -1564,6 +1564,12 @@ int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries
   st = make_plan(c, q_heads, n_queries, causal, &bound, nullptr);
   if (st != IQ_OK) return st;
   if (workspace_bytes < bound.bytes) return fail(IQ_ERR_WORKSPACE, "workspace smaller than iq_attend_workspace()");
+  if (n_new == 0 && prefill_shape(c, q_heads, n_queries, mask_kind)) {
+    st = prefill_attend(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32,
+                        reinterpret_cast<unsigned*>(workspace), stream);
+    if (st == IQ_OK) read_marks().record(c);
+    return st;
+  }
   static thread_local std::vector<int> tiles;
   tiles.assign(bound.units, 0);
   unit_tiles(c, q_heads / c->kv_heads, n_queries, causal, bound.gt, bound.nqt, bound.tile, tiles.data());

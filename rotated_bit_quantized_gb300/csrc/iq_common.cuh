@@ -33,6 +33,11 @@ bool format_supported(int head_dim, int group_size, int k_bits, int v_bits);
 int append_any(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n, const uint16_t* rot,
                iq_stream_t stream);
 int attend_any_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* bytes);
+// Prefill shapes (iq_prefill.cu): many query rows per kv head, tuned format,
+// no explicit mask: the tensor-memory kernel.
+bool prefill_shape(const iq_cache* c, int q_heads, int n_queries, int mask_kind);
+int prefill_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
+                   const uint16_t* rot, void* out, int out_f32, unsigned* status, iq_stream_t stream);
 int attend_any(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
                const uint16_t* rot, void* out, int out_f32, void* workspace, size_t workspace_bytes,
                iq_stream_t stream, int mask_kind, const void* mask, long long mask_stride);

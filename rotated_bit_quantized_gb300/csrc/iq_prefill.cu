@@ -1,0 +1,571 @@
+// libiqkv: attention of many query rows per kv head (prefill chunks) over the
+// packed K4/V3 cache on the 5th-generation tensor cores (tcgen05, accumulators
+// in tensor memory).
+//
+// Method source: page "sparkle mlx_streaming/core/cache/quant_kv.py",
+// `asym_quantized_sdpa` (scaled queries, GQA: query head h reads kv head
+// h / rep, quantised q.K^T, causal mask at kL - qL + i, softmax, P.V, output in
+// rotated value space, undone here by M_b^T) and `rotate_last` (the query
+// rotation).  Same arithmetic readings as the split-KV kernels: q'' =
+// bf16(bf16(q @ M_b) * scale); keys enter exactly (codes times q'' per 64-dim
+// group, then the group's scale and bias in fp32); fp32 softmax; P and the
+// dequantised values enter the P.V product as fp16.
+//
+// One CTA per (sequence, kv head, tile of 128 query rows); its keys stream in
+// 64-key tiles.  Warp roles (320 threads):
+//  * warps 0-3, one thread per query row (= tensor-memory lane): rotate and
+//    store the row's q'' (fp16 MMA operand) and per-group sums; per key tile
+//    read the four group products S_g from tensor memory, fold in the key
+//    scales and biases, mask, online softmax in log2 units with a lazily
+//    moving reference max (P <= 2^8), write P (fp16 MMA operand); at the end
+//    normalise, undo the rotation and store;
+//  * warps 4-7: turn each staged tile's 4-bit key codes into fp16 (exact
+//    integers, the S MMA operand) and its 3-bit value codes into fp16 values
+//    s*c+b, transposed to dims x keys (the P.V MMA operand);
+//  * warp 8, one lane: bulk copies of the packed tiles into a two-stage ring;
+//  * warp 9, one lane: issues the MMAs: S_g = Q_g . Khat_g^T (M=128 rows,
+//    N=64 keys, K=64 dims, one accumulator per group) and O += P . Vhat
+//    (M=128, N=256 dims, K=64 keys), each committed to an mbarrier.
+// Shared-memory operands use the 128-byte swizzle (K-major, 8-row groups
+// 1024 bytes apart).  Tensor memory: S_0..S_3 in columns 0..255, O in
+// 256..511.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "iq_common.cuh"
+
+namespace iq {
+namespace pre {
+
+constexpr int ROWS = 128;  // query rows per CTA
+constexpr int KT = 64;     // keys per tile
+constexpr int NSTG = 2;    // staged packed tiles
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float NEG = -__builtin_huge_valf();
+constexpr float TAU = 8.0f;  // the reference max moves when a score exceeds it by 2^8
+
+// shared memory (from a 1024-byte aligned base)
+constexpr int OFF_Q = 0;                       // 4 blocks x [128 rows x 128 B]: q'' fp16
+constexpr int OFF_K = OFF_Q + 4 * ROWS * 128;  // 4 blocks x [64 keys x 128 B]: key codes fp16
+constexpr int OFF_V = OFF_K + 4 * KT * 128;    // [256 dims x 128 B]: values fp16, dims x keys
+constexpr int OFF_P = OFF_V + 256 * 128;       // [128 rows x 128 B]: P fp16
+constexpr int OFF_STG = OFF_P + ROWS * 128;    // NSTG packed tiles
+constexpr int STG_KC = 0, STG_VC = KT * 128, STG_KS = STG_VC + KT * 96, STG_KB = STG_KS + KT * 8,
+              STG_VS = STG_KB + KT * 8, STG_VB = STG_VS + KT * 8, STG_BYTES = STG_VB + KT * 8;
+constexpr int OFF_SC = OFF_STG + NSTG * STG_BYTES;  // [64 keys][8] f32: key scales s_0..3, biases b_0..3
+constexpr int OFF_BAR = OFF_SC + KT * 8 * 4;
+constexpr int SMEM = OFF_BAR + 128 + 1024;  // + alignment slack
+static_assert(STG_BYTES == 16384 && OFF_STG % 1024 == 0 && OFF_SC % 16 == 0, "layout");
+constexpr int THREADS = 320;
+
+struct Params {
+  const uint32_t* k_codes;
+  const uint16_t* k_scales;
+  const uint16_t* k_biases;
+  const uint32_t* v_codes;
+  const uint16_t* v_scales;
+  const uint16_t* v_biases;
+  const uint16_t* q;
+  const uint16_t* rot;
+  void* out;
+  unsigned* status;
+  int out_f32, kv_heads, rep, nq, cap, causal, rtiles;
+  float scale;
+  int lens[IQ_MAX_BATCH];
+};
+
+// Bounded wait on an mbarrier phase: gives up after 100 ms (no stage of this
+// kernel takes a fraction of that), so a failure ends the kernel quickly with
+// a status bit instead of holding the GPU.
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = now_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity, 2000u)) return true;
+    if (now_ns() - t0 > 100000000ull) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {  // K-major, 128-byte swizzle
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;                 // leading byte offset (unused with this swizzle)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;         // 8-row groups 1024 B apart
+  d |= static_cast<uint64_t>(1) << 46;                 // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                 // 128-byte swizzle
+  return d;
+}
+// f32 accumulate, fp16 A and B, both K-major, N and M
+__host__ __device__ constexpr uint32_t idesc(int n, int m) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void proxy_fence() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])));
+}
+__device__ __forceinline__ void ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// byte offset of the 16-byte chunk `c` (0..7) of row `r` inside one 128-byte
+// swizzled column block
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // [NSTG]
+  uint64_t* empty = full + NSTG;                                  // [NSTG]
+  uint64_t* kv_ready = empty + NSTG;                              // operands of tile i written
+  uint64_t* s_ready = kv_ready + 1;                               // S_g of tile i in tensor memory
+  uint64_t* p_ready = s_ready + 1;                                // P of tile i written (and O rescaled)
+  uint64_t* o_ready = p_ready + 1;                                // P.V of tile i done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_ready + 1);
+  float* sc = reinterpret_cast<float*>(smem + OFF_SC);
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x;
+  const int z = unit % p.rtiles, bh = unit / p.rtiles;
+  const int b = bh / p.kv_heads, h = bh % p.kv_heads;
+  const int T = p.lens[b];
+  const int rows = p.rep * p.nq;
+  const int r_last = min(z * ROWS + ROWS - 1, rows - 1);
+  const int kmax = p.causal ? T - p.nq + r_last / p.rep + 1 : T;  // keys some row of the tile sees
+  const int ntiles = (kmax + KT - 1) / KT;
+  const long long row0 = static_cast<long long>(bh) * p.cap;
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTG; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    mbar_init(kv_ready, 4);
+    mbar_init(s_ready, 1);
+    mbar_init(p_ready, 4);
+    mbar_init(o_ready, 1);
+    mbar_fence_init();
+  }
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i, ++issued) {
+        const int st = i % NSTG;
+        if (i >= NSTG && !wait_phase(&empty[st], static_cast<uint32_t>(i / NSTG - 1) & 1)) {
+          atomicOr(p.status, 1u | 0x100u);
+          break;
+        }
+        uint8_t* g = smem + OFF_STG + st * STG_BYTES;
+        const long long r = row0 + static_cast<long long>(i) * KT;
+        mbar_arrive_expect_tx(&full[st], STG_BYTES);
+        bulk_g2s(g + STG_KC, p.k_codes + r * kKWords, KT * 128, &full[st], pol);
+        bulk_g2s(g + STG_VC, p.v_codes + r * kVWords, KT * 96, &full[st], pol);
+        bulk_g2s(g + STG_KS, p.k_scales + r * kGroups, KT * 8, &full[st], pol);
+        bulk_g2s(g + STG_KB, p.k_biases + r * kGroups, KT * 8, &full[st], pol);
+        bulk_g2s(g + STG_VS, p.v_scales + r * kGroups, KT * 8, &full[st], pol);
+        bulk_g2s(g + STG_VB, p.v_biases + r * kGroups, KT * 8, &full[st], pol);
+      }
+      for (int s = 0; s < NSTG && s < issued; ++s) {  // no copy left in flight
+        const int last = s + NSTG * ((issued - 1 - s) / NSTG);
+        wait_phase(&full[s], static_cast<uint32_t>(last / NSTG) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA issuer
+    named_bar(1, 128 + 32);  // q'' written by the row threads
+    if (lane == 0) {
+      tc_after();
+      int done = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        if (!wait_phase(kv_ready, static_cast<uint32_t>(i) & 1)) {
+          atomicOr(p.status, 2u | 0x200u);
+          break;
+        }
+        tc_after();
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma(tmem + 64 * g, sdesc(sbase + OFF_Q + g * ROWS * 128 + 32 * ks),
+                sdesc(sbase + OFF_K + g * KT * 128 + 32 * ks), idesc(KT, ROWS), ks > 0 ? 1u : 0u);
+        commit(s_ready);
+        if (!wait_phase(p_ready, static_cast<uint32_t>(i) & 1)) {
+          atomicOr(p.status, 2u | 0x400u);
+          break;
+        }
+        tc_after();
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma(tmem + 256, sdesc(sbase + OFF_P + 32 * ks), sdesc(sbase + OFF_V + 32 * ks), idesc(256, ROWS),
+              (i > 0 || ks > 0) ? 1u : 0u);
+        commit(o_ready);
+        done = i + 1;
+      }
+      if (done > 0) wait_phase(o_ready, static_cast<uint32_t>(done - 1) & 1);  // nothing left in flight
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- operand builders
+    const int dt = threadIdx.x - 128;  // 0..127
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % NSTG;
+      bool ok = wait_phase(&full[st], static_cast<uint32_t>(i / NSTG) & 1);
+      if (!ok) atomicOr(p.status, 0x800u);
+      if (ok && i > 0) {
+        ok = wait_phase(o_ready, static_cast<uint32_t>(i - 1) & 1);  // operands free again
+        if (!ok) atomicOr(p.status, 0x1000u);
+      }
+      if (!ok) {
+        atomicOr(p.status, 1u);
+        break;
+      }
+      const uint8_t* g = smem + OFF_STG + st * STG_BYTES;
+      // key codes -> fp16 c (exact): item (key t, 8-dim chunk c), the chunk is word c of the row
+      for (int it = dt; it < KT * 32; it += 128) {
+        const int t = it >> 5, c = it & 31;
+        const uint32_t w = reinterpret_cast<const uint32_t*>(g + STG_KC)[t * 32 + c];
+        uint32_t hv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t x = ((w >> (8 * j)) & 0xFu) | (((w >> (8 * j + 4)) & 0xFu) << 16);
+          uint32_t y;
+          asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(x | 0x64006400u), "r"(0x64006400u));
+          hv[j] = y;  // (c_2j, c_2j+1) as fp16
+        }
+        *reinterpret_cast<uint4*>(smem + OFF_K + (c >> 3) * KT * 128 + swz(t, c & 7)) =
+            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      }
+      // values -> fp16 s*c+b, transposed: item (8-dim block db, 8-key block tb)
+      for (int it = dt; it < 32 * 8; it += 128) {
+        const int db = it >> 3, tb = it & 7;
+        const int gi = db >> 3;  // 64-dim group
+        const int w0 = (3 * db) >> 2, sh = (24 * db) & 31;
+        float v[8][8];  // [key][dim]
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int t = 8 * tb + k;
+          const uint32_t* row = reinterpret_cast<const uint32_t*>(g + STG_VC) + t * 24;
+          const uint32_t f = __funnelshift_r(row[w0], row[w0 + 1 < 24 ? w0 + 1 : w0], sh);
+          const uint16_t* vs = reinterpret_cast<const uint16_t*>(g + STG_VS) + t * 4;
+          const uint16_t* vb = reinterpret_cast<const uint16_t*>(g + STG_VB) + t * 4;
+          const float s = bf16_to_f32(vs[gi]), bb = bf16_to_f32(vb[gi]);
+          const bool stale = i * KT + t >= T;  // rows past the length may hold anything: P is 0 there, and 0 * NaN is not
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            v[k][e] = stale ? 0.f : fmaf(s, __uint_as_float(0x4B000000u | ((f >> (3 * e)) & 7u)) - 8388608.0f, bb);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int d = 8 * db + e;
+          *reinterpret_cast<uint4*>(smem + OFF_V + swz(d, tb)) =
+              make_uint4(pack_h2(v[0][e], v[1][e]), pack_h2(v[2][e], v[3][e]), pack_h2(v[4][e], v[5][e]),
+                         pack_h2(v[6][e], v[7][e]));
+        }
+      }
+      // the key scales and biases of the tile, for the row threads
+      for (int it = dt; it < KT * 4; it += 128) {
+        const int t = it >> 2, gi = it & 3;
+        sc[t * 8 + gi] = bf16_to_f32(reinterpret_cast<const uint16_t*>(g + STG_KS)[t * 4 + gi]);
+        sc[t * 8 + 4 + gi] = bf16_to_f32(reinterpret_cast<const uint16_t*>(g + STG_KB)[t * 4 + gi]);
+      }
+      proxy_fence();  // generic-proxy stores before the tensor cores read them
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(kv_ready);
+        mbar_arrive(&empty[st]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- row threads
+    const int r = threadIdx.x;  // row in the tile = tensor-memory lane
+    const int R = z * ROWS + r;
+    const bool live = R < rows;
+    const int qi = live ? R / p.rep : 0, hr = live ? R % p.rep : 0;
+    const int qpos = live ? (p.causal ? T - p.nq + qi : T - 1) : -1;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    // q'' = bf16(bf16(q @ M_b) * scale) as fp16, and its per-group sums
+    float qs[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const uint16_t* qrow =
+          p.q + ((static_cast<long long>(b) * p.kv_heads * p.rep + h * p.rep + hr) * p.nq + qi) * kHeadDim;
+      for (int c = 0; c < 32; ++c) {  // 8-dim chunk c: rotation blocks 2c, 2c+1
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (live) raw = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c));
+        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t hv[4];
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          float x[4], y[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t w = rw[(4 * blk + e) >> 1];
+            x[e] = bf16_to_f32(((4 * blk + e) & 1) ? (w >> 16) : (w & 0xFFFFu));
+          }
+          const uint16_t* mb = p.rot + (2 * c + blk) * 16;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float a = __fmul_rn(x[0], bf16_to_f32(__ldg(mb + j)));
+#pragma unroll
+            for (int k = 1; k < 4; ++k) a = __fadd_rn(a, __fmul_rn(x[k], bf16_to_f32(__ldg(mb + 4 * k + j))));
+            y[j] = round_bf16(__fmul_rn(round_bf16(a), p.scale));
+          }
+          const uint32_t h0 = pack_h2(y[0], y[1]), h1 = pack_h2(y[2], y[3]);
+          hv[2 * blk] = h0;
+          hv[2 * blk + 1] = h1;
+          // the sums use the fp16 values the MMA multiplies
+          const __half2 a0 = *reinterpret_cast<const __half2*>(&h0), a1 = *reinterpret_cast<const __half2*>(&h1);
+          qs[c >> 3] += __low2float(a0) + __high2float(a0) + __low2float(a1) + __high2float(a1);
+        }
+        *reinterpret_cast<uint4*>(smem + OFF_Q + (c >> 3) * ROWS * 128 + swz(r, c & 7)) =
+            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      }
+    }
+    proxy_fence();
+    named_bar(1, 128 + 32);  // (arrive side for the MMA warp)
+
+    float mref = NEG, lsum = 0.f;
+    bool ok = true;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      // tensor-memory loads and stores are warp-collective: every decision that
+      // guards them is made the same for the whole warp
+      if (!__all_sync(0xffffffffu, wait_phase(s_ready, static_cast<uint32_t>(i) & 1))) {
+        atomicOr(p.status, 2u | 0x2000u);
+        ok = false;
+        break;
+      }
+      tc_after();
+      float x[KT];  // scores of the tile's keys in log2 units
+#pragma unroll
+      for (int c16 = 0; c16 < KT / 16; ++c16) {
+        float s0[16], s1[16], s2[16], s3[16];
+        ld16(lane_addr + 0 * 64 + 16 * c16, s0);
+        ld16(lane_addr + 1 * 64 + 16 * c16, s1);
+        ld16(lane_addr + 2 * 64 + 16 * c16, s2);
+        ld16(lane_addr + 3 * 64 + 16 * c16, s3);
+        ld_wait();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int tl = 16 * c16 + k, t = i * KT + tl;
+          const float4 ks = *reinterpret_cast<const float4*>(sc + tl * 8);
+          const float4 kb = *reinterpret_cast<const float4*>(sc + tl * 8 + 4);
+          float s = ks.x * s0[k];
+          s = fmaf(ks.y, s1[k], s);
+          s = fmaf(ks.z, s2[k], s);
+          s = fmaf(ks.w, s3[k], s);
+          s = fmaf(kb.x, qs[0], s);
+          s = fmaf(kb.y, qs[1], s);
+          s = fmaf(kb.z, qs[2], s);
+          s = fmaf(kb.w, qs[3], s);
+          x[tl] = t <= qpos ? s * LOG2E : NEG;
+        }
+      }
+      float mx = NEG;
+#pragma unroll
+      for (int k = 0; k < KT; ++k) mx = fmaxf(mx, x[k]);
+      // P and the O accumulator of the previous tile are free once its P.V is done
+      if (i > 0 && !__all_sync(0xffffffffu, wait_phase(o_ready, static_cast<uint32_t>(i - 1) & 1))) {
+        atomicOr(p.status, 2u | 0x4000u);
+        ok = false;
+        break;
+      }
+      const bool move = mx != NEG && (mref == NEG || mx > mref + TAU);
+      const float mnew = move ? (mref == NEG ? mx : fmaxf(mref, mx)) : mref;
+      const float alpha = !move ? 1.f : mref == NEG ? 0.f : ex2_approx(mref - mnew);
+      if (i > 0 && __any_sync(0xffffffffu, move)) {  // O holds earlier tiles' sums: rescale the rows that moved
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 16) {
+          float o[16];
+          ld16(lane_addr + 256 + c, o);
+          ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) o[j] *= alpha;
+          st16(lane_addr + 256 + c, o);
+        }
+        st_wait();
+      }
+      lsum *= alpha;
+      mref = mnew;
+      // P = 2^(x - mref) (fp16), and its row sum
+#pragma unroll
+      for (int c = 0; c < KT / 8; ++c) {
+        uint32_t hv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a = mref == NEG ? 0.f : ex2_approx(x[8 * c + 2 * j] - mref);
+          const float bq = mref == NEG ? 0.f : ex2_approx(x[8 * c + 2 * j + 1] - mref);
+          lsum += a + bq;
+          hv[j] = pack_h2(a, bq);
+        }
+        *reinterpret_cast<uint4*>(smem + OFF_P + swz(r, c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      }
+      proxy_fence();
+      tc_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_ready);
+    }
+    // ---- output: O / l, undo the rotation, store
+    if (ok && ntiles > 0 && __all_sync(0xffffffffu, wait_phase(o_ready, static_cast<uint32_t>(ntiles - 1) & 1))) {
+      tc_after();
+      const float inv = 1.f / lsum;
+      if (live && !(lsum > 0.f)) atomicOr(p.status, 4u);
+      const long long orow = (static_cast<long long>(b) * p.kv_heads * p.rep + h * p.rep + hr) * p.nq + qi;
+#pragma unroll 1
+      for (int c = 0; c < 256; c += 16) {
+        float o[16];
+        ld16(lane_addr + 256 + c, o);
+        ld_wait();
+        if (!live) continue;
+        float y[16];
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          const uint16_t* mb = p.rot + ((c >> 2) + blk) * 16;
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii) {
+            float acc = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc = fmaf(o[4 * blk + jj] * inv, bf16_to_f32(__ldg(mb + 4 * ii + jj)), acc);
+            y[4 * blk + ii] = acc;
+          }
+        }
+        if (p.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHeadDim + c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kHeadDim + c);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            uint4 w;
+            w.x = f32_to_bf16_bits(y[8 * j]) | (f32_to_bf16_bits(y[8 * j + 1]) << 16);
+            w.y = f32_to_bf16_bits(y[8 * j + 2]) | (f32_to_bf16_bits(y[8 * j + 3]) << 16);
+            w.z = f32_to_bf16_bits(y[8 * j + 4]) | (f32_to_bf16_bits(y[8 * j + 5]) << 16);
+            w.w = f32_to_bf16_bits(y[8 * j + 6]) | (f32_to_bf16_bits(y[8 * j + 7]) << 16);
+            dst[j] = w;
+          }
+        }
+      }
+    } else if (live) {
+      atomicOr(p.status, 2u | 0x8000u);
+    }
+  }
+  tc_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+  }
+}
+
+}  // namespace pre
+
+// Rows per kv head from which attention takes the tensor-memory kernel.
+#ifndef IQ_PREFILL_MIN_ROWS
+#define IQ_PREFILL_MIN_ROWS 128
+#endif
+
+bool prefill_shape(const iq_cache* c, int q_heads, int n_queries, int mask_kind) {
+  return tuned_format(c) && mask_kind <= 1 && (q_heads / c->kv_heads) * n_queries >= IQ_PREFILL_MIN_ROWS;
+}
+
+int prefill_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
+                   const uint16_t* rot, void* out, int out_f32, unsigned* status, iq_stream_t stream) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    IQ_CUDA(cudaFuncSetAttribute(pre::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pre::SMEM));
+    attr_set[dev] = true;
+  }
+  pre::Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.k_codes = c->k_codes;
+  p.k_scales = static_cast<const uint16_t*>(c->k_scales);
+  p.k_biases = static_cast<const uint16_t*>(c->k_biases);
+  p.v_codes = c->v_codes;
+  p.v_scales = static_cast<const uint16_t*>(c->v_scales);
+  p.v_biases = static_cast<const uint16_t*>(c->v_biases);
+  p.q = q;
+  p.rot = rot;
+  p.out = out;
+  p.status = status;
+  p.out_f32 = out_f32 ? 1 : 0;
+  p.kv_heads = c->kv_heads;
+  p.rep = q_heads / c->kv_heads;
+  p.nq = n_queries;
+  p.cap = c->capacity;
+  p.causal = causal;
+  p.rtiles = (p.rep * n_queries + pre::ROWS - 1) / pre::ROWS;
+  p.scale = scale;
+  for (int b = 0; b < c->batch; ++b) p.lens[b] = c->lens[b];
+  const long long grid = static_cast<long long>(c->batch) * c->kv_heads * p.rtiles;
+  if (grid > 0x7FFFFFFFLL) return fail(IQ_ERR_UNSUPPORTED, "too many query tiles");
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(pre::THREADS);
+  cfg.dynamicSmemBytes = pre::SMEM;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  IQ_CUDA(cudaLaunchKernelEx(&cfg, pre::prefill_kernel, p));
+  return IQ_OK;
+}
+
+}  // namespace iq
