@@ -26,6 +26,9 @@
 //  * warp 9, one lane: issues the MMAs: S_g = Q_g . Khat_g^T (M=128 rows,
 //    N=64 keys, K=64 dims, one accumulator per group) and O += P . Vhat
 //    (M=128, N=256 dims, K=64 keys), each committed to an mbarrier.
+// The key operand of tile i+1 is built while the row threads work on tile i
+// (it is free once S(i) is done), so S(i+1) follows P.V(i) at once; the value
+// operand waits for P.V(i).
 // Shared-memory operands use the 128-byte swizzle (K-major, 8-row groups
 // 1024 bytes apart).  Tensor memory: S_0..S_3 in columns 0..255, O in
 // 256..511.
@@ -55,8 +58,8 @@ constexpr int OFF_P = OFF_V + 256 * 128;       // [128 rows x 128 B]: P fp16
 constexpr int OFF_STG = OFF_P + ROWS * 128;    // NSTG packed tiles
 constexpr int STG_KC = 0, STG_VC = KT * 128, STG_KS = STG_VC + KT * 96, STG_KB = STG_KS + KT * 8,
               STG_VS = STG_KB + KT * 8, STG_VB = STG_VS + KT * 8, STG_BYTES = STG_VB + KT * 8;
-constexpr int OFF_SC = OFF_STG + NSTG * STG_BYTES;  // [64 keys][8] f32: key scales s_0..3, biases b_0..3
-constexpr int OFF_BAR = OFF_SC + KT * 8 * 4;
+constexpr int OFF_SC = OFF_STG + NSTG * STG_BYTES;  // 2 x [64 keys][8] f32: key scales s_0..3, biases b_0..3
+constexpr int OFF_BAR = OFF_SC + 2 * KT * 8 * 4;
 constexpr int SMEM = OFF_BAR + 128 + 1024;  // + alignment slack
 static_assert(STG_BYTES == 16384 && OFF_STG % 1024 == 0 && OFF_SC % 16 == 0, "layout");
 constexpr int THREADS = 320;
@@ -159,8 +162,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // [NSTG]
   uint64_t* empty = full + NSTG;                                  // [NSTG]
-  uint64_t* kv_ready = empty + NSTG;                              // operands of tile i written
-  uint64_t* s_ready = kv_ready + 1;                               // S_g of tile i in tensor memory
+  uint64_t* k_ready = empty + NSTG;                               // key operand (and key scales) of tile i written
+  uint64_t* v_ready = k_ready + 1;                                // value operand of tile i written
+  uint64_t* s_ready = v_ready + 1;                                // S_g of tile i in tensor memory
   uint64_t* p_ready = s_ready + 1;                                // P of tile i written (and O rescaled)
   uint64_t* o_ready = p_ready + 1;                                // P.V of tile i done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(o_ready + 1);
@@ -185,7 +189,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 4);
     }
-    mbar_init(kv_ready, 4);
+    mbar_init(k_ready, 4);
+    mbar_init(v_ready, 4);
     mbar_init(s_ready, 1);
     mbar_init(p_ready, 4);
     mbar_init(o_ready, 1);
@@ -228,15 +233,12 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
+    // S(i+1) goes in right behind P.V(i): its keys are built while the row
+    // threads work on tile i, and the S columns are free once P(i) is written
     named_bar(1, 128 + 32);  // q'' written by the row threads
     if (lane == 0) {
       tc_after();
-      int done = 0;
-      for (int i = 0; i < ntiles; ++i) {
-        if (!wait_phase(kv_ready, static_cast<uint32_t>(i) & 1)) {
-          atomicOr(p.status, 2u | 0x200u);
-          break;
-        }
+      auto issue_s = [&](int i) {
         tc_after();
 #pragma unroll
         for (int g = 0; g < 4; ++g)
@@ -245,7 +247,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             mma(tmem + 64 * g, sdesc(sbase + OFF_Q + g * ROWS * 128 + 32 * ks),
                 sdesc(sbase + OFF_K + g * KT * 128 + 32 * ks), idesc(KT, ROWS), ks > 0 ? 1u : 0u);
         commit(s_ready);
-        if (!wait_phase(p_ready, static_cast<uint32_t>(i) & 1)) {
+      };
+      int done = 0;
+      bool ok = ntiles > 0 && wait_phase(k_ready, 0u);
+      if (ntiles > 0 && !ok) atomicOr(p.status, 2u | 0x200u);
+      if (ok) issue_s(0);
+      for (int i = 0; ok && i < ntiles; ++i) {
+        if (!wait_phase(p_ready, static_cast<uint32_t>(i) & 1) || !wait_phase(v_ready, static_cast<uint32_t>(i) & 1)) {
           atomicOr(p.status, 2u | 0x400u);
           break;
         }
@@ -256,6 +264,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
               (i > 0 || ks > 0) ? 1u : 0u);
         commit(o_ready);
         done = i + 1;
+        if (i + 1 < ntiles) {
+          if (!wait_phase(k_ready, static_cast<uint32_t>(i + 1) & 1)) {
+            atomicOr(p.status, 2u | 0x200u);
+            break;
+          }
+          issue_s(i + 1);
+        }
       }
       if (done > 0) wait_phase(o_ready, static_cast<uint32_t>(done - 1) & 1);  // nothing left in flight
     }
@@ -266,14 +281,15 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       const int st = i % NSTG;
       bool ok = wait_phase(&full[st], static_cast<uint32_t>(i / NSTG) & 1);
       if (!ok) atomicOr(p.status, 0x800u);
-      if (ok && i > 0) {
-        ok = wait_phase(o_ready, static_cast<uint32_t>(i - 1) & 1);  // operands free again
+      if (ok && i > 0) {  // the key operand is free once S(i-1) is done
+        ok = wait_phase(s_ready, static_cast<uint32_t>(i - 1) & 1);
         if (!ok) atomicOr(p.status, 0x1000u);
       }
       if (!ok) {
         atomicOr(p.status, 1u);
         break;
       }
+      float* sci = sc + (i & 1) * KT * 8;  // read by the row threads of tile i (tile i-2 was done before S(i-1))
       const uint8_t* g = smem + OFF_STG + st * STG_BYTES;
       // key codes -> fp16 c (exact): item (key t, 8-dim chunk c), the chunk is word c of the row
       for (int it = dt; it < KT * 32; it += 128) {
@@ -289,6 +305,19 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         }
         *reinterpret_cast<uint4*>(smem + OFF_K + (c >> 3) * KT * 128 + swz(t, c & 7)) =
             make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      }
+      // the key scales and biases of the tile, for the row threads
+      for (int it = dt; it < KT * 4; it += 128) {
+        const int t = it >> 2, gi = it & 3;
+        sci[t * 8 + gi] = bf16_to_f32(reinterpret_cast<const uint16_t*>(g + STG_KS)[t * 4 + gi]);
+        sci[t * 8 + 4 + gi] = bf16_to_f32(reinterpret_cast<const uint16_t*>(g + STG_KB)[t * 4 + gi]);
+      }
+      proxy_fence();  // generic-proxy stores before the tensor cores read them
+      __syncwarp();
+      if (lane == 0) mbar_arrive(k_ready);
+      if (i > 0 && !wait_phase(o_ready, static_cast<uint32_t>(i - 1) & 1)) {  // the value operand: after P.V(i-1)
+        atomicOr(p.status, 1u | 0x1000u);
+        break;
       }
       // values -> fp16 s*c+b, transposed: item (8-dim block db, 8-key block tb)
       for (int it = dt; it < 32 * 8; it += 128) {
@@ -317,16 +346,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
                          pack_h2(v[6][e], v[7][e]));
         }
       }
-      // the key scales and biases of the tile, for the row threads
-      for (int it = dt; it < KT * 4; it += 128) {
-        const int t = it >> 2, gi = it & 3;
-        sc[t * 8 + gi] = bf16_to_f32(reinterpret_cast<const uint16_t*>(g + STG_KS)[t * 4 + gi]);
-        sc[t * 8 + 4 + gi] = bf16_to_f32(reinterpret_cast<const uint16_t*>(g + STG_KB)[t * 4 + gi]);
-      }
-      proxy_fence();  // generic-proxy stores before the tensor cores read them
+      proxy_fence();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(kv_ready);
+        mbar_arrive(v_ready);
         mbar_arrive(&empty[st]);
       }
     }
@@ -401,8 +424,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int tl = 16 * c16 + k, t = i * KT + tl;
-          const float4 ks = *reinterpret_cast<const float4*>(sc + tl * 8);
-          const float4 kb = *reinterpret_cast<const float4*>(sc + tl * 8 + 4);
+          const float4 ks = *reinterpret_cast<const float4*>(sc + (i & 1) * KT * 8 + tl * 8);
+          const float4 kb = *reinterpret_cast<const float4*>(sc + (i & 1) * KT * 8 + tl * 8 + 4);
           float s = ks.x * s0[k];
           s = fmaf(ks.y, s1[k], s);
           s = fmaf(ks.z, s2[k], s);
