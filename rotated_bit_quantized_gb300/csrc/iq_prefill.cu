@@ -172,8 +172,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   const uint32_t sbase = smem_u32(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.x;
-  const int z = unit % p.rtiles, bh = unit / p.rtiles;
+  // longest first: causal row tiles late in the chunk see the most keys, and
+  // CTAs are dispatched in block order
+  const int nbh = gridDim.x / p.rtiles;
+  const int z = p.rtiles - 1 - static_cast<int>(blockIdx.x) / nbh, bh = static_cast<int>(blockIdx.x) % nbh;
   const int b = bh / p.kv_heads, h = bh % p.kv_heads;
   const int T = p.lens[b];
   const int rows = p.rep * p.nq;
