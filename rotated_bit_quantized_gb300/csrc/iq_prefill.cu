@@ -414,69 +414,88 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         break;
       }
       tc_after();
-      float x[KT];  // scores of the tile's keys in log2 units
-#pragma unroll
-      for (int c16 = 0; c16 < KT / 16; ++c16) {
-        float s0[16], s1[16], s2[16], s3[16];
-        ld16(lane_addr + 0 * 64 + 16 * c16, s0);
-        ld16(lane_addr + 1 * 64 + 16 * c16, s1);
-        ld16(lane_addr + 2 * 64 + 16 * c16, s2);
-        ld16(lane_addr + 3 * 64 + 16 * c16, s3);
-        ld_wait();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int tl = 16 * c16 + k, t = i * KT + tl;
-          const float4 ks = *reinterpret_cast<const float4*>(sc + (i & 1) * KT * 8 + tl * 8);
-          const float4 kb = *reinterpret_cast<const float4*>(sc + (i & 1) * KT * 8 + tl * 8 + 4);
-          float s = ks.x * s0[k];
-          s = fmaf(ks.y, s1[k], s);
-          s = fmaf(ks.z, s2[k], s);
-          s = fmaf(ks.w, s3[k], s);
-          s = fmaf(kb.x, qs[0], s);
-          s = fmaf(kb.y, qs[1], s);
-          s = fmaf(kb.z, qs[2], s);
-          s = fmaf(kb.w, qs[3], s);
-          x[tl] = t <= qpos ? s * LOG2E : NEG;
-        }
-      }
-      float mx = NEG;
-#pragma unroll
-      for (int k = 0; k < KT; ++k) mx = fmaxf(mx, x[k]);
-      // P and the O accumulator of the previous tile are free once its P.V is done
+      // P(i-1) and the O of the earlier tiles are final: P.V(i-1) was issued
+      // before S(i), and S(i)'s commit covers it (the wait returns at once)
       if (i > 0 && !__all_sync(0xffffffffu, wait_phase(o_ready, static_cast<uint32_t>(i - 1) & 1))) {
         atomicOr(p.status, 2u | 0x4000u);
         ok = false;
         break;
       }
-      const bool move = mx != NEG && (mref == NEG || mx > mref + TAU);
-      const float mnew = move ? (mref == NEG ? mx : fmaxf(mref, mx)) : mref;
-      const float alpha = !move ? 1.f : mref == NEG ? 0.f : ex2_approx(mref - mnew);
-      if (i > 0 && __any_sync(0xffffffffu, move)) {  // O holds earlier tiles' sums: rescale the rows that moved
+      const float* sci = sc + (i & 1) * KT * 8;
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 16) {
-          float o[16];
-          ld16(lane_addr + 256 + c, o);
+      for (int c16 = 0; c16 < KT / 16; ++c16) {  // 16 keys at a time
+        float x[16];  // scores in log2 units
+        {
+          float s0[16], s1[16], s2[16], s3[16];
+          ld16(lane_addr + 0 * 64 + 16 * c16, s0);
+          ld16(lane_addr + 1 * 64 + 16 * c16, s1);
+          ld16(lane_addr + 2 * 64 + 16 * c16, s2);
+          ld16(lane_addr + 3 * 64 + 16 * c16, s3);
           ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) o[j] *= alpha;
-          st16(lane_addr + 256 + c, o);
+          for (int k = 0; k < 16; ++k) {
+            const int tl = 16 * c16 + k, t = i * KT + tl;
+            const float4 ks = *reinterpret_cast<const float4*>(sci + tl * 8);
+            const float4 kb = *reinterpret_cast<const float4*>(sci + tl * 8 + 4);
+            float sv = ks.x * s0[k];
+            sv = fmaf(ks.y, s1[k], sv);
+            sv = fmaf(ks.z, s2[k], sv);
+            sv = fmaf(ks.w, s3[k], sv);
+            sv = fmaf(kb.x, qs[0], sv);
+            sv = fmaf(kb.y, qs[1], sv);
+            sv = fmaf(kb.z, qs[2], sv);
+            sv = fmaf(kb.w, qs[3], sv);
+            x[k] = t <= qpos ? sv * LOG2E : NEG;
+          }
         }
-        st_wait();
-      }
-      lsum *= alpha;
-      mref = mnew;
-      // P = 2^(x - mref) (fp16), and its row sum
+        float mx = NEG;
 #pragma unroll
-      for (int c = 0; c < KT / 8; ++c) {
-        uint32_t hv[4];
+        for (int k = 0; k < 16; ++k) mx = fmaxf(mx, x[k]);
+        const bool move = mx != NEG && (mref == NEG || mx > mref + TAU);
+        if (__any_sync(0xffffffffu, move)) {  // warp-uniform: the O rescale is warp-collective
+          const float mnew = move ? (mref == NEG ? mx : fmaxf(mref, mx)) : mref;
+          const float alpha = !move ? 1.f : mref == NEG ? 0.f : ex2_approx(mref - mnew);
+          if (i > 0) {  // O holds earlier tiles' sums
+#pragma unroll 1
+            for (int c = 0; c < 256; c += 16) {
+              float o[16];
+              ld16(lane_addr + 256 + c, o);
+              ld_wait();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float a = mref == NEG ? 0.f : ex2_approx(x[8 * c + 2 * j] - mref);
-          const float bq = mref == NEG ? 0.f : ex2_approx(x[8 * c + 2 * j + 1] - mref);
-          lsum += a + bq;
-          hv[j] = pack_h2(a, bq);
+              for (int j = 0; j < 16; ++j) o[j] *= alpha;
+              st16(lane_addr + 256 + c, o);
+            }
+            st_wait();
+          }
+          if (move) {  // this row's P chunks already written in this tile
+            for (int c = 0; c < 2 * c16; ++c) {
+              uint4* pc = reinterpret_cast<uint4*>(smem + OFF_P + swz(r, c));
+              uint4 w = *pc;
+              uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const __half2 h2 = *reinterpret_cast<const __half2*>(&wv[j]);
+                wv[j] = pack_h2(__low2float(h2) * alpha, __high2float(h2) * alpha);
+              }
+              *pc = w;
+            }
+          }
+          lsum *= alpha;
+          mref = mnew;
         }
-        *reinterpret_cast<uint4*>(smem + OFF_P + swz(r, c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        // P = 2^(x - mref) (fp16), and its row sum
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t hv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float a = mref == NEG ? 0.f : ex2_approx(x[8 * c + 2 * j] - mref);
+            const float bq = mref == NEG ? 0.f : ex2_approx(x[8 * c + 2 * j + 1] - mref);
+            lsum += a + bq;
+            hv[j] = pack_h2(a, bq);
+          }
+          *reinterpret_cast<uint4*>(smem + OFF_P + swz(r, 2 * c16 + c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        }
       }
       proxy_fence();
       tc_before();

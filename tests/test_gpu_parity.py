@@ -121,6 +121,10 @@ CASES = [
     (2, 1, 8, 20, 1, False, None),
     (1, 2, 8, 600, 64, True, None),
     (1, 1, 8, 5000, 1, False, None),
+    # >= 128 query rows per kv head: the tensor-memory prefill kernel
+    (1, 2, 8, 700, 20, True, None),      # 160 rows: a full and a ragged row tile
+    (2, 1, 4, 900, 40, False, [0, 130]),  # rep 4, no mask, ragged lengths
+    (1, 2, 2, 1100, 100, True, None),    # rep 2, 200 rows
 ]
 
 
