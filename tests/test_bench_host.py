@@ -80,3 +80,20 @@ def test_reference_arm_prints_one_line_on_cpu():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["value"] > 0 and rec["unit"] == bench.UNIT
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_prefill_flops_closed_form():
+    # causal chunked prefill: chunk c of n queries sees c*n earlier keys plus
+    # 1..n of its own; sum over chunks = n^2 * C(C-1)/2 + C * n(n+1)/2 pairs,
+    # each 4 * D flops per query head (q.k and p.v)
+    n, C, H, D = 2048, 16, 16, 256
+    pairs = n * n * C * (C - 1) // 2 + C * n * (n + 1) // 2
+    assert bench.prefill_flops(n, C, H, D) == pairs * H * 4 * D
+    assert abs(bench.prefill_flops(n, C, H, D) - 8.796e12) < 1e9
+    assert bench.prefill_flops(1, 1, 1, 1) == 4.0
+
+
+@pytest.mark.parametrize("bits,gs,want", [(4, 64, 144), (3, 64, 112), (8, 128, 264), (2, 32, 96), (5, 32, 192)])
+def test_row_bytes(bits, gs, want):
+    # 256 dims * bits / 8 bytes of codes + a bf16 scale and bias per group
+    assert bench.row_bytes(bits, gs) == want
