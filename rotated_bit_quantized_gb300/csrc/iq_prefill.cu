@@ -321,9 +321,12 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         atomicOr(p.status, 1u | 0x1000u);
         break;
       }
-      // values -> fp16 s*c+b, transposed: item (8-dim block db, 8-key block tb)
-      for (int it = dt; it < 32 * 8; it += 128) {
-        const int db = it >> 3, tb = it & 7;
+      // values -> fp16 s*c+b, transposed: item (8-dim block db, 8-key block tb);
+      // lane db of operand warp w takes key blocks (db + w) % 8 and (db + w + 4) % 8,
+      // so a warp's lanes read different key rows (192 words apart: the same bank
+      // offset, different words) and store into distinct swizzled chunks
+      for (int half = 0; half < 2; ++half) {
+        const int db = lane, tb = (lane + (warp - 4) + 4 * half) & 7;
         const int gi = db >> 3;  // 64-dim group
         const int w0 = (3 * db) >> 2, sh = (24 * db) & 31;
         float v[8][8];  // [key][dim]
