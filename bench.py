@@ -47,8 +47,8 @@ def row_bytes(bits: int, group_size: int) -> int:
 # combine_kernel; profiles/attend_kernel_batched_decode_32x32k.md).  Reported
 # only while the attention source is the one that was measured.
 TRAFFIC = {"source": "rotated_bit_quantized_gb300/csrc/iq_attend.cu",
-           "sha256": "0f06176a212589f824f56a6d00dc3cdc636768b94a4ef8714f95893b746a2629",
-           "bytes": ((539.382784 + 3.305984 + 2.930432) + (539.387392 + 0.483072 + 2.928896)) / 2 * 1e6}
+           "sha256": "2b7ca3d2548851f30d5eb2bacaf1bd95a5138ceba7fa4ea3b93b7efeffcee44b",
+           "bytes": ((539.385088 + 2.981632 + 2.929664) + (539.400960 + 0.520960 + 2.928896)) / 2 * 1e6}
 
 
 def measured_traffic():
