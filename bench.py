@@ -63,6 +63,12 @@ def measured_traffic():
     return TRAFFIC["bytes"] if digest == TRAFFIC["sha256"] else None
 
 
+# nominal GB300 figures, reported beside the measured peaks: HBM3e "~8 TB/s"
+# (the metric's roofline) and dense bf16 tensor throughput
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -350,7 +356,9 @@ def run_ours(args):
                                    "iq_cache_append_attend: attend_kernel (split-KV attention, new rows encoded "
                                    "in-kernel for decode steps) + combine_kernel (split merge)",
                          "achieved": achieved, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": measured_traffic() if fmt == (4, 3, 64) else None,
+                         "frac": achieved / hbm, "nominal_peak": NOMINAL_HBM_GBS,
+                         "nominal_frac": achieved / NOMINAL_HBM_GBS,
+                         "traffic": measured_traffic() if fmt == (4, 3, 64) else None,
                          "bytes_per_token_head": k_row + v_row, "token_heads_per_launch": token_heads,
                          "bytes_per_call": call_bytes, "avg_launch_us": call_s * 1e6,
                          "timing": "CUDA events at the two ends of the timed region over its K calls (each "
@@ -545,7 +553,8 @@ def run_prefill(args):
            "config": {"workload": f"chunked_prefill: B={B}, Hq={Hq}/Hkv={Hkv}, head_dim=256, {K} chunks of {n} "
                                   f"tokens, each appended then attended by its {n} queries (causal)"},
            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "peak_kind": kind,
-                        "unit": "TFLOP/s", "frac": tflops / peak, "flops": flops,
+                        "unit": "TFLOP/s", "frac": tflops / peak, "nominal_peak": NOMINAL_BF16_TFLOPS,
+                        "nominal_frac": tflops / NOMINAL_BF16_TFLOPS, "flops": flops,
                         "tokens_per_s": B * n * K / (ms / 1e3)},
            "clocks": clk.summary(), "device_status": cache.device_status()}
     print(json.dumps(rec), flush=True)
