@@ -206,18 +206,21 @@ def test_golden_quantize(name):
     assert codes[0].tolist() == g["codes"]
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 8])
-def test_quantize_error_bound_and_extremes(bits):
-    rng = np.random.default_rng(10 + bits)
+@pytest.mark.parametrize("gs", [32, 64, 128])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
+def test_quantize_error_bound_and_extremes(bits, gs):
+    rng = np.random.default_rng(10 + bits + gs)
     x = bf16.round_bf16(rng.standard_normal((500, 256)).astype(np.float32) * rng.uniform(0.1, 30, (500, 1)))
-    codes, s, b = codec.quantize(x, bits, 64)
-    deq = codec.dequantize(codes, s, b, 64)
-    g = x.reshape(500, 4, 64).astype(np.float64)
+    codes, s, b = codec.quantize(x, bits, gs)
+    assert s.shape == b.shape == (500, 256 // gs)
+    deq = codec.dequantize(codes, s, b, gs)
+    # groups are runs of gs consecutive dims
+    g = x.reshape(500, 256 // gs, gs).astype(np.float64)
     scale = (g.max(-1) - g.min(-1)) / (2 ** bits - 1)
     bound = s / 2 + (2 ** bits - 1) * np.abs(scale - s) + 1e-6 * np.abs(g).max(-1)
-    err = np.abs(deq.reshape(500, 4, 64) - g)
+    err = np.abs(deq.reshape(500, 256 // gs, gs) - g)
     assert (err <= bound[..., None]).all()
-    cg = codes.reshape(500, 4, 64)
+    cg = codes.reshape(500, 256 // gs, gs)
     amin = g.argmin(-1)
     amax = g.argmax(-1)
     assert (np.take_along_axis(cg, amin[..., None], -1) == 0).all()
@@ -225,11 +228,12 @@ def test_quantize_error_bound_and_extremes(bits):
     assert (top >= 2 ** bits - 2).all()
 
 
-def test_quantize_brute_force_nearest_level():
-    rng = np.random.default_rng(20)
-    x = bf16.round_bf16(rng.standard_normal((300, 64)).astype(np.float32))
-    for bits in (3, 4):
-        codes, s, b = codec.quantize(x, bits, 64)
+@pytest.mark.parametrize("gs", [32, 64, 128])
+def test_quantize_brute_force_nearest_level(gs):
+    rng = np.random.default_rng(20 + gs)
+    x = bf16.round_bf16(rng.standard_normal((300, gs)).astype(np.float32))
+    for bits in (2, 3, 4, 5, 6, 8):
+        codes, s, b = codec.quantize(x, bits, gs)
         levels = s[:, :, None].astype(np.float64) * np.arange(2 ** bits) + b[:, :, None]
         dist = np.abs(x.astype(np.float64)[:, :, None] - levels[:, 0][:, None, :])
         best = dist.min(-1)
