@@ -285,3 +285,50 @@ def test_mask_special_cases(mb):
             np.testing.assert_allclose(out[b, h, 2], vh.mean(0) @ rotation.dense(mb).T, atol=1e-12)
     with pytest.raises(ValueError):
         attention.attend(q, c, mb, causal=True, mask=keep)
+
+
+# ---------------------------------------------------------------- other formats
+
+FORMATS = [(2, 2, 32), (3, 5, 128), (5, 6, 64), (8, 8, 128), (6, 3, 32)]
+
+
+@pytest.mark.parametrize("kb,vb,gs", FORMATS)
+def test_other_formats_decode_within_the_quantiser_bound(mb, kb, vb, gs):
+    """Rows of a cache in another format (widths 2-8, groups 32/64/128) decode
+    to the rotated inputs within the quantiser's error bound, after an append,
+    a trim and an append over the trimmed rows."""
+    c = OracleCache(2, 1, k_bits=kb, v_bits=vb, group_size=gs)
+    k1, v1 = si.kv_tokens(40, 2, 1, 50, outliers=True)
+    k2, v2 = si.kv_tokens(41, 2, 1, 30, outliers=True)
+    c.append(f32(k1), f32(v1), mb)
+    c.trim(np.array([20, 0]))
+    c.append(f32(k2), f32(v2), mb)
+    assert c.lens.tolist() == [60, 80]
+    for b in range(2):
+        keep = 30 if b == 0 else 50
+        for x_all, bits, which in ((np.concatenate([f32(k1)[b, 0, :keep], f32(k2)[b, 0]]), kb, 0),
+                                   (np.concatenate([f32(v1)[b, 0, :keep], f32(v2)[b, 0]]), vb, 1)):
+            xr = codec.rotate(x_all, mb).astype(np.float64)
+            deq = c.dequantized(b, 0)[which]
+            assert c.k[0].shape[-1] == 256 * kb // 32 and c.v[0].shape[-1] == 256 * vb // 32
+            g = xr.reshape(len(xr), 256 // gs, gs)
+            s = (c.k if which == 0 else c.v)[1][b, 0, :len(xr)].astype(np.float64)
+            scale = (g.max(-1) - g.min(-1)) / (2 ** bits - 1)
+            bound = s / 2 + (2 ** bits - 1) * np.abs(scale - s) + 1e-6 * np.abs(g).max(-1)
+            err = np.abs(deq.reshape(g.shape) - g)
+            assert (err <= bound[..., None]).all()
+
+
+@pytest.mark.parametrize("kb,vb,gs", FORMATS)
+def test_other_formats_attention_matches_dense_brute_force(mb, kb, vb, gs):
+    c = OracleCache(1, 2, k_bits=kb, v_bits=vb, group_size=gs)
+    k, v = si.kv_tokens(42, 1, 2, 45, outliers=True)
+    c.append(f32(k), f32(v), mb)
+    q = f32(si.queries(43, 1, 16, 2))
+    out = attention.attend(q, c, mb, causal=True)
+    m = rotation.dense(mb)
+    for h in range(16):
+        kh, vh = c.dequantized(0, h // 8)
+        qr = codec.rotate(q[0, h], mb)
+        o = dense_attention_f32(qr, kh, vh, 1 / 16, np.arange(43, 45))
+        np.testing.assert_allclose(out[0, h], o.astype(np.float64) @ m.T, atol=1e-5)
