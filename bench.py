@@ -335,7 +335,8 @@ def run_ours(args):
         achieved = call_bytes / call_s / 1e9
         h2d = (dsteps[0][0].numel() + dsteps[0][1].numel() + dsteps[0][2].numel()) * 2
         d2h = out.numel() * 2
-        cpu = None if args.no_cpu_baseline else cpu_baseline_sample(args.workload, budget_s=args.cpu_seconds)
+        cpu = None if args.no_cpu_baseline else cpu_baseline_sample(args.workload, budget_s=args.cpu_seconds,
+                                                                    one_core_s=args.cpu_one_core_seconds)
         append = append_throughput(dev, rot)
         rec = {
             "metric": METRIC, "value": tokens_all / (ms_max / 1e3), "unit": UNIT, "n_gpus": ws,
@@ -452,10 +453,29 @@ def _time_oracle_steps(prep, budget_s: float, max_steps: int):
     return tokens, spent, n
 
 
-def cpu_baseline_sample(wid: int, budget_s: float = 15.0):
+def one_core_sample(wid: int, budget_s: float):
+    """The same oracle sample on one core: a fresh interpreter (spawned, no
+    CUDA) pinned to one CPU with one BLAS thread.  None if it fails."""
+    code = ("import json, os, sys; os.sched_setaffinity(0, {min(os.sched_getaffinity(0))}); "
+            f"sys.path.insert(0, {ROOT!r}); import bench; "
+            f"t, s, n = bench._time_oracle_steps(bench._oracle_sequence({int(wid)}, 0), {float(budget_s)!r}, 10 ** 6); "
+            "print(json.dumps([t, s, n]))")
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=10 * budget_s + 300)
+        tokens, spent, n = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+    return {"value": tokens / spent, "unit": UNIT, "cores": 1, "seconds": spent, "steps": n}
+
+
+def cpu_baseline_sample(wid: int, budget_s: float = 15.0, one_core_s: float = 6.0):
     """The oracle as it stands on a bounded sample of the workload's step: one
     sequence (its prefill encoded once, untimed), whole steps (append + attend)
-    repeated on copies until about `budget_s` seconds of timed work."""
+    repeated on copies until about `budget_s` seconds of timed work, on every
+    core the process may use; then the same on one core (`one_core`)."""
     prep = _oracle_sequence(wid, 0)
     w = prep[0]
     tokens, spent, n = _time_oracle_steps(prep, budget_s, 10 ** 6)
@@ -464,7 +484,8 @@ def cpu_baseline_sample(wid: int, budget_s: float = 15.0):
             "sample": f"{n} repetitions of one sequence's step (append {w['append']} + attend over "
                       f"{w['prefill'] + w['append']} tokens x {w['Hkv']} kv heads, {w['Hq']} query heads); "
                       f"NumPy oracle, BLAS threads up to {cores}; prefill encode untimed",
-            "seconds": spent}
+            "seconds": spent,
+            "one_core": one_core_sample(wid, one_core_s) if one_core_s > 0 else None}
 
 
 def run_reference(args):
@@ -568,6 +589,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4, 5])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-one-core-seconds", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mask", default="none", choices=["none", "bool", "add"],
                     help="attend with an explicit bool / additive mask [B, L, S] instead of the causal one")

@@ -82,6 +82,13 @@ def test_reference_arm_prints_one_line_on_cpu():
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
 
 
+def test_one_core_oracle_sample():
+    """The one-core leg of the CPU baseline: a spawned interpreter pinned to
+    one CPU, timing whole oracle steps of the single-stream decode workload."""
+    rec = bench.one_core_sample(2, 0.3)
+    assert rec is not None and rec["cores"] == 1 and rec["value"] > 0 and rec["steps"] >= 1
+
+
 def test_prefill_flops_closed_form():
     # causal chunked prefill: chunk c of n queries sees c*n earlier keys plus
     # 1..n of its own; sum over chunks = n^2 * C(C-1)/2 + C * n(n+1)/2 pairs,
