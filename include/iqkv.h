@@ -190,12 +190,19 @@ int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_
  *    attention grid and, as its programmatic dependent, the split combine,
  *    which merges each split unit as soon as its partials are stored and
  *    completes after the attention grid.
- * Scores, softmax and P.V accumulate in float32 on tensor cores; dequantised
- * key codes enter the products exactly; P times the value scale enters as fp16.
+ * Scores, softmax and P.V accumulate in float32 on tensor cores.  Key and
+ * value codes enter the products exactly (as bare fp16 bit fields), queries as
+ * q'' times a per-row power of two that keeps them inside fp16 (any bf16
+ * query), P times the value scale as fp16 with the softmax reference raised
+ * when a value scale reaches 2^9 (value groups of any bf16 range).  Calls with
+ * 128 or more query rows per kv head take the tensor-memory prefill kernel,
+ * whose dequantised values are fp16: a value at or above 2^15 in magnitude
+ * sets status bit 16 there.
  * Errors: INVALID_ARG (null, bad causal flag, empty sequence, lens[b] <
  * n_queries when causal), WORKSPACE, UNSUPPORTED, CUDA.  A kernel-side failure
- * (a pipeline wait that timed out, an empty softmax row) sets a bit in the
- * workspace status word, reported by iq_read_status.
+ * (a pipeline wait that timed out, an empty softmax row, a value outside the
+ * prefill kernel's range) sets a bit in the workspace status word, reported by
+ * iq_read_status.
  */
 int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
               float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,

@@ -24,15 +24,18 @@
 //    copies) into a multi-stage shared-memory ring guarded by mbarriers, running
 //    ahead across unit boundaries; its warpgroup hands most of its registers
 //    to the consumer warps;
-//  * consumer warps unpack codes in registers with bit tricks and run m16n8k16
-//    tensor-core MMAs: S_G = (off + K_codes) . q (even dims bf16 with off =
-//    128, odd dims fp16 with off = 64, per 64-dim group, fp32 accumulate)
-//    scaled by the group scale on CUDA cores, plus the per-token bias
-//    sum_G b_G sum(q_G) - s_G sum(off q_G) from two bf16 MMAs over the raw
-//    scale/bias words; online softmax in fp32 with a lazily moving
-//    reference max; O^T += (V_codes - 4)^T
-//    . (P * s_v) with P transposed in registers by movmatrix; the value bias
-//    term sum_t p_t (b_t + 4 s_t) on CUDA cores.
+//  * consumer warps run m16n8k16 tensor-core MMAs on codes that enter as bare
+//    bit fields: a code masked in place inside a 16-bit half, with every other
+//    bit zero, is the fp16 subnormal c * 2^(L - 24) (L its bit position, at
+//    most 10 - width), so one AND per register turns packed codes into exact
+//    MMA operands and the power of two is undone once per unit.  Scores:
+//    S_G = K_codes . q_s per 64-dim group (q_s = q'' times a per-row power of
+//    two that keeps it inside fp16), folded with the group scale on CUDA cores,
+//    plus the per-token bias sum_G b_G sum(q_G) from one bf16 MMA over the raw
+//    bias words; online softmax in fp32 with a lazily moving reference max;
+//    O^T += V_codes^T . (P * s_v) with P transposed in registers by movmatrix;
+//    the value bias term sum_t p_t b_t on CUDA cores, the codes centred on
+//    3.5 by one more MMA over an all-ones operand.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -87,14 +90,34 @@ constexpr float NEG_INF = -__builtin_huge_valf();
 // uniformly, like the page's where(mask, s, finfo.min) softmax; and small
 // enough that its log2 and the running max agree to a fraction of a unit.
 constexpr float MASKED_SCORE = -1e6f;
-// Lazy running max: the reference max of a row moves only when a score exceeds
-// it by more than 2^TAU (log2 units), so p = 2^(s - m) stays below 2^TAU and
-// p * s_v stays inside fp16 for value scales below 2^(16 - TAU).
-constexpr float TAU = 6.0f;
-// Value codes enter the P.V product centred: c - VCENTRE in [-4, 3] (exact in
-// fp16), which halves the worst-case effect of rounding P * s_v to fp16; the
-// VCENTRE * s_v part joins the fp32 bias term.
-constexpr float VCENTRE = 4.0f;
+#ifndef IQ_QREG
+#define IQ_QREG 0  // 1: keep the query fragments in registers (measured slower: register spills)
+#endif
+// Lazy running max: the reference of a row moves only when a score exceeds it
+// by more than 2^tau (log2 units), so p = 2^(s - m) stays below 2^tau.  The
+// reference is kept E above the row max, where E (per warp, 0 until a value
+// scale of 2^(9 + E) or more shows up) keeps p * s_v below 2^15, inside fp16:
+// tau = TAU - E, and raising E shifts the reference (a common factor of P,
+// the row sum and the value bias, so the softmax is unchanged).
+constexpr int TAU = 6;
+constexpr int kScaleExpBase = 127 + 15 - TAU;  // bf16 exponent field of 2^(15 - TAU)
+// Queries enter the score MMAs as fp16 q_s = q'' * 2^-e with e chosen per row
+// so that max |q_s| lies in [2^14, 2^15); e is clamped to this range (rows
+// whose largest entry is below 2^-86 keep the clamp and lose low bits).
+constexpr int kQExpMin = -100, kQExpMax = 100;
+// Value code k (0..7) of a lane's 24-bit field sits at bit LPOS(k) of its
+// 16-bit window (windows start at field bits 0, 8, 16): the MMA sees
+// c * 2^(LPOS - 24), undone per output dim at the end of a unit.
+__host__ __device__ constexpr int vpos(int k) { return (0x52741630 >> (4 * k)) & 15; }
+static_assert(vpos(0) == 0 && vpos(1) == 3 && vpos(2) == 6 && vpos(3) == 1 && vpos(5) == 7 && vpos(7) == 5,
+              "3-bit field positions");
+// The P.V product multiplies codes c in [0, 7] by w_hat = fp16(p * s_v); its
+// rounding error w - w_hat weighs (c - VCENTRE) instead of c: one more MMA
+// against an all-ones operand gives sum_t w_hat exactly as the tensor core
+// saw it, VCENTRE times that is taken off, and VCENTRE * sum_t p s_v (fp32)
+// joins the bias term.
+constexpr float VCENTRE = 3.5f;
+constexpr uint32_t kOnesF16x2 = 0x3C003C00u;  // fp16 (1, 1)
 // Row of the 16-token sub-tile that MMA token slot m (0..7) reads; slot m+8
 // reads row mu(m)+8.  Chosen so the swizzled K reads and the 96-byte-pitch V
 // reads are free of shared-memory bank conflicts.
@@ -236,23 +259,17 @@ __device__ __forceinline__ float pick_bf16(uint2 v, int G) {
   return bf16_to_f32((G & 1) ? (w >> 16) : (w & 0xFFFFu));
 }
 
-// Key codes enter the q.K product without any shift: the code in the low
-// nibble of a byte (an even dim) becomes the bf16 value 128 + c (the nibble
-// ORed into the mantissa of 0x4300, whose unit step is bit 0) and the code in
-// the high nibble (an odd dim) becomes the fp16 value 64 + c (the nibble in
-// bits 4..7 of 0x5400, whose unit step is bit 4).  Even dims therefore meet
-// q'' in bf16 MMAs (q'' is a bf16 value: exact) and odd dims in fp16 MMAs
-// (q'' converted to fp16, exact for 2^-14 <= |q''| < 65504); both accumulate
-// into the same fp32 scores.  The offsets 128 sum(q''_even) + 64 sum(q''_odd)
-// are cancelled inside the per-token bias product.
-constexpr float KOFF_EVEN = 128.0f;
-constexpr float KOFF_ODD = 64.0f;
+// Key codes enter the q.K product as bare fields: the code in the low nibble
+// of a byte (an even dim) masked in place is the fp16 subnormal c * 2^-24, the
+// code in the high nibble (an odd dim) is c * 2^-20.  Every MMA multiplies
+// fp16 codes by fp16 queries (exact products, fp32 accumulation); the odd-dim
+// query operand is pre-scaled by 2^-4 so all products carry 2^-24.
 
 // The 16 codes of two consecutive words (dims 0..7 in w0, 8..15 in w1) ->
-// eight registers; register m holds the dims k_pair(m, 0..1): even m as bf16x2
-// 128 + (c_a, c_b) (even dims), odd m as fp16x2 64 + (c_a, c_b) (odd dims).
-// Two byte permutes bring the nibbles of bytes 1 and 3 down; every register is
-// then one AND-OR.
+// eight registers; register m holds the dims k_pair(m, 0..1): even m the
+// low-nibble codes (even dims), odd m the high-nibble codes (odd dims).  Two
+// byte permutes bring the nibbles of bytes 1 and 3 down; every register is
+// then one AND.
 __host__ __device__ constexpr int k_pair(int m, int h) {
   // {0,4} {1,5} {8,12} {9,13} {2,10} {3,11} {6,14} {7,15}
   return h == 0 ? (m < 4 ? (m & 1) + 8 * (m >> 1) : (m == 4 ? 2 : m == 5 ? 3 : m)) : k_pair(m, 0) + (m < 4 ? 4 : 8);
@@ -260,58 +277,47 @@ __host__ __device__ constexpr int k_pair(int m, int h) {
 static_assert(k_pair(0, 1) == 4 && k_pair(3, 0) == 9 && k_pair(3, 1) == 13 && k_pair(4, 1) == 10 &&
                   k_pair(6, 0) == 6 && k_pair(7, 1) == 15 && k_pair(2, 0) == 8,
               "register -> dim map");
-// Registers of k-step s of a 16-dim chunk: steps 0, 1 are the bf16 (even-dim)
-// MMAs over registers (0, 2) and (4, 6), steps 2, 3 the fp16 (odd-dim) MMAs
-// over (1, 3) and (5, 7); h = 0 feeds k-slots 2t, 2t+1, h = 1 slots 2t+8, 2t+9.
+// Registers of k-step s of a 16-dim chunk: steps 0, 1 are the even-dim MMAs
+// over registers (0, 2) and (4, 6), steps 2, 3 the odd-dim MMAs over (1, 3)
+// and (5, 7); h = 0 feeds k-slots 2t, 2t+1, h = 1 slots 2t+8, 2t+9.
 __host__ __device__ constexpr int kreg(int s, int h) { return s < 2 ? 4 * s + 2 * h : 4 * (s - 2) + 2 * h + 1; }
 static_assert(k_pair(kreg(0, 0), 0) % 2 == 0 && k_pair(kreg(1, 1), 1) % 2 == 0 && k_pair(kreg(2, 0), 0) % 2 == 1 &&
                   k_pair(kreg(3, 1), 1) % 2 == 1,
-              "bf16 steps hold even dims, fp16 steps odd dims");
+              "steps 0, 1 hold even dims, steps 2, 3 odd dims");
 __device__ __forceinline__ void unpack_k16(uint32_t w0, uint32_t w1, uint32_t* r) {
-  constexpr uint32_t LO_MAGIC = 0x43004300u;  // bf16 128.0 in each half
-  constexpr uint32_t HI_MAGIC = 0x54005400u;  // fp16 64.0 in each half
   constexpr uint32_t LO = 0x000F000Fu, HI = 0x00F000F0u;
   const uint32_t x = __byte_perm(w0, w1, 0x0501);  // bytes w0.b1 (nibbles 2, 3), w1.b1
   const uint32_t y = __byte_perm(w0, w1, 0x0703);  // bytes w0.b3 (nibbles 6, 7), w1.b3
-  r[0] = and_or(w0, LO, LO_MAGIC);  // (0, 4)
-  r[1] = and_or(w0, HI, HI_MAGIC);  // (1, 5)
-  r[2] = and_or(w1, LO, LO_MAGIC);  // (8, 12)
-  r[3] = and_or(w1, HI, HI_MAGIC);  // (9, 13)
-  r[4] = and_or(x, LO, LO_MAGIC);   // (2, 10)
-  r[5] = and_or(x, HI, HI_MAGIC);   // (3, 11)
-  r[6] = and_or(y, LO, LO_MAGIC);   // (6, 14)
-  r[7] = and_or(y, HI, HI_MAGIC);   // (7, 15)
+  r[0] = w0 & LO;  // (0, 4)
+  r[1] = w0 & HI;  // (1, 5)
+  r[2] = w1 & LO;  // (8, 12)
+  r[3] = w1 & HI;  // (9, 13)
+  r[4] = x & LO;   // (2, 10)
+  r[5] = x & HI;   // (3, 11)
+  r[6] = y & LO;   // (6, 14)
+  r[7] = y & HI;   // (7, 15)
 }
 
-// bf16 bits -> fp16 bits (round to nearest; exact for normal fp16 values)
-__device__ __forceinline__ uint32_t bf16_to_f16_bits(uint32_t bits16) {
-  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(bf16_to_f32(bits16))));
+// fp32 -> fp16 bits, round to nearest even (subnormal results rounded, not flushed)
+__device__ __forceinline__ uint32_t f32_to_f16_bits(float x) {
+  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x)));
 }
-
-// 3-bit code at bit `L` (0..7) of each 16-bit half of x -> fp16x2 (code - 4)
-template <int L>
-__device__ __forceinline__ uint32_t dq3(uint32_t x) {
-  constexpr uint32_t mask = 0x00070007u << L;
-  constexpr uint32_t sc = (15u - L) << 10;                          // 2^-L
-  constexpr uint32_t ng = 0x8000u | ((25u - L) << 10) | (4u << L);  // -(2^(10-L) + 4)
-  return fma_f16x2(and_or(x, mask, 0x64006400u), sc | (sc << 16), ng | (ng << 16));
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
 }
 
 // Two 24-bit fields (8 codes each; token a in fa, token b in fb) -> 8 fp16x2
-// pairs (code k of a in the low half, of b in the high half).
+// pairs (code k of a in the low half, of b in the high half), code k as the
+// bare field c * 2^(vpos(k) - 24).
 __device__ __forceinline__ void unpack_v3_pair(uint32_t fa, uint32_t fb, uint32_t* h) {
   const uint32_t x0 = __byte_perm(fa, fb, 0x5410);  // bits 0..15 of each
   const uint32_t x1 = __byte_perm(fa, fb, 0x6521);  // bits 8..23
   const uint32_t x2 = __byte_perm(fa, fb, 0x7632);  // bits 16..31
-  h[0] = dq3<0>(x0);
-  h[1] = dq3<3>(x0);
-  h[2] = dq3<6>(x0);
-  h[3] = dq3<1>(x1);
-  h[4] = dq3<4>(x1);
-  h[5] = dq3<7>(x1);
-  h[6] = dq3<2>(x2);
-  h[7] = dq3<5>(x2);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) h[k] = (k < 3 ? x0 : k < 6 ? x1 : x2) & (0x00070007u << vpos(k));
 }
+// 2^k as a float (exponent field), |k| <= 126
+__device__ __forceinline__ float exp2i(int k) { return __int_as_float((127 + k) << 23); }
 
 template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES>
 struct Cfg : Tiling<TILE_> {
@@ -346,8 +352,10 @@ struct Cfg : Tiling<TILE_> {
   static constexpr int OFF_XBUF = OFF_LBUF + STREAMS * GT * 4;
   static constexpr int XBUF_BYTES = DS > 1 ? STREAMS * 2 * 2 * DS * NT * 32 * 16 : 0;  // x2 parities x2 sub-tiles
   static constexpr int OFF_QB = OFF_XBUF + XBUF_BYTES;
-  static constexpr int QB_BYTES = DS * GPW * 4 * NT * 32 * 8;       // q'' MMA B fragments
-  static constexpr int OFF_BAR = OFF_QB + QB_BYTES;
+  static constexpr int QB_BYTES = DS * GPW * 4 * NT * 32 * 8;       // q_s MMA B fragments
+  static constexpr int OFF_RMX = OFF_QB + QB_BYTES;                  // per (row, group): max |q''| (bf16 bits)
+  static constexpr int OFF_REXP = OFF_RMX + GT * 4 * 4;              // per row: the query exponent e
+  static constexpr int OFF_BAR = (OFF_REXP + GT * 4 + 7) / 8 * 8;
   static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8 + 8;  // + the fused-append barrier
   // explicit-mask rows of a stage (the unit's queries, at most GT, x TILE keys,
   // 4-byte elements at most): the last area, part of the launch only with a mask
@@ -531,17 +539,24 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
   int qpos[NT][2];
   int qrow[NT][2];  // query index of rows 2t, 2t+1 of each n-tile (explicit masks)
   int qlo = 0;      // the unit's first query (its mask row is the stage's first)
-  // B fragments of the per-token bias product (two bf16 MMAs per n-tile):
-  // k-slots [b_0..b_3, s_0..s_3, b_0..b_3, s_0..s_3] of a key row against
-  // [S_hi, -F_hi, S_mid, -F_mid] and [S_lo, -F_lo, 0, 0], S_G = sum of q''
-  // over group G for this lane's query row and F_G = sum of off * q'' (the
-  // code offsets' share), each split into three bf16 parts that add up to it
-  // exactly
-  uint32_t kbq[NT][2][2];
+  // B fragments of the per-token bias product (one bf16 MMA per n-tile):
+  // k-slots [b_0..b_3, b_0..b_3, b_0..b_3, 0 x 4] of a key row against
+  // [S_hi, S_mid, S_lo, 0], S_G = 2^-24 * sum of q_s over group G for this
+  // lane's query row, split into three bf16 parts that add up to it exactly
+  uint32_t kbq[NT][2];
+  float kmul[NT][2];  // per row: log2(e) * 2^(24 + e), raw score -> log2 units
   float O[GPW][4][NT][4];
   float bacc[GPW][NT][2];
+  float wsum[GPW][NT][4];
+#if IQ_QREG
+  uint2 qreg[GPW][4][NT];  // this warp's q_s MMA B fragments (from shared memory, once per unit)
+#endif  // sum of w_hat per (group, query row) (rows g, g+8 alike)
   float msc[NT][2], lrow[NT][2];  // reference max (log2 units), partial row sum
   int xpar = 0;
+  int E = 0;  // value-scale shift of the reference (see TAU)
+  float* rmx = reinterpret_cast<float*>(smem + C::OFF_RMX);
+  int* rexp = reinterpret_cast<int*>(smem + C::OFF_REXP);
+  static_assert(NT * 4 <= CW, "one query item (n-tile, group) per consumer warp");
 
   // ---- start unit u: rotate and scale its queries, load the MMA fragments, reset the state
   auto begin_unit = [&](int u) {
@@ -556,22 +571,25 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     qmin = MASKED ? -1 : p.causal ? T - p.nq + (qt * GT) / p.rep : T - 1;
     qlo = (qt * GT) / p.rep;
     named_bar(bar_all, NCT);  // every consumer is done with the previous unit's fragments and sums
-    // q' = bf16(q @ M_b), q'' = bf16(q' * scale), written straight into the fp16
-    // MMA B fragments in shared memory, [dim group][k-step][n-tile][lane].  Item
-    // (n-tile j, group G) goes to one warp; its thread (g, t) rotates row 8j+g,
-    // dims 64G+16t .. +15 (rotation blocks 16G+4t .. +3), whose register m
-    // holds the dims k_pair(m, 0..1); k-step s uses registers 2s (slots 2t,
-    // 2t+1) and 2s+1.  An item's global loads are issued together.  Rows
-    // r <-> (query R/rep, head R%rep); rows past the queries are zero.
-    for (int item = cw; item < NT * 4; item += CW) {
-      const int j = item >> 2, G = item & 3;
-      const int R = qt * GT + 8 * j + g, i = R / p.rep, hr = R % p.rep;
-      uint32_t yb[16];  // q'' (bf16 bits) of the thread's 16 dims
+    // q' = bf16(q @ M_b), q'' = bf16(q' * scale).  Item (n-tile j, group G)
+    // goes to one warp; its thread (g, t) rotates row 8j+g, dims 64G+16t ..
+    // +15 (rotation blocks 16G+4t .. +3), whose register m holds the dims
+    // k_pair(m, 0..1); k-step s uses registers 2s (slots 2t, 2t+1) and 2s+1.
+    // Rows r <-> (query R/rep, head R%rep); rows past the queries are zero.
+    // Phase 1: q'' and the row's largest magnitude (per group, in shared
+    // memory); phase 2: the row exponent e and the fp16 fragments of
+    // q_s = q'' * 2^-e ([dim group][k-step][n-tile][lane] in shared memory).
+    const int item = cw;
+    const bool has_item = item < NT * 4;
+    const int j_it = item >> 2, G_it = item & 3;
+    uint32_t yb[16];  // q'' (bf16 bits) of the thread's 16 dims
+    if (has_item) {
+      const int R = qt * GT + 8 * j_it + g, i = R / p.rep, hr = R % p.rep;
       if (i < p.nq) {
         const long long qrow =
             (static_cast<long long>(b) * p.kv_heads * p.rep + kvh * p.rep + hr) * p.nq + i;
-        const uint4* qv = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim + 64 * G + 16 * t);
-        const uint4* rv = reinterpret_cast<const uint4*>(p.rot + (16 * G + 4 * t) * 16);
+        const uint4* qv = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim + 64 * G_it + 16 * t);
+        const uint4* rv = reinterpret_cast<const uint4*>(p.rot + (16 * G_it + 4 * t) * 16);
         uint4 qw4[2], mw4[8];
 #pragma unroll
         for (int c = 0; c < 2; ++c) qw4[c] = __ldg(qv + c);
@@ -604,13 +622,29 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
         for (int d = 0; d < 16; ++d) yb[d] = 0u;
       }
-      // sums of the operand values the MMAs multiply: even dims as bf16 (q''
-      // itself), odd dims as fp16
-      float qe = 0.f, qo = 0.f;
+      uint32_t mx = 0;  // largest |q''| as bf16 bits (monotonic in the magnitude)
 #pragma unroll
-      for (int d = 0; d < 16; d += 2) {
-        qe += bf16_to_f32(yb[d]);
-        qo += __half2float(__ushort_as_half(static_cast<unsigned short>(bf16_to_f16_bits(yb[d + 1]))));
+      for (int d = 0; d < 16; ++d) mx = max(mx, yb[d] & 0x7FFFu);
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      if (t == 0) reinterpret_cast<uint32_t*>(rmx)[(8 * j_it + g) * 4 + G_it] = mx;
+    }
+    named_bar(bar_all, NCT);  // every row's group maxima stored
+    if (has_item) {
+      const int row = 8 * j_it + g;
+      const uint32_t* rm = reinterpret_cast<const uint32_t*>(rmx) + row * 4;
+      const uint32_t mx = max(max(rm[0], rm[1]), max(rm[2], rm[3]));
+      // e: max |q''| in [2^(e+14), 2^(e+15)); a zero row keeps e = 0
+      int e = mx == 0 ? 0 : static_cast<int>(max(mx >> 7, 1u)) - 127 - 14;
+      e = min(max(e, kQExpMin), kQExpMax);
+      const float down = exp2i(-e), down16 = exp2i(-e - 4);
+      uint32_t hb[16];  // the fp16 operand of each dim (odd dims carry an extra 2^-4)
+      float qs = 0.f;   // sum of the operand values at one scale (2^-e q'')
+#pragma unroll
+      for (int d = 0; d < 16; ++d) {
+        const float v = bf16_to_f32(yb[d]);
+        hb[d] = f32_to_f16_bits(__fmul_rn(v, (d & 1) ? down16 : down));
+        qs += (d & 1) ? 16.0f * f16_bits_to_f32(hb[d]) : f16_bits_to_f32(hb[d]);
       }
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
@@ -618,25 +652,22 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int m = kreg(s, h);
-          h2[h] = s < 2 ? (yb[k_pair(m, 0)] | (yb[k_pair(m, 1)] << 16))
-                        : (bf16_to_f16_bits(yb[k_pair(m, 0)]) | (bf16_to_f16_bits(yb[k_pair(m, 1)]) << 16));
+          h2[h] = hb[k_pair(m, 0)] | (hb[k_pair(m, 1)] << 16);
         }
-        qbs[((G * 4 + s) * NT + j) * 32 + lane] = make_uint2(h2[0], h2[1]);
+        qbs[((G_it * 4 + s) * NT + j_it) * 32 + lane] = make_uint2(h2[0], h2[1]);
       }
-#pragma unroll
-      for (int o = 1; o < 4; o <<= 1) {
-        qe += __shfl_xor_sync(0xffffffffu, qe, o);
-        qo += __shfl_xor_sync(0xffffffffu, qo, o);
-      }
-      if (t == 0) {  // sum(q''_G) for the bias, and the code offsets' share
-        qsum[((8 * j + g) * 4 + G) * 2] = qe + qo;
-        qsum[((8 * j + g) * 4 + G) * 2 + 1] = fmaf(KOFF_EVEN, qe, KOFF_ODD * qo);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+      if (t == 0) {
+        qsum[row * 4 + G_it] = qs;
+        if (G_it == 0) rexp[row] = e;
       }
     }
-    named_bar(bar_all, NCT);  // fragments and sums visible to every warp
-    // this lane's k-slots: 2t, 2t+1 (and 2t+8, 2t+9) = groups 2(t&1), 2(t&1)+1
-    // of b (t < 2, against S_G) or of s (t >= 2, against -F_G); groups another warp of the
-    // stream owns contribute there instead
+    named_bar(bar_all, NCT);  // fragments, sums and exponents visible to every warp
+    // this lane's k-slots: 2t, 2t+1 = groups 2(t&1), 2(t&1)+1 of part t>>1
+    // (hi for t < 2, mid for t >= 2); slots 2t+8, 2t+9 = the same groups' lo
+    // part (t < 2) or nothing; groups another warp of the stream owns
+    // contribute there instead
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       uint32_t parts[3] = {0u, 0u, 0u};  // bf16x2 of (group 2(t&1), group 2(t&1)+1) per part
@@ -644,7 +675,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       for (int h = 0; h < 2; ++h) {
         const int G = 2 * (t & 1) + h;
         const bool mine = G >= dg * GPW && G < dg * GPW + GPW;
-        float x = mine ? (t < 2 ? qsum[((8 * j + g) * 4 + G) * 2] : -qsum[((8 * j + g) * 4 + G) * 2 + 1]) : 0.0f;
+        float x = mine ? qsum[(8 * j + g) * 4 + G] * 0x1p-24f : 0.0f;
 #pragma unroll
         for (int k = 0; k < 3; ++k) {  // x = hi + mid + lo exactly (each a bf16)
           const uint32_t bits = f32_to_bf16_bits(x);
@@ -652,10 +683,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
           x -= bf16_to_f32(bits);
         }
       }
-      kbq[j][0][0] = parts[0];
-      kbq[j][0][1] = parts[1];
-      kbq[j][1][0] = parts[2];
-      kbq[j][1][1] = 0u;
+      kbq[j][0] = t < 2 ? parts[0] : parts[1];
+      kbq[j][1] = t < 2 ? parts[2] : 0u;
     }
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -665,12 +694,14 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         const int i = min(R / p.rep, p.nq - 1);
         qpos[j][e] = p.causal ? T - p.nq + i : T - 1;
         qrow[j][e] = i;
+        kmul[j][e] = LOG2E * exp2i(24 + rexp[8 * j + 2 * t + e]);
       }
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi)
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         bacc[gi][j][0] = bacc[gi][j][1] = 0.f;
+        wsum[gi][j][0] = wsum[gi][j][1] = wsum[gi][j][2] = wsum[gi][j][3] = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) O[gi][i][j][0] = O[gi][i][j][1] = O[gi][i][j][2] = O[gi][i][j][3] = 0.f;
       }
@@ -679,6 +710,15 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       msc[j][0] = msc[j][1] = NEG_INF;
       lrow[j][0] = lrow[j][1] = 0.f;
     }
+    E = 0;
+#if IQ_QREG
+#pragma unroll
+    for (int gi = 0; gi < GPW; ++gi)
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) qreg[gi][s][j] = qbs[(((dg * GPW + gi) * 4 + s) * NT + j) * 32 + lane];
+#endif
   };
 
   // ---- N (1 or 2) of this warp's 16-token sub-tiles of one stage, processed
@@ -693,9 +733,9 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     int rr0[N], rr1[N];
     uint2 ksc0[N], ksc1[N];
     float sc[N][NT][4];
-    // per-token bias: sum_G (b_G - 64 s_G) sum(q''_G), by two bf16 MMAs whose A
-    // operand is the raw bias/scale words of the two token rows
-    const uint32_t bs_off = (t < 2 ? OFF_KB : OFF_KS) + (t & 1) * 4;
+    // per-token bias: sum_G b_G S_G, by one bf16 MMA whose A operand is the
+    // raw bias words of the two token rows
+    const uint32_t bs_off = OFF_KB + (t & 1) * 4;
 #pragma unroll
     for (int n = 0; n < N; ++n) {
       rr0[n] = subs[n] * 16 + rS0;
@@ -707,12 +747,11 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         sc[n][j][0] = sc[n][j][1] = sc[n][j][2] = sc[n][j][3] = 0.f;
-        mma_bf16(sc[n][j], A, kbq[j][0][0], kbq[j][0][1]);
-        mma_bf16(sc[n][j], A, kbq[j][1][0], kbq[j][1][1]);
+        mma_bf16(sc[n][j], A, kbq[j][0], kbq[j][1]);
       }
     }
 
-    // scores: per group, S_G = (off + codes) . q'' (fp32), added as s_G * S_G
+    // scores: per group, S_G = codes . q_s (fp32), added as s_G * S_G
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
       const int Gr = dg * GPW + gi;
@@ -735,14 +774,15 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       for (int s = 0; s < 4; ++s)
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
+#if IQ_QREG
+          const uint2 bq = qreg[gi][s][j];
+#else
           const uint2 bq = qbs[((Gr * 4 + s) * NT + j) * 32 + lane];
+#endif
 #pragma unroll
           for (int n = 0; n < N; ++n) {
             const uint32_t A[4] = {RA[n][kreg(s, 0)], RB[n][kreg(s, 0)], RA[n][kreg(s, 1)], RB[n][kreg(s, 1)]};
-            if (s < 2)
-              mma_bf16(acc[n][j], A, bq.x, bq.y);
-            else
-              mma_f16(acc[n][j], A, bq.x, bq.y);
+            mma_f16(acc[n][j], A, bq.x, bq.y);
           }
         }
 #pragma unroll
@@ -780,62 +820,116 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       xpar ^= 1;
     }
 
-    // mask (ragged tail, causal): only on sub-tiles that need it
+    // value scales and biases of the two token rows (the scale test below
+    // reads the scales before the softmax)
+    uint2 vsc0[N], vsc1[N], vbi0[N], vbi1[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      vsc0[n] = lds64(sb + OFF_VS + rr0[n] * 8);
+      vsc1[n] = lds64(sb + OFF_VS + rr1[n] * 8);
+      vbi0[n] = lds64(sb + OFF_VB + rr0[n] * 8);
+      vbi1[n] = lds64(sb + OFF_VB + rr1[n] * 8);
+    }
+
+    // scores in log2 units relative to the row reference: x = y - m, with
+    // y = raw * kmul (masked entries -inf, explicit masks applied to y)
     bool valid[N][NT][4];
-    if constexpr (!FULL) {
+    float x[N][NT][4];
+    float ysv[N][NT][4];  // y itself (used by the masked sub-tiles' slow path)
+    bool in_tok[N][2];
 #pragma unroll
-      for (int n = 0; n < N; ++n) {
-        const int tok0 = tokbase[n] + rS0, tok1 = tok0 + 8;
-        const bool in0 = tok0 < limit, in1 = tok1 < limit;
+    for (int n = 0; n < N; ++n) {
+      const int tok0 = tokbase[n] + rS0, tok1 = tok0 + 8;
+      in_tok[n][0] = FULL || tok0 < limit;
+      in_tok[n][1] = FULL || tok1 < limit;
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          valid[n][j][0] = in0 && tok0 <= qpos[j][0];
-          valid[n][j][1] = in0 && tok0 <= qpos[j][1];
-          valid[n][j][2] = in1 && tok1 <= qpos[j][0];
-          valid[n][j][3] = in1 && tok1 <= qpos[j][1];
-          if constexpr (MASKED) {  // explicit mask (staged with the tile): added, or masked
+      for (int j = 0; j < NT; ++j) {
+        if constexpr (FULL) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (!valid[n][j][e]) continue;
-              const int mi = (qrow[j][e & 1] - qlo) * TILE + subs[n] * 16 + rS0 + (e < 2 ? 0 : 8);
-              if (p.mask_kind == 2)
-                sc[n][j][e] += __uint_as_float(lds32(msk + mi * 4));
-              else if (lds8(msk + mi) == 0)
-                sc[n][j][e] = MASKED_SCORE;
+          for (int e = 0; e < 4; ++e) x[n][j][e] = fmaf(sc[n][j][e], kmul[j][e & 1], -msc[j][e & 1]);
+        } else {
+          valid[n][j][0] = in_tok[n][0] && tok0 <= qpos[j][0];
+          valid[n][j][1] = in_tok[n][0] && tok0 <= qpos[j][1];
+          valid[n][j][2] = in_tok[n][1] && tok1 <= qpos[j][0];
+          valid[n][j][3] = in_tok[n][1] && tok1 <= qpos[j][1];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float y = sc[n][j][e] * kmul[j][e & 1];
+            if constexpr (MASKED) {  // explicit mask (staged with the tile): added, or masked
+              if (valid[n][j][e]) {
+                const int mi = (qrow[j][e & 1] - qlo) * TILE + subs[n] * 16 + rS0 + (e < 2 ? 0 : 8);
+                if (p.mask_kind == 2)
+                  y = fmaf(__uint_as_float(lds32(msk + mi * 4)), LOG2E, y);
+                else if (lds8(msk + mi) == 0)
+                  y = MASKED_SCORE * LOG2E;
+              }
             }
+            y = valid[n][j][e] ? y : NEG_INF;
+            ysv[n][j][e] = y;
+            x[n][j][e] = y - msc[j][e & 1];
           }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sc[n][j][e] = valid[n][j][e] ? sc[n][j][e] : NEG_INF;
         }
       }
     }
-
-    // online softmax with a lazily moving reference max (one vote for the N sub-tiles)
-    float x[N][NT][4];
+    // lazy max: a row moves its reference only when a score passes it by
+    // 2^tau; the value-scale test: a scale at or above 2^(9 + E) raises E
+    const float tau = static_cast<float>(TAU - E);
     bool trig = false;
 #pragma unroll
     for (int n = 0; n < N; ++n)
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          x[n][j][e] = fmaf(sc[n][j][e], LOG2E, -msc[j][e & 1]);
-          trig |= !(x[n][j][e] <= TAU);
+        for (int e = 0; e < 4; ++e) trig |= !(x[n][j][e] <= tau);
+    const uint32_t thr = static_cast<uint32_t>(min(kScaleExpBase + E, 255)) << 7;
+    const uint32_t addc = (0x8000u - thr) * 0x10001u;  // bit 15 of a half set iff the half >= thr
+    uint32_t over = 0;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      const uint2 a = in_tok[n][0] ? vsc0[n] : make_uint2(0u, 0u);
+      const uint2 c = in_tok[n][1] ? vsc1[n] : make_uint2(0u, 0u);
+      over |= (a.x + addc) | (a.y + addc) | (c.x + addc) | (c.y + addc);
+    }
+    const bool strig = (over & 0x80008000u) != 0;
+    if (__any_sync(0xffffffffu, trig || strig)) {
+      int dE = 0;
+      if (__any_sync(0xffffffffu, strig)) {  // largest valid scale (bf16 bits: monotonic) over the warp
+        uint32_t hm = 0;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+          const uint2 a = in_tok[n][0] ? vsc0[n] : make_uint2(0u, 0u);
+          const uint2 c = in_tok[n][1] ? vsc1[n] : make_uint2(0u, 0u);
+          const uint32_t w4[4] = {a.x, a.y, c.x, c.y};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) hm = max(hm, max(w4[q] & 0xFFFFu, w4[q] >> 16));
         }
-    if (__any_sync(0xffffffffu, trig)) {
+        hm = __reduce_max_sync(0xffffffffu, hm);
+        // smallest E with hm < 2^(9 + E), i.e. (hm >> 7) < kScaleExpBase + E
+        const int En = min(max(E, static_cast<int>(hm >> 7) - kScaleExpBase + 1), 255 - kScaleExpBase);
+        dE = En - E;
+        E = En;
+      }
       float alpha[NT][2];
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          float mx = fmaxf(sc[0][j][e], sc[0][j][e + 2]);
+          float mx = NEG_INF;
 #pragma unroll
-          for (int n = 1; n < N; ++n) mx = fmaxf(mx, fmaxf(sc[n][j][e], sc[n][j][e + 2]));
+          for (int n = 0; n < N; ++n)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int ee = e + 2 * h;
+              const float y = FULL ? sc[n][j][ee] * kmul[j][e] : ysv[n][j][ee];
+              mx = fmaxf(mx, y);
+            }
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mnew = fmaxf(msc[j][e], mx * LOG2E);
-          alpha[j][e] = mnew == NEG_INF ? 1.f : ex2_approx(msc[j][e] - mnew);
+          const float mold = msc[j][e];
+          // the reference sits E above the row max, and a raised E shifts it
+          const float mnew = fmaxf(mold + static_cast<float>(dE), mx + static_cast<float>(E));
+          alpha[j][e] = mnew == NEG_INF ? 1.f : ex2_approx(mold - mnew);
           msc[j][e] = mnew;
         }
 #pragma unroll
@@ -846,6 +940,10 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         for (int gi = 0; gi < GPW; ++gi) {
           bacc[gi][j][0] *= alpha[j][0];
           bacc[gi][j][1] *= alpha[j][1];
+          wsum[gi][j][0] *= alpha[j][0];
+          wsum[gi][j][2] *= alpha[j][0];
+          wsum[gi][j][1] *= alpha[j][1];
+          wsum[gi][j][3] *= alpha[j][1];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             O[gi][i][j][0] *= alpha[j][0];
@@ -859,7 +957,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float m = msc[j][e & 1];
-            x[n][j][e] = fmaf(sc[n][j][e], LOG2E, m == NEG_INF ? 0.f : -m);
+            const float y = FULL ? sc[n][j][e] * kmul[j][e & 1] : ysv[n][j][e];
+            x[n][j][e] = y - (m == NEG_INF ? 0.f : m);
           }
       }
     }
@@ -874,15 +973,10 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         lrow[j][1] += pr[n][j][1] + pr[n][j][3];
       }
 
-    // values: O^T += (V_codes - 4)^T . (P * s_v); bias term on CUDA cores
-    uint2 vsc0[N], vsc1[N], vbi0[N], vbi1[N];
+    // values: O^T += V_codes^T . (P * s_v) (codes as bare fields); bias term on CUDA cores
     uint32_t vrow[N][4];
 #pragma unroll
     for (int n = 0; n < N; ++n) {
-      vsc0[n] = lds64(sb + OFF_VS + rr0[n] * 8);
-      vsc1[n] = lds64(sb + OFF_VS + rr1[n] * 8);
-      vbi0[n] = lds64(sb + OFF_VB + rr0[n] * 8);
-      vbi1[n] = lds64(sb + OFF_VB + rr1[n] * 8);
       vrow[n][0] = sb + OFF_V + (subs[n] * 16 + rV0) * 96;
       vrow[n][1] = sb + OFF_V + (subs[n] * 16 + rV1) * 96;
       vrow[n][2] = vrow[n][0] + 8 * 96;
@@ -916,6 +1010,8 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
           }
           bp[j][0] = movmatrix_trans(pack_f16x2(q0, q1));
           bp[j][1] = movmatrix_trans(pack_f16x2(q2, q3));
+          const uint32_t ones[4] = {kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2};
+          mma_f16(wsum[gi][j], ones, bp[j][0], bp[j][1]);
         }
         uint32_t f[4];
 #pragma unroll
@@ -959,9 +1055,11 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
           bs += __shfl_xor_sync(0xffffffffu, bs, 8);
           bs += __shfl_xor_sync(0xffffffffu, bs, 16);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            O[gi][i][j][e] += bs;
-            O[gi][i][j][e + 2] += bs;
+          bs = fmaf(-VCENTRE, wsum[gi][j][e], bs);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {  // undo the field positions of the value codes (exact powers of two)
+            O[gi][i][j][e] = fmaf(O[gi][i][j][e], exp2i(24 - vpos(2 * i)), bs);
+            O[gi][i][j][e + 2] = fmaf(O[gi][i][j][e + 2], exp2i(24 - vpos(2 * i + 1)), bs);
           }
         }
       }

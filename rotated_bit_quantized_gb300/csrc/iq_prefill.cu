@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const int gi = db >> 3;  // 64-dim group
         const int w0 = (3 * db) >> 2, sh = (24 * db) & 31;
         float v[8][8];  // [key][dim]
+        float vmax = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int t = 8 * tb + k;
@@ -340,9 +341,15 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           const float s = bf16_to_f32(vs[gi]), bb = bf16_to_f32(vb[gi]);
           const bool stale = i * KT + t >= T;  // rows past the length may hold anything: P is 0 there, and 0 * NaN is not
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
+          for (int e = 0; e < 8; ++e) {
             v[k][e] = stale ? 0.f : fmaf(s, __uint_as_float(0x4B000000u | ((f >> (3 * e)) & 7u)) - 8388608.0f, bb);
+            vmax = fmaxf(vmax, fabsf(v[k][e]));
+          }
         }
+        // dequantised values enter the P.V product as fp16: a value at or above
+        // 2^15 in magnitude (a value group spanning more than about 3e4) is
+        // outside what this kernel serves and is reported (status bit 16)
+        if (!(vmax < 32768.f)) atomicOr(p.status, 16u);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int d = 8 * db + e;
@@ -366,11 +373,29 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     const int qi = live ? R / p.rep : 0, hr = live ? R % p.rep : 0;
     const int qpos = live ? (p.causal ? T - p.nq + qi : T - 1) : -1;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-    // q'' = bf16(bf16(q @ M_b) * scale) as fp16, and its per-group sums
+    // q'' = bf16(bf16(q @ M_b) * scale), entering the MMA as the fp16 q_s =
+    // q'' * 2^-e, and its per-group sums.  The rotation keeps every |q''|
+    // below 2.03 * max|q| * |scale| (a row of M_b has an L1 norm of at most
+    // 2, plus bf16 rounding), so with max|q| * |scale| in [2^E0, 2^(E0+1))
+    // e = E0 - 12 puts |q_s| below 2^15 (fp16) and its largest entry above 2^8.
     float qs[4] = {0.f, 0.f, 0.f, 0.f};
+    float kmul = LOG2E;  // raw score -> log2 units: log2(e) * 2^e
     {
       const uint16_t* qrow =
           p.q + ((static_cast<long long>(b) * p.kv_heads * p.rep + h * p.rep + hr) * p.nq + qi) * kHeadDim;
+      uint32_t amax = 0;  // largest |q| as bf16 bits (monotonic in the magnitude)
+      if (live)
+        for (int c = 0; c < 32; ++c) {
+          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c));
+          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) amax = max(amax, max(rw[j] & 0x7FFFu, (rw[j] >> 16) & 0x7FFFu));
+        }
+      const float m = bf16_to_f32(amax) * fabsf(p.scale);
+      int e = 0;
+      if (m > 0.f) e = min(max(static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127 - 12, -100), 100);
+      const float down = __int_as_float((127 - e) << 23);
+      kmul = LOG2E * __int_as_float((127 + e) << 23);
       for (int c = 0; c < 32; ++c) {  // 8-dim chunk c: rotation blocks 2c, 2c+1
         uint4 raw = make_uint4(0, 0, 0, 0);
         if (live) raw = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c));
@@ -390,7 +415,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             float a = __fmul_rn(x[0], bf16_to_f32(__ldg(mb + j)));
 #pragma unroll
             for (int k = 1; k < 4; ++k) a = __fadd_rn(a, __fmul_rn(x[k], bf16_to_f32(__ldg(mb + 4 * k + j))));
-            y[j] = round_bf16(__fmul_rn(round_bf16(a), p.scale));
+            y[j] = __fmul_rn(round_bf16(__fmul_rn(round_bf16(a), p.scale)), down);  // exact: a power of two
           }
           const uint32_t h0 = pack_h2(y[0], y[1]), h1 = pack_h2(y[2], y[3]);
           hv[2 * blk] = h0;
@@ -448,7 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             sv = fmaf(kb.y, qs[1], sv);
             sv = fmaf(kb.z, qs[2], sv);
             sv = fmaf(kb.w, qs[3], sv);
-            x[k] = t <= qpos ? sv * LOG2E : NEG;
+            x[k] = t <= qpos ? sv * kmul : NEG;
           }
         }
         float mx = NEG;
