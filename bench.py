@@ -44,8 +44,8 @@ def row_bytes(bits: int, group_size: int) -> int:
 
 # DRAM bytes (read + write) per iq_attend call on the default workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of attend_kernel and
-# combine_kernel; profiles/attend_kernel_batched_decode_32x32k.md).  Reported
-# only while the attention source is the one that was measured.
+# combine_kernel).  Reported only while the attention source is the one that
+# was measured.
 TRAFFIC = {"source": "rotated_bit_quantized_gb300/csrc/iq_attend.cu",
            "sha256": "2b7ca3d2548851f30d5eb2bacaf1bd95a5138ceba7fa4ea3b93b7efeffcee44b",
            "bytes": ((539.385088 + 2.981632 + 2.929664) + (539.400960 + 0.520960 + 2.928896)) / 2 * 1e6}
@@ -195,6 +195,13 @@ def make_workload(wid: int, steps_total: int, dev, batch: int | None = None, fmt
     return w, rot, cache, steps
 
 
+def preroll(dev, steps: int, per_step_s: float = 250e-6) -> None:
+    """Keep the GPU busy (a spin kernel on the current stream) while the host
+    queues the timed steps, so the region measures the device, not the host's
+    first launches; the spin itself runs before the start event."""
+    torch.cuda._sleep(int(2.1e9 * (1e-3 + per_step_s * steps)))
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -260,17 +267,28 @@ def run_ours(args):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
+    region_ms = []
     with ClockSampler(gpu_index) as clk:
         time.sleep(0.25)
         # timed region: K whole steps, events only at its ends (an event between
         # the append and the attention would stop the attention grid's launch
-        # from overlapping the append)
-        start.record(stream)
-        for i in range(K):
-            tokens += int(cache.lens.sum()) + B * w["append"]
-            step(W + i)
-        stop.record(stream)
-        torch.cuda.synchronize(dev)
+        # from overlapping the append); repeated from the same cache state and
+        # the median taken
+        for r in range(args.repeats):
+            cache.trim(cache.lens - base_len)
+            torch.cuda.synchronize(dev)
+            if ws > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize(dev)
+            preroll(dev, K)
+            start.record(stream)
+            tokens = 0
+            for i in range(K):
+                tokens += int(cache.lens.sum()) + B * w["append"]
+                step(W + i)
+            stop.record(stream)
+            torch.cuda.synchronize(dev)
+            region_ms.append(start.elapsed_time(stop))
         # the same K steps again from the same cache state, with events around
         # every iq_attend call: the attention call's own duration (roofline)
         cache.trim(cache.lens - base_len)
@@ -283,7 +301,7 @@ def run_ours(args):
         while time.time() - extra_t0 < 0.6:
             cache.attend(dsteps[W + K - 1][2], rot, causal=w["causal"], out=out)
             torch.cuda.synchronize(dev)
-    ms = start.elapsed_time(stop)
+    ms = statistics.median(region_ms)
     attn_ms = [a.elapsed_time(bq) for a, bq in attn_ev]
     status = cache.device_status()
     ms_max, tokens_all = reduce_across_ranks(ms, tokens, dev)
@@ -338,10 +356,23 @@ def run_ours(args):
         cpu = None if args.no_cpu_baseline else cpu_baseline_sample(args.workload, budget_s=args.cpu_seconds,
                                                                     one_core_s=args.cpu_one_core_seconds)
         append = append_throughput(dev, rot)
+        append.append(append_decode_record(dev, rot))
+        extra = {}
+        if not args.no_sub_records and fmt == (4, 3, 64) and mask is None and args.workload == 4:
+            del dsteps, steps, cache  # free the decode cache before the verify workload's
+            torch.cuda.empty_cache()
+            extra["single_stream"] = single_stream_record(dev, rot)
+            extra["verify"] = verify_record(dev, rot, hbm)
+            extra["prefill"] = prefill_record(dev, rot)
         rec = {
             "metric": METRIC, "value": tokens_all / (ms_max / 1e3), "unit": UNIT, "n_gpus": ws,
             "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "repeats": {"n": len(region_ms), "ms_per_step_min": min(region_ms) / K,
+                        "ms_per_step_max": max(region_ms) / K,
+                        "how": "the K-step region timed n times from the same cache state; value and "
+                               "ms_per_step from the median region"},
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 in/out, fp32 accumulate (fp16/bf16 tensor-core operands)",
             "data": "synthetic (seeded N(0,1); keys with x20 outlier channels)",
             "config": {"workload": f"{w['name']}: B={B} seqs, Hq={Hq}/Hkv={Hkv}, head_dim=256, "
                                    f"{w['prefill']}-token K{fmt[0]}/V{fmt[1]} cache (groups of {fmt[2]}), "
@@ -364,7 +395,8 @@ def run_ours(args):
                          "bytes_per_call": call_bytes, "avg_launch_us": call_s * 1e6,
                          "timing": "CUDA events at the two ends of the timed region over its K calls (each "
                                    "call's attention grid starts streaming while the previous call's grids "
-                                   "finish)",
+                                   "finish); a spin kernel ahead of the start event lets the host queue the "
+                                   "steps first",
                          "isolated_call_us": attn_avg_s * 1e6,
                          "isolated_frac": call_bytes / attn_avg_s / 1e9 / hbm,
                          "isolated_timing": "CUDA events around every call in a second pass over the same K "
@@ -377,6 +409,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "append": append,
         }
+        rec.update(extra)
         print(json.dumps(rec), flush=True)
     if ws > 1:
         torch.distributed.barrier()
@@ -415,6 +448,160 @@ def append_throughput(dev, rot, reps: int = 10):
                     "gbs": th * (4 * 256 + K_ROW + V_ROW) / sec / 1e9, "us_per_call": sec * 1e6,
                     "bytes_per_token_head": 4 * 256 + K_ROW + V_ROW})
     return res
+
+
+def append_decode_record(dev, rot, reps: int = 50):
+    """The append kernel alone at n = 1 (the decode step's append when it does
+    not fuse): 32 sequences x 2 kv heads, one token each, CUDA events around
+    `reps` back-to-back calls, each undone by a host trim."""
+    from rotated_bit_quantized_gb300 import IQCache
+    w = si.WORKLOADS[4]
+    B, H = w["B"], w["Hkv"]
+    cache = IQCache(B, H, device=dev, capacity=512)
+    k, v = si.kv_tokens(w["seed"], B, H, 1, outliers=True, step=0)
+    k, v = k.to(dev), v.to(dev)
+    for _ in range(5):
+        cache.append(k, v, rot)
+        cache.trim(1)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    preroll(dev, reps, 60e-6)
+    e0.record(stream)
+    for _ in range(reps):
+        cache.append(k, v, rot)
+        cache.trim(1)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = e0.elapsed_time(e1) / 1e3 / reps
+    th = B * H
+    return {"workload": f"batched_decode append: B={B} x {H} kv heads x 1 token per call",
+            "appended_tokens_per_s": B / sec, "token_heads_per_s": th / sec,
+            "gbs": th * (4 * 256 + K_ROW + V_ROW) / sec / 1e9, "us_per_call": sec * 1e6,
+            "bytes_per_token_head": 4 * 256 + K_ROW + V_ROW}
+
+
+def single_stream_record(dev, rot, reps: int = 200):
+    """Single-stream decode (1 sequence, 16/2 heads, 4096-token cache, one
+    query): microseconds per attention call, back to back (events at the ends
+    of `reps` calls) and isolated (events around each call)."""
+    from rotated_bit_quantized_gb300 import IQCache
+    w = si.WORKLOADS[2]
+    B, H, Hq = w["B"], w["Hkv"], w["Hq"]
+    cache = IQCache(B, H, device=dev, capacity=w["prefill"] + 256)
+    k, v = si.kv_tokens(w["seed"], B, H, w["prefill"], outliers=True)
+    cache.append(k.to(dev), v.to(dev), rot)
+    q = si.queries(w["seed"], B, Hq, 1).to(dev)
+    out = torch.empty((B, Hq, 1, 256), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(10):
+        cache.attend(q, rot, out=out)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    preroll(dev, reps, 60e-6)
+    e0.record(stream)
+    for _ in range(reps):
+        cache.attend(q, rot, out=out)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    iso = []
+    for _ in range(50):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        cache.attend(q, rot, out=out)
+        b.record(stream)
+        iso.append((a, b))
+    torch.cuda.synchronize(dev)
+    iso_us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in iso)
+    th = B * H * w["prefill"]
+    return {"workload": f"single_stream_decode: B={B}, Hq={Hq}/Hkv={H}, {w['prefill']}-token cache, one query",
+            "us_per_call": us, "isolated_us_per_call": iso_us, "kv_tokens_per_s": B * w["prefill"] / (us / 1e6),
+            "bytes_per_call": th * (K_ROW + V_ROW), "gbs": th * (K_ROW + V_ROW) / (us / 1e6) / 1e9,
+            "bound": "launch latency (2.1 MB per call)", "device_status": cache.device_status()}
+
+
+def verify_record(dev, rot, hbm: float, steps: int = 16, warmup: int = 3):
+    """Speculative verify (8 sequences, 131072-token caches, 16/2 heads): per
+    step append 4 draft tokens, attend 4 causal queries, trim the rejected
+    suffix (accepted lengths from the seeded draw).  Events at the two ends of
+    the timed steps; KV tokens scanned per second and the HBM fraction of the
+    scanned bytes (256 B per token-head) plus the append."""
+    w = si.WORKLOADS[5]
+    _, _, cache, steps_in = make_workload(5, warmup + steps, dev)
+    B, H, Hq, L = w["B"], w["Hkv"], w["Hq"], w["queries"]
+    base = cache.lens.copy()
+    dsteps = [(k.to(dev), v.to(dev), q.to(dev)) for k, v, q in steps_in]
+    acc = si.accepted_lengths(warmup + steps, B, w["append"], w["accept_seed"])
+    out = torch.empty((B, Hq, L, 256), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        cache.append_attend(*dsteps[i], rot, causal=True, out=out)
+        cache.commit_verified_prefix(w["append"], acc[i])
+    cache.trim(cache.lens - base)
+    torch.cuda.synchronize(dev)
+    tokens, scanned = 0, 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    preroll(dev, steps, 600e-6)
+    e0.record(stream)
+    for i in range(warmup, warmup + steps):
+        tokens += int(cache.lens.sum()) + B * w["append"]
+        cache.append_attend(*dsteps[i], rot, causal=True, out=out)
+        cache.commit_verified_prefix(w["append"], acc[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = e0.elapsed_time(e1) / 1e3 / steps
+    step_bytes = tokens / steps * H * (K_ROW + V_ROW) + B * H * w["append"] * (4 * 256 + K_ROW + V_ROW)
+    return {"workload": f"spec_verify: B={B}, Hq={Hq}/Hkv={H}, {w['prefill']}-token caches, append {w['append']} + "
+                        f"attend {L} causal queries + trim the rejected suffix per step",
+            "us_per_step": sec * 1e6, "kv_tokens_per_s": tokens / steps / sec, "bytes_per_step": step_bytes,
+            "gbs": step_bytes / sec / 1e9, "hbm_frac": step_bytes / sec / 1e9 / hbm,
+            "nominal_frac": step_bytes / sec / 1e9 / NOMINAL_HBM_GBS, "steps": steps,
+            "launches_per_step": 3, "device_status": cache.device_status()}
+
+
+def prefill_record(dev, rot, chunks: int | None = None, warmup: int = 2):
+    """Chunked prefill (1 sequence, 16/2 heads): 16 chunks of 2048 tokens, each
+    appended and then attended by its own 2048 causal queries over the cache so
+    far; attention TFLOP/s (2 * 256 flop for q.k and 2 * 256 for p.v per
+    visible query-key pair and query head) against the sustained bf16 peak."""
+    from rotated_bit_quantized_gb300 import IQCache
+    w = si.WORKLOADS[3]
+    B, Hkv, Hq, n = w["B"], w["Hkv"], w["Hq"], w["append"]
+    K = w["steps"] if chunks is None else min(chunks, w["steps"])
+    cache = IQCache(B, Hkv, device=dev, capacity=256)
+    cache.reserve(n * w["steps"] + 256)
+    ch = []
+    for s_ in range(w["steps"]):
+        k, v = si.kv_tokens(w["seed"], B, Hkv, n, outliers=w["outliers"], step=s_)
+        q = si.queries(w["seed"], B, Hq, n, step=s_)
+        ch.append((k.to(dev), v.to(dev), q.to(dev)))
+    out = torch.empty((B, Hq, n, 256), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        cache.append_attend(*ch[i % len(ch)], rot, causal=True, out=out)
+    torch.cuda.synchronize(dev)
+    cache.trim(cache.lens)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    preroll(dev, K, 100e-6)
+    e0.record(stream)
+    for i in range(K):
+        cache.append_attend(*ch[i], rot, causal=True, out=out)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    flops = prefill_flops(n, K, Hq)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops_sustained"]), "measured (sustained)"
+    except Exception:
+        peak, kind = 1700.0, "fallback (sustained)"
+    tflops = flops / (ms / 1e3) / 1e12
+    return {"workload": f"chunked_prefill: B={B}, Hq={Hq}/Hkv={Hkv}, {K} chunks of {n} tokens, each appended "
+                        f"then attended by its {n} causal queries",
+            "ms_per_chunk": ms / K, "tflops": tflops, "peak_tflops": peak, "peak_kind": kind,
+            "frac": tflops / peak, "nominal_frac": tflops / NOMINAL_BF16_TFLOPS, "flops": flops,
+            "appended_tokens_per_s": B * n * K / (ms / 1e3), "device_status": cache.device_status()}
 
 
 def _oracle_sequence(wid: int, b: int):
@@ -520,11 +707,8 @@ def prefill_flops(chunk: int, chunks: int, q_heads: int, head_dim: int = 256) ->
 
 
 def run_prefill(args):
-    """Chunked prefill (workload 3): 16 chunks of 2048 tokens, each appended and
-    then attended by its own 2048 queries (causal) over the cache so far.  A
-    step is one chunk; the timed region covers K chunks after W warm-up chunks,
-    from an empty cache.  Reported against the bf16 tensor peak (the attention
-    is a dense contraction; the append is HBM-bound and small)."""
+    """Chunked prefill (workload 3) as its own bench line: the `prefill`
+    sub-record of the default run, reported against the bf16 tensor peak."""
     ws, rank, local = dist_env()
     if rank != 0:
         return
@@ -532,52 +716,21 @@ def run_prefill(args):
     torch.cuda.set_device(dev)
     from rotated_bit_quantized_gb300 import build as b
     b.build()
-    from rotated_bit_quantized_gb300 import IQCache, Rotation
-    w = si.WORKLOADS[3]
-    B, Hkv, Hq, n = w["B"], w["Hkv"], w["Hq"], w["append"]
-    K = min(args.steps, w["steps"])
-    W = args.warmup
+    from rotated_bit_quantized_gb300 import Rotation
     rot = Rotation(0, 256, dev)
-    cache = IQCache(B, Hkv, device=dev, capacity=256)
-    cache.reserve(n * w["steps"] + 256)
-    chunks = []
-    for s_ in range(w["steps"]):
-        k, v = si.kv_tokens(w["seed"], B, Hkv, n, outliers=w["outliers"], step=s_)
-        q = si.queries(w["seed"], B, Hq, n, step=s_)
-        chunks.append((k.to(dev), v.to(dev), q.to(dev)))
-    out = torch.empty((B, Hq, n, 256), dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    for i in range(W):
-        cache.append_attend(*chunks[i % len(chunks)], rot, causal=True, out=out)
-    torch.cuda.synchronize(dev)
-    cache.trim(cache.lens)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(physical_gpu(local)) as clk:
         time.sleep(0.25)
-        e0.record(stream)
-        for i in range(K):
-            cache.append_attend(*chunks[i], rot, causal=True, out=out)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
-    flops = prefill_flops(n, K, Hq)
-    peak = None
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peak, kind = float(json.load(f)["bf16_tflops_sustained"]), "measured (sustained)"
-    except Exception:
-        peak, kind = 1700.0, "fallback (sustained)"
-    tflops = flops / (ms / 1e3) / 1e12
-    rec = {"metric": "chunked prefill: attention TFLOP/s", "value": tflops, "unit": "TFLOP/s", "n_gpus": 1,
-           "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "f16/bf16 MMA, f32 accumulate", "data": "synthetic",
-           "config": {"workload": f"chunked_prefill: B={B}, Hq={Hq}/Hkv={Hkv}, head_dim=256, {K} chunks of {n} "
-                                  f"tokens, each appended then attended by its {n} queries (causal)"},
-           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "peak_kind": kind,
-                        "unit": "TFLOP/s", "frac": tflops / peak, "nominal_peak": NOMINAL_BF16_TFLOPS,
-                        "nominal_frac": tflops / NOMINAL_BF16_TFLOPS, "flops": flops,
-                        "tokens_per_s": B * n * K / (ms / 1e3)},
-           "clocks": clk.summary(), "device_status": cache.device_status()}
+        r = prefill_record(dev, rot, chunks=args.steps, warmup=args.warmup)
+    rec = {"metric": "chunked prefill: attention TFLOP/s", "value": r["tflops"], "unit": "TFLOP/s", "n_gpus": 1,
+           "steps": min(args.steps, 16),
+           "warmup": args.warmup, "ms_per_step": r["ms_per_chunk"], "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16 in/out, fp32 accumulate (fp16 tensor-core operands)",
+           "data": "synthetic", "config": {"workload": r["workload"]},
+           "roofline": {"bound": "tensor", "achieved": r["tflops"], "peak": r["peak_tflops"], "peak_kind": r["peak_kind"],
+                        "unit": "TFLOP/s", "frac": r["frac"], "nominal_peak": NOMINAL_BF16_TFLOPS,
+                        "nominal_frac": r["nominal_frac"], "flops": r["flops"],
+                        "tokens_per_s": r["appended_tokens_per_s"]},
+           "clocks": clk.summary(), "device_status": r["device_status"]}
     print(json.dumps(rec), flush=True)
 
 
@@ -597,6 +750,9 @@ def main():
                     help="k_bits,v_bits,group_size of the cache (4,3,64 runs the tuned kernels)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per step instead of the workload's own count (smaller profiling cases)")
+    ap.add_argument("--repeats", type=int, default=5, help="times the K-step region is timed (median reported)")
+    ap.add_argument("--no-sub-records", action="store_true",
+                    help="skip the single-stream, verify and prefill sub-records")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
