@@ -273,23 +273,59 @@ int iq_cache_append_attend(iq_cache* cache, const uint16_t* keys, const uint16_t
  * GPU using this entry point keeps until the process exits.  It allocates
  * nothing and calls no allocating routine; the caller still passes q and out.
  *
- * Set-up: the first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.
+ * Set-up: the first call on a device (this one or iq_noalloc_read_status)
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current.  With CUDA's lazy module loading that is also when the array's
+ * memory is reserved on the device, so make the first call at start-up:
+ * before the caller's own allocator takes the rest of device memory, and
+ * before any stream capture (iq_noalloc_read_status does the set-up and
+ * nothing else when nothing has run).
  * Sharing: every call uses the same array and it keeps the last call's
  * contents (the partials are written before they are read; the head, zero at
- * load, keeps its counters at zero between calls and its status word only
- * gains bits).  Calls that can run at the same time on the GPU
- * (different streams without ordering) race on the array: serialise them.
+ * load, returns its unit counters to zero after every call, also one whose
+ * wait ran out, and its status word only gains bits until
+ * iq_noalloc_read_status clears it).  Calls that can run at the same time on
+ * the GPU (different streams without ordering) race on the array: serialise
+ * them.
  * Errors: as iq_attend, plus WORKSPACE when the call needs more scratch than
- * IQ_NOALLOC_SCRATCH_BYTES (use iq_attend with a caller workspace then).
- * Kernel-side failures land in the shared status word, which this entry point
- * does not report; use iq_attend + iq_read_status where that matters.
+ * IQ_NOALLOC_SCRATCH_BYTES (use iq_attend with a caller workspace then); calls
+ * that take the tensor-memory prefill kernel need only the 4352-byte head.
+ * Kernel-side failures land in the shared status word: read it with
+ * iq_noalloc_read_status.
  */
 #define IQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
                       float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
                       iq_stream_t stream);
+
+/*
+ * iq_noalloc_read_status — iq_read_status for the library-owned scratch of
+ * iq_attend_noalloc on the current device (no counterpart on the pages):
+ * synchronise `stream`, read the status word the noalloc calls left, and clear
+ * it (after a failure, the whole head).  Allocates nothing.  Blocks the
+ * calling thread.  *device_status is 0 when every kernel completed normally.
+ */
+int iq_noalloc_read_status(iq_stream_t stream, int* device_status);
+
+/*
+ * iq_debug_inject — a fault-injection hook for tests (no counterpart on the
+ * pages).  The next split-KV attention call made from this host thread (the
+ * decode / verify kernels; not the prefill kernel or the generic formats)
+ * uses `spin_limit` mbarrier tests per pipeline wait (0: the default, seconds)
+ * and a combine wait of `combine_wait_ns` (0: the default, 4 s), and injects
+ * the failures in `flags`:
+ *   IQ_INJECT_COMBINE_WAIT: the combine waits for one partial more than will
+ *     ever be stored, so its wait runs out (status bit 8);
+ *   IQ_INJECT_STAGE_NEVER_FILLED: each CTA's producer leaves its first tile
+ *     unloaded, so the consumers' wait on it runs out (status bit 2, and bit 1
+ *     when the producer's own wait for the stage to be released runs out).
+ * Every wait still ends within its limit and the kernels return normally (no
+ * fault, trap or unbounded wait); outputs of that call are not meaningful.
+ * The setting then resets.  Errors: INVALID_ARG (unknown flag).
+ */
+#define IQ_INJECT_COMBINE_WAIT 1
+#define IQ_INJECT_STAGE_NEVER_FILLED 2
+int iq_debug_inject(int flags, unsigned spin_limit, unsigned long long combine_wait_ns);
 
 /*
  * iq_read_status — synchronise `stream`, read the status word that the

@@ -134,3 +134,21 @@ def commit_verified_prefix(cache: OracleCache, verified_len: int, accepted_len) 
     if (rejected < 0).any():
         raise ValueError("accepted_len cannot exceed verified_len")
     return cache.trim(np.broadcast_to(rejected, cache.lens.shape))
+
+
+def commit_verified_snapshot(cache: OracleCache, snapshots, accepted_len: int, verified_len=None) -> bool:
+    """Page "kv_cache.py", `commit_verified_snapshot`: roll the cache back to the
+    snapshot taken after `accepted_len` verified tokens.
+
+    Its four branches, in the page's order: every verified token accepted
+    (accepted_len == verified_len, when given) keeps the cache and returns True;
+    accepted_len <= 0 returns False; accepted_len beyond the snapshots taken
+    returns False; otherwise snapshot accepted_len - 1 is restored (a copy: the
+    snapshot stays intact) and True is returned.
+    """
+    if verified_len is not None and accepted_len == verified_len:
+        return True
+    if accepted_len <= 0 or accepted_len > len(snapshots):
+        return False
+    cache.restore(snapshots[accepted_len - 1])
+    return True

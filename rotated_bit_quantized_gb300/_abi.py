@@ -22,11 +22,13 @@ IQ_MAX_BATCH = 256
 IQ_STEP = 256
 IQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 IQ_MASK_NONE, IQ_MASK_CAUSAL, IQ_MASK_ADD_F32, IQ_MASK_BOOL_U8 = 0, 1, 2, 3
+IQ_INJECT_COMBINE_WAIT, IQ_INJECT_STAGE_NEVER_FILLED = 1, 2
 
 EXPORTS = ("iq_status_string", "iq_last_error", "iq_build_rotation", "iq_cache_bytes",
            "iq_cache_check", "iq_cache_nbytes", "iq_cache_append", "iq_cache_trim",
            "iq_cache_gather", "iq_attend_workspace", "iq_attend", "iq_read_status",
-           "iq_attend_noalloc", "iq_cache_append_attend", "iq_attend_mask")
+           "iq_attend_noalloc", "iq_cache_append_attend", "iq_attend_mask", "iq_noalloc_read_status",
+           "iq_debug_inject")
 
 
 class IQCacheDesc(ctypes.Structure):
@@ -74,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.iq_attend_noalloc.argtypes = [DESC, P, I, I, ctypes.c_float, I, P, P, I, P]
         L.iq_cache_append_attend.argtypes = [DESC, P, P, I, P, I, I, ctypes.c_float, I, P, P, I, P, S, P]
         L.iq_attend_mask.argtypes = [DESC, P, I, I, ctypes.c_float, I, P, ctypes.c_longlong, P, P, I, P, S, P]
+        L.iq_noalloc_read_status.argtypes = [P, ctypes.POINTER(I)]
+        L.iq_debug_inject.argtypes = [I, ctypes.c_uint, ctypes.c_ulonglong]
         for name in EXPORTS:
             if name not in ("iq_status_string", "iq_last_error", "iq_cache_nbytes"):
                 getattr(L, name).restype = I

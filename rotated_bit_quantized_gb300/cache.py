@@ -162,8 +162,57 @@ class IQCache:
         return int(lib().iq_cache_nbytes(ctypes.byref(d)))
 
     @property
+    def state(self):
+        """(keys, values), each the (codes, scales, biases) triple [B, Hkv, n, ...]
+        of rows [0, n), n = the longest sequence (page `state`: the buffers
+        sliced to the offset).  The tensors are copies, so later writes to the
+        cache never change them."""
+        n = int(self.lens.max()) if self.batch else 0
+
+        def cut(t):
+            return t[:, :, :n].clone()
+        return ((cut(self.k_codes), cut(self.k_scales), cut(self.k_biases)),
+                (cut(self.v_codes), cut(self.v_scales), cut(self.v_biases)))
+
+    @state.setter
+    def state(self, v) -> None:
+        """Install (keys, values) triples of n rows: every sequence's length
+        becomes n (page `state` setter: the offset becomes the arrays' length).
+        The bit widths and group size follow the arrays' shapes, as the page's
+        `meta_state` labels them."""
+        (kc, ks, kb), (vc, vs, vb) = v
+        B, H, n = kc.shape[0], kc.shape[1], kc.shape[2]
+        if (B, H) != (self.batch, self.kv_heads):
+            raise ValueError("state batch / kv heads differ from the cache's")
+        k_bits, v_bits = kc.shape[3] * 32 // self.head_dim, vc.shape[3] * 32 // self.head_dim
+        group = self.head_dim // ks.shape[3]
+        for t, name in zip((kc, ks, kb, vc, vs, vb), self.BUFFERS):
+            want = getattr(self, name)
+            if t.dtype != want.dtype or t.shape[:3] != (B, H, n):
+                raise ValueError(f"state tensor for {name} has dtype {t.dtype} / shape {tuple(t.shape)}")
+        if (k_bits, v_bits, group) != (self.k_bits, self.v_bits, self.group_size):
+            self.k_bits, self.v_bits, self.group_size = k_bits, v_bits, group
+            self.lens[:] = 0
+            self._workspace = None
+            self._alloc(max(IQ_STEP, int(math.ceil(max(n, 1) / IQ_STEP) * IQ_STEP)))
+        self.reserve(n)
+        for t, name in zip((kc, ks, kb, vc, vs, vb), self.BUFFERS):
+            getattr(self, name)[:, :, :n].copy_(t.to(self.device))
+        self.lens[:] = n
+
+    @property
     def meta_state(self):
+        """(group_size, k_bits, v_bits) as strings (page `meta_state`)."""
         return str(self.group_size), str(self.k_bits), str(self.v_bits)
+
+    @meta_state.setter
+    def meta_state(self, v) -> None:
+        """The page's setter takes the labels of arrays installed by `state`; here
+        the format is already fixed by those arrays, so the labels must agree."""
+        gs, kb, vb = (int(x) for x in v)
+        if (gs, kb, vb) != (self.group_size, self.k_bits, self.v_bits):
+            raise ValueError(f"meta_state {v} disagrees with the cache's format "
+                             f"({self.group_size}, {self.k_bits}, {self.v_bits})")
 
     def _fresh(self, batch: int, capacity: int) -> "IQCache":
         return IQCache(batch, self.kv_heads, self.head_dim, self.group_size, self.k_bits,

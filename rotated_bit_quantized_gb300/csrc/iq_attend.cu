@@ -135,7 +135,17 @@ struct Params {
   float* part_o;       // [slots][GT][256]
   float* part_ml;      // [slots][GT][2] (running max in log2 units, running sum)
   unsigned* status;
-  unsigned* counters;  // [UNIT_CAP]: partials stored per unit of this launch (the combine resets them)
+  // [UNIT_CAP]: partials stored per unit of this launch; the combine takes its
+  // unit's expected count off again (also when its wait runs out), so every
+  // counter is back at zero once the attention grid has completed
+  unsigned* counters;
+  // bounded waits: mbarrier tests per wait, the combine's wait in ns
+  unsigned spin_limit;
+  unsigned long long combine_wait_ns;
+  // test hook (iq_debug_inject): bit 0 the combine expects one arrival that
+  // never comes; bit 1 the producer leaves its first tile unloaded (no copy, no
+  // arrival), so the consumers' wait on it runs out
+  int inject;
   // fused append (n_new > 0): the new rows [lens[b] - n_new, lens[b]) of every
   // (sequence, kv head) are encoded from these bf16 [B][Hkv][n_new][256] rows
   // by the CTA that streams the unit's last tile, which holds them all
@@ -245,6 +255,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 constexpr unsigned long long kCombineWaitNs = 4000000000ull;  // 4 s: far above any attention grid
+// The next attention call of this host thread uses these limits and injected
+// failures (iq_debug_inject; zero = the defaults, nothing injected), then they reset.
+struct DebugInject {
+  int flags = 0;
+  unsigned spin_limit = 0;
+  unsigned long long wait_ns = 0;
+};
+thread_local DebugInject t_inject;
 
 // Programmatic dependent launch: a grid launched with programmatic stream
 // serialization may start once every CTA of its predecessor has executed
@@ -473,7 +491,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       for (long long gt = g0; gt < g1; ++gt, ++k) {
         while (gt >= p.prefix[u + 1]) ++u;
         if (!enc_seen && gt == p.prefix[u + 1] - 1) {  // a last tile: its new rows must be stored first
-          if (!mbar_wait(encoded, 0)) {
+          if (!mbar_wait(encoded, 0, p.spin_limit)) {
             atomicOr(p.status, 1u);
             break;
           }
@@ -482,7 +500,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
         const int ug = p.unit_base + u;
         const int bb = ug / (p.kv_heads * p.nqt), hh = (ug / p.nqt) % p.kv_heads;
         const int st = static_cast<int>(k % NSTAGE);
-        if (k >= NSTAGE && !mbar_wait(&empty[st], static_cast<uint32_t>((k / NSTAGE) - 1) & 1)) {
+        if (k >= NSTAGE && !mbar_wait(&empty[st], static_cast<uint32_t>((k / NSTAGE) - 1) & 1, p.spin_limit)) {
           atomicOr(p.status, 1u);
           break;
         }
@@ -504,6 +522,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
                                    elem,
                            bytes, &full[st]);
         } else {
+          if ((p.inject & 2) && gt == g0) continue;  // test hook: this stage is never filled
           mbar_arrive_expect_tx(&full[st], STAGE_TX);
         }
         tensor2d_g2s(sbp + OFF_K, &kmap, 0, static_cast<int>(row0), &full[st], pol);
@@ -516,7 +535,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       // never leave with copies in flight: wait for the last tile issued to each stage
       for (long long s = 0; s < NSTAGE && s < k; ++s) {
         const long long last = s + NSTAGE * ((k - 1 - s) / NSTAGE);
-        mbar_wait(&full[s], static_cast<uint32_t>(last / NSTAGE) & 1);
+        mbar_wait(&full[s], static_cast<uint32_t>(last / NSTAGE) & 1, p.spin_limit);
       }
     }
     return;
@@ -1192,7 +1211,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     const int tile0 = static_cast<int>(p.prefix[u]);
     for (; gt < seg_end; ++gt, ++k) {
       const int st = static_cast<int>(k % NSTAGE);
-      if (!mbar_wait(&full[st], static_cast<uint32_t>(k / NSTAGE) & 1)) {
+      if (!mbar_wait(&full[st], static_cast<uint32_t>(k / NSTAGE) & 1, p.spin_limit)) {
         atomicOr(p.status, 2u);
         ok = false;
         break;
@@ -1248,21 +1267,30 @@ __device__ __forceinline__ void combine_unit(const Params& p, int u) {
   // Wait (bounded, in time) until every CTA holding tiles of the unit has
   // stored its partial, so units are merged while the attention grid still
   // runs; every attention CTA started before this grid was launched.
+  // The count is compared signed and taken off with an atomic subtract, on
+  // success and on a timeout alike: the arrivals still missing at a timeout
+  // land before this grid completes (it completes after the attention grid),
+  // so the counter is zero again before any later call stores a partial.
+  unsigned expect = 0;
+  for (int k = k_first; k <= k_last; ++k) expect += p.cstart[k] < p.cstart[k + 1];
   if (threadIdx.x == 0) {
-    unsigned expect = 0;
-    for (int k = k_first; k <= k_last; ++k) expect += p.cstart[k] < p.cstart[k + 1];
+    const int want = static_cast<int>(expect) + ((p.inject & 1) ? 1 : 0);
+    const unsigned long long limit = p.combine_wait_ns ? p.combine_wait_ns : kCombineWaitNs;
     const unsigned long long t0 = global_ns();
     int ready = 0;
     for (;;) {
-      if (ld_acquire_gpu(p.counters + u) >= expect) { ready = 1; break; }
-      if (global_ns() - t0 > kCombineWaitNs) break;
+      if (static_cast<int>(ld_acquire_gpu(p.counters + u)) >= want) { ready = 1; break; }
+      if (global_ns() - t0 > limit) break;
       __nanosleep(32);
     }
     s_ready = ready;
   }
   __syncthreads();
   if (!s_ready) {
-    if (threadIdx.x == 0) atomicOr(p.status, 8u);
+    if (threadIdx.x == 0) {
+      atomicOr(p.status, 8u);
+      atomicSub(p.counters + u, expect);
+    }
     return;
   }
   const long long slot0 = static_cast<long long>(u) + k_first;
@@ -1312,7 +1340,7 @@ __device__ __forceinline__ void combine_unit(const Params& p, int u) {
     store_out<GT>(p, ub, r, l8, acc, L, mw);
   }
   __syncthreads();
-  if (threadIdx.x == 0) p.counters[u] = 0;  // ready for the next call
+  if (threadIdx.x == 0) atomicSub(p.counters + u, expect);  // back to zero for the next call
 }
 
 
@@ -1713,6 +1741,10 @@ int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries
   prm.v_new = v_new;
   prm.n_new = n_new;
   prm.encode_wait = encode_wait ? 1 : 0;
+  prm.spin_limit = t_inject.spin_limit ? t_inject.spin_limit : kSpinLimit;
+  prm.combine_wait_ns = t_inject.wait_ns;
+  prm.inject = t_inject.flags;
+  t_inject = DebugInject{};  // one call only
   prm.mask_kind = mask_kind;
   prm.mask = mask;
   prm.mask_stride = mask_stride;
@@ -1815,6 +1847,16 @@ int iq_attend_mask(const iq_cache* c, const uint16_t* q, int q_heads, int n_quer
     if (mask_stride < c->lens[b]) return fail(IQ_ERR_INVALID_ARG, "mask row shorter than a sequence");
   return attend_impl(c, q, q_heads, n_queries, scale, 0, rot_bf16, out, out_f32, workspace, workspace_bytes,
                      stream, nullptr, nullptr, 0, mask_kind, mask, mask_stride);
+}
+
+int iq_debug_inject(int flags, unsigned spin_limit, unsigned long long combine_wait_ns) {
+  clear_error();
+  if (flags & ~(IQ_INJECT_COMBINE_WAIT | IQ_INJECT_STAGE_NEVER_FILLED))
+    return fail(IQ_ERR_INVALID_ARG, "unknown injection flag");
+  t_inject.flags = flags;
+  t_inject.spin_limit = spin_limit;
+  t_inject.wait_ns = combine_wait_ns;
+  return IQ_OK;
 }
 
 int iq_read_status(void* workspace, iq_stream_t stream, int* device_status) {

@@ -109,10 +109,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, ui
 #ifndef IQ_SUSPEND_NS
 #define IQ_SUSPEND_NS 20000u
 #endif
-// Bounded wait: true when the phase completed, false after kSpinLimit tests
+// Bounded wait: true when the phase completed, false after `limit` tests
 // (each of which may suspend the warp for up to IQ_SUSPEND_NS).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity, IQ_SUSPEND_NS)) return true;
   return false;
 }

@@ -54,9 +54,17 @@ int scratch_address(void** out) {
 extern "C" int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
                                  float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
                                  iq_stream_t stream) {
-  size_t need = 0;
-  int st = iq_attend_workspace(cache, q_heads, n_queries, &need);
+  iq::clear_error();
+  int st = iq_cache_check(cache);
   if (st != IQ_OK) return st;
+  size_t need = 0;
+  if (n_queries >= 1 && q_heads >= 1 && q_heads % cache->kv_heads == 0 &&
+      iq::prefill_shape(cache, q_heads, n_queries, 0)) {
+    need = IQ_WORKSPACE_HEAD_BYTES;  // the prefill kernel uses only the status word of the head
+  } else {
+    st = iq_attend_workspace(cache, q_heads, n_queries, &need);
+    if (st != IQ_OK) return st;
+  }
   if (need > IQ_NOALLOC_SCRATCH_BYTES)
     return iq::fail(IQ_ERR_WORKSPACE,
                     "iq_attend_noalloc: this call needs " + std::to_string(need) +
@@ -67,7 +75,24 @@ extern "C" int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q
   st = iq::scratch_address(&scratch);
   if (st != IQ_OK) return st;
   // The array is zero when the library loads, so its status word starts
-  // clear; the split partials are written before they are read.
+  // clear; the split partials are written before they are read, and the unit
+  // counters return to zero after every call (also one whose wait ran out).
   return iq_attend(cache, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, scratch,
                    IQ_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" int iq_noalloc_read_status(iq_stream_t stream, int* device_status) {
+  iq::clear_error();
+  if (!device_status) return iq::fail(IQ_ERR_INVALID_ARG, "null device_status");
+  void* scratch = nullptr;
+  int st = iq::scratch_address(&scratch);
+  if (st != IQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  IQ_CUDA(cudaStreamSynchronize(s));
+  IQ_CUDA(cudaMemcpy(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost));
+  // after a failure, clear the whole head (status word and unit counters)
+  if (v) IQ_CUDA(cudaMemset(scratch, 0, IQ_WORKSPACE_HEAD_BYTES));
+  *device_status = static_cast<int>(v);
+  return v ? iq::fail(IQ_ERR_DEVICE, "a kernel reported a failure (status bits set)") : IQ_OK;
 }

@@ -118,3 +118,13 @@ def test_rotation_rejects(L):
     assert L.iq_build_rotation(255, draws.ctypes.data, p, p, None) == 1
     assert L.iq_build_rotation(128, draws.ctypes.data, p, p, None) == 4
     assert L.iq_build_rotation(256, None, p, p, None) == 1
+
+
+def test_debug_inject_and_noalloc_status_reject_bad_arguments(L):
+    from rotated_bit_quantized_gb300._abi import IQ_INJECT_COMBINE_WAIT, IQ_INJECT_STAGE_NEVER_FILLED
+    assert L.iq_debug_inject(4, 0, 0) == 1  # unknown flag
+    assert b"flag" in L.iq_last_error()
+    # a valid setting is host state only (it applies to this thread's next attention call), then clear it
+    assert L.iq_debug_inject(IQ_INJECT_COMBINE_WAIT | IQ_INJECT_STAGE_NEVER_FILLED, 64, 1000000) == 0
+    assert L.iq_debug_inject(0, 0, 0) == 0
+    assert L.iq_noalloc_read_status(None, None) == 1  # null out pointer, checked before any device work

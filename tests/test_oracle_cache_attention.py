@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 from oracle import attention, bf16, codec, rotation
-from oracle.cache import OracleCache, commit_verified_prefix
+from oracle.cache import OracleCache, commit_verified_prefix, commit_verified_snapshot
 import seeded_inputs as si
 
 
@@ -89,6 +89,59 @@ def test_commit_verified_prefix(mb):
     assert t.tolist() == [0, 4, 2] and c.lens.tolist() == [8, 4, 6]
     with pytest.raises(ValueError):
         commit_verified_prefix(c, 4, np.array([5, 0, 0]))
+
+
+def _rows(c, b=0, h=0):
+    L = int(c.lens[b])
+    return c.k[0][b, h, :L].copy(), c.v[0][b, h, :L].copy()
+
+
+def test_commit_verified_snapshot_branches(mb):
+    """The page's four branches against a list model: stepwise verify appends
+    one draft token at a time and snapshots after each; committing accepted_len
+    leaves exactly the prefix plus `accepted_len` drafts."""
+    base_k, base_v = si.kv_tokens(4, 1, 1, 30)
+    drafts = [si.kv_tokens(4, 1, 1, 1, step=s) for s in range(4)]
+
+    def verified_cache():
+        c = OracleCache(1, 1)
+        c.append(f32(base_k), f32(base_v), mb)
+        snaps, states = [], []
+        for k, v in drafts:  # verify step i appends draft i, then snapshots
+            c.append(f32(k), f32(v), mb)
+            snaps.append(c.snapshot())
+            states.append(_rows(c))
+        return c, snaps, states
+
+    # branch 1: every verified token accepted -> True, cache untouched (holds all 4 drafts)
+    c, snaps, states = verified_cache()
+    assert commit_verified_snapshot(c, snaps, 4, verified_len=4) is True
+    assert int(c.lens[0]) == 34 and all((a == b).all() for a, b in zip(_rows(c), states[3]))
+    # branch 2: nothing accepted -> False, cache untouched
+    c, snaps, states = verified_cache()
+    assert commit_verified_snapshot(c, snaps, 0, verified_len=4) is False
+    assert int(c.lens[0]) == 34
+    # branch 3: more accepted than snapshots taken -> False, cache untouched
+    c, snaps, states = verified_cache()
+    assert commit_verified_snapshot(c, snaps[:2], 3, verified_len=4) is False
+    assert int(c.lens[0]) == 34
+    # branch 4: accepted_len in 1..len(snapshots) -> the state after that many drafts
+    for acc in (1, 2, 3):
+        c, snaps, states = verified_cache()
+        assert commit_verified_snapshot(c, snaps, acc, verified_len=4) is True
+        assert int(c.lens[0]) == 30 + acc
+        k_rows, v_rows = _rows(c)
+        want_k = codec.encode_rows(np.concatenate([f32(base_k)] + [f32(d[0]) for d in drafts[:acc]], axis=2),
+                                   mb, 4, 64)[0][0, 0]
+        np.testing.assert_array_equal(k_rows, want_k)
+        np.testing.assert_array_equal(v_rows, states[acc - 1][1])
+        # the restored cache does not alias the snapshot: later appends leave it intact
+        c.append(f32(drafts[0][0]), f32(drafts[0][1]), mb)
+        np.testing.assert_array_equal(snaps[acc - 1][2][0][0, 0, :30 + acc], want_k)
+    # without verified_len the first branch never applies: accepted == len(snapshots) restores the last
+    c, snaps, states = verified_cache()
+    c.trim(10)
+    assert commit_verified_snapshot(c, snaps, 4) is True and int(c.lens[0]) == 34
 
 
 def test_snapshot_does_not_alias(mb):
