@@ -114,8 +114,34 @@ typedef struct {
 int iq_cache_bytes(int batch, int kv_heads, int head_dim, int group_size, int k_bits,
                    int v_bits, int capacity, size_t out_bytes[6]);
 
-/* iq_cache_check — validate a descriptor (shapes, alignment, lens in [0, capacity]). */
+/*
+ * iq_cache_alloc — bind the caller's six buffers and host lengths array into a
+ * descriptor of an empty cache (quant_kv.py, `AsymmetricQuantizedKVCache`
+ * construction: offset 0, buffers sized by `_init_quant` / `_packed_words`).
+ * buffers: device pointers in descriptor order (k_codes, k_scales, k_biases,
+ * v_codes, v_scales, v_biases), each at least the size iq_cache_bytes gives
+ * and 16-byte aligned; lens_host: host int32 [batch], set to 0.  Nothing is
+ * copied or launched.  Errors: INVALID_ARG, UNSUPPORTED (as iq_cache_check).
+ */
+int iq_cache_alloc(iq_cache* cache, int batch, int kv_heads, int head_dim, int group_size, int k_bits,
+                   int v_bits, int capacity, void* const buffers[6], int32_t* lens_host);
+
+/*
+ * iq_cache_check — validate a descriptor (quant_kv.py, the buffer layout of
+ * `AsymmetricQuantizedKVCache`: shapes of a supported format, 16-byte aligned
+ * buffers, lens in [0, capacity]).
+ */
 int iq_cache_check(const iq_cache* cache);
+
+/*
+ * iq_cache_grow — copy rows [0, lens[b]) of every sequence of `src` into the
+ * larger `dst` and set dst.lens = src.lens (quant_kv.py, `update_and_fetch`'s
+ * growth branch: a buffer ceil(n/256)*256 tokens larger, the old rows copied).
+ * dst: the same batch, kv heads and format, capacity >= every src length,
+ * buffers disjoint from src.  The same copy as iq_cache_gather with the
+ * identity map.  Errors: as iq_cache_gather.
+ */
+int iq_cache_grow(const iq_cache* src, iq_cache* dst, iq_stream_t stream);
 
 /* iq_cache_nbytes — total bytes of the six buffers (quant_kv.py, `nbytes`). */
 size_t iq_cache_nbytes(const iq_cache* cache);

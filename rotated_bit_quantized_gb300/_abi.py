@@ -28,7 +28,7 @@ EXPORTS = ("iq_status_string", "iq_last_error", "iq_build_rotation", "iq_cache_b
            "iq_cache_check", "iq_cache_nbytes", "iq_cache_append", "iq_cache_trim",
            "iq_cache_gather", "iq_attend_workspace", "iq_attend", "iq_read_status",
            "iq_attend_noalloc", "iq_cache_append_attend", "iq_attend_mask", "iq_noalloc_read_status",
-           "iq_debug_inject")
+           "iq_debug_inject", "iq_cache_alloc", "iq_cache_grow")
 
 
 class IQCacheDesc(ctypes.Structure):
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.iq_attend_mask.argtypes = [DESC, P, I, I, ctypes.c_float, I, P, ctypes.c_longlong, P, P, I, P, S, P]
         L.iq_noalloc_read_status.argtypes = [P, ctypes.POINTER(I)]
         L.iq_debug_inject.argtypes = [I, ctypes.c_uint, ctypes.c_ulonglong]
+        L.iq_cache_alloc.argtypes = [DESC, I, I, I, I, I, I, I, ctypes.POINTER(P), I32P]
+        L.iq_cache_grow.argtypes = [DESC, DESC, P]
         for name in EXPORTS:
             if name not in ("iq_status_string", "iq_last_error", "iq_cache_nbytes"):
                 getattr(L, name).restype = I

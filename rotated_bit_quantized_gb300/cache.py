@@ -112,6 +112,13 @@ class IQCache:
         self._workspace = None
         self._ws_need = {}
         self._alloc(capacity)
+        # bind the buffers through the library (validates them, zeroes the lengths)
+        d = IQCacheDesc()
+        bufs = (ctypes.c_void_p * 6)(*[getattr(self, n).data_ptr() for n in self.BUFFERS])
+        check(lib().iq_cache_alloc(ctypes.byref(d), batch, kv_heads, head_dim, group_size, k_bits, v_bits,
+                                   capacity, bufs, self.lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+              "iq_cache_alloc")
+        self._desc, self._desc_lens = d, self.lens
 
     # ---------------------------------------------------------------- storage
     def _alloc(self, capacity: int):
@@ -236,8 +243,12 @@ class IQCache:
         old = IQCache.__new__(IQCache)
         old.__dict__.update(self.__dict__)
         old.lens = self.lens.copy()
+        old._desc = None
         self._alloc(new_cap)
-        self._gather_from(old, np.arange(self.batch))
+        ds, dd = old.desc(), self.desc()
+        with self._on:
+            check(lib().iq_cache_grow(ctypes.byref(ds), ctypes.byref(dd), _stream(self.device.index)),
+                  "iq_cache_grow")
 
     # ---------------------------------------------------------------- page API
     def append(self, keys: torch.Tensor, values: torch.Tensor, rotation: Rotation) -> None:

@@ -265,6 +265,43 @@ int iq_cache_check(const iq_cache* c) {
   return IQ_OK;
 }
 
+int iq_cache_alloc(iq_cache* c, int batch, int kv_heads, int head_dim, int group_size, int k_bits, int v_bits,
+                   int capacity, void* const buffers[6], int32_t* lens_host) {
+  clear_error();
+  if (!c || !buffers || !lens_host) return fail(IQ_ERR_INVALID_ARG, "null cache, buffers or lens");
+  iq_cache d;
+  d.batch = batch;
+  d.kv_heads = kv_heads;
+  d.head_dim = head_dim;
+  d.group_size = group_size;
+  d.k_bits = k_bits;
+  d.v_bits = v_bits;
+  d.capacity = capacity;
+  d.k_codes = static_cast<uint32_t*>(buffers[0]);
+  d.k_scales = static_cast<uint16_t*>(buffers[1]);
+  d.k_biases = static_cast<uint16_t*>(buffers[2]);
+  d.v_codes = static_cast<uint32_t*>(buffers[3]);
+  d.v_scales = static_cast<uint16_t*>(buffers[4]);
+  d.v_biases = static_cast<uint16_t*>(buffers[5]);
+  d.lens = lens_host;
+  if (batch > 0 && batch <= IQ_MAX_BATCH)
+    for (int b = 0; b < batch; ++b) lens_host[b] = 0;  // an empty cache (the page's offset 0)
+  int st = iq_cache_check(&d);
+  if (st != IQ_OK) return st;
+  *c = d;
+  return IQ_OK;
+}
+
+int iq_cache_grow(const iq_cache* src, iq_cache* dst, iq_stream_t stream) {
+  clear_error();
+  if (!src || !dst) return fail(IQ_ERR_INVALID_ARG, "null cache");
+  if (src->batch != dst->batch) return fail(IQ_ERR_INVALID_ARG, "src and dst batch differ");
+  if (src->batch <= 0 || src->batch > IQ_MAX_BATCH) return fail(IQ_ERR_INVALID_ARG, "bad batch");
+  int32_t ident[IQ_MAX_BATCH];
+  for (int b = 0; b < src->batch; ++b) ident[b] = b;
+  return iq_cache_gather(src, dst, ident, stream);
+}
+
 size_t iq_cache_nbytes(const iq_cache* c) {
   size_t bytes[6];
   if (!c || iq_cache_bytes(c->batch, c->kv_heads, c->head_dim, c->group_size, c->k_bits, c->v_bits,

@@ -128,3 +128,32 @@ def test_debug_inject_and_noalloc_status_reject_bad_arguments(L):
     assert L.iq_debug_inject(IQ_INJECT_COMBINE_WAIT | IQ_INJECT_STAGE_NEVER_FILLED, 64, 1000000) == 0
     assert L.iq_debug_inject(0, 0, 0) == 0
     assert L.iq_noalloc_read_status(None, None) == 1  # null out pointer, checked before any device work
+
+
+def test_cache_alloc_binds_and_validates(L):
+    from rotated_bit_quantized_gb300._abi import IQCacheDesc
+    d = IQCacheDesc()
+    lens = np.array([7, 9], dtype=np.int32)
+    P32 = ctypes.POINTER(ctypes.c_int32)
+    bufs = (ctypes.c_void_p * 6)(*[0x10000000 + i * 0x1000000 for i in range(6)])
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 512, bufs, lens.ctypes.data_as(P32)) == 0
+    assert (d.batch, d.kv_heads, d.capacity, d.k_bits, d.v_bits) == (2, 2, 512, 4, 3)
+    assert d.v_biases == 0x15000000 and lens.tolist() == [0, 0]  # an empty cache
+    bad = (ctypes.c_void_p * 6)(*[0x10000008 + i * 0x1000000 for i in range(6)])  # not 16-byte aligned
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 512, bad, lens.ctypes.data_as(P32)) == 1
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 7, 3, 512, bufs, lens.ctypes.data_as(P32)) == 4
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 500, bufs, lens.ctypes.data_as(P32)) == 1
+
+
+def test_cache_grow_rejects_before_copying(L):
+    src, _ = fake_desc(batch=2, cap=256, lens=(100, 200))
+    dst, dlens = fake_desc(batch=2, cap=512, lens=(0, 0))
+    dst.k_codes = src.k_codes  # a shared buffer
+    assert L.iq_cache_grow(ctypes.byref(src), ctypes.byref(dst), None) == 1
+    small, _ = fake_desc(batch=2, cap=256, lens=(0, 0))
+    for i, name in enumerate(("k_codes", "k_scales", "k_biases", "v_codes", "v_scales", "v_biases")):
+        setattr(small, name, 0x40000000 + i * 0x1000000)
+    big_src, _ = fake_desc(batch=2, cap=512, lens=(300, 10))
+    assert L.iq_cache_grow(ctypes.byref(big_src), ctypes.byref(small), None) == 2  # dst capacity too small
+    one, _ = fake_desc(batch=1, cap=512, lens=(0,))
+    assert L.iq_cache_grow(ctypes.byref(src), ctypes.byref(one), None) == 1  # batch differs
