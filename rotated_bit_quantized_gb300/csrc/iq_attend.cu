@@ -1426,7 +1426,7 @@ int blocks_per_sm() {
 #define IQ_DECODE_PAIR 2
 #endif
 #ifndef IQ_DECODE_BOUNDARY
-#define IQ_DECODE_BOUNDARY 3
+#define IQ_DECODE_BOUNDARY 4
 #endif
 #define IQ_DECODE_CFG \
   1, 1, IQ_DECODE_STREAMS, IQ_DECODE_STAGES, IQ_DECODE_MINB, IQ_DECODE_TILE, IQ_DECODE_PAIR, IQ_DECODE_HALVES
