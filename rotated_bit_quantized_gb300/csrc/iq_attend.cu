@@ -1073,7 +1073,6 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
           bs += __shfl_xor_sync(0xffffffffu, bs, 4);
           bs += __shfl_xor_sync(0xffffffffu, bs, 8);
           bs += __shfl_xor_sync(0xffffffffu, bs, 16);
-#pragma unroll
           bs = fmaf(-VCENTRE, wsum[gi][j][e], bs);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {  // undo the field positions of the value codes (exact powers of two)
