@@ -342,9 +342,10 @@ int iq_noalloc_read_status(iq_stream_t stream, int* device_status);
  * the failures in `flags`:
  *   IQ_INJECT_COMBINE_WAIT: the combine waits for one partial more than will
  *     ever be stored, so its wait runs out (status bit 8);
- *   IQ_INJECT_STAGE_NEVER_FILLED: each CTA's producer leaves its first tile
- *     unloaded, so the consumers' wait on it runs out (status bit 2, and bit 1
- *     when the producer's own wait for the stage to be released runs out).
+ *   IQ_INJECT_STAGE_NEVER_FILLED: the consumers wait, in place of their first
+ *     stage, on a barrier that nothing completes in a call without new rows
+ *     (iq_attend), so their wait runs out (status bit 2, and bit 1 when the
+ *     producer's own wait for the stage to be released runs out).
  * Every wait still ends within its limit and the kernels return normally (no
  * fault, trap or unbounded wait); outputs of that call are not meaningful.
  * The setting then resets.  Errors: INVALID_ARG (unknown flag).

@@ -143,8 +143,8 @@ struct Params {
   unsigned spin_limit;
   unsigned long long combine_wait_ns;
   // test hook (iq_debug_inject): bit 0 the combine expects one arrival that
-  // never comes; bit 1 the producer leaves its first tile unloaded (no copy, no
-  // arrival), so the consumers' wait on it runs out
+  // never comes; bit 1 the consumers wait on a barrier no one arrives at (in
+  // place of their first stage), so that wait runs out
   int inject;
   // fused append (n_new > 0): the new rows [lens[b] - n_new, lens[b]) of every
   // (sequence, kv head) are encoded from these bf16 [B][Hkv][n_new][256] rows
@@ -522,7 +522,6 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
                                    elem,
                            bytes, &full[st]);
         } else {
-          if ((p.inject & 2) && gt == g0) continue;  // test hook: this stage is never filled
           mbar_arrive_expect_tx(&full[st], STAGE_TX);
         }
         tensor2d_g2s(sbp + OFF_K, &kmap, 0, static_cast<int>(row0), &full[st], pol);
@@ -1210,7 +1209,9 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     const int tile0 = static_cast<int>(p.prefix[u]);
     for (; gt < seg_end; ++gt, ++k) {
       const int st = static_cast<int>(k % NSTAGE);
-      if (!mbar_wait(&full[st], static_cast<uint32_t>(k / NSTAGE) & 1, p.spin_limit)) {
+      // (test hook: a wait on the fused-append barrier, which no one arrives at
+      // in a call without new rows, runs out like a stage that is never filled)
+      if (!mbar_wait((p.inject & 2) ? encoded : &full[st], static_cast<uint32_t>(k / NSTAGE) & 1, p.spin_limit)) {
         atomicOr(p.status, 2u);
         ok = false;
         break;
