@@ -18,6 +18,10 @@ Readings:
   bfloat16).  The page's MLX kernels would round intermediates to the query
   dtype; the method's accuracy target (bf16 I/O, fp32 accumulation) is read as
   "no intermediate rounding".
+* float32 caches (page: `rotate_last` in the queries' dtype, scores in it):
+  q' = q @ M with `codec.rotate_f32`, times the scale rounded to float32; the
+  inverse rotation uses the float32 blocks of M; a bool mask's masked scores
+  become float32's most negative finite value.
 * Causally masked scores are -inf (the page uses the dtype's most negative
   finite value; with at least one unmasked key per row the two give the same
   softmax).
@@ -37,10 +41,10 @@ from . import codec
 from .bf16 import round_bf16
 
 
-def inverse_rotate(o, blocks_b) -> np.ndarray:
-    """o @ M_b^T per 4-wide block, float64."""
+def inverse_rotate(o, blocks) -> np.ndarray:
+    """o @ M^T per 4-wide block in float64 (M_b, or the float32 M of a float32 cache)."""
     o = np.asarray(o, dtype=np.float64)
-    m = np.asarray(blocks_b, dtype=np.float64)
+    m = np.asarray(blocks, dtype=np.float64)
     nb = m.shape[0]
     o4 = o.reshape(o.shape[:-1] + (nb, 4))
     out = np.einsum('...bj,bij->...bi', o4, m)
@@ -55,18 +59,23 @@ def softmax_rows(s) -> np.ndarray:
 
 
 BF16_MIN = -3.3895313892515355e38  # most negative finite bfloat16: (2 - 2^-7) * 2^127
+F32_MIN = -3.4028234663852886e38   # most negative finite float32: (2 - 2^-23) * 2^127
 
 
-def attend_slice(q_rows, k_hat, v_hat, blocks_b, scale, causal, q_pos=None, mask_rows=None):
+def attend_slice(q_rows, k_hat, v_hat, blocks, scale, causal, q_pos=None, mask_rows=None, dtype="bf16"):
     """Attention for query rows of one kv head.
 
-    q_rows float32 [R, D] (bfloat16 values, unrotated); k_hat, v_hat float64 [T, D];
+    q_rows float32 [R, D] (unrotated; bfloat16 values when dtype is "bf16");
+    k_hat, v_hat float64 [T, D]; blocks: M_b ("bf16") or the float32 M ("f32");
     q_pos int [R]: absolute position of each row's query (causal limit t <= q_pos);
     mask_rows [R, T] bool (keep where True) or float (added to the scores).
     Returns float64 [R, D] in unrotated space.
     """
-    qr = codec.rotate(q_rows, blocks_b) * np.float32(scale)
-    qr = round_bf16(qr.astype(np.float32)).astype(np.float64)
+    if dtype == "bf16":
+        qr = codec.rotate(q_rows, blocks) * np.float32(scale)
+        qr = round_bf16(qr.astype(np.float32)).astype(np.float64)
+    else:
+        qr = (codec.rotate_f32(q_rows, blocks) * np.float32(scale)).astype(np.float32).astype(np.float64)
     s = qr @ k_hat.T
     if causal:
         t = np.arange(k_hat.shape[0])
@@ -74,18 +83,19 @@ def attend_slice(q_rows, k_hat, v_hat, blocks_b, scale, causal, q_pos=None, mask
     if mask_rows is not None:
         mask_rows = np.asarray(mask_rows)
         if mask_rows.dtype == np.bool_:
-            s = np.where(mask_rows, s, BF16_MIN)
+            s = np.where(mask_rows, s, BF16_MIN if dtype == "bf16" else F32_MIN)
         else:
             s = s + mask_rows.astype(np.float64)
     p = softmax_rows(s)
-    return inverse_rotate(p @ v_hat, blocks_b)
+    return inverse_rotate(p @ v_hat, blocks)
 
 
-def attend(q, cache, blocks_b, scale=None, causal=False, heads=None, batches=None,
+def attend(q, cache, blocks, scale=None, causal=False, heads=None, batches=None,
            query_index=None, mask=None):
     """Full oracle attention.
 
-    q float32 [B, Hq, L, D]; cache an `OracleCache` already holding the queries'
+    q float32 [B, Hq, L, D]; blocks: M_b for a "bf16" cache, the float32 M
+    for an "f32" one; cache an `OracleCache` already holding the queries'
     own keys/values when causal; mask None or [B, L, S] (bool: keep where True;
     float: added to the scores), S >= every length, shared by the heads.
     Returns float64 [B, Hq, L, D] (entries of skipped rows left as NaN when
@@ -114,7 +124,7 @@ def attend(q, cache, blocks_b, scale=None, causal=False, heads=None, batches=Non
             rows = q[b, hl][:, qi].reshape(-1, D)
             pos = np.tile(T - L + qi, len(hl))
             mrows = None if mask is None else np.tile(np.asarray(mask[b])[qi, :T], (len(hl), 1))
-            o = attend_slice(rows, kh, vh, blocks_b, scale, causal, pos, mrows)
+            o = attend_slice(rows, kh, vh, blocks, scale, causal, pos, mrows, cache.dtype)
             o = o.reshape(len(hl), len(qi), D)
             for j, h in enumerate(hl):
                 out[b, h, qi] = o[j]

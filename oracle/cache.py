@@ -15,6 +15,9 @@ Readings:
   always stays a multiple of 256 (the page's slice-to-offset quirk before
   growing only changes `nbytes`).
 * Rows at or past `lens[b]` are stale; nothing may read them.
+* `dtype` "bf16" or "f32" is the input dtype (page `_init_quant(..., dt)`):
+  scales and biases are bfloat16 or float32 values, and `append` takes M_b or
+  the float32 blocks of M accordingly.
 """
 from __future__ import annotations
 
@@ -29,9 +32,12 @@ STEP = 256
 
 class OracleCache:
     def __init__(self, batch: int, kv_heads: int, head_dim: int = 256, group_size: int = 64,
-                 k_bits: int = 4, v_bits: int = 3):
+                 k_bits: int = 4, v_bits: int = 3, dtype: str = "bf16"):
+        if dtype not in ("bf16", "f32"):
+            raise ValueError("dtype must be 'bf16' or 'f32'")
         self.batch, self.kv_heads, self.head_dim = batch, kv_heads, head_dim
         self.group_size, self.k_bits, self.v_bits = group_size, k_bits, v_bits
+        self.dtype = dtype
         self.capacity = 0
         self.lens = np.zeros(batch, dtype=np.int64)
         self.k = self.v = None
@@ -58,14 +64,17 @@ class OracleCache:
                 dst[:, :, :self.capacity] = src
         self.k, self.v, self.capacity = k, v, new_cap
 
-    def append(self, keys, values, blocks_b):
-        """Encode keys/values float32 [B, Hkv, n, D] and write rows [lens[b], lens[b]+n)."""
+    def append(self, keys, values, blocks):
+        """Encode keys/values float32 [B, Hkv, n, D] and write rows [lens[b], lens[b]+n).
+
+        blocks: M_b for a "bf16" cache, the float32 blocks of M for an "f32" one.
+        """
         keys = np.asarray(keys, np.float32)
         values = np.asarray(values, np.float32)
         n = keys.shape[2]
         self._grow_for(n)
-        kw, ks, kb = codec.encode_rows(keys, blocks_b, self.k_bits, self.group_size)
-        vw, vs, vb = codec.encode_rows(values, blocks_b, self.v_bits, self.group_size)
+        kw, ks, kb = codec.encode_rows(keys, blocks, self.k_bits, self.group_size, self.dtype)
+        vw, vs, vb = codec.encode_rows(values, blocks, self.v_bits, self.group_size, self.dtype)
         for b in range(self.batch):
             lo = int(self.lens[b])
             for dst, src in zip(self.k + self.v, (kw, ks, kb, vw, vs, vb)):
@@ -86,7 +95,8 @@ class OracleCache:
             return 0
         B, H, cap, D, gs = self.batch, self.kv_heads, self.capacity, self.head_dim, self.group_size
         words = codec.packed_words(D, self.k_bits) + codec.packed_words(D, self.v_bits)
-        return B * H * cap * (4 * words + 2 * 4 * (D // gs))
+        esz = 2 if self.dtype == "bf16" else 4
+        return B * H * cap * (4 * words + esz * 4 * (D // gs))
 
     def dequantized(self, b: int, h: int):
         """(k_hat, v_hat) float64 [len, D] of rows [0, lens[b]) of slice (b, h)."""

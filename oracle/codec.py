@@ -20,6 +20,13 @@ Readings:
 * Packing is a pure LSB-first bit stream per row: element i occupies stream
   bits [i*b, i*b + b); 32-bit word w holds stream bits [32w, 32w + 32).
   Rows hold dim*bits/32 words (`_packed_words`).
+* float32 inputs (the page's `rotate_last` casts M to the input's dtype and
+  `_init_quant` stores scales and biases in it): `x @ M` in float32 is read
+  as a row vector times the 4x4 block taken in index order, every product
+  and every partial sum rounded to float32, i.e.
+  (((x0*M[0][j] + x1*M[1][j]) + x2*M[2][j]) + x3*M[3][j]) with no fused
+  multiply-add; the scale is stored as computed (no bfloat16 rounding), the
+  bias is the float32 minimum, and the codes come from them exactly as above.
 """
 from __future__ import annotations
 
@@ -45,12 +52,29 @@ def rotate(x, blocks_b) -> np.ndarray:
     return round_bf16(acc.reshape(x.shape))
 
 
-def quantize(x, bits: int, group_size: int):
-    """Affine group quantisation of float32 rows [..., D] (bfloat16 values).
+def rotate_f32(x, blocks) -> np.ndarray:
+    """x @ M per 4-wide block for float32 x and the float32 blocks of M:
+    products and sums rounded to float32 one at a time, in index order."""
+    x = np.asarray(x, dtype=np.float32)
+    m = np.asarray(blocks, dtype=np.float32)
+    nb = m.shape[0]
+    x4 = x.reshape(x.shape[:-1] + (nb, 4))
+    acc = (x4[..., 0, None] * m[:, 0, :]).astype(np.float32)
+    for i in range(1, 4):
+        prod = (x4[..., i, None] * m[:, i, :]).astype(np.float32)
+        acc = (acc + prod).astype(np.float32)
+    return acc.reshape(x.shape)
 
-    Returns (codes uint8 [..., D], s_hat float32 [..., D/gs], b_hat float32 [..., D/gs]);
-    s_hat and b_hat are bfloat16 values.
+
+def quantize(x, bits: int, group_size: int, meta: str = "bf16"):
+    """Affine group quantisation of float32 rows [..., D].
+
+    Returns (codes uint8 [..., D], s_hat float32 [..., D/gs], b_hat float32 [..., D/gs]).
+    meta "bf16": the rows hold bfloat16 values and s_hat is the scale rounded
+    to bfloat16; meta "f32": s_hat is the float32 scale itself.
     """
+    if meta not in ("bf16", "f32"):
+        raise ValueError("meta must be 'bf16' or 'f32'")
     x = np.asarray(x, dtype=np.float32)
     d = x.shape[-1]
     g = x.reshape(x.shape[:-1] + (d // group_size, group_size))
@@ -58,7 +82,7 @@ def quantize(x, bits: int, group_size: int):
     mx = g.max(axis=-1)
     levels = np.float32(2 ** bits - 1)
     scale = ((mx - mn).astype(np.float32) / levels).astype(np.float32)
-    s_hat = round_bf16(scale)
+    s_hat = round_bf16(scale) if meta == "bf16" else scale
     b_hat = mn.astype(np.float32)
     diff = (g - b_hat[..., None]).astype(np.float32)
     safe = np.where(s_hat == 0, np.float32(1), s_hat).astype(np.float32)
@@ -108,11 +132,13 @@ def unpack(words, bits: int, dim: int) -> np.ndarray:
     return out.astype(np.uint8)
 
 
-def encode_rows(x, blocks_b, bits: int, group_size: int):
+def encode_rows(x, blocks, bits: int, group_size: int, dtype: str = "bf16"):
     """One cache row per input row: rotate, quantise, pack.
 
+    dtype "bf16": x holds bfloat16 values and `blocks` is M_b; dtype "f32": x is
+    float32 and `blocks` the float32 blocks of M.
     Returns (words uint32 [..., D*b/32], s_hat f32 [..., D/gs], b_hat f32 [..., D/gs]).
     """
-    xr = rotate(x, blocks_b)
-    codes, s_hat, b_hat = quantize(xr, bits, group_size)
+    xr = rotate(x, blocks) if dtype == "bf16" else rotate_f32(x, blocks)
+    codes, s_hat, b_hat = quantize(xr, bits, group_size, meta=dtype)
     return pack(codes, bits), s_hat, b_hat

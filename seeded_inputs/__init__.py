@@ -15,7 +15,8 @@ Recipe (stated once here, restated in the design notes):
 * Token data is drawn per (sequence b, kv head h) slice from its own generator
   ``default_rng((data_seed, stream, ...))`` so that any slice can be rebuilt on
   its own.  Values are float32 standard normals (``dtype=float32`` ziggurat),
-  rounded to bfloat16 by round-to-nearest-even (torch's conversion).  Keys of
+  rounded to bfloat16 by round-to-nearest-even (torch's conversion), or left
+  as float32 draws when float32 data is asked for (``dtype=torch.float32``).  Keys of
   the outlier workloads get 8 distinct channels per (b, h), chosen with
   ``rng.choice(256, 8, replace=False)`` before any token is drawn, scaled by 20
   before rounding.  Decode/verify steps draw new tokens from a generator keyed
@@ -93,10 +94,17 @@ def outlier_channels(data_seed: int, b: int, h: int, head_dim: int = 256) -> np.
     return _outliers(rng, head_dim)
 
 
+def _as(x: np.ndarray, dtype) -> torch.Tensor:
+    if dtype == torch.float32:
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return to_bf16(x)
+
+
 def kv_tokens(data_seed: int, batch: int, kv_heads: int, n: int, head_dim: int = 256,
               outliers: bool = False, step: int | None = None,
-              slices: list[tuple[int, int]] | None = None):
-    """K and V tokens as CPU bfloat16 tensors [B, Hkv, n, D].
+              slices: list[tuple[int, int]] | None = None, dtype=torch.bfloat16):
+    """K and V tokens as CPU tensors [B, Hkv, n, D] (bfloat16, or the float32
+    draws themselves for ``dtype=torch.float32``).
 
     ``step=None`` gives the prefill draw of every slice; ``step=s`` the tokens
     appended at decode/verify step ``s``.  ``slices`` restricts the draw to the
@@ -104,36 +112,36 @@ def kv_tokens(data_seed: int, batch: int, kv_heads: int, n: int, head_dim: int =
     only what it samples.
     """
     stream = STREAM_PREFILL if step is None else STREAM_STEP
-    k = torch.zeros((batch, kv_heads, n, head_dim), dtype=torch.bfloat16)
+    k = torch.zeros((batch, kv_heads, n, head_dim), dtype=dtype)
     v = torch.zeros_like(k)
     todo = slices if slices is not None else [(b, h) for b in range(batch) for h in range(kv_heads)]
 
     def work(bh):
         b, h = bh
         kk, vv = _slice_tokens(data_seed, b, h, n, head_dim, outliers, stream, step)
-        k[b, h] = to_bf16(kk)
-        v[b, h] = to_bf16(vv)
+        k[b, h] = _as(kk, dtype)
+        v[b, h] = _as(vv, dtype)
 
     list(_pool().map(work, todo))
     return k, v
 
 
 def kv_slice(data_seed: int, b: int, h: int, n: int, head_dim: int = 256,
-             outliers: bool = False, step: int | None = None):
-    """K and V tokens of the single slice (b, h) as CPU bfloat16 tensors [n, D];
+             outliers: bool = False, step: int | None = None, dtype=torch.bfloat16):
+    """K and V tokens of the single slice (b, h) as CPU tensors [n, D];
     identical to ``kv_tokens(...)[.][b, h]``."""
     stream = STREAM_PREFILL if step is None else STREAM_STEP
     k, v = _slice_tokens(data_seed, b, h, n, head_dim, outliers, stream, step)
-    return to_bf16(k), to_bf16(v)
+    return _as(k, dtype), _as(v, dtype)
 
 
 def queries(data_seed: int, batch: int, q_heads: int, n: int, head_dim: int = 256,
-            step: int = 0) -> torch.Tensor:
-    """Queries as a CPU bfloat16 tensor [B, Hq, n, D], ~N(0, 1)."""
-    out = torch.empty((batch, q_heads, n, head_dim), dtype=torch.bfloat16)
+            step: int = 0, dtype=torch.bfloat16) -> torch.Tensor:
+    """Queries as a CPU tensor [B, Hq, n, D], ~N(0, 1) (bfloat16, or float32 draws)."""
+    out = torch.empty((batch, q_heads, n, head_dim), dtype=dtype)
     for b in range(batch):
         rng = np.random.default_rng((data_seed, STREAM_QUERY, step, b))
-        out[b] = to_bf16(rng.standard_normal((q_heads, n, head_dim), dtype=np.float32))
+        out[b] = _as(rng.standard_normal((q_heads, n, head_dim), dtype=np.float32), dtype)
     return out
 
 
