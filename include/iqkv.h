@@ -14,7 +14,13 @@
  *  - Work is enqueued asynchronously on the caller's stream (`iq_stream_t` is a
  *    `cudaStream_t`; NULL is the legacy default stream).  No entry point
  *    synchronises the device, except `iq_read_status`, which says so.
- *  - bfloat16 values travel as `uint16_t` bit patterns.
+ *  - A cache has an element dtype, bfloat16 (IQ_DTYPE_BF16) or float32
+ *    (IQ_DTYPE_F32): the dtype of the keys, values and queries it is fed, of
+ *    its scales and biases (the page's `_init_quant(..., dt)` takes `dt` from
+ *    the keys), and of the rotation blocks it is given (the page's
+ *    `rotate_last` casts M to the input's dtype: M_b for bfloat16, M itself
+ *    for float32).  Data arguments are `const void*` of that dtype; bfloat16
+ *    values are 16-bit patterns.
  *  - Functions return an `iq_status`; nothing is thrown across the ABI.  On an
  *    error nothing is enqueued and nothing the caller owns is modified, and
  *    `iq_last_error()` holds a one-line explanation (per host thread).
@@ -23,10 +29,11 @@
  *    1 <= batch <= IQ_MAX_BATCH, kv heads >= 1, query heads a multiple of kv
  *    heads with at most 8 query heads per kv head and 8 % rep == 0.  Anything
  *    else returns IQ_ERR_UNSUPPORTED.  k_bits 4, v_bits 3, group 64 runs the
- *    tuned kernels; every other format runs a generic path (same arithmetic,
- *    float32 attention over shared-memory tiles) that serves at most 64 query
- *    rows (query heads per kv head x n_queries) per call and never fuses the
- *    append into the attention.
+ *    tuned kernels when the dtype is bfloat16; every other format, and every
+ *    float32 cache, runs a generic path (same arithmetic, float32 attention
+ *    over shared-memory tiles) that serves at most 64 query rows (query heads
+ *    per kv head x n_queries) per call and never fuses the append into the
+ *    attention.
  */
 #ifndef IQKV_H
 #define IQKV_H
@@ -42,6 +49,9 @@ extern "C" {
 #define IQ_STEP 256 /* capacity granule, the page's `AsymmetricQuantizedKVCache.step` */
 
 typedef void* iq_stream_t; /* a cudaStream_t */
+
+#define IQ_DTYPE_BF16 0 /* bfloat16 data, scales and biases (the tuned kernels) */
+#define IQ_DTYPE_F32 1  /* float32 data, scales and biases (generic path) */
 
 typedef enum {
   IQ_OK = 0,
@@ -67,9 +77,10 @@ const char* iq_last_error(void);
  *   each block's left then right quaternion, in generator order (the caller
  *   draws them; the library normalises them in float32 and forms
  *   L(qL) . R(qR) with float64 accumulation, rounded once to float32).
- * rot_f32: device float32 [head_dim/4][4][4] out (the blocks of M).
- * rot_bf16: device bf16 [head_dim/4][4][4] out (M_b = bf16(M), what the cache
- *   and attention use).
+ * rot_f32: device float32 [head_dim/4][4][4] out (the blocks of M, what
+ *   float32 caches use).
+ * rot_bf16: device bf16 [head_dim/4][4][4] out (M_b = bf16(M), what bfloat16
+ *   caches use).
  * The draws are copied to the device before the call returns, so the host
  * buffer may be reused at once.  Errors: INVALID_ARG (null, head_dim not a
  * positive multiple of 4), UNSUPPORTED (head_dim != 256), CUDA.
@@ -82,11 +93,13 @@ int iq_build_rotation(int head_dim, const float* draws_host, float* rot_f32,
  * (quant_kv.py, `AsymmetricQuantizedKVCache`: keys and values each stored as a
  * (wq, scales, biases) triple).  The caller owns every pointer.
  *
+ *   dtype    IQ_DTYPE_BF16 or IQ_DTYPE_F32: the element type of the scales and
+ *            biases and of every data argument the cache is used with
  *   k_codes  uint32 [B][Hkv][capacity][head_dim*k_bits/32]  (LSB-first stream)
- *   k_scales bf16   [B][Hkv][capacity][head_dim/group_size]
- *   k_biases bf16   [B][Hkv][capacity][head_dim/group_size]
+ *   k_scales dtype  [B][Hkv][capacity][head_dim/group_size]
+ *   k_biases dtype  [B][Hkv][capacity][head_dim/group_size]
  *   v_codes  uint32 [B][Hkv][capacity][head_dim*v_bits/32]
- *   v_scales, v_biases bf16 as above
+ *   v_scales, v_biases dtype as above
  *   lens     HOST int32 [B]: tokens held by each sequence.  This host array is
  *            the authoritative length; the library reads it to size launches
  *            and passes lengths to kernels by value, and updates it in
@@ -95,24 +108,25 @@ int iq_build_rotation(int head_dim, const float* draws_host, float* rot_f32,
  * of IQ_STEP.  Rows at or past lens[b] are stale and are never read.
  */
 typedef struct {
-  int32_t batch, kv_heads, head_dim, group_size, k_bits, v_bits, capacity;
+  int32_t batch, kv_heads, head_dim, group_size, k_bits, v_bits, capacity, dtype;
   uint32_t* k_codes;
-  uint16_t* k_scales;
-  uint16_t* k_biases;
+  void* k_scales;
+  void* k_biases;
   uint32_t* v_codes;
-  uint16_t* v_scales;
-  uint16_t* v_biases;
+  void* v_scales;
+  void* v_biases;
   int32_t* lens;
 } iq_cache;
 
 /*
  * iq_cache_bytes — byte sizes of the six device buffers of a cache
  * (quant_kv.py, `_init_quant`, `_packed_words`), in descriptor order
- * (k_codes, k_scales, k_biases, v_codes, v_scales, v_biases).
- * Errors: INVALID_ARG, UNSUPPORTED.
+ * (k_codes, k_scales, k_biases, v_codes, v_scales, v_biases); scales and
+ * biases take 2 bytes each for IQ_DTYPE_BF16 and 4 for IQ_DTYPE_F32.
+ * Errors: INVALID_ARG (bad sizes, unknown dtype), UNSUPPORTED.
  */
 int iq_cache_bytes(int batch, int kv_heads, int head_dim, int group_size, int k_bits,
-                   int v_bits, int capacity, size_t out_bytes[6]);
+                   int v_bits, int capacity, int dtype, size_t out_bytes[6]);
 
 /*
  * iq_cache_alloc — bind the caller's six buffers and host lengths array into a
@@ -124,7 +138,7 @@ int iq_cache_bytes(int batch, int kv_heads, int head_dim, int group_size, int k_
  * copied or launched.  Errors: INVALID_ARG, UNSUPPORTED (as iq_cache_check).
  */
 int iq_cache_alloc(iq_cache* cache, int batch, int kv_heads, int head_dim, int group_size, int k_bits,
-                   int v_bits, int capacity, void* const buffers[6], int32_t* lens_host);
+                   int v_bits, int capacity, int dtype, void* const buffers[6], int32_t* lens_host);
 
 /*
  * iq_cache_check — validate a descriptor (quant_kv.py, the buffer layout of
@@ -152,14 +166,21 @@ size_t iq_cache_nbytes(const iq_cache* cache);
  * `update_and_fetch`; quantiser scale = (max-min)/(2^b-1), bias = min,
  * code = clamp(round-half-even((x - bias)/scale))).
  *
- * keys, values: device bf16 [B][Hkv][n][head_dim], contiguous, unrotated.
- * rot_bf16: device bf16 blocks from iq_build_rotation.
+ * keys, values: device [B][Hkv][n][head_dim] of the cache's dtype,
+ *   contiguous, unrotated.
+ * rot: device rotation blocks from iq_build_rotation in the cache's dtype
+ *   (rot_bf16 for a bfloat16 cache, rot_f32 for a float32 one).
+ * bfloat16: each rotated element is the float32 sum, in block-row order, of
+ * exact bf16 x bf16 products, rounded once to bf16; the scale is rounded to
+ * bf16 before the codes are formed from it.  float32: products and sums
+ * rounded to float32 one by one in block-row order; scale and bias stored as
+ * computed.  Either way codes come from the stored scale and bias.
  * On success lens[b] += n for every b.  n == 0 is a no-op.
  * Errors: INVALID_ARG, CAPACITY (some lens[b] + n > capacity; grow first —
  * see iq_cache_gather), UNSUPPORTED, CUDA.
  */
-int iq_cache_append(iq_cache* cache, const uint16_t* keys, const uint16_t* values, int n,
-                    const uint16_t* rot_bf16, iq_stream_t stream);
+int iq_cache_append(iq_cache* cache, const void* keys, const void* values, int n, const void* rot,
+                    iq_stream_t stream);
 
 /*
  * iq_cache_trim — drop the last tokens of each sequence
@@ -180,7 +201,7 @@ int iq_cache_trim(iq_cache* cache, const int32_t* n_host, int32_t* trimmed_host)
  * tiling a batch-1 cache to P paths (kv_cache.py `tile_caches`: all zeros) and
  * keeping the winning path (kv_cache.py `commit_tree_row`: one index).
  * src_of: host int32 [dst.batch].  src and dst must share kv_heads, head_dim,
- * group_size and bits, and must not overlap in memory.
+ * group_size, bits and dtype, and must not overlap in memory.
  * Errors: INVALID_ARG, CAPACITY (dst capacity too small), UNSUPPORTED, CUDA.
  */
 int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of,
@@ -199,14 +220,16 @@ int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_
  * cache (quant_kv.py, `asym_quantized_sdpa`, followed by the inverse rotation
  * the page leaves to its caller).
  *
- * q: device bf16 [B][Hq][n_queries][head_dim], unrotated.  The library
- *    rotates it with M_b (bf16 result), multiplies by `scale` (bf16 result;
- *    1/sqrt(head_dim) is the usual value), and lets query head h read kv head
- *    h / (Hq/Hkv).
+ * q: device [B][Hq][n_queries][head_dim] of the cache's dtype, unrotated.
+ *    The library rotates it with the blocks `rot` (the cache's dtype, as in
+ *    iq_cache_append; result rounded to that dtype), multiplies by `scale`
+ *    (result rounded likewise; 1/sqrt(head_dim) is the usual value), and lets
+ *    query head h read kv head h / (Hq/Hkv).
  * causal: 0 = every query sees all lens[b] tokens; 1 = query i sees tokens
  *    t <= lens[b] - n_queries + i (its own token already appended).
  * out: device [B][Hq][n_queries][head_dim], bf16 (out_f32 == 0) or float32
- *    (out_f32 == 1), in unrotated space: out = bf16(o @ M_b^T).
+ *    (out_f32 == 1), in unrotated space: out = o @ rot^T rounded to the
+ *    output type.
  * workspace: device buffer of at least iq_attend_workspace() bytes,
  *    256-byte aligned.  Its first IQ_WORKSPACE_HEAD_BYTES (the status word
  *    and per-unit partial counters) must be zero before the first call (e.g.
@@ -216,7 +239,8 @@ int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_
  *    attention grid and, as its programmatic dependent, the split combine,
  *    which merges each split unit as soon as its partials are stored and
  *    completes after the attention grid.
- * Scores, softmax and P.V accumulate in float32 on tensor cores.  Key and
+ * Scores, softmax and P.V accumulate in float32; for bfloat16 caches of the
+ * tuned format they run on tensor cores.  Key and
  * value codes enter the products exactly (as bare fp16 bit fields), queries as
  * q'' times a per-row power of two that keeps them inside fp16 (any bf16
  * query), P times the value scale as fp16 with the softmax reference raised
@@ -230,8 +254,8 @@ int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_
  * prefill kernel's range) sets a bit in the workspace status word, reported by
  * iq_read_status.
  */
-int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
-              float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
+int iq_attend(const iq_cache* cache, const void* q, int q_heads, int n_queries,
+              float scale, int causal, const void* rot, void* out, int out_f32,
               void* workspace, size_t workspace_bytes, iq_stream_t stream);
 
 /*
@@ -258,15 +282,16 @@ int iq_attend(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queri
 #define IQ_MASK_CAUSAL 1
 #define IQ_MASK_ADD_F32 2
 #define IQ_MASK_BOOL_U8 3
-int iq_attend_mask(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries, float scale,
-                   int mask_kind, const void* mask, long long mask_stride, const uint16_t* rot_bf16,
+int iq_attend_mask(const iq_cache* cache, const void* q, int q_heads, int n_queries, float scale,
+                   int mask_kind, const void* mask, long long mask_stride, const void* rot,
                    void* out, int out_f32, void* workspace, size_t workspace_bytes, iq_stream_t stream);
 
 /*
  * iq_cache_append_attend — iq_cache_append(keys, values, n) followed by
  * iq_attend(q, ...), the page's decode step (quant_kv.py: `update_and_fetch`,
  * then `asym_quantized_sdpa` over the updated cache), with the same results
- * as the two calls.  When every (sequence, kv head) holds at most 8 query
+ * as the two calls.  For a bfloat16 cache of the tuned format, when every
+ * (sequence, kv head) holds at most 8 query
  * rows (q_heads / kv_heads * n_queries <= 8) and each sequence's n new rows
  * fall in one 128-token tile, it is one attention launch whose CTAs encode the
  * new rows themselves before streaming the tiles that hold them; otherwise it
@@ -281,9 +306,9 @@ int iq_attend_mask(const iq_cache* cache, const uint16_t* q, int q_heads, int n_
  * Writing the cache by other means (outside this library's calls) while a call
  * on the same stream is in flight is not supported.
  */
-int iq_cache_append_attend(iq_cache* cache, const uint16_t* keys, const uint16_t* values, int n,
-                           const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
-                           const uint16_t* rot_bf16, void* out, int out_f32, void* workspace,
+int iq_cache_append_attend(iq_cache* cache, const void* keys, const void* values, int n,
+                           const void* q, int q_heads, int n_queries, float scale, int causal,
+                           const void* rot, void* out, int out_f32, void* workspace,
                            size_t workspace_bytes, iq_stream_t stream);
 
 /*
@@ -320,8 +345,8 @@ int iq_cache_append_attend(iq_cache* cache, const uint16_t* keys, const uint16_t
  * iq_noalloc_read_status.
  */
 #define IQ_NOALLOC_SCRATCH_BYTES (16u << 20)
-int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
-                      float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
+int iq_attend_noalloc(const iq_cache* cache, const void* q, int q_heads, int n_queries,
+                      float scale, int causal, const void* rot, void* out, int out_f32,
                       iq_stream_t stream);
 
 /*

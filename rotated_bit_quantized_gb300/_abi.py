@@ -23,6 +23,7 @@ IQ_STEP = 256
 IQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 IQ_MASK_NONE, IQ_MASK_CAUSAL, IQ_MASK_ADD_F32, IQ_MASK_BOOL_U8 = 0, 1, 2, 3
 IQ_INJECT_COMBINE_WAIT, IQ_INJECT_STAGE_NEVER_FILLED = 1, 2
+IQ_DTYPE_BF16, IQ_DTYPE_F32 = 0, 1
 
 EXPORTS = ("iq_status_string", "iq_last_error", "iq_build_rotation", "iq_cache_bytes",
            "iq_cache_check", "iq_cache_nbytes", "iq_cache_append", "iq_cache_trim",
@@ -35,7 +36,7 @@ class IQCacheDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("group_size", ctypes.c_int32),
                 ("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32),
-                ("capacity", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("k_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
                 ("k_biases", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
                 ("v_scales", ctypes.c_void_p), ("v_biases", ctypes.c_void_p),
@@ -64,7 +65,7 @@ def lib() -> ctypes.CDLL:
         L.iq_status_string.argtypes, L.iq_status_string.restype = [I], ctypes.c_char_p
         L.iq_last_error.argtypes, L.iq_last_error.restype = [], ctypes.c_char_p
         L.iq_build_rotation.argtypes = [I, P, P, P, P]
-        L.iq_cache_bytes.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(S)]
+        L.iq_cache_bytes.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(S)]
         L.iq_cache_check.argtypes = [DESC]
         L.iq_cache_nbytes.argtypes, L.iq_cache_nbytes.restype = [DESC], S
         L.iq_cache_append.argtypes = [DESC, P, P, I, P, P]
@@ -78,7 +79,7 @@ def lib() -> ctypes.CDLL:
         L.iq_attend_mask.argtypes = [DESC, P, I, I, ctypes.c_float, I, P, ctypes.c_longlong, P, P, I, P, S, P]
         L.iq_noalloc_read_status.argtypes = [P, ctypes.POINTER(I)]
         L.iq_debug_inject.argtypes = [I, ctypes.c_uint, ctypes.c_ulonglong]
-        L.iq_cache_alloc.argtypes = [DESC, I, I, I, I, I, I, I, ctypes.POINTER(P), I32P]
+        L.iq_cache_alloc.argtypes = [DESC, I, I, I, I, I, I, I, I, ctypes.POINTER(P), I32P]
         L.iq_cache_grow.argtypes = [DESC, DESC, P]
         for name in EXPORTS:
             if name not in ("iq_status_string", "iq_last_error", "iq_cache_nbytes"):

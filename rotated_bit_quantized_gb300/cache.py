@@ -90,20 +90,31 @@ class Rotation:
                   "iq_build_rotation")
 
 
+_DTYPE_CODES = {torch.bfloat16: _abi.IQ_DTYPE_BF16, torch.float32: _abi.IQ_DTYPE_F32}
+
+
 class IQCache:
     """Rotated K4/V3 bit-packed KV cache with one length per sequence.
 
     Buffers follow the page's `(wq, scales, biases)` triples for keys and
     values; `lens` (host int32 [B]) is the authoritative length of each
     sequence.  Capacity grows in steps of 256 tokens, copying rows [0, len).
+    `dtype` (bfloat16 or float32) is the dtype of the keys, values and
+    queries the cache takes and of its scales and biases (the page's
+    `_init_quant` stores them in the keys' dtype); a float32 cache rotates
+    with the float32 blocks of M, a bfloat16 one with M_b.
     """
 
     BUFFERS = ("k_codes", "k_scales", "k_biases", "v_codes", "v_scales", "v_biases")
 
     def __init__(self, batch: int, kv_heads: int, head_dim: int = 256, group_size: int = 64,
-                 k_bits: int = 4, v_bits: int = 3, capacity: int = IQ_STEP, device=None):
+                 k_bits: int = 4, v_bits: int = 3, capacity: int = IQ_STEP, device=None,
+                 dtype=torch.bfloat16):
+        if dtype not in _DTYPE_CODES:
+            raise ValueError("dtype must be torch.bfloat16 or torch.float32")
         self.batch, self.kv_heads, self.head_dim = batch, kv_heads, head_dim
         self.group_size, self.k_bits, self.v_bits = group_size, k_bits, v_bits
+        self.dtype = dtype
         self.device = torch.device(device or "cuda")
         if self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
@@ -116,7 +127,8 @@ class IQCache:
         d = IQCacheDesc()
         bufs = (ctypes.c_void_p * 6)(*[getattr(self, n).data_ptr() for n in self.BUFFERS])
         check(lib().iq_cache_alloc(ctypes.byref(d), batch, kv_heads, head_dim, group_size, k_bits, v_bits,
-                                   capacity, bufs, self.lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+                                   capacity, _DTYPE_CODES[dtype], bufs,
+                                   self.lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
               "iq_cache_alloc")
         self._desc, self._desc_lens = d, self.lens
 
@@ -124,17 +136,18 @@ class IQCache:
     def _alloc(self, capacity: int):
         sizes = (ctypes.c_size_t * 6)()
         check(lib().iq_cache_bytes(self.batch, self.kv_heads, self.head_dim, self.group_size,
-                                   self.k_bits, self.v_bits, capacity, sizes), "iq_cache_bytes")
+                                   self.k_bits, self.v_bits, capacity, _DTYPE_CODES[self.dtype], sizes),
+              "iq_cache_bytes")
         B, H = self.batch, self.kv_heads
         dev = self.device
         kw, vw = self.head_dim * self.k_bits // 32, self.head_dim * self.v_bits // 32
         ng = self.head_dim // self.group_size
         self.k_codes = torch.empty((B, H, capacity, kw), dtype=torch.int32, device=dev)
-        self.k_scales = torch.empty((B, H, capacity, ng), dtype=torch.bfloat16, device=dev)
-        self.k_biases = torch.empty((B, H, capacity, ng), dtype=torch.bfloat16, device=dev)
+        self.k_scales = torch.empty((B, H, capacity, ng), dtype=self.dtype, device=dev)
+        self.k_biases = torch.empty((B, H, capacity, ng), dtype=self.dtype, device=dev)
         self.v_codes = torch.empty((B, H, capacity, vw), dtype=torch.int32, device=dev)
-        self.v_scales = torch.empty((B, H, capacity, ng), dtype=torch.bfloat16, device=dev)
-        self.v_biases = torch.empty((B, H, capacity, ng), dtype=torch.bfloat16, device=dev)
+        self.v_scales = torch.empty((B, H, capacity, ng), dtype=self.dtype, device=dev)
+        self.v_biases = torch.empty((B, H, capacity, ng), dtype=self.dtype, device=dev)
         for name, n in zip(self.BUFFERS, sizes):
             assert getattr(self, name).numel() * getattr(self, name).element_size() == n
         self.capacity = capacity
@@ -147,7 +160,7 @@ class IQCache:
         d = self._desc
         if d is None or self._desc_lens is not self.lens:
             d = IQCacheDesc(self.batch, self.kv_heads, self.head_dim, self.group_size, self.k_bits,
-                            self.v_bits, self.capacity)
+                            self.v_bits, self.capacity, _DTYPE_CODES[self.dtype])
             for name in self.BUFFERS:
                 setattr(d, name, getattr(self, name).data_ptr())
             if self.lens.dtype != np.int32 or not self.lens.flags["C_CONTIGUOUS"]:
@@ -186,19 +199,22 @@ class IQCache:
         """Install (keys, values) triples of n rows: every sequence's length
         becomes n (page `state` setter: the offset becomes the arrays' length).
         The bit widths and group size follow the arrays' shapes, as the page's
-        `meta_state` labels them."""
+        `meta_state` labels them, and the dtype follows the scales' dtype."""
         (kc, ks, kb), (vc, vs, vb) = v
         B, H, n = kc.shape[0], kc.shape[1], kc.shape[2]
         if (B, H) != (self.batch, self.kv_heads):
             raise ValueError("state batch / kv heads differ from the cache's")
         k_bits, v_bits = kc.shape[3] * 32 // self.head_dim, vc.shape[3] * 32 // self.head_dim
         group = self.head_dim // ks.shape[3]
+        dtype = ks.dtype
+        if dtype not in _DTYPE_CODES:
+            raise ValueError(f"state scales have dtype {dtype}; bfloat16 or float32 expected")
         for t, name in zip((kc, ks, kb, vc, vs, vb), self.BUFFERS):
-            want = getattr(self, name)
-            if t.dtype != want.dtype or t.shape[:3] != (B, H, n):
+            want = torch.int32 if name.endswith("codes") else dtype
+            if t.dtype != want or t.shape[:3] != (B, H, n):
                 raise ValueError(f"state tensor for {name} has dtype {t.dtype} / shape {tuple(t.shape)}")
-        if (k_bits, v_bits, group) != (self.k_bits, self.v_bits, self.group_size):
-            self.k_bits, self.v_bits, self.group_size = k_bits, v_bits, group
+        if (k_bits, v_bits, group, dtype) != (self.k_bits, self.v_bits, self.group_size, self.dtype):
+            self.k_bits, self.v_bits, self.group_size, self.dtype = k_bits, v_bits, group, dtype
             self.lens[:] = 0
             self._workspace = None
             self._alloc(max(IQ_STEP, int(math.ceil(max(n, 1) / IQ_STEP) * IQ_STEP)))
@@ -223,7 +239,7 @@ class IQCache:
 
     def _fresh(self, batch: int, capacity: int) -> "IQCache":
         return IQCache(batch, self.kv_heads, self.head_dim, self.group_size, self.k_bits,
-                       self.v_bits, capacity, self.device)
+                       self.v_bits, capacity, self.device, self.dtype)
 
     def _gather_from(self, src: "IQCache", src_of) -> None:
         m = np.ascontiguousarray(src_of, dtype=np.int32)
@@ -250,14 +266,18 @@ class IQCache:
             check(lib().iq_cache_grow(ctypes.byref(ds), ctypes.byref(dd), _stream(self.device.index)),
                   "iq_cache_grow")
 
+    def _rot(self, rotation: Rotation) -> ctypes.c_void_p:
+        """The rotation blocks in the cache's dtype (the page's `R.astype(x.dtype)`)."""
+        return _ptr(rotation.blocks_f32 if self.dtype == torch.float32 else rotation.blocks_bf16)
+
     # ---------------------------------------------------------------- page API
     def append(self, keys: torch.Tensor, values: torch.Tensor, rotation: Rotation) -> None:
         """Rotate, quantise, pack and append n tokens per sequence (page `update_and_fetch`).
 
-        keys, values: bfloat16 CUDA tensors [B, Hkv, n, D], unrotated.
+        keys, values: CUDA tensors [B, Hkv, n, D] of the cache's dtype, unrotated.
         """
-        keys = _need_cuda(keys, torch.bfloat16, "keys")
-        values = _need_cuda(values, torch.bfloat16, "values")
+        keys = _need_cuda(keys, self.dtype, "keys")
+        values = _need_cuda(values, self.dtype, "values")
         n = keys.shape[2]
         if tuple(keys.shape) != (self.batch, self.kv_heads, n, self.head_dim) or values.shape != keys.shape:
             raise ValueError("keys/values must be [B, Hkv, n, D]")
@@ -267,7 +287,7 @@ class IQCache:
         d = self.desc()
         with self._on:
             check(lib().iq_cache_append(ctypes.byref(d), _ptr(keys), _ptr(values), n,
-                                        _ptr(rotation.blocks_bf16), _stream(self.device.index)),
+                                        self._rot(rotation), _stream(self.device.index)),
                   "iq_cache_append")
 
     def trim(self, n) -> np.ndarray:
@@ -293,9 +313,11 @@ class IQCache:
         return nb
 
     def attend(self, q: torch.Tensor, rotation: Rotation, causal: bool = False, scale: float | None = None,
-               out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+               out: torch.Tensor | None = None, out_dtype=None,
                mask: torch.Tensor | None = None) -> torch.Tensor:
-        """Attention of q [B, Hq, L, D] (bf16, unrotated) over the cache (page `asym_quantized_sdpa`).
+        """Attention of q [B, Hq, L, D] (the cache's dtype, unrotated) over the cache
+        (page `asym_quantized_sdpa`).  The output is bf16 or float32 (`out_dtype`,
+        default the cache's dtype, as the page returns the queries' dtype).
 
         mask: optional CUDA tensor [B, L, S] (S >= every length), shared by the
         heads: bool (keep where True) or float32 (added to the scores); not
@@ -304,14 +326,14 @@ class IQCache:
         """
         if mask is not None:
             return self._attend_mask(q, rotation, mask, causal, scale, out, out_dtype)
-        q = _need_cuda(q, torch.bfloat16, "q")
+        q = _need_cuda(q, self.dtype, "q")
         B, Hq, L, D = q.shape
         if B != self.batch or D != self.head_dim:
             raise ValueError("q must be [B, Hq, L, D] matching the cache")
         if scale is None:
             scale = 1.0 / math.sqrt(D)
         if out is None:
-            out = torch.empty((B, Hq, L, D), dtype=out_dtype, device=q.device)
+            out = torch.empty((B, Hq, L, D), dtype=out_dtype or self.dtype, device=q.device)
         out_f32 = 1 if out.dtype == torch.float32 else 0
         if out.dtype not in (torch.float32, torch.bfloat16) or not out.is_contiguous():
             raise ValueError("out must be a contiguous bf16 or f32 tensor")
@@ -322,14 +344,14 @@ class IQCache:
         d = self.desc()
         with self._on:
             check(lib().iq_attend(ctypes.byref(d), _ptr(q), Hq, L, float(scale), 1 if causal else 0,
-                                  _ptr(rotation.blocks_bf16), _ptr(out), out_f32, _ptr(self._workspace),
+                                  self._rot(rotation), _ptr(out), out_f32, _ptr(self._workspace),
                                   self._workspace.numel(), _stream(self.device.index)), "iq_attend")
         return out
 
     def _attend_mask(self, q, rotation, mask, causal, scale, out, out_dtype):
         if causal:
             raise ValueError("give either causal or an explicit mask")
-        q = _need_cuda(q, torch.bfloat16, "q")
+        q = _need_cuda(q, self.dtype, "q")
         B, Hq, L, D = q.shape
         if B != self.batch or D != self.head_dim:
             raise ValueError("q must be [B, Hq, L, D] matching the cache")
@@ -351,7 +373,7 @@ class IQCache:
         if scale is None:
             scale = 1.0 / math.sqrt(D)
         if out is None:
-            out = torch.empty((B, Hq, L, D), dtype=out_dtype, device=q.device)
+            out = torch.empty((B, Hq, L, D), dtype=out_dtype or self.dtype, device=q.device)
         if out.dtype not in (torch.float32, torch.bfloat16) or not out.is_contiguous():
             raise ValueError("out must be a contiguous bf16 or f32 tensor")
         need = self.workspace_bytes(Hq, L)
@@ -360,20 +382,20 @@ class IQCache:
         d = self.desc()
         with self._on:
             check(lib().iq_attend_mask(ctypes.byref(d), _ptr(q), Hq, L, float(scale), kind, _ptr(mask),
-                                       mask.shape[2], _ptr(rotation.blocks_bf16), _ptr(out),
+                                       mask.shape[2], self._rot(rotation), _ptr(out),
                                        1 if out.dtype == torch.float32 else 0, _ptr(self._workspace),
                                        self._workspace.numel(), _stream(self.device.index)), "iq_attend_mask")
         return out
 
     def append_attend(self, keys: torch.Tensor, values: torch.Tensor, q: torch.Tensor, rotation: Rotation,
                       causal: bool = False, scale: float | None = None, out: torch.Tensor | None = None,
-                      out_dtype=torch.bfloat16) -> torch.Tensor:
+                      out_dtype=None) -> torch.Tensor:
         """`append(keys, values)` then `attend(q)` in one library call (the page's
         `update_and_fetch` followed by `asym_quantized_sdpa`): one kernel launch
         for decode-shaped steps, the same results as the two calls."""
-        keys = _need_cuda(keys, torch.bfloat16, "keys")
-        values = _need_cuda(values, torch.bfloat16, "values")
-        q = _need_cuda(q, torch.bfloat16, "q")
+        keys = _need_cuda(keys, self.dtype, "keys")
+        values = _need_cuda(values, self.dtype, "values")
+        q = _need_cuda(q, self.dtype, "q")
         n = keys.shape[2]
         if tuple(keys.shape) != (self.batch, self.kv_heads, n, self.head_dim) or values.shape != keys.shape:
             raise ValueError("keys/values must be [B, Hkv, n, D]")
@@ -386,7 +408,7 @@ class IQCache:
         if scale is None:
             scale = 1.0 / math.sqrt(D)
         if out is None:
-            out = torch.empty((B, Hq, L, D), dtype=out_dtype, device=q.device)
+            out = torch.empty((B, Hq, L, D), dtype=out_dtype or self.dtype, device=q.device)
         if out.dtype not in (torch.float32, torch.bfloat16) or not out.is_contiguous():
             raise ValueError("out must be a contiguous bf16 or f32 tensor")
         out_f32 = 1 if out.dtype == torch.float32 else 0
@@ -396,7 +418,7 @@ class IQCache:
         d = self.desc()
         with self._on:
             check(lib().iq_cache_append_attend(ctypes.byref(d), _ptr(keys), _ptr(values), n, _ptr(q), Hq, L,
-                                               float(scale), 1 if causal else 0, _ptr(rotation.blocks_bf16),
+                                               float(scale), 1 if causal else 0, self._rot(rotation),
                                                _ptr(out), out_f32, _ptr(self._workspace), self._workspace.numel(),
                                                _stream(self.device.index)), "iq_cache_append_attend")
         return out

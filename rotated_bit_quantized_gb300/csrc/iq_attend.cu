@@ -1544,8 +1544,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-int validate(const iq_cache* c, const uint16_t* q, int q_heads, int nq, int causal, const void* rot,
-             const void* out) {
+int validate(const iq_cache* c, const void* q, int q_heads, int nq, int causal, const void* rot, const void* out) {
   int st = iq_cache_check(c);
   if (st != IQ_OK) return st;
   if (!q || !rot || !out) return fail(IQ_ERR_INVALID_ARG, "null q/rotation/out");
@@ -1673,17 +1672,22 @@ ReadMarks& read_marks() {
 // sequence (already counted in c->lens) are first encoded from k_new / v_new
 // inside the same kernel (see the fused append in attend_kernel); encode_wait
 // makes those writes wait for the previous grids.
-int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
-                const uint16_t* rot_bf16, void* out, int out_f32, void* workspace, size_t workspace_bytes,
-                iq_stream_t stream, const uint16_t* k_new, const uint16_t* v_new, int n_new, int mask_kind = 0,
+int attend_impl(const iq_cache* c, const void* q_in, int q_heads, int n_queries, float scale, int causal,
+                const void* rot_in, void* out, int out_f32, void* workspace, size_t workspace_bytes,
+                iq_stream_t stream, const void* k_new_in, const void* v_new_in, int n_new, int mask_kind = 0,
                 const void* mask = nullptr, long long mask_stride = 0, int encode_wait = 1) {
-  int st = validate(c, q, q_heads, n_queries, causal, rot_bf16, out);
+  int st = validate(c, q_in, q_heads, n_queries, causal, rot_in, out);
   if (st != IQ_OK) return st;
   if (!tuned_format(c)) {
     if (n_new > 0) return fail(IQ_ERR_UNSUPPORTED, "fused append for this cache format");
-    return attend_any(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
+    return attend_any(c, q_in, q_heads, n_queries, scale, causal, rot_in, out, out_f32, workspace, workspace_bytes,
                       stream, mask_kind, mask, mask_stride);
   }
+  // the tuned format holds bfloat16 data
+  const uint16_t* q = static_cast<const uint16_t*>(q_in);
+  const uint16_t* rot_bf16 = static_cast<const uint16_t*>(rot_in);
+  const uint16_t* k_new = static_cast<const uint16_t*>(k_new_in);
+  const uint16_t* v_new = static_cast<const uint16_t*>(v_new_in);
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
     return fail(IQ_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
   Plan bound;  // what iq_attend_workspace promised: an upper bound of this call's needs
@@ -1726,11 +1730,11 @@ int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries
   static thread_local Params prm;  // ~5 KB: kept off the stack
   std::memset(&prm, 0, sizeof(prm));
   prm.k_codes = c->k_codes;
-  prm.k_scales = c->k_scales;
-  prm.k_biases = c->k_biases;
+  prm.k_scales = static_cast<const uint16_t*>(c->k_scales);
+  prm.k_biases = static_cast<const uint16_t*>(c->k_biases);
   prm.v_codes = c->v_codes;
-  prm.v_scales = c->v_scales;
-  prm.v_biases = c->v_biases;
+  prm.v_scales = static_cast<const uint16_t*>(c->v_scales);
+  prm.v_biases = static_cast<const uint16_t*>(c->v_biases);
   prm.q = q;
   prm.rot = rot_bf16;
   prm.part_o = part_o;
@@ -1782,22 +1786,22 @@ int attend_impl(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries
 
 extern "C" {
 
-int iq_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
-              const uint16_t* rot_bf16, void* out, int out_f32, void* workspace, size_t workspace_bytes,
+int iq_attend(const iq_cache* c, const void* q, int q_heads, int n_queries, float scale, int causal,
+              const void* rot, void* out, int out_f32, void* workspace, size_t workspace_bytes,
               iq_stream_t stream) {
   clear_error();
-  return attend_impl(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
+  return attend_impl(c, q, q_heads, n_queries, scale, causal, rot, out, out_f32, workspace, workspace_bytes,
                      stream, nullptr, nullptr, 0);
 }
 
-int iq_cache_append_attend(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n, const uint16_t* q,
-                           int q_heads, int n_queries, float scale, int causal, const uint16_t* rot_bf16,
+int iq_cache_append_attend(iq_cache* c, const void* keys, const void* values, int n, const void* q,
+                           int q_heads, int n_queries, float scale, int causal, const void* rot,
                            void* out, int out_f32, void* workspace, size_t workspace_bytes, iq_stream_t stream) {
   clear_error();
   int st = iq_cache_check(c);
   if (st != IQ_OK) return st;
   if (n < 1) return fail(IQ_ERR_INVALID_ARG, "append_attend needs n >= 1 new tokens");
-  if (!keys || !values || !rot_bf16) return fail(IQ_ERR_INVALID_ARG, "null keys/values/rotation");
+  if (!keys || !values || !rot) return fail(IQ_ERR_INVALID_ARG, "null keys/values/rotation");
   if (reinterpret_cast<uintptr_t>(keys) % 16 || reinterpret_cast<uintptr_t>(values) % 16)
     return fail(IQ_ERR_INVALID_ARG, "keys/values not 16-byte aligned");
   for (int b = 0; b < c->batch; ++b)
@@ -1812,27 +1816,27 @@ int iq_cache_append_attend(iq_cache* c, const uint16_t* keys, const uint16_t* va
   for (int b = 0; b < c->batch && fused; ++b)
     fused = c->lens[b] / tile == (c->lens[b] + n - 1) / tile;
   if (!fused) {
-    st = iq_cache_append(c, keys, values, n, rot_bf16, stream);
+    st = iq_cache_append(c, keys, values, n, rot, stream);
     if (st != IQ_OK) return st;
-    return iq_attend(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
+    return iq_attend(c, q, q_heads, n_queries, scale, causal, rot, out, out_f32, workspace, workspace_bytes,
                      stream);
   }
   static_assert(Cfg<IQ_DECODE_CFG>::TILE <= kFreshRows, "a fused append writes at most kFreshRows rows");
   const int encode_wait = read_marks().append_clear(c) ? 0 : 1;
   for (int b = 0; b < c->batch; ++b) c->lens[b] += n;
-  st = attend_impl(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, workspace, workspace_bytes,
+  st = attend_impl(c, q, q_heads, n_queries, scale, causal, rot, out, out_f32, workspace, workspace_bytes,
                    stream, keys, values, n, 0, nullptr, 0, encode_wait);
   if (st != IQ_OK)
     for (int b = 0; b < c->batch; ++b) c->lens[b] -= n;  // nothing was launched
   return st;
 }
 
-int iq_attend_mask(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int mask_kind,
-                   const void* mask, long long mask_stride, const uint16_t* rot_bf16, void* out, int out_f32,
+int iq_attend_mask(const iq_cache* c, const void* q, int q_heads, int n_queries, float scale, int mask_kind,
+                   const void* mask, long long mask_stride, const void* rot, void* out, int out_f32,
                    void* workspace, size_t workspace_bytes, iq_stream_t stream) {
   clear_error();
   if (mask_kind == IQ_MASK_NONE || mask_kind == IQ_MASK_CAUSAL)
-    return attend_impl(c, q, q_heads, n_queries, scale, mask_kind, rot_bf16, out, out_f32, workspace,
+    return attend_impl(c, q, q_heads, n_queries, scale, mask_kind, rot, out, out_f32, workspace,
                        workspace_bytes, stream, nullptr, nullptr, 0);
   if (mask_kind != IQ_MASK_ADD_F32 && mask_kind != IQ_MASK_BOOL_U8)
     return fail(IQ_ERR_INVALID_ARG, "unknown mask kind");
@@ -1845,7 +1849,7 @@ int iq_attend_mask(const iq_cache* c, const uint16_t* q, int q_heads, int n_quer
     return fail(IQ_ERR_INVALID_ARG, "mask not 16-byte aligned or its row stride not a multiple of 128");
   for (int b = 0; b < c->batch; ++b)
     if (mask_stride < c->lens[b]) return fail(IQ_ERR_INVALID_ARG, "mask row shorter than a sequence");
-  return attend_impl(c, q, q_heads, n_queries, scale, 0, rot_bf16, out, out_f32, workspace, workspace_bytes,
+  return attend_impl(c, q, q_heads, n_queries, scale, 0, rot, out, out_f32, workspace, workspace_bytes,
                      stream, nullptr, nullptr, 0, mask_kind, mask, mask_stride);
 }
 

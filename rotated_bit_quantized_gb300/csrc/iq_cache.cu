@@ -229,21 +229,23 @@ int iq_build_rotation(int head_dim, const float* draws_host, float* rot_f32, uin
 }
 
 int iq_cache_bytes(int batch, int kv_heads, int head_dim, int group_size, int k_bits, int v_bits,
-                   int capacity, size_t out_bytes[6]) {
+                   int capacity, int dtype, size_t out_bytes[6]) {
   clear_error();
   if (!out_bytes) return fail(IQ_ERR_INVALID_ARG, "null out_bytes");
   if (batch <= 0 || kv_heads <= 0 || capacity <= 0 || capacity % IQ_STEP)
     return fail(IQ_ERR_INVALID_ARG, "batch, kv_heads > 0 and capacity a positive multiple of 256 required");
+  if (dtype != IQ_DTYPE_BF16 && dtype != IQ_DTYPE_F32)
+    return fail(IQ_ERR_INVALID_ARG, "dtype must be IQ_DTYPE_BF16 or IQ_DTYPE_F32");
   if (!format_supported(head_dim, group_size, k_bits, v_bits))
     return fail(IQ_ERR_UNSUPPORTED,
                 "built formats: head_dim 256, group 32/64/128, k_bits and v_bits 2/3/4/5/6/8");
   if (batch > IQ_MAX_BATCH) return fail(IQ_ERR_UNSUPPORTED, "batch above IQ_MAX_BATCH");
   const size_t rows = static_cast<size_t>(batch) * kv_heads * capacity;
-  const size_t ng = head_dim / group_size;
+  const size_t ng = head_dim / group_size, esz = dtype == IQ_DTYPE_F32 ? 4 : 2;
   out_bytes[0] = rows * (head_dim * k_bits / 32) * 4;
-  out_bytes[1] = out_bytes[2] = rows * ng * 2;
+  out_bytes[1] = out_bytes[2] = rows * ng * esz;
   out_bytes[3] = rows * (head_dim * v_bits / 32) * 4;
-  out_bytes[4] = out_bytes[5] = rows * ng * 2;
+  out_bytes[4] = out_bytes[5] = rows * ng * esz;
   return IQ_OK;
 }
 
@@ -252,7 +254,7 @@ int iq_cache_check(const iq_cache* c) {
   if (!c) return fail(IQ_ERR_INVALID_ARG, "null cache");
   size_t bytes[6];
   int st = iq_cache_bytes(c->batch, c->kv_heads, c->head_dim, c->group_size, c->k_bits, c->v_bits,
-                          c->capacity, bytes);
+                          c->capacity, c->dtype, bytes);
   if (st != IQ_OK) return st;
   const void* ptrs[6] = {c->k_codes, c->k_scales, c->k_biases, c->v_codes, c->v_scales, c->v_biases};
   for (int i = 0; i < 6; ++i) {
@@ -266,7 +268,7 @@ int iq_cache_check(const iq_cache* c) {
 }
 
 int iq_cache_alloc(iq_cache* c, int batch, int kv_heads, int head_dim, int group_size, int k_bits, int v_bits,
-                   int capacity, void* const buffers[6], int32_t* lens_host) {
+                   int capacity, int dtype, void* const buffers[6], int32_t* lens_host) {
   clear_error();
   if (!c || !buffers || !lens_host) return fail(IQ_ERR_INVALID_ARG, "null cache, buffers or lens");
   iq_cache d;
@@ -277,12 +279,13 @@ int iq_cache_alloc(iq_cache* c, int batch, int kv_heads, int head_dim, int group
   d.k_bits = k_bits;
   d.v_bits = v_bits;
   d.capacity = capacity;
+  d.dtype = dtype;
   d.k_codes = static_cast<uint32_t*>(buffers[0]);
-  d.k_scales = static_cast<uint16_t*>(buffers[1]);
-  d.k_biases = static_cast<uint16_t*>(buffers[2]);
+  d.k_scales = buffers[1];
+  d.k_biases = buffers[2];
   d.v_codes = static_cast<uint32_t*>(buffers[3]);
-  d.v_scales = static_cast<uint16_t*>(buffers[4]);
-  d.v_biases = static_cast<uint16_t*>(buffers[5]);
+  d.v_scales = buffers[4];
+  d.v_biases = buffers[5];
   d.lens = lens_host;
   if (batch > 0 && batch <= IQ_MAX_BATCH)
     for (int b = 0; b < batch; ++b) lens_host[b] = 0;  // an empty cache (the page's offset 0)
@@ -305,7 +308,7 @@ int iq_cache_grow(const iq_cache* src, iq_cache* dst, iq_stream_t stream) {
 size_t iq_cache_nbytes(const iq_cache* c) {
   size_t bytes[6];
   if (!c || iq_cache_bytes(c->batch, c->kv_heads, c->head_dim, c->group_size, c->k_bits, c->v_bits,
-                           c->capacity, bytes) != IQ_OK)
+                           c->capacity, c->dtype, bytes) != IQ_OK)
     return 0;
   size_t t = 0;
   for (int i = 0; i < 6; ++i) t += bytes[i];
@@ -328,15 +331,15 @@ int append_blocks_per_sm() {
 }
 }  // namespace
 
-int iq_cache_append(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n,
-                    const uint16_t* rot_bf16, iq_stream_t stream) {
+int iq_cache_append(iq_cache* c, const void* keys, const void* values, int n, const void* rot,
+                    iq_stream_t stream) {
   int st = iq_cache_check(c);
   if (st != IQ_OK) return st;
   if (n < 0) return fail(IQ_ERR_INVALID_ARG, "negative token count");
   if (n == 0) return IQ_OK;
-  if (!keys || !values || !rot_bf16) return fail(IQ_ERR_INVALID_ARG, "null keys/values/rotation");
+  if (!keys || !values || !rot) return fail(IQ_ERR_INVALID_ARG, "null keys/values/rotation");
   if (reinterpret_cast<uintptr_t>(keys) % 16 || reinterpret_cast<uintptr_t>(values) % 16 ||
-      reinterpret_cast<uintptr_t>(rot_bf16) % 16)
+      reinterpret_cast<uintptr_t>(rot) % 16)
     return fail(IQ_ERR_INVALID_ARG, "keys/values/rotation not 16-byte aligned");
   for (int b = 0; b < c->batch; ++b)
     if (static_cast<long long>(c->lens[b]) + n > c->capacity)
@@ -344,22 +347,22 @@ int iq_cache_append(iq_cache* c, const uint16_t* keys, const uint16_t* values, i
   if (static_cast<long long>(c->batch) * c->kv_heads * c->capacity >= (1LL << 31))
     return fail(IQ_ERR_UNSUPPORTED, "cache rows exceed 2^31");
   if (!tuned_format(c)) {
-    st = append_any(c, keys, values, n, rot_bf16, stream);
+    st = append_any(c, keys, values, n, rot, stream);
     if (st != IQ_OK) return st;
     for (int b = 0; b < c->batch; ++b) c->lens[b] += n;
     return IQ_OK;
   }
   AppendParams p;
   std::memset(&p, 0, sizeof(p));
-  p.keys = keys;
-  p.values = values;
+  p.keys = static_cast<const uint16_t*>(keys);
+  p.values = static_cast<const uint16_t*>(values);
   p.k_codes = c->k_codes;
-  p.k_scales = c->k_scales;
-  p.k_biases = c->k_biases;
+  p.k_scales = static_cast<uint16_t*>(c->k_scales);
+  p.k_biases = static_cast<uint16_t*>(c->k_biases);
   p.v_codes = c->v_codes;
-  p.v_scales = c->v_scales;
-  p.v_biases = c->v_biases;
-  p.rot = rot_bf16;
+  p.v_scales = static_cast<uint16_t*>(c->v_scales);
+  p.v_biases = static_cast<uint16_t*>(c->v_biases);
+  p.rot = static_cast<const uint16_t*>(rot);
   p.batch = c->batch;
   p.heads = c->kv_heads;
   p.n = n;
@@ -418,8 +421,9 @@ int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of, i
   if (st != IQ_OK) return st;
   if (!src_of) return fail(IQ_ERR_INVALID_ARG, "null src_of");
   if (src->kv_heads != dst->kv_heads || src->head_dim != dst->head_dim ||
-      src->group_size != dst->group_size || src->k_bits != dst->k_bits || src->v_bits != dst->v_bits)
-    return fail(IQ_ERR_INVALID_ARG, "src and dst shapes differ");
+      src->group_size != dst->group_size || src->k_bits != dst->k_bits || src->v_bits != dst->v_bits ||
+      src->dtype != dst->dtype)
+    return fail(IQ_ERR_INVALID_ARG, "src and dst shapes or dtypes differ");
   GatherParams p;
   std::memset(&p, 0, sizeof(p));
   int max_len = 0;
@@ -432,7 +436,8 @@ int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of, i
   }
   const void* sp[6] = {src->k_codes, src->k_scales, src->k_biases, src->v_codes, src->v_scales, src->v_biases};
   void* dp[6] = {dst->k_codes, dst->k_scales, dst->k_biases, dst->v_codes, dst->v_scales, dst->v_biases};
-  const int ngw = dst->head_dim / dst->group_size / 2;  // bf16 scales (or biases) per row, in 4-byte words
+  // scales (or biases) per row in 4-byte words: two bf16 or one f32 per word
+  const int ngw = dst->head_dim / dst->group_size / (dst->dtype == IQ_DTYPE_F32 ? 1 : 2);
   const int units[6] = {dst->head_dim * dst->k_bits / 32, ngw, ngw, dst->head_dim * dst->v_bits / 32, ngw, ngw};
   for (int i = 0; i < 6; ++i) {
     if (sp[i] == dp[i]) return fail(IQ_ERR_INVALID_ARG, "src and dst share a buffer");

@@ -27,19 +27,19 @@ void clear_error();
 int num_sms();  // multiprocessor count of the current device (cached per device)
 
 // Cache formats (iq_generic.cu): the tuned one (k 4 bits, v 3 bits, 64-dim
-// groups) runs the tuned kernels, every other supported one the generic path.
+// groups, bfloat16) runs the tuned kernels, every other supported one (any
+// float32 cache included) the generic path.
 bool tuned_format(const iq_cache* c);
 bool format_supported(int head_dim, int group_size, int k_bits, int v_bits);
-int append_any(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n, const uint16_t* rot,
-               iq_stream_t stream);
+int append_any(iq_cache* c, const void* keys, const void* values, int n, const void* rot, iq_stream_t stream);
 int attend_any_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* bytes);
 // Prefill shapes (iq_prefill.cu): many query rows per kv head, tuned format,
 // no explicit mask: the tensor-memory kernel.
 bool prefill_shape(const iq_cache* c, int q_heads, int n_queries, int mask_kind);
 int prefill_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
                    const uint16_t* rot, void* out, int out_f32, unsigned* status, iq_stream_t stream);
-int attend_any(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
-               const uint16_t* rot, void* out, int out_f32, void* workspace, size_t workspace_bytes,
+int attend_any(const iq_cache* c, const void* q, int q_heads, int n_queries, float scale, int causal,
+               const void* rot, void* out, int out_f32, void* workspace, size_t workspace_bytes,
                iq_stream_t stream, int mask_kind, const void* mask, long long mask_stride);
 
 // ------------------------------------------------------------------ device side

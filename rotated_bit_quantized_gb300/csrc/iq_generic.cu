@@ -1,7 +1,8 @@
 // libiqkv: every cache format the page's cache class can be built with, other
-// than the tuned one (4-bit keys, 3-bit values, 64-dim groups): key and value
-// widths of 2, 3, 4, 5, 6 or 8 bits and groups of 32, 64 or 128 dims, head_dim
-// 256, bf16 scales and biases.
+// than the tuned one (4-bit keys, 3-bit values, 64-dim groups, bfloat16): key
+// and value widths of 2, 3, 4, 5, 6 or 8 bits, groups of 32, 64 or 128 dims,
+// head_dim 256, and bfloat16 or float32 data (the page's `_init_quant` stores
+// scales and biases in the keys' dtype, and `rotate_last` casts M to it).
 //
 // Method source: page "sparkle mlx_streaming/core/cache/quant_kv.py":
 // `AsymmetricQuantizedKVCache(k_bits, v_bits, group_size)` with
@@ -11,13 +12,17 @@
 // `asym_quantized_sdpa` (GQA, causal or explicit masks, softmax, P.V, output
 // left in rotated space, undone here by M_b^T).
 //
-// The arithmetic is the tuned path's (same rotation, same quantiser rounding,
-// same bf16 output rounding), written for run-time widths: the append encodes
-// a row per warp; the attention dequantises each key and value row in float32
-// (k = s * c + b with one rounding) and accumulates scores, softmax and P.V in
-// float32, split over the keys, then a merge kernel combines the splits.  It
-// is a correctness-first path for these formats: the performance work went to
-// the tuned format.
+// The bfloat16 arithmetic is the tuned path's (same rotation, same quantiser
+// rounding, same bf16 output rounding), written for run-time widths: the
+// append encodes a row per warp; the attention dequantises each key and value
+// row in float32 (k = s * c + b with one rounding) and accumulates scores,
+// softmax and P.V in float32, split over the keys, then a merge kernel
+// combines the splits.  float32 data takes the same steps with float32
+// rounding in place of bfloat16: the rotation's products and sums are each
+// rounded to float32 in block-row order (the f32 M blocks), the scale is kept
+// as computed, queries are rotated and scaled in float32, and the scales and
+// biases are read as float32.  It is a correctness-first path for these
+// formats: the performance work went to the tuned format.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -38,16 +43,74 @@ bool supported_group(int g) { return g == 32 || g == 64 || g == 128; }
 
 // ------------------------------------------------------------------ encode
 
-// Rotate, quantise and pack one row held by a warp with `bits`-bit codes and
-// `gs`-dim groups: lane l owns dims 8l..8l+7, group g is lanes
+// The two f32 M blocks 2*lane and 2*lane+1 (32 floats) as m[c][i][j].
+__device__ __forceinline__ void load_row_rotation_f32(const float* rot, int lane, float (&m)[2][4][4]) {
+  const float4* r4 = reinterpret_cast<const float4*>(rot) + lane * 8;
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = __ldg(r4 + 4 * c + i);
+      m[c][i][0] = v.x;
+      m[c][i][1] = v.y;
+      m[c][i][2] = v.z;
+      m[c][i][3] = v.w;
+    }
+}
+
+// The lane's 8 float32 dims rotated by its two M blocks:
+// y[4c+j] = (((x0*M[0][j] + x1*M[1][j]) + x2*M[2][j]) + x3*M[3][j]) with
+// x_i = x[4c+i], every product and every sum rounded to float32 (no fused
+// multiply-add), i.e. a float32 row-vector times matrix taken in index order.
+__device__ __forceinline__ void rotate_row_f32(const float (&x)[8], const float (&m)[2][4][4], float (&y)[8]) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float a = __fmul_rn(x[4 * c], m[c][0][j]);
+#pragma unroll
+      for (int i = 1; i < 4; ++i) a = __fadd_rn(a, __fmul_rn(x[4 * c + i], m[c][i][j]));
+      y[4 * c + j] = a;
+    }
+}
+
+// Load the lane's 8 dims of row `row` of a [.., D] array of the data dtype
+// and rotate them (rounded to that dtype).
+template <bool F32>
+__device__ __forceinline__ void load_rotate_row(const void* base, long long row, int lane, const float (&m)[2][4][4],
+                                                float (&y)[8]) {
+  if constexpr (F32) {
+    const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * kHeadDim + lane * 8);
+    const float4 a = __ldg(p4), b = __ldg(p4 + 1);
+    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    rotate_row_f32(x, m, y);
+  } else {
+    const uint4 raw =
+        __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + row * kHeadDim + lane * 8));
+    rotate_row_bf16(raw, m, y);
+  }
+}
+
+template <bool F32>
+__device__ __forceinline__ void load_rotation(const void* rot, int lane, float (&m)[2][4][4]) {
+  if constexpr (F32)
+    load_row_rotation_f32(static_cast<const float*>(rot), lane, m);
+  else
+    load_row_rotation(static_cast<const uint16_t*>(rot), lane, m);
+}
+
+// Quantise and pack one rotated row held by a warp (y: the lane's 8 dims,
+// already rounded to the data dtype) with `bits`-bit codes and `gs`-dim
+// groups: lane l owns dims 8l..8l+7, group g is lanes
 // g*gs/8 .. (g+1)*gs/8 - 1, the lane's 8 codes are stream bits
-// [8*bits*l, 8*bits*(l+1)) of the row's 8*bits words.
-__device__ void encode_row_any(const uint4 raw, const float (&m)[2][4][4], int lane, long long dst, int bits, int gs,
-                               uint32_t* codes_out, uint16_t* scales_out, uint16_t* biases_out) {
+// [8*bits*l, 8*bits*(l+1)) of the row's 8*bits words.  The scale is rounded
+// to bfloat16 (bfloat16 data) or kept (float32 data) before the codes are
+// formed from it; scales and biases are stored in the data dtype.
+template <bool F32>
+__device__ void encode_row_any(const float (&y)[8], int lane, long long dst, int bits, int gs, uint32_t* codes_out,
+                               void* scales_out, void* biases_out) {
   const int levels = (1 << bits) - 1;
   const int words = 8 * bits, span = 8 * bits, ng = kHeadDim / gs;
-  float y[8];
-  rotate_row_bf16(raw, m, y);
   float mn = y[0], mx = y[0];
 #pragma unroll
   for (int e = 1; e < 8; ++e) {
@@ -59,8 +122,8 @@ __device__ void encode_row_any(const uint4 raw, const float (&m)[2][4][4], int l
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
   const float scale = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(levels));
-  const uint32_t s_bits = f32_to_bf16_bits(scale);
-  const float s_hat = bf16_to_f32(s_bits);
+  const uint32_t s_bits = F32 ? __float_as_uint(scale) : f32_to_bf16_bits(scale);
+  const float s_hat = F32 ? scale : bf16_to_f32(s_bits);
   // code = clamp(rint(d / s_hat)), d = y - mn, IEEE quotient.  The product
   // d * (1/s_hat) (both correctly rounded) is within 3 * 2^-24 * q of that
   // quotient, below 2^-14 for q < 256, so it rounds the same way unless it lies
@@ -107,44 +170,51 @@ __device__ void encode_row_any(const uint4 raw, const float (&m)[2][4][4], int l
     }
   }
   // scales and biases: group g's values from its first lane
-  const uint32_t b_bits = f32_to_bf16_bits(mn);
+  const uint32_t b_bits = F32 ? __float_as_uint(mn) : f32_to_bf16_bits(mn);
   const int src = min(lane, ng - 1) * (gs / 8);
   const uint32_t sg = __shfl_sync(0xffffffffu, s_bits, src);
   const uint32_t bg = __shfl_sync(0xffffffffu, b_bits, src);
   if (lane < ng) {
-    scales_out[dst * ng + lane] = static_cast<uint16_t>(sg);
-    biases_out[dst * ng + lane] = static_cast<uint16_t>(bg);
+    if constexpr (F32) {
+      static_cast<uint32_t*>(scales_out)[dst * ng + lane] = sg;
+      static_cast<uint32_t*>(biases_out)[dst * ng + lane] = bg;
+    } else {
+      static_cast<uint16_t*>(scales_out)[dst * ng + lane] = static_cast<uint16_t>(sg);
+      static_cast<uint16_t*>(biases_out)[dst * ng + lane] = static_cast<uint16_t>(bg);
+    }
   }
 }
 
 struct AppendArgs {
-  const uint16_t* keys;
-  const uint16_t* values;
+  const void* keys;
+  const void* values;
   uint32_t* k_codes;
-  uint16_t* k_scales;
-  uint16_t* k_biases;
+  void* k_scales;
+  void* k_biases;
   uint32_t* v_codes;
-  uint16_t* v_scales;
-  uint16_t* v_biases;
-  const uint16_t* rot;
+  void* v_scales;
+  void* v_biases;
+  const void* rot;
   int heads, n, cap, kbits, vbits, gs;
   int lens[IQ_MAX_BATCH];
 };
 
 // One warp per token row (sequence b, kv head h, token i); blockIdx.y = b * heads + h.
+template <bool F32>
 __global__ void __launch_bounds__(256) append_any_kernel(const __grid_constant__ AppendArgs p) {
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
   float m[2][4][4];
-  load_row_rotation(p.rot, lane, m);
+  load_rotation<F32>(p.rot, lane, m);
   const long long dst0 = static_cast<long long>(bh) * p.cap + p.lens[bh / p.heads];
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < p.n; i += warps) {
-    const long long src = (static_cast<long long>(bh) * p.n + i) * kHeadDim + lane * 8;
-    const uint4 rk = __ldg(reinterpret_cast<const uint4*>(p.keys + src));
-    const uint4 rv = __ldg(reinterpret_cast<const uint4*>(p.values + src));
-    encode_row_any(rk, m, lane, dst0 + i, p.kbits, p.gs, p.k_codes, p.k_scales, p.k_biases);
-    encode_row_any(rv, m, lane, dst0 + i, p.vbits, p.gs, p.v_codes, p.v_scales, p.v_biases);
+    const long long row = static_cast<long long>(bh) * p.n + i;
+    float yk[8], yv[8];
+    load_rotate_row<F32>(p.keys, row, lane, m, yk);
+    load_rotate_row<F32>(p.values, row, lane, m, yv);
+    encode_row_any<F32>(yk, lane, dst0 + i, p.kbits, p.gs, p.k_codes, p.k_scales, p.k_biases);
+    encode_row_any<F32>(yv, lane, dst0 + i, p.vbits, p.gs, p.v_codes, p.v_scales, p.v_biases);
   }
 }
 
@@ -152,13 +222,13 @@ __global__ void __launch_bounds__(256) append_any_kernel(const __grid_constant__
 
 struct AttendArgs {
   const uint32_t* k_codes;
-  const uint16_t* k_scales;
-  const uint16_t* k_biases;
+  const void* k_scales;
+  const void* k_biases;
   const uint32_t* v_codes;
-  const uint16_t* v_scales;
-  const uint16_t* v_biases;
-  const uint16_t* q;
-  const uint16_t* rot;
+  const void* v_scales;
+  const void* v_biases;
+  const void* q;
+  const void* rot;
   void* out;
   float* part_o;   // [B*Hkv][rtiles][nch][8][256]
   float* part_ml;  // [B*Hkv][rtiles][nch][8][2]: max (log2 units) and sum
@@ -184,9 +254,9 @@ __device__ __forceinline__ LaneBits lane_bits(int bits, int gs, int lane) {
 // Dequantised dims 8*lane .. 8*lane+7 of row r of a staged tile, BITS-bit
 // codes: s * c + b with one rounding each (c < 2^23 becomes a float exactly by
 // the 2^23 magic number).  The lane's window is at most 64 bits, so two words
-// hold it.
-template <int BITS>
-__device__ __forceinline__ void dequant_bits(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+// hold it.  Scales and biases are bfloat16 or float32 (F32) values.
+template <int BITS, bool F32>
+__device__ __forceinline__ void dequant_bits(const uint32_t* codes, const uint32_t* scales, const uint32_t* biases,
                                              int r, int ng, LaneBits lb, float (&x)[8]) {
   constexpr int WORDS = 8 * BITS;
   constexpr uint32_t MASK = (1u << BITS) - 1u;
@@ -194,7 +264,14 @@ __device__ __forceinline__ void dequant_bits(const uint32_t* codes, const uint16
   const uint32_t a = row[lb.w0];
   const uint32_t b = lb.w0 + 1 < WORDS ? row[lb.w0 + 1] : 0u;
   const uint32_t lo = __funnelshift_r(a, b, lb.sh), hi = __funnelshift_r(b, 0u, lb.sh);
-  const float s = bf16_to_f32(scales[r * ng + lb.g]), bb = bf16_to_f32(biases[r * ng + lb.g]);
+  float s, bb;
+  if constexpr (F32) {
+    s = __uint_as_float(scales[r * ng + lb.g]);
+    bb = __uint_as_float(biases[r * ng + lb.g]);
+  } else {
+    s = bf16_to_f32(reinterpret_cast<const uint16_t*>(scales)[r * ng + lb.g]);
+    bb = bf16_to_f32(reinterpret_cast<const uint16_t*>(biases)[r * ng + lb.g]);
+  }
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int off = BITS * e;
@@ -209,15 +286,16 @@ __device__ __forceinline__ void dequant_bits(const uint32_t* codes, const uint16
   }
 }
 
-__device__ __forceinline__ void dequant_lane(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+template <bool F32>
+__device__ __forceinline__ void dequant_lane(const uint32_t* codes, const uint32_t* scales, const uint32_t* biases,
                                              int r, int bits, int ng, LaneBits lb, float (&x)[8]) {
   switch (bits) {  // uniform over the grid
-    case 2: dequant_bits<2>(codes, scales, biases, r, ng, lb, x); break;
-    case 3: dequant_bits<3>(codes, scales, biases, r, ng, lb, x); break;
-    case 4: dequant_bits<4>(codes, scales, biases, r, ng, lb, x); break;
-    case 5: dequant_bits<5>(codes, scales, biases, r, ng, lb, x); break;
-    case 6: dequant_bits<6>(codes, scales, biases, r, ng, lb, x); break;
-    default: dequant_bits<8>(codes, scales, biases, r, ng, lb, x); break;
+    case 2: dequant_bits<2, F32>(codes, scales, biases, r, ng, lb, x); break;
+    case 3: dequant_bits<3, F32>(codes, scales, biases, r, ng, lb, x); break;
+    case 4: dequant_bits<4, F32>(codes, scales, biases, r, ng, lb, x); break;
+    case 5: dequant_bits<5, F32>(codes, scales, biases, r, ng, lb, x); break;
+    case 6: dequant_bits<6, F32>(codes, scales, biases, r, ng, lb, x); break;
+    default: dequant_bits<8, F32>(codes, scales, biases, r, ng, lb, x); break;
   }
 }
 
@@ -229,12 +307,12 @@ __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_
 
 constexpr int kTileKeys = 32;                                // keys per staged tile
 constexpr int kTileCodeBytes = kTileKeys * kHeadDim;         // 32 rows x 256 B (8-bit codes at most)
-constexpr int kTileMetaBytes = kTileKeys * (kHeadDim / 32) * 2;  // 32 rows x 8 groups x bf16 at most
+constexpr int kTileMetaBytes = kTileKeys * (kHeadDim / 32) * 4;  // 32 rows x 8 groups x f32 at most
 
 struct Stage {
   uint32_t kc[kTileCodeBytes / 4];
   uint32_t vc[kTileCodeBytes / 4];
-  uint16_t ks[kTileMetaBytes / 2], kb[kTileMetaBytes / 2], vs[kTileMetaBytes / 2], vb[kTileMetaBytes / 2];
+  uint32_t ks[kTileMetaBytes / 4], kb[kTileMetaBytes / 4], vs[kTileMetaBytes / 4], vb[kTileMetaBytes / 4];
 };
 
 // grid (nch, B*Hkv, rtiles), 128 threads.  CTA (x, bh, z): the 8 query rows of
@@ -242,7 +320,8 @@ struct Stage {
 // through shared memory in 32-key tiles, two in flight (cp.async, 16-byte
 // pieces: every row and every tile's scale block starts 16-byte aligned); warp
 // w owns rows 2w and 2w+1 over every key, lane l dims 8l .. 8l+7.  Softmax
-// state in log2 units.
+// state in log2 units.  F32: float32 queries, rotation, scales and biases.
+template <bool F32>
 __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__ AttendArgs p) {
   constexpr float LOG2E = 1.4426950408889634f;
   constexpr float NEG = -__builtin_huge_valf();
@@ -255,8 +334,9 @@ __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__
   const int c0 = x * per;
 
   float m[2][4][4];
-  load_row_rotation(p.rot, lane, m);
-  // q'' = bf16(bf16(q @ M_b) * scale) of the warp's two rows, the lane's 8 dims
+  load_rotation<F32>(p.rot, lane, m);
+  // q'' = rnd(rnd(q @ M) * scale) of the warp's two rows, the lane's 8 dims,
+  // rnd rounding to the data dtype (M = M_b for bfloat16 data)
   float qq[2][8];
   int qpos[2], qidx[2];
   int cmax = -1;  // the last key some row of the tile may see
@@ -266,15 +346,13 @@ __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__
     const bool rv = R < p.rows;
     qidx[j] = min(i, p.nq - 1);
     qpos[j] = rv ? (p.causal ? T - p.nq + i : T - 1) : -1;
-    uint4 raw = make_uint4(0, 0, 0, 0);
+    float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (rv) {
       const long long qrow = (static_cast<long long>(b) * p.kv_heads * p.rep + h * p.rep + hr) * p.nq + i;
-      raw = __ldg(reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim + 8 * lane));
+      load_rotate_row<F32>(p.q, qrow, lane, m, y);
     }
-    float y[8];
-    rotate_row_bf16(raw, m, y);
 #pragma unroll
-    for (int d = 0; d < 8; ++d) qq[j][d] = round_bf16(__fmul_rn(y[d], p.scale));
+    for (int d = 0; d < 8; ++d) qq[j][d] = F32 ? __fmul_rn(y[d], p.scale) : round_bf16(__fmul_rn(y[d], p.scale));
   }
   {
     const int R = min(8 * z + 7, p.rows - 1), i = R / p.rep;
@@ -284,7 +362,8 @@ __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__
 
   // staging of tile [t, t + 32): codes rows, then the scale and bias blocks
   const int kbytes = kTileKeys * 32 * p.kbits, vbytes = kTileKeys * 32 * p.vbits;
-  const int ng = kHeadDim / p.gs, mbytes = kTileKeys * ng * 2;
+  constexpr int esz = F32 ? 4 : 2;  // bytes per scale or bias
+  const int ng = kHeadDim / p.gs, mbytes = kTileKeys * ng * esz;
   const LaneBits klb = lane_bits(p.kbits, p.gs, lane), vlb = lane_bits(p.vbits, p.gs, lane);
   const long long row0 = static_cast<long long>(bh) * p.cap;
   auto stage = [&](int s, int t) {
@@ -294,12 +373,12 @@ __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__
       cp_async16(reinterpret_cast<uint8_t*>(st[s].kc) + o, kc + o);
     for (int o = threadIdx.x * 16; o < vbytes; o += blockDim.x * 16)
       cp_async16(reinterpret_cast<uint8_t*>(st[s].vc) + o, vc + o);
-    const long long mo = (row0 + t) * ng * 2;
+    const long long mo = (row0 + t) * ng * esz;
     for (int o = threadIdx.x * 16; o < 4 * mbytes; o += blockDim.x * 16) {
       const int which = o / mbytes, oo = o % mbytes;
-      const uint16_t* src = which == 0 ? p.k_scales : which == 1 ? p.k_biases : which == 2 ? p.v_scales : p.v_biases;
-      uint16_t* dst = which == 0 ? st[s].ks : which == 1 ? st[s].kb : which == 2 ? st[s].vs : st[s].vb;
-      cp_async16(reinterpret_cast<uint8_t*>(dst) + oo, reinterpret_cast<const uint8_t*>(src) + mo + oo);
+      const void* src = which == 0 ? p.k_scales : which == 1 ? p.k_biases : which == 2 ? p.v_scales : p.v_biases;
+      uint32_t* dst = which == 0 ? st[s].ks : which == 1 ? st[s].kb : which == 2 ? st[s].vs : st[s].vb;
+      cp_async16(reinterpret_cast<uint8_t*>(dst) + oo, static_cast<const uint8_t*>(src) + mo + oo);
     }
   };
 
@@ -325,8 +404,8 @@ __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int r = min(r0 + u, nk - 1);  // a second key past the end repeats the first (masked below)
-        dequant_lane(S.kc, S.ks, S.kb, r, p.kbits, ng, klb, k[u]);
-        dequant_lane(S.vc, S.vs, S.vb, r, p.vbits, ng, vlb, v[u]);
+        dequant_lane<F32>(S.kc, S.ks, S.kb, r, p.kbits, ng, klb, k[u]);
+        dequant_lane<F32>(S.vc, S.vs, S.vb, r, p.vbits, ng, vlb, v[u]);
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u)
@@ -389,7 +468,9 @@ __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__
 
 // grid (B*Hkv, rtiles), 256 threads: thread (row r, lane) merges dims
 // 8*lane .. 8*lane+7 of row 8*z + r over the splits, normalises, undoes the
-// rotation (out[4c+i] = sum_j o[4c+j] * M_b[c][i][j]) and stores.
+// rotation (out[4c+i] = sum_j o[4c+j] * M[c][i][j], M = M_b for bfloat16
+// data) and stores.
+template <bool F32>
 __global__ void __launch_bounds__(256) merge_any_kernel(const __grid_constant__ AttendArgs p) {
   const int bh = blockIdx.x, z = blockIdx.y;
   const int r = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -414,7 +495,7 @@ __global__ void __launch_bounds__(256) merge_any_kernel(const __grid_constant__ 
   if (!(L > 0.f)) atomicOr(p.status, 4u);  // no key of the row has a finite score
   const float inv = 1.f / L;
   float m[2][4][4];
-  load_row_rotation(p.rot, lane, m);
+  load_rotation<F32>(p.rot, lane, m);
   float yv[8];
 #pragma unroll
   for (int c = 0; c < 2; ++c)
@@ -452,25 +533,26 @@ int chunks(int batch, int kv_heads, int rtiles) {
 
 // ------------------------------------------------------------------ host entry points
 
-bool tuned_format(const iq_cache* c) { return c->group_size == kGroup && c->k_bits == 4 && c->v_bits == 3; }
+bool tuned_format(const iq_cache* c) {
+  return c->dtype == IQ_DTYPE_BF16 && c->group_size == kGroup && c->k_bits == 4 && c->v_bits == 3;
+}
 
 bool format_supported(int head_dim, int group_size, int k_bits, int v_bits) {
   return head_dim == kHeadDim && gen::supported_group(group_size) && gen::supported_bits(k_bits) &&
          gen::supported_bits(v_bits);
 }
 
-int append_any(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n, const uint16_t* rot,
-               iq_stream_t stream) {
+int append_any(iq_cache* c, const void* keys, const void* values, int n, const void* rot, iq_stream_t stream) {
   gen::AppendArgs p;
   std::memset(&p, 0, sizeof(p));
   p.keys = keys;
   p.values = values;
   p.k_codes = c->k_codes;
-  p.k_scales = static_cast<uint16_t*>(c->k_scales);
-  p.k_biases = static_cast<uint16_t*>(c->k_biases);
+  p.k_scales = c->k_scales;
+  p.k_biases = c->k_biases;
   p.v_codes = c->v_codes;
-  p.v_scales = static_cast<uint16_t*>(c->v_scales);
-  p.v_biases = static_cast<uint16_t*>(c->v_biases);
+  p.v_scales = c->v_scales;
+  p.v_biases = c->v_biases;
   p.rot = rot;
   p.heads = c->kv_heads;
   p.n = n;
@@ -482,8 +564,11 @@ int append_any(iq_cache* c, const uint16_t* keys, const uint16_t* values, int n,
   const int bh = c->batch * c->kv_heads;
   long long gx = (static_cast<long long>(n) + 7) / 8;
   gx = std::min<long long>(gx, std::max(1LL, static_cast<long long>(num_sms()) * 8 / bh));
-  gen::append_any_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(bh)), 256, 0,
-                           static_cast<cudaStream_t>(stream)>>>(p);
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(bh));
+  if (c->dtype == IQ_DTYPE_F32)
+    gen::append_any_kernel<true><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  else
+    gen::append_any_kernel<false><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
   IQ_CUDA(cudaGetLastError());
   return IQ_OK;
 }
@@ -499,8 +584,8 @@ int attend_any_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* 
   return IQ_OK;
 }
 
-int attend_any(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
-               const uint16_t* rot, void* out, int out_f32, void* workspace, size_t workspace_bytes,
+int attend_any(const iq_cache* c, const void* q, int q_heads, int n_queries, float scale, int causal,
+               const void* rot, void* out, int out_f32, void* workspace, size_t workspace_bytes,
                iq_stream_t stream, int mask_kind, const void* mask, long long mask_stride) {
   size_t need = 0;
   int st = attend_any_workspace(c, q_heads, n_queries, &need);
@@ -511,11 +596,11 @@ int attend_any(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries,
   gen::AttendArgs p;
   std::memset(&p, 0, sizeof(p));
   p.k_codes = c->k_codes;
-  p.k_scales = static_cast<const uint16_t*>(c->k_scales);
-  p.k_biases = static_cast<const uint16_t*>(c->k_biases);
+  p.k_scales = c->k_scales;
+  p.k_biases = c->k_biases;
   p.v_codes = c->v_codes;
-  p.v_scales = static_cast<const uint16_t*>(c->v_scales);
-  p.v_biases = static_cast<const uint16_t*>(c->v_biases);
+  p.v_scales = c->v_scales;
+  p.v_biases = c->v_biases;
   p.q = q;
   p.rot = rot;
   p.out = out;
@@ -543,9 +628,17 @@ int attend_any(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries,
   for (int b = 0; b < c->batch; ++b) p.lens[b] = c->lens[b];
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned bh = static_cast<unsigned>(c->batch * c->kv_heads);
-  gen::attend_any_kernel<<<dim3(static_cast<unsigned>(p.nch), bh, static_cast<unsigned>(p.rtiles)), 128, 0, s>>>(p);
-  IQ_CUDA(cudaGetLastError());
-  gen::merge_any_kernel<<<dim3(bh, static_cast<unsigned>(p.rtiles)), 256, 0, s>>>(p);
+  const dim3 grid(static_cast<unsigned>(p.nch), bh, static_cast<unsigned>(p.rtiles));
+  const dim3 mgrid(bh, static_cast<unsigned>(p.rtiles));
+  if (c->dtype == IQ_DTYPE_F32) {
+    gen::attend_any_kernel<true><<<grid, 128, 0, s>>>(p);
+    IQ_CUDA(cudaGetLastError());
+    gen::merge_any_kernel<true><<<mgrid, 256, 0, s>>>(p);
+  } else {
+    gen::attend_any_kernel<false><<<grid, 128, 0, s>>>(p);
+    IQ_CUDA(cudaGetLastError());
+    gen::merge_any_kernel<false><<<mgrid, 256, 0, s>>>(p);
+  }
   IQ_CUDA(cudaGetLastError());
   return IQ_OK;
 }

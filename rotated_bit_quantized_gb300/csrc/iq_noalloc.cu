@@ -51,8 +51,8 @@ int scratch_address(void** out) {
 }  // namespace
 }  // namespace iq
 
-extern "C" int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q_heads, int n_queries,
-                                 float scale, int causal, const uint16_t* rot_bf16, void* out, int out_f32,
+extern "C" int iq_attend_noalloc(const iq_cache* cache, const void* q, int q_heads, int n_queries,
+                                 float scale, int causal, const void* rot, void* out, int out_f32,
                                  iq_stream_t stream) {
   iq::clear_error();
   int st = iq_cache_check(cache);
@@ -77,7 +77,7 @@ extern "C" int iq_attend_noalloc(const iq_cache* cache, const uint16_t* q, int q
   // The array is zero when the library loads, so its status word starts
   // clear; the split partials are written before they are read, and the unit
   // counters return to zero after every call (also one whose wait ran out).
-  return iq_attend(cache, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32, scratch,
+  return iq_attend(cache, q, q_heads, n_queries, scale, causal, rot, out, out_f32, scratch,
                    IQ_NOALLOC_SCRATCH_BYTES, stream);
 }
 

@@ -40,14 +40,18 @@ def test_status_strings(L):
 
 def test_cache_bytes(L):
     out = (ctypes.c_size_t * 6)()
-    assert L.iq_cache_bytes(2, 3, 256, 64, 4, 3, 512, out) == 0
+    assert L.iq_cache_bytes(2, 3, 256, 64, 4, 3, 512, 0, out) == 0
     rows = 2 * 3 * 512
     assert list(out) == [rows * 128, rows * 8, rows * 8, rows * 96, rows * 8, rows * 8]
-    assert L.iq_cache_bytes(2, 3, 256, 64, 4, 3, 500, out) == 1        # not a multiple of 256
-    assert L.iq_cache_bytes(2, 3, 128, 64, 4, 3, 512, out) == 4        # other head_dim
-    assert L.iq_cache_bytes(2, 3, 256, 64, 7, 3, 512, out) == 4        # a width the page does not list
-    assert L.iq_cache_bytes(2, 3, 256, 16, 4, 3, 512, out) == 4        # group size not built
-    assert L.iq_cache_bytes(300, 3, 256, 64, 4, 3, 512, out) == 4      # batch above maximum
+    # float32 scales and biases (page `_init_quant(..., dt)` with float32 keys): 4 bytes per group
+    assert L.iq_cache_bytes(2, 3, 256, 64, 4, 3, 512, 1, out) == 0
+    assert list(out) == [rows * 128, rows * 16, rows * 16, rows * 96, rows * 16, rows * 16]
+    assert L.iq_cache_bytes(2, 3, 256, 64, 4, 3, 512, 2, out) == 1     # unknown dtype
+    assert L.iq_cache_bytes(2, 3, 256, 64, 4, 3, 500, 0, out) == 1     # not a multiple of 256
+    assert L.iq_cache_bytes(2, 3, 128, 64, 4, 3, 512, 0, out) == 4     # other head_dim
+    assert L.iq_cache_bytes(2, 3, 256, 64, 7, 3, 512, 0, out) == 4     # a width the page does not list
+    assert L.iq_cache_bytes(2, 3, 256, 16, 4, 3, 512, 0, out) == 4     # group size not built
+    assert L.iq_cache_bytes(300, 3, 256, 64, 4, 3, 512, 0, out) == 4   # batch above maximum
     assert b"256" in L.iq_last_error() or L.iq_last_error()
 
 
@@ -56,16 +60,17 @@ def test_cache_bytes_other_formats(L, kb, vb, gs):
     # page `_packed_words`: dim * bits / 32 words per row; one bf16 scale and
     # bias per group
     out = (ctypes.c_size_t * 6)()
-    assert L.iq_cache_bytes(1, 2, 256, gs, kb, vb, 256, out) == 0
     rows = 2 * 256
     ng = 256 // gs
-    assert list(out) == [rows * 8 * kb * 4, rows * ng * 2, rows * ng * 2, rows * 8 * vb * 4, rows * ng * 2,
-                         rows * ng * 2]
+    for dtype, esz in ((0, 2), (1, 4)):
+        assert L.iq_cache_bytes(1, 2, 256, gs, kb, vb, 256, dtype, out) == 0
+        assert list(out) == [rows * 8 * kb * 4, rows * ng * esz, rows * ng * esz, rows * 8 * vb * 4,
+                             rows * ng * esz, rows * ng * esz]
 
 
-def fake_desc(batch=2, cap=256, lens=(3, 4), align=0):
+def fake_desc(batch=2, cap=256, lens=(3, 4), align=0, dtype=0):
     from rotated_bit_quantized_gb300._abi import IQCacheDesc
-    d = IQCacheDesc(batch, 2, 256, 64, 4, 3, cap)
+    d = IQCacheDesc(batch, 2, 256, 64, 4, 3, cap, dtype)
     base = 0x10000000 + align
     for i, name in enumerate(("k_codes", "k_scales", "k_biases", "v_codes", "v_scales", "v_biases")):
         setattr(d, name, base + i * 0x1000000)
@@ -90,6 +95,11 @@ def test_check_and_trim_host_only(L):
     assert L.iq_cache_trim(ctypes.byref(d), neg.ctypes.data_as(P), out.ctypes.data_as(P)) == 1
     assert lens.tolist() == [0, 3]
     assert L.iq_cache_nbytes(ctypes.byref(d)) == 2 * 2 * 256 * 256
+    df, _ = fake_desc(dtype=1)
+    assert L.iq_cache_check(ctypes.byref(df)) == 0
+    assert L.iq_cache_nbytes(ctypes.byref(df)) == 2 * 2 * 256 * (128 + 96 + 4 * 16)
+    dx, _ = fake_desc(dtype=5)
+    assert L.iq_cache_check(ctypes.byref(dx)) == 1
 
 
 def test_append_and_attend_reject_before_launch(L):
@@ -136,13 +146,16 @@ def test_cache_alloc_binds_and_validates(L):
     lens = np.array([7, 9], dtype=np.int32)
     P32 = ctypes.POINTER(ctypes.c_int32)
     bufs = (ctypes.c_void_p * 6)(*[0x10000000 + i * 0x1000000 for i in range(6)])
-    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 512, bufs, lens.ctypes.data_as(P32)) == 0
-    assert (d.batch, d.kv_heads, d.capacity, d.k_bits, d.v_bits) == (2, 2, 512, 4, 3)
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 512, 0, bufs, lens.ctypes.data_as(P32)) == 0
+    assert (d.batch, d.kv_heads, d.capacity, d.k_bits, d.v_bits, d.dtype) == (2, 2, 512, 4, 3, 0)
     assert d.v_biases == 0x15000000 and lens.tolist() == [0, 0]  # an empty cache
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 512, 1, bufs, lens.ctypes.data_as(P32)) == 0
+    assert d.dtype == 1
     bad = (ctypes.c_void_p * 6)(*[0x10000008 + i * 0x1000000 for i in range(6)])  # not 16-byte aligned
-    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 512, bad, lens.ctypes.data_as(P32)) == 1
-    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 7, 3, 512, bufs, lens.ctypes.data_as(P32)) == 4
-    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 500, bufs, lens.ctypes.data_as(P32)) == 1
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 512, 0, bad, lens.ctypes.data_as(P32)) == 1
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 7, 3, 512, 0, bufs, lens.ctypes.data_as(P32)) == 4
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 500, 0, bufs, lens.ctypes.data_as(P32)) == 1
+    assert L.iq_cache_alloc(ctypes.byref(d), 2, 2, 256, 64, 4, 3, 512, 3, bufs, lens.ctypes.data_as(P32)) == 1
 
 
 def test_cache_grow_rejects_before_copying(L):
@@ -157,3 +170,7 @@ def test_cache_grow_rejects_before_copying(L):
     assert L.iq_cache_grow(ctypes.byref(big_src), ctypes.byref(small), None) == 2  # dst capacity too small
     one, _ = fake_desc(batch=1, cap=512, lens=(0,))
     assert L.iq_cache_grow(ctypes.byref(src), ctypes.byref(one), None) == 1  # batch differs
+    f32dst, _ = fake_desc(batch=2, cap=512, lens=(0, 0), dtype=1)
+    for i, name in enumerate(("k_codes", "k_scales", "k_biases", "v_codes", "v_scales", "v_biases")):
+        setattr(f32dst, name, 0x50000000 + i * 0x1000000)
+    assert L.iq_cache_grow(ctypes.byref(src), ctypes.byref(f32dst), None) == 1  # dtype differs

@@ -26,8 +26,9 @@ def _call_noalloc(cache, q, rot, causal, out):
     from rotated_bit_quantized_gb300._abi import lib
     d = cache.desc()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    blocks = rot.blocks_f32 if cache.dtype == torch.float32 else rot.blocks_bf16
     return lib().iq_attend_noalloc(ctypes.byref(d), ctypes.c_void_p(q.data_ptr()), q.shape[1], q.shape[2],
-                                   1.0 / 16, 1 if causal else 0, ctypes.c_void_p(rot.blocks_bf16.data_ptr()),
+                                   1.0 / 16, 1 if causal else 0, ctypes.c_void_p(blocks.data_ptr()),
                                    ctypes.c_void_p(out.data_ptr()), 1 if out.dtype == torch.float32 else 0,
                                    stream)
 
@@ -87,6 +88,23 @@ def test_noalloc_other_paths(fmt, B, H, Hq, T, L):
         ref, out = _ref_and_noalloc(cache, rot, q, True)
         err = (out - ref).abs().max().item()
         assert err <= ATOL, f"call {call}: max abs difference {err}"
+    assert _read_noalloc_status() == (0, 0)
+    assert cache.device_status() == 0
+
+
+def test_noalloc_float32_cache():
+    """A float32 cache (float32 queries, scales and biases; the generic path)
+    through the no-allocation entry point: the same result as with a caller
+    workspace."""
+    from rotated_bit_quantized_gb300 import IQCache, Rotation
+    rot = Rotation(0, 256)
+    cache = IQCache(2, 2, dtype=torch.float32)
+    k, v = si.kv_tokens(64, 2, 2, 1200, outliers=True, dtype=torch.float32)
+    cache.append(k.cuda(), v.cuda(), rot)
+    for call in range(2):
+        q = si.queries(70 + call, 2, 16, 2, dtype=torch.float32).cuda()
+        ref, out = _ref_and_noalloc(cache, rot, q, True)
+        assert (out - ref).abs().max().item() <= 1e-6
     assert _read_noalloc_status() == (0, 0)
     assert cache.device_status() == 0
 
