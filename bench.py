@@ -47,8 +47,8 @@ def row_bytes(bits: int, group_size: int) -> int:
 # combine_kernel).  Reported only while the attention source is the one that
 # was measured.
 TRAFFIC = {"source": "rotated_bit_quantized_gb300/csrc/iq_attend.cu",
-           "sha256": "2b7ca3d2548851f30d5eb2bacaf1bd95a5138ceba7fa4ea3b93b7efeffcee44b",
-           "bytes": ((539.385088 + 2.981632 + 2.929664) + (539.400960 + 0.520960 + 2.928896)) / 2 * 1e6}
+           "sha256": "a9322bafef25b26dbed25735ddbd62bd66c8ff0578ca2eeda07ef56df781a4f6",
+           "bytes": ((539.406592 + 3.501056 + 2.929408) + (539.395328 + 0.417024 + 2.929664)) / 2 * 1e6}
 
 
 def measured_traffic():
