@@ -12,13 +12,16 @@
 // dequantised values enter the P.V product as fp16.
 //
 // One CTA per (sequence, kv head, tile of 128 query rows); its keys stream in
-// 64-key tiles.  Warp roles (320 threads):
-//  * warps 0-3, one thread per query row (= tensor-memory lane): rotate and
-//    store the row's q'' (fp16 MMA operand) and per-group sums; per key tile
-//    read the four group products S_g from tensor memory, fold in the key
-//    scales and biases, mask, online softmax in log2 units with a lazily
-//    moving reference max (P <= 2^8), write P (fp16 MMA operand); at the end
-//    normalise, undo the rotation and store;
+// 64-key tiles.  Warp roles (448 threads):
+//  * warps 0-3 and 10-13, two threads per query row (= tensor-memory lane;
+//    warp w reaches lanes 32 (w % 4) .. + 31): rotate and store the row's q''
+//    (fp16 MMA operand, half of the dims each) and per-group sums; per key tile
+//    each reads the four group products S_g of its 32 keys from tensor memory,
+//    folds in the key scales and biases and masks; the two agree on the row's
+//    reference max (online softmax in log2 units, a lazily moving reference,
+//    P <= 2^8) through shared memory, then each writes its half of P (fp16 MMA
+//    operand); at the end they add their row sums, normalise, undo the
+//    rotation and store half of the output dims each;
 //  * warps 4-7: turn each staged tile's 4-bit key codes into fp16 (exact
 //    integers, the S MMA operand) and its 3-bit value codes into fp16 values
 //    s*c+b, transposed to dims x keys (the P.V MMA operand);
@@ -27,8 +30,11 @@
 //    N=64 keys, K=64 dims, one accumulator per group) and O += P . Vhat
 //    (M=128, N=256 dims, K=64 keys), each committed to an mbarrier.
 // The key operand of tile i+1 is built while the row threads work on tile i
-// (it is free once S(i) is done), so S(i+1) follows P.V(i) at once; the value
-// operand waits for P.V(i).
+// (it is free once S(i) is done), and S(i+1) is issued as soon as the row
+// threads have read S(i), so it runs under their softmax; P.V(i) follows once
+// P(i) is written, and the row threads write P(i+1) after P.V(i) is done.  The
+// value operand is double-buffered by tile parity: tile i's is built while
+// P.V(i-1) runs.
 // Shared-memory operands use the 128-byte swizzle (K-major, 8-row groups
 // 1024 bytes apart).  Tensor memory: S_0..S_3 in columns 0..255, O in
 // 256..511.
@@ -53,16 +59,18 @@ constexpr float TAU = 8.0f;  // the reference max moves when a score exceeds it 
 // shared memory (from a 1024-byte aligned base)
 constexpr int OFF_Q = 0;                       // 4 blocks x [128 rows x 128 B]: q'' fp16
 constexpr int OFF_K = OFF_Q + 4 * ROWS * 128;  // 4 blocks x [64 keys x 128 B]: key codes fp16
-constexpr int OFF_V = OFF_K + 4 * KT * 128;    // [256 dims x 128 B]: values fp16, dims x keys
-constexpr int OFF_P = OFF_V + 256 * 128;       // [128 rows x 128 B]: P fp16
+constexpr int OFF_V = OFF_K + 4 * KT * 128;    // 2 x [256 dims x 128 B]: values fp16, dims x keys (tile parity)
+constexpr int OFF_P = OFF_V + 2 * 256 * 128;   // [128 rows x 128 B]: P fp16
 constexpr int OFF_STG = OFF_P + ROWS * 128;    // NSTG packed tiles
 constexpr int STG_KC = 0, STG_VC = KT * 128, STG_KS = STG_VC + KT * 96, STG_KB = STG_KS + KT * 8,
               STG_VS = STG_KB + KT * 8, STG_VB = STG_VS + KT * 8, STG_BYTES = STG_VB + KT * 8;
 constexpr int OFF_SC = OFF_STG + NSTG * STG_BYTES;  // 2 x [64 keys][8] f32: key scales s_0..3, biases b_0..3
-constexpr int OFF_BAR = OFF_SC + 2 * KT * 8 * 4;
+constexpr int OFF_XCH = OFF_SC + 2 * KT * 8 * 4;  // row threads' exchange area (1280 floats)
+constexpr int XCH_QS = 2 * 2 * ROWS, XCH_L = XCH_QS + 2 * ROWS * 2;
+constexpr int OFF_BAR = OFF_XCH + (XCH_L + 2 * ROWS) * 4;
 constexpr int SMEM = OFF_BAR + 128 + 1024;  // + alignment slack
 static_assert(STG_BYTES == 16384 && OFF_STG % 1024 == 0 && OFF_SC % 16 == 0, "layout");
-constexpr int THREADS = 320;
+constexpr int THREADS = 448;
 
 struct Params {
   const uint32_t* k_codes;
@@ -166,8 +174,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   uint64_t* v_ready = k_ready + 1;                                // value operand of tile i written
   uint64_t* s_ready = v_ready + 1;                                // S_g of tile i in tensor memory
   uint64_t* p_ready = s_ready + 1;                                // P of tile i written (and O rescaled)
-  uint64_t* o_ready = p_ready + 1;                                // P.V of tile i done
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_ready + 1);
+  uint64_t* o_ready = p_ready + 1;  // [2]: P.V of tile i done, on o_ready[i & 1] (phase i / 2)
+  uint64_t* s_free = o_ready + 2;                                 // S of tile i read (S(i+1) may be issued)
+  uint64_t* row_bar = s_free + 1;                                 // barrier of the 8 row warps (bounded)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(row_bar + 1);
   float* sc = reinterpret_cast<float*>(smem + OFF_SC);
   const uint32_t sbase = smem_u32(smem);
 
@@ -194,8 +204,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     mbar_init(k_ready, 4);
     mbar_init(v_ready, 4);
     mbar_init(s_ready, 1);
-    mbar_init(p_ready, 4);
-    mbar_init(o_ready, 1);
+    mbar_init(p_ready, 8);
+    mbar_init(&o_ready[0], 1);
+    mbar_init(&o_ready[1], 1);
+    mbar_init(s_free, 8);
+    mbar_init(row_bar, 8);
     mbar_fence_init();
   }
   if (warp == 9) {
@@ -235,9 +248,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
-    // S(i+1) goes in right behind P.V(i): its keys are built while the row
-    // threads work on tile i, and the S columns are free once P(i) is written
-    named_bar(1, 128 + 32);  // q'' written by the row threads
+    // S(i+1) goes in as soon as the row threads have read S(i) (its keys are
+    // built while they work on tile i), so it runs under their softmax; P.V(i)
+    // follows once P(i) is written
+    named_bar(1, 2 * 128 + 32);  // q'' written by the row threads
     if (lane == 0) {
       tc_after();
       auto issue_s = [&](int i) {
@@ -255,6 +269,14 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       if (ntiles > 0 && !ok) atomicOr(p.status, 2u | 0x200u);
       if (ok) issue_s(0);
       for (int i = 0; ok && i < ntiles; ++i) {
+        if (i + 1 < ntiles) {
+          if (!wait_phase(s_free, static_cast<uint32_t>(i) & 1) ||
+              !wait_phase(k_ready, static_cast<uint32_t>(i + 1) & 1)) {
+            atomicOr(p.status, 2u | 0x200u);
+            break;
+          }
+          issue_s(i + 1);
+        }
         if (!wait_phase(p_ready, static_cast<uint32_t>(i) & 1) || !wait_phase(v_ready, static_cast<uint32_t>(i) & 1)) {
           atomicOr(p.status, 2u | 0x400u);
           break;
@@ -262,21 +284,14 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         tc_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma(tmem + 256, sdesc(sbase + OFF_P + 32 * ks), sdesc(sbase + OFF_V + 32 * ks), idesc(256, ROWS),
+          mma(tmem + 256, sdesc(sbase + OFF_P + 32 * ks), sdesc(sbase + OFF_V + (i & 1) * 32768 + 32 * ks), idesc(256, ROWS),
               (i > 0 || ks > 0) ? 1u : 0u);
-        commit(o_ready);
+        commit(&o_ready[i & 1]);
         done = i + 1;
-        if (i + 1 < ntiles) {
-          if (!wait_phase(k_ready, static_cast<uint32_t>(i + 1) & 1)) {
-            atomicOr(p.status, 2u | 0x200u);
-            break;
-          }
-          issue_s(i + 1);
-        }
       }
-      if (done > 0) wait_phase(o_ready, static_cast<uint32_t>(done - 1) & 1);  // nothing left in flight
+      if (done > 0) wait_phase(&o_ready[(done - 1) & 1], static_cast<uint32_t>((done - 1) >> 1) & 1);  // nothing left in flight
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------------- operand builders
     const int dt = threadIdx.x - 128;  // 0..127
     for (int i = 0; i < ntiles; ++i) {
@@ -317,7 +332,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       proxy_fence();  // generic-proxy stores before the tensor cores read them
       __syncwarp();
       if (lane == 0) mbar_arrive(k_ready);
-      if (i > 0 && !wait_phase(o_ready, static_cast<uint32_t>(i - 1) & 1)) {  // the value operand: after P.V(i-1)
+      // this tile's value buffer was last read by P.V(i-2) (its own completion
+      // barrier, so a phase two tiles back is never confused with the latest)
+      if (i > 1 && !wait_phase(&o_ready[i & 1], static_cast<uint32_t>((i - 2) >> 1) & 1)) {
         atomicOr(p.status, 1u | 0x1000u);
         break;
       }
@@ -353,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int d = 8 * db + e;
-          *reinterpret_cast<uint4*>(smem + OFF_V + swz(d, tb)) =
+          *reinterpret_cast<uint4*>(smem + OFF_V + (i & 1) * 32768 + swz(d, tb)) =
               make_uint4(pack_h2(v[0][e], v[1][e]), pack_h2(v[2][e], v[3][e]), pack_h2(v[4][e], v[5][e]),
                          pack_h2(v[6][e], v[7][e]));
         }
@@ -367,36 +384,57 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     }
   } else {
     // ---------------------------------------------------------------- row threads
-    const int r = threadIdx.x;  // row in the tile = tensor-memory lane
+    // Two threads per query row (= tensor-memory lane): warps 0-3 take keys
+    // 0..31 of every tile and output dims 0..127, warps 10-13 keys 32..63 and
+    // dims 128..255 (a warp reaches the lanes 32 * (warp % 4) ..  + 31).  The
+    // two threads of a row agree on its reference max each tile through
+    // shared memory and a bounded barrier of the 8 row warps.
+    const int hf = warp >= 10 ? 1 : 0;
+    const int r = 32 * (warp & 3) + lane;  // row in the tile = tensor-memory lane
     const int R = z * ROWS + r;
     const bool live = R < rows;
     const int qi = live ? R / p.rep : 0, hr = live ? R % p.rep : 0;
     const int qpos = live ? (p.causal ? T - p.nq + qi : T - 1) : -1;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);  // [2 parities][2 halves][128 rows]
+    uint32_t gph = 0;  // completed phases of row_sync
+    auto row_sync = [&]() -> bool {  // every row thread's shared-memory writes before the reads after it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(row_bar);
+      const bool ok = __all_sync(0xffffffffu, wait_phase(row_bar, gph & 1));
+      ++gph;
+      return ok;
+    };
     // q'' = bf16(bf16(q @ M_b) * scale), entering the MMA as the fp16 q_s =
     // q'' * 2^-e, and its per-group sums.  The rotation keeps every |q''|
     // below 2.03 * max|q| * |scale| (a row of M_b has an L1 norm of at most
     // 2, plus bf16 rounding), so with max|q| * |scale| in [2^E0, 2^(E0+1))
     // e = E0 - 12 puts |q_s| below 2^15 (fp16) and its largest entry above 2^8.
+    // Each thread of the row takes half of its dims (8-dim chunks 16 hf .. 16 hf + 15).
     float qs[4] = {0.f, 0.f, 0.f, 0.f};
     float kmul = LOG2E;  // raw score -> log2 units: log2(e) * 2^e
+    bool ok = true;
     {
       const uint16_t* qrow =
           p.q + ((static_cast<long long>(b) * p.kv_heads * p.rep + h * p.rep + hr) * p.nq + qi) * kHeadDim;
       uint32_t amax = 0;  // largest |q| as bf16 bits (monotonic in the magnitude)
       if (live)
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 16 * hf; c < 16 * hf + 16; ++c) {
           const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c));
           const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) amax = max(amax, max(rw[j] & 0x7FFFu, (rw[j] >> 16) & 0x7FFFu));
         }
+      xch[XCH_L + hf * ROWS + r] = __uint_as_float(amax);
+      ok = row_sync();
+      amax = max(amax, __float_as_uint(xch[XCH_L + (1 - hf) * ROWS + r]));
       const float m = bf16_to_f32(amax) * fabsf(p.scale);
       int e = 0;
       if (m > 0.f) e = min(max(static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127 - 12, -100), 100);
       const float down = __int_as_float((127 - e) << 23);
       kmul = LOG2E * __int_as_float((127 + e) << 23);
-      for (int c = 0; c < 32; ++c) {  // 8-dim chunk c: rotation blocks 2c, 2c+1
+      float qh[2] = {0.f, 0.f};  // sums of this thread's two groups
+      for (int c = 16 * hf; c < 16 * hf + 16; ++c) {  // 8-dim chunk c: rotation blocks 2c, 2c+1
         uint4 raw = make_uint4(0, 0, 0, 0);
         if (live) raw = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c));
         const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -422,17 +460,24 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           hv[2 * blk + 1] = h1;
           // the sums use the fp16 values the MMA multiplies
           const __half2 a0 = *reinterpret_cast<const __half2*>(&h0), a1 = *reinterpret_cast<const __half2*>(&h1);
-          qs[c >> 3] += __low2float(a0) + __high2float(a0) + __low2float(a1) + __high2float(a1);
+          qh[(c >> 3) & 1] += __low2float(a0) + __high2float(a0) + __low2float(a1) + __high2float(a1);
         }
         *reinterpret_cast<uint4*>(smem + OFF_Q + (c >> 3) * ROWS * 128 + swz(r, c & 7)) =
             make_uint4(hv[0], hv[1], hv[2], hv[3]);
       }
+      // exchange the group sums: this thread holds groups 2 hf, 2 hf + 1
+      xch[XCH_QS + hf * ROWS * 2 + 2 * r] = qh[0];
+      xch[XCH_QS + hf * ROWS * 2 + 2 * r + 1] = qh[1];
+      ok = row_sync() && ok;
+      qs[2 * hf] = qh[0];
+      qs[2 * hf + 1] = qh[1];
+      qs[2 - 2 * hf] = xch[XCH_QS + (1 - hf) * ROWS * 2 + 2 * r];
+      qs[3 - 2 * hf] = xch[XCH_QS + (1 - hf) * ROWS * 2 + 2 * r + 1];
     }
     proxy_fence();
-    named_bar(1, 128 + 32);  // (arrive side for the MMA warp)
+    named_bar(1, 2 * 128 + 32);  // (arrive side for the MMA warp)
 
     float mref = NEG, lsum = 0.f;
-    bool ok = true;
     for (int i = 0; i < ntiles && ok; ++i) {
       // tensor-memory loads and stores are warp-collective: every decision that
       // guards them is made the same for the whole warp
@@ -442,102 +487,112 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         break;
       }
       tc_after();
-      // P(i-1) and the O of the earlier tiles are final: P.V(i-1) was issued
-      // before S(i), and S(i)'s commit covers it (the wait returns at once)
-      if (i > 0 && !__all_sync(0xffffffffu, wait_phase(o_ready, static_cast<uint32_t>(i - 1) & 1))) {
+      const float* sci = sc + (i & 1) * KT * 8;
+      float x[32];  // scores of this thread's 32 keys, log2 units
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c16 = 2 * hf + cc;  // 16-key chunk of the tile
+        float s0[16], s1[16], s2[16], s3[16];
+        ld16(lane_addr + 0 * 64 + 16 * c16, s0);
+        ld16(lane_addr + 1 * 64 + 16 * c16, s1);
+        ld16(lane_addr + 2 * 64 + 16 * c16, s2);
+        ld16(lane_addr + 3 * 64 + 16 * c16, s3);
+        ld_wait();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int tl = 16 * c16 + k, t = i * KT + tl;
+          const float4 ks = *reinterpret_cast<const float4*>(sci + tl * 8);
+          const float4 kb = *reinterpret_cast<const float4*>(sci + tl * 8 + 4);
+          float sv = ks.x * s0[k];
+          sv = fmaf(ks.y, s1[k], sv);
+          sv = fmaf(ks.z, s2[k], sv);
+          sv = fmaf(ks.w, s3[k], sv);
+          sv = fmaf(kb.x, qs[0], sv);
+          sv = fmaf(kb.y, qs[1], sv);
+          sv = fmaf(kb.z, qs[2], sv);
+          sv = fmaf(kb.w, qs[3], sv);
+          x[16 * cc + k] = t <= qpos ? sv * kmul : NEG;
+        }
+      }
+      // S(i) is read: S(i+1) may overwrite it
+      tc_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+      float mx = NEG;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) mx = fmaxf(mx, x[k]);
+      xch[(i & 1) * 2 * ROWS + hf * ROWS + r] = mx;
+      if (!row_sync()) {
+        atomicOr(p.status, 2u | 0x10000u);
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, xch[(i & 1) * 2 * ROWS + (1 - hf) * ROWS + r]);  // the row's max over the tile
+      const bool move = mx != NEG && (mref == NEG || mx > mref + TAU);
+      bool o_done = i == 0;  // O(i-1) complete (P and O may be touched)
+      if (__any_sync(0xffffffffu, move)) {  // the same for the row's other warp: the rows are the same
+        const float mnew = move ? (mref == NEG ? mx : fmaxf(mref, mx)) : mref;
+        const float alpha = !move ? 1.f : mref == NEG ? 0.f : ex2_approx(mref - mnew);
+        if (i > 0) {  // O holds earlier tiles' sums: rescale this thread's half of its columns
+          if (!__all_sync(0xffffffffu, wait_phase(&o_ready[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1))) {
+            atomicOr(p.status, 2u | 0x4000u);
+            ok = false;
+            break;
+          }
+          o_done = true;
+          tc_after();
+#pragma unroll 1
+          for (int c = 128 * hf; c < 128 * hf + 128; c += 16) {
+            float o[16];
+            ld16(lane_addr + 256 + c, o);
+            ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] *= alpha;
+            st16(lane_addr + 256 + c, o);
+          }
+          st_wait();
+        }
+        lsum *= alpha;
+        mref = mnew;
+      }
+      // P = 2^(x - mref) (fp16) into this thread's half of the row, once P.V(i-1) is done with P
+#pragma unroll
+      for (int k = 0; k < 32; ++k) x[k] = mref == NEG ? 0.f : ex2_approx(x[k] - mref);
+      if (!o_done && !__all_sync(0xffffffffu, wait_phase(&o_ready[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1))) {
         atomicOr(p.status, 2u | 0x4000u);
         ok = false;
         break;
       }
-      const float* sci = sc + (i & 1) * KT * 8;
-#pragma unroll 1
-      for (int c16 = 0; c16 < KT / 16; ++c16) {  // 16 keys at a time
-        float x[16];  // scores in log2 units
-        {
-          float s0[16], s1[16], s2[16], s3[16];
-          ld16(lane_addr + 0 * 64 + 16 * c16, s0);
-          ld16(lane_addr + 1 * 64 + 16 * c16, s1);
-          ld16(lane_addr + 2 * 64 + 16 * c16, s2);
-          ld16(lane_addr + 3 * 64 + 16 * c16, s3);
-          ld_wait();
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int tl = 16 * c16 + k, t = i * KT + tl;
-            const float4 ks = *reinterpret_cast<const float4*>(sci + tl * 8);
-            const float4 kb = *reinterpret_cast<const float4*>(sci + tl * 8 + 4);
-            float sv = ks.x * s0[k];
-            sv = fmaf(ks.y, s1[k], sv);
-            sv = fmaf(ks.z, s2[k], sv);
-            sv = fmaf(ks.w, s3[k], sv);
-            sv = fmaf(kb.x, qs[0], sv);
-            sv = fmaf(kb.y, qs[1], sv);
-            sv = fmaf(kb.z, qs[2], sv);
-            sv = fmaf(kb.w, qs[3], sv);
-            x[k] = t <= qpos ? sv * kmul : NEG;
-          }
+      for (int c = 0; c < 4; ++c) {
+        uint32_t hv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a = x[8 * c + 2 * j], bq = x[8 * c + 2 * j + 1];
+          lsum += a + bq;
+          hv[j] = pack_h2(a, bq);
         }
-        float mx = NEG;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) mx = fmaxf(mx, x[k]);
-        const bool move = mx != NEG && (mref == NEG || mx > mref + TAU);
-        if (__any_sync(0xffffffffu, move)) {  // warp-uniform: the O rescale is warp-collective
-          const float mnew = move ? (mref == NEG ? mx : fmaxf(mref, mx)) : mref;
-          const float alpha = !move ? 1.f : mref == NEG ? 0.f : ex2_approx(mref - mnew);
-          if (i > 0) {  // O holds earlier tiles' sums
-#pragma unroll 1
-            for (int c = 0; c < 256; c += 16) {
-              float o[16];
-              ld16(lane_addr + 256 + c, o);
-              ld_wait();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) o[j] *= alpha;
-              st16(lane_addr + 256 + c, o);
-            }
-            st_wait();
-          }
-          if (move) {  // this row's P chunks already written in this tile
-            for (int c = 0; c < 2 * c16; ++c) {
-              uint4* pc = reinterpret_cast<uint4*>(smem + OFF_P + swz(r, c));
-              uint4 w = *pc;
-              uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const __half2 h2 = *reinterpret_cast<const __half2*>(&wv[j]);
-                wv[j] = pack_h2(__low2float(h2) * alpha, __high2float(h2) * alpha);
-              }
-              *pc = w;
-            }
-          }
-          lsum *= alpha;
-          mref = mnew;
-        }
-        // P = 2^(x - mref) (fp16), and its row sum
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t hv[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float a = mref == NEG ? 0.f : ex2_approx(x[8 * c + 2 * j] - mref);
-            const float bq = mref == NEG ? 0.f : ex2_approx(x[8 * c + 2 * j + 1] - mref);
-            lsum += a + bq;
-            hv[j] = pack_h2(a, bq);
-          }
-          *reinterpret_cast<uint4*>(smem + OFF_P + swz(r, 2 * c16 + c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        }
+        *reinterpret_cast<uint4*>(smem + OFF_P + swz(r, 4 * hf + c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
       }
       proxy_fence();
       tc_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_ready);
     }
-    // ---- output: O / l, undo the rotation, store
-    if (ok && ntiles > 0 && __all_sync(0xffffffffu, wait_phase(o_ready, static_cast<uint32_t>(ntiles - 1) & 1))) {
+    // ---- output: O / l (the row's two partial sums), undo the rotation, store this thread's half
+    bool fin = ok && ntiles > 0;
+    if (fin) {
+      xch[XCH_L + hf * ROWS + r] = lsum;
+      fin = row_sync();
+    }
+    if (fin) lsum += xch[XCH_L + (1 - hf) * ROWS + r];
+    if (fin && __all_sync(0xffffffffu, wait_phase(&o_ready[(ntiles - 1) & 1], static_cast<uint32_t>((ntiles - 1) >> 1) & 1))) {
       tc_after();
       const float inv = 1.f / lsum;
-      if (live && !(lsum > 0.f)) atomicOr(p.status, 4u);
+      if (live && hf == 0 && !(lsum > 0.f)) atomicOr(p.status, 4u);
       const long long orow = (static_cast<long long>(b) * p.kv_heads * p.rep + h * p.rep + hr) * p.nq + qi;
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 16) {
+      for (int c = 128 * hf; c < 128 * hf + 128; c += 16) {
         float o[16];
         ld16(lane_addr + 256 + c, o);
         ld_wait();
@@ -571,7 +626,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           }
         }
       }
-    } else if (live) {
+    } else if (live && hf == 0) {
       atomicOr(p.status, 2u | 0x8000u);
     }
   }
