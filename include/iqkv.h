@@ -212,7 +212,7 @@ int iq_cache_gather(const iq_cache* src, iq_cache* dst, const int32_t* src_of,
  * and these shapes (status word and the split-KV partial results); the size
  * does not depend on the lengths.
  */
-#define IQ_WORKSPACE_HEAD_BYTES 4352u
+#define IQ_WORKSPACE_HEAD_BYTES 8448u
 int iq_attend_workspace(const iq_cache* cache, int q_heads, int n_queries, size_t* bytes);
 
 /*

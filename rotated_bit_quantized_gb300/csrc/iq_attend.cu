@@ -137,11 +137,25 @@ struct Params {
   unsigned* status;
   // [UNIT_CAP]: partials stored per unit of this launch; the combine takes its
   // unit's expected count off again (also when its wait runs out), so every
-  // counter is back at zero once the attention grid has completed
+  // counter is back at zero once the attention grid has completed.  Two sets
+  // in the workspace, used by alternate launches on it (see early).
   unsigned* counters;
+  // 1: every CTA releases the dependent launch (this launch's combine) as soon
+  // as it starts, so the combine's CTAs sit beside the attention CTAs from the
+  // start and the next launch takes each SM this one leaves.  The host sets it
+  // only for a grid of one CTA per SM (two attention CTAs never share an SM,
+  // so once all of this grid's CTAs have started, every CTA of the launch two
+  // before has completed, and with it the combine before that, which used the
+  // same counter set) and when it knows the previous launch on the workspace
+  // used the other counter set.  0: release after griddepcontrol.wait, in
+  // end_unit (the combine then starts after the previous one has completed).
+  int early;
   // bounded waits: mbarrier tests per wait, the combine's wait in ns
   unsigned spin_limit;
   unsigned long long combine_wait_ns;
+  // partial blocks (kCombineRows rows of one segment) the combine stages in
+  // shared memory per round: as many as fit beside the attention CTA
+  int combine_blocks;
   // test hook (iq_debug_inject): bit 0 the combine expects one arrival that
   // never comes; bit 1 the consumers wait on a barrier no one arrives at (in
   // place of their first stage), so that wait runs out
@@ -337,6 +351,12 @@ __device__ __forceinline__ void unpack_v3_pair(uint32_t fa, uint32_t fb, uint32_
 // 2^k as a float (exponent field), |k| <= 126
 __device__ __forceinline__ float exp2i(int k) { return __int_as_float((127 + k) << 23); }
 
+// The split combine runs as small CTAs beside the attention CTAs: registers
+// are split evenly over the four warp schedulers of an SM, so next to an
+// attention CTA (three warps of 160 registers per scheduler) one warp of at
+// most 32 registers per scheduler fits.
+constexpr int kCombineThreads = 128, kCombineRegs = 32;
+
 template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES>
 struct Cfg : Tiling<TILE_> {
   using Tiling<TILE_>::STAGE;
@@ -351,12 +371,18 @@ struct Cfg : Tiling<TILE_> {
   // schedulers, so neither half is served first (two CTAs on one SM are not:
   // the scheduler favours the older one, which finishes ~12% earlier).
   static constexpr int THREADS = (HALVES * CW + 4) * 32;
-  static constexpr int LAUNCH_REGS = (65536 / (MINB * THREADS)) / 8 * 8;
+  // registers left free beside each CTA on its SM: one combine CTA fits next
+  // to it, so a split merge never needs an SM of its own (see combine_kernel)
+  static constexpr int RESERVE_REGS = kCombineThreads * kCombineRegs;
+
+  static constexpr int LAUNCH_REGS = ((65536 / MINB - RESERVE_REGS) / THREADS) / 8 * 8;
+  static_assert(MINB > 1 || (THREADS % 128 == 0 && THREADS / 128 * LAUNCH_REGS * 32 + kCombineRegs * 32 <= 16384),
+                "a combine warp fits beside the CTA on every warp scheduler");
   static constexpr int PRODUCER_REGS = 24;
   static constexpr int CONSUMER_REGS =
-      ((65536 / MINB - 128 * PRODUCER_REGS) / (HALVES * CW * 32)) / 8 * 8 > 248
+      ((LAUNCH_REGS * THREADS - 128 * PRODUCER_REGS) / (HALVES * CW * 32)) / 8 * 8 > 248
           ? 248
-          : ((65536 / MINB - 128 * PRODUCER_REGS) / (HALVES * CW * 32)) / 8 * 8;
+          : ((LAUNCH_REGS * THREADS - 128 * PRODUCER_REGS) / (HALVES * CW * 32)) / 8 * 8;
   static_assert(CW % 4 == 0, "consumer warps form whole warpgroups");
   static_assert(HALVES == 1 || (HALVES == 2 && CW == 4), "two halves of one consumer warpgroup each");
   static_assert(CONSUMER_REGS >= LAUNCH_REGS && PRODUCER_REGS <= LAUNCH_REGS, "register split");
@@ -373,17 +399,24 @@ struct Cfg : Tiling<TILE_> {
   static constexpr int QB_BYTES = DS * GPW * 4 * NT * 32 * 8;       // q_s MMA B fragments
   static constexpr int OFF_RMX = OFF_QB + QB_BYTES;                  // per (row, group): max |q''| (bf16 bits)
   static constexpr int OFF_REXP = OFF_RMX + GT * 4 * 4;              // per row: the query exponent e
-  static constexpr int OFF_BAR = (OFF_REXP + GT * 4 + 7) / 8 * 8;
+  // per row of the segment being finished: max and sum over the streams
+  static constexpr int OFF_MLR = (OFF_REXP + GT * 4 + 15) / 16 * 16;
+  static constexpr int OFF_BAR = (OFF_MLR + GT * 8 + 7) / 8 * 8;
   static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8 + 8;  // + the fused-append barrier
   // explicit-mask rows of a stage (the unit's queries, at most GT, x TILE keys,
   // 4-byte elements at most): the last area, part of the launch only with a mask
   static constexpr int MSK_STAGE = GT * TILE_ * 4;
   static constexpr int OFF_MSK = (OFF_FLAG + 16 + 127) / 128 * 128;
+  // without a mask, that area holds instead the first unit segment of a range
+  // that has several (its O, per-row max and sum), kept until the range ends
+  static constexpr int OFF_DBUF = OFF_MSK;
+  static constexpr int OFF_DML = OFF_DBUF + OBUF_BYTES;
   // one half's area, a multiple of the 1024-byte swizzle atom
-  static constexpr int HALF_PLAIN = (OFF_MSK + 1023) / 1024 * 1024;
+  static constexpr int HALF_PLAIN = (OFF_DML + GT * 8 + 1023) / 1024 * 1024;
   static constexpr int HALF_MASK = (OFF_MSK + NSTAGE * MSK_STAGE + 1023) / 1024 * 1024;
   static constexpr int SMEM = HALVES * HALF_PLAIN + 1024;  // + alignment slack
   static constexpr int SMEM_MASK = HALVES * HALF_MASK + 1024;
+  static_assert(SMEM <= 227 * 1024 && SMEM_MASK <= 227 * 1024, "shared memory per CTA");
   static_assert(OFF_XBUF % 16 == 0 && OFF_OBUF % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
   static_assert(4 % DS == 0, "shape");
   // the masked variant's producer also copies mask rows: it takes 8 registers
@@ -399,7 +432,7 @@ struct Cfg : Tiling<TILE_> {
 };
 
 template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES, bool MASKED>
-__global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>::THREADS, MINB)
+__global__ void __maxnreg__((Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>::LAUNCH_REGS))
     attend_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap kmap) {
   using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>;
   constexpr int TILE = C::TILE, SUBS = C::SUBS, STAGE = C::STAGE;
@@ -458,6 +491,7 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     mbar_fence_init();
   }
   __syncthreads();
+  if (p.early) pdl_launch_dependents();
 
   // ---- this half's share of the launch's tiles
   const int k_cta = blockIdx.x * HALVES + (half < HALVES ? half : 0);
@@ -484,12 +518,18 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     setmaxnreg_dec<MASKED ? C::PRODUCER_REGS_MASK : C::PRODUCER_REGS>();
     if (half < HALVES && lane == 0 && g0 < g1) {
       const uint64_t pol = policy_evict_first();
-      int u = u0;
       long long k = 0;
       bool enc_seen = p.n_new == 0;
       bool waited = false;  // griddepcontrol.wait done
-      for (long long gt = g0; gt < g1; ++gt, ++k) {
-        while (gt >= p.prefix[u + 1]) ++u;
+      // the range's unit segments, last unit first (the consumers' order)
+      int u = u1;
+      int gt = max(static_cast<int>(g0), p.prefix[u1]);
+      for (;; ++gt, ++k) {
+        if (gt >= min(static_cast<int>(g1), p.prefix[u + 1])) {
+          if (u == u0) break;
+          --u;
+          gt = max(static_cast<int>(g0), p.prefix[u]);
+        }
         if (!enc_seen && gt == p.prefix[u + 1] - 1) {  // a last tile: its new rows must be stored first
           if (!mbar_wait(encoded, 0, p.spin_limit)) {
             atomicOr(p.status, 1u);
@@ -540,7 +580,10 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     return;
   }
   setmaxnreg_inc<MASKED ? C::CONSUMER_REGS_MASK : C::CONSUMER_REGS>();
-  if (g0 >= g1) return;  // a half without tiles
+  if (g0 >= g1) {  // a half without tiles (it still waits, so its exit implies the previous grid's completion)
+    pdl_wait();
+    return;
+  }
 
   // ------------------------------------------------------------ consumers
   const int stream = cw / DS, dg = cw % DS;
@@ -1048,15 +1091,45 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     }
   };
 
-  // ---- finish this CTA's segment of unit u: fold the value-bias sums into O
-  // and merge the token streams (log-sum-exp) into obuf; a unit held by this
-  // CTA alone is finalised at once, a shared one leaves a partial (O, running
-  // max in log2 units, running sum) for the combine.
-  auto end_unit = [&](int u) {
-    // the previous grids' writes of the output, partials and counters are done
-    // (the first call waits, later ones return at once); the next grid may launch
-    pdl_wait();
-    pdl_launch_dependents();
+  // ---- publish this range's segment of unit u (O in buf, per-row running max
+  // in log2 units and sum in ml): a unit held by this range alone is
+  // finalised; otherwise its partial goes to slot u + k_cta and is counted
+  // for the combine.  Every write here follows griddepcontrol.wait.
+  float2* mlr = reinterpret_cast<float2*>(smem + C::OFF_MLR);
+  const float* dbuf = reinterpret_cast<const float*>(smem + C::OFF_DBUF);
+  const float2* dml = reinterpret_cast<const float2*>(smem + C::OFF_DML);
+  auto publish = [&](int u, const float* buf, const float2* ml) {
+    const int ub = p.unit_base + u;
+    if (p.prefix[u] >= g0 && p.prefix[u + 1] <= g1) {  // the whole unit is here: finalise
+      for (int idx = ctid; idx < GT * 32; idx += NCT) {
+        const int r = idx >> 5, l8 = idx & 31;
+        if (((ub % p.nqt) * GT + r) / p.rep >= p.nq) continue;
+        uint32_t mw[16];
+        load_rot(p, l8, mw);
+        const float4 o0 = reinterpret_cast<const float4*>(buf + r * kHeadDim + 8 * l8)[0];
+        const float4 o1 = reinterpret_cast<const float4*>(buf + r * kHeadDim + 8 * l8)[1];
+        const float acc[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+        store_out<GT>(p, ub, r, l8, acc, ml[r].y, mw);
+      }
+    } else {  // partial for the combine: slot u + k_cta
+      const long long slot = static_cast<long long>(u) + k_cta;
+      float4* po = reinterpret_cast<float4*>(p.part_o + slot * GT * kHeadDim);
+      for (int idx = ctid; idx < GT * kHeadDim / 4; idx += NCT) po[idx] = reinterpret_cast<const float4*>(buf)[idx];
+      for (int r = ctid; r < GT; r += NCT) reinterpret_cast<float2*>(p.part_ml)[slot * GT + r] = ml[r];
+      named_bar(bar_all, NCT);  // every thread's partial stores precede the arrival
+      if (ctid == 0) {
+        __threadfence();
+        atomicAdd(p.counters + u, 1u);
+      }
+    }
+  };
+
+  // ---- finish this range's segment of unit u: fold the value-bias sums into
+  // O, merge the token streams (log-sum-exp) into obuf with each row's max and
+  // sum in mlr, then publish it, or (defer: the first of several segments of
+  // the range) keep it in shared memory until the range ends, so the range's
+  // first griddepcontrol.wait comes at its end.
+  auto end_unit = [&](int u, bool defer) {
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -1128,43 +1201,34 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       }
       named_bar(bar_all, NCT);
     }
-    // obuf holds the CTA's O for the unit; per row M = max and L = sum over the streams
-    const int ub = p.unit_base + u;
-    if (p.prefix[u] >= g0 && p.prefix[u + 1] <= g1) {  // the whole unit is here: finalise
-      for (int idx = ctid; idx < GT * 32; idx += NCT) {
-        const int r = idx >> 5, l8 = idx & 31;
-        if ((qt * GT + r) / p.rep >= p.nq) continue;
-        uint32_t mw[16];
-        load_rot(p, l8, mw);
-        float L = lbuf[r];
+    // obuf holds the range's O for the unit; per row M = max and L = sum over the streams
+    for (int r = ctid; r < GT; r += NCT) {
+      float M = mbuf[r], L = lbuf[r];
 #pragma unroll
-        for (int s = 1; s < STREAMS; ++s) L += lbuf[s * GT + r];
-        const float4 o0 = reinterpret_cast<const float4*>(obuf + r * kHeadDim + 8 * l8)[0];
-        const float4 o1 = reinterpret_cast<const float4*>(obuf + r * kHeadDim + 8 * l8)[1];
-        const float acc[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-        store_out<GT>(p, ub, r, l8, acc, L, mw);
+      for (int s = 1; s < STREAMS; ++s) {
+        M = fmaxf(M, mbuf[s * GT + r]);
+        L += lbuf[s * GT + r];
       }
-    } else {  // partial for the combine: slot u + k_cta
-      const long long slot = static_cast<long long>(u) + k_cta;
-      float4* po = reinterpret_cast<float4*>(p.part_o + slot * GT * kHeadDim);
-      for (int idx = ctid; idx < GT * kHeadDim / 4; idx += NCT)
-        po[idx] = reinterpret_cast<const float4*>(obuf)[idx];
-      for (int r = ctid; r < GT; r += NCT) {
-        float M = mbuf[r], L = lbuf[r];
-#pragma unroll
-        for (int s = 1; s < STREAMS; ++s) {
-          M = fmaxf(M, mbuf[s * GT + r]);
-          L += lbuf[s * GT + r];
-        }
-        reinterpret_cast<float2*>(p.part_ml)[slot * GT + r] = make_float2(M, L);
-      }
-      named_bar(bar_all, NCT);  // every thread's partial stores precede the arrival
-      if (ctid == 0) {
-        __threadfence();
-        atomicAdd(p.counters + u, 1u);
+      mlr[r] = make_float2(M, L);
+    }
+    named_bar(bar_all, NCT);
+    if constexpr (!MASKED) {
+      if (defer) {
+        float4* d4 = reinterpret_cast<float4*>(smem + C::OFF_DBUF);
+        for (int idx = ctid; idx < GT * kHeadDim / 4; idx += NCT) d4[idx] = reinterpret_cast<const float4*>(obuf)[idx];
+        for (int r = ctid; r < GT; r += NCT) reinterpret_cast<float2*>(smem + C::OFF_DML)[r] = mlr[r];
+        named_bar(bar_all, NCT);  // obuf and mlr are free again
+        return;
       }
     }
+    // the previous grids' writes of the output, partials and counters are done
+    // (the first wait of the range blocks, later ones return at once); without
+    // the early release, the combine may launch now
+    pdl_wait();
+    pdl_launch_dependents();
+    publish(u, obuf, mlr);
   };
+
 
   // ------------------------------------------------------------ fused append
   // This CTA holds the last tile of units u0 .. u1 - 1, and of u1 when its
@@ -1197,17 +1261,20 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
     if (lane == 0) mbar_arrive(encoded);
   }
 
-  // ------------------------------------------------------------ main loop over this CTA's tiles
-  // One pass per unit segment, so the per-unit prologue and epilogue each have a
-  // single call site outside the hot per-tile loop.
-  int u = u0;
-  long long k = 0, gt = g0;
+  // ------------------------------------------------------------ main loop over this range's tiles
+  // One pass per unit segment, last unit first (the producer's order: a unit's
+  // last tiles, which may hold the previous call's fused rows, come at the
+  // range's end), so the per-unit prologue and epilogue each have a single
+  // call site outside the hot per-tile loop.
+  long long k = 0;
   bool ok = true;
-  for (;;) {
+  int def_u = -1;  // the unit whose segment waits in shared memory for the range's end
+  for (int u = u1; u >= u0; --u) {
+    const bool defer = !MASKED && u == u1 && u1 > u0;
     begin_unit(u);
     const long long seg_end = p.prefix[u + 1] < g1 ? p.prefix[u + 1] : g1;
     const int tile0 = static_cast<int>(p.prefix[u]);
-    for (; gt < seg_end; ++gt, ++k) {
+    for (long long gt = p.prefix[u] > g0 ? p.prefix[u] : g0; gt < seg_end; ++gt, ++k) {
       const int st = static_cast<int>(k % NSTAGE);
       // (test hook: a wait on the fused-append barrier, which no one arrives at
       // in a call without new rows, runs out like a stage that is never filled)
@@ -1241,36 +1308,48 @@ __global__ void __launch_bounds__(Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-    end_unit(u);
-    if (!ok || gt >= g1) break;
-    ++u;
+    end_unit(u, defer);
+    if (defer) def_u = u;
+    if (!ok) break;
+  }
+  if (def_u >= 0) {
+    pdl_wait();
+    pdl_launch_dependents();
+    publish(def_u, dbuf, dml);
   }
 }
 
 
 // ------------------------------------------------------------------ combine
-// One CTA per unit of the launch; units held by a single CTA were finalised by
-// it and are skipped.  Each thread merges one (row, 8-dim chunk) over the
-// unit's segments (log-sum-exp over batches of eight segments whose loads are
-// in flight together), then normalises, undoes the rotation and stores.
+// One small CTA (kCombineThreads threads of at most kCombineRegs registers:
+// it fits beside an attention CTA on any SM) per unit of the launch; units
+// held by a single range were finalised by it and are skipped.  The unit's
+// rows are merged kCombineRows at a time: per pass, one thread bulk-copies
+// those rows of up to p.combine_blocks segments' partials (O and the running
+// max and sum) into shared memory, so a pass costs one round trip to L2, then
+// every thread merges one (row, 8-dim chunk) item over the segments (online
+// log-sum-exp) and, after the last segment, normalises, undoes the rotation
+// and stores.
+constexpr int kCombineRows = kCombineThreads / 32;
+constexpr int kCombineBlockBytes = kCombineRows * kHeadDim * 4 + kCombineRows * 8;  // O rows + (max, sum)
+
 template <int GT>
 __device__ __forceinline__ void combine_unit(const Params& p, int u) {
+  extern __shared__ __align__(128) uint8_t csm[];
   __shared__ int s_ready;
+  __shared__ __align__(8) uint64_t cbar;
   int k_first, k_last;
   seg_range(p, u, k_first, k_last);
   if (k_first == k_last) return;  // finished by the CTA that held the whole unit
   const int nseg = k_last - k_first + 1;
-  // every item of this thread has the same 8-dim chunk (blockDim is a multiple
-  // of 32): its two rotation blocks load while the unit is awaited
-  uint32_t mw[16];
-  load_rot(p, threadIdx.x & 31, mw);
   // Wait (bounded, in time) until every CTA holding tiles of the unit has
   // stored its partial, so units are merged while the attention grid still
   // runs; every attention CTA started before this grid was launched.
   // The count is compared signed and taken off with an atomic subtract, on
   // success and on a timeout alike: the arrivals still missing at a timeout
   // land before this grid completes (it completes after the attention grid),
-  // so the counter is zero again before any later call stores a partial.
+  // so the counter is zero again before any later launch on this counter set
+  // stores a partial.
   unsigned expect = 0;
   for (int k = k_first; k <= k_last; ++k) expect += p.cstart[k] < p.cstart[k + 1];
   if (threadIdx.x == 0) {
@@ -1281,9 +1360,13 @@ __device__ __forceinline__ void combine_unit(const Params& p, int u) {
     for (;;) {
       if (static_cast<int>(ld_acquire_gpu(p.counters + u)) >= want) { ready = 1; break; }
       if (global_ns() - t0 > limit) break;
-      __nanosleep(32);
+      __nanosleep(256);
     }
     s_ready = ready;
+    mbar_init(&cbar, 1);
+    mbar_fence_init();
+    // the partials (stored by other CTAs, acquired above) are read next by bulk copies
+    asm volatile("fence.proxy.async.global;" ::: "memory");
   }
   __syncthreads();
   if (!s_ready) {
@@ -1295,57 +1378,66 @@ __device__ __forceinline__ void combine_unit(const Params& p, int u) {
   }
   const long long slot0 = static_cast<long long>(u) + k_first;
   const int ub = p.unit_base + u;
-  for (int idx = threadIdx.x; idx < GT * 32; idx += blockDim.x) {
-    const int r = idx >> 5, l8 = idx & 31;
-    if (((ub % p.nqt) * GT + r) / p.rep >= p.nq) continue;
+  const int nb = p.combine_blocks;
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int r0 = 0; r0 < GT && ok; r0 += kCombineRows) {
+    const int r = r0 + (threadIdx.x >> 5), l8 = threadIdx.x & 31;
     float M = NEG_INF, L = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s0 = 0; s0 < nseg; s0 += 8) {
-      float2 ml[8];
-      float4 oa[8], ob[8];
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const int kk = k_first + s0 + q8;
-        if (s0 + q8 < nseg && p.cstart[kk] < p.cstart[kk + 1]) {
-          const long long sl = slot0 + s0 + q8;
-          ml[q8] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl * GT + r);
-          const float4* o = reinterpret_cast<const float4*>(p.part_o + (sl * GT + r) * kHeadDim + 8 * l8);
-          oa[q8] = __ldcg(o);
-          ob[q8] = __ldcg(o + 1);
-        } else {
-          ml[q8] = make_float2(NEG_INF, 0.f);
-          oa[q8] = ob[q8] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < nseg; q0 += nb) {
+      const int qn = min(nb, nseg - q0);
+      if (threadIdx.x == 0) {
+        uint32_t bytes = 0;
+        for (int j = 0; j < qn; ++j) bytes += p.cstart[k_first + q0 + j] < p.cstart[k_first + q0 + j + 1] ? kCombineBlockBytes : 0;
+        mbar_arrive_expect_tx(&cbar, bytes);
+        for (int j = 0; j < qn; ++j) {
+          const int kk = k_first + q0 + j;
+          if (p.cstart[kk] >= p.cstart[kk + 1]) continue;  // a range without tiles stored nothing
+          const long long sl = slot0 + q0 + j;
+          uint8_t* blk = csm + j * kCombineBlockBytes;
+          bulk_g2s_plain(blk, p.part_o + (sl * GT + r0) * kHeadDim, kCombineRows * kHeadDim * 4, &cbar);
+          bulk_g2s_plain(blk + kCombineRows * kHeadDim * 4, p.part_ml + (sl * GT + r0) * 2, kCombineRows * 8, &cbar);
         }
       }
-      // merge the batch: its max first, then independent weights (empty
-      // segments and CTAs without tiles carry a max of -inf and weigh 0)
-      float Mb = M;
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) Mb = fmaxf(Mb, ml[q8].x);
-      if (Mb == NEG_INF) continue;
-      const float so = M == NEG_INF ? 0.f : ex2_approx(M - Mb);
-#pragma unroll
-      for (int d = 0; d < 8; ++d) acc[d] *= so;
-      L *= so;
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const float w = ml[q8].x == NEG_INF ? 0.f : ex2_approx(ml[q8].x - Mb);
-        const float v[8] = {oa[q8].x, oa[q8].y, oa[q8].z, oa[q8].w, ob[q8].x, ob[q8].y, ob[q8].z, ob[q8].w};
-#pragma unroll
-        for (int d = 0; d < 8; ++d) acc[d] = fmaf(w, v[d], acc[d]);
-        L = fmaf(w, ml[q8].y, L);
+      if (!__syncthreads_and(mbar_wait(&cbar, phase, p.spin_limit))) {  // one decision for all threads
+        if (threadIdx.x == 0) atomicOr(p.status, 8u);
+        ok = false;
+        break;
       }
-      M = Mb;
+      phase ^= 1;
+      for (int j = 0; j < qn; ++j) {  // online log-sum-exp over the round's segments
+        const int kk = k_first + q0 + j;
+        if (p.cstart[kk] >= p.cstart[kk + 1]) continue;
+        const uint8_t* blk = csm + j * kCombineBlockBytes;
+        const float2 ml = reinterpret_cast<const float2*>(blk + kCombineRows * kHeadDim * 4)[r - r0];
+        if (ml.x == NEG_INF) continue;  // a segment with no visible key weighs 0
+        const float4 oa = reinterpret_cast<const float4*>(blk)[((r - r0) * kHeadDim + 8 * l8) / 4];
+        const float4 ob = reinterpret_cast<const float4*>(blk)[((r - r0) * kHeadDim + 8 * l8) / 4 + 1];
+        const float Mn = fmaxf(M, ml.x);
+        const float so = M == NEG_INF ? 0.f : ex2_approx(M - Mn), w = ex2_approx(ml.x - Mn);
+        const float v[8] = {oa.x, oa.y, oa.z, oa.w, ob.x, ob.y, ob.z, ob.w};
+#pragma unroll
+        for (int d = 0; d < 8; ++d) acc[d] = fmaf(w, v[d], acc[d] * so);
+        L = fmaf(w, ml.y, L * so);
+        M = Mn;
+      }
+      __syncthreads();  // every read of the blocks precedes the next round's copies
     }
-    store_out<GT>(p, ub, r, l8, acc, L, mw);
+    if (ok && r < GT && ((ub % p.nqt) * GT + r) / p.rep < p.nq) {
+      uint32_t mw[16];
+      load_rot(p, l8, mw);
+      store_out<GT>(p, ub, r, l8, acc, L, mw);
+    }
   }
   __syncthreads();
-  if (threadIdx.x == 0) atomicSub(p.counters + u, expect);  // back to zero for the next call
+  if (threadIdx.x == 0) atomicSub(p.counters + u, expect);  // back to zero for a later launch
 }
 
 
 template <int GT>
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kCombineThreads, 65536 / (kCombineThreads * kCombineRegs))
+    combine_kernel(const __grid_constant__ Params p) {
   pdl_launch_dependents();  // the next kernel may launch; it waits for this grid before reading
   const int u = blockIdx.x;
   if (u < p.num_units) combine_unit<GT>(p, u);
@@ -1361,17 +1453,18 @@ constexpr int kMaxLaunches = 64;
 
 struct Plan {
   int nt, gt, nqt, tile, launches, grid[kMaxLaunches];
+  bool full[kMaxLaunches];  // one CTA on every SM (the early release may be used)
   size_t units, slots, head_bytes, bytes;
 };
 
-// workspace: [status word, padded to 256 B][per-unit partial counters:
-// UNIT_CAP x u32][partial O: slots x GT x 256 f32][partial (max, sum): slots x
-// GT x 2 f32].  The head (status word and counters) starts zeroed; the status
+// workspace: [status word, padded to 256 B][per-unit partial counters: two
+// sets of UNIT_CAP x u32][partial O: slots x GT x 256 f32][partial (max, sum):
+// slots x GT x 2 f32].  The head (status word and counters) starts zeroed; the status
 // word accumulates failure bits until iq_read_status reads it, and the combine
 // returns each counter to zero (iq_read_status re-zeroes the whole head after a
 // failure).  Partials are written before they are read.
 constexpr size_t kStatusBytes = 256;
-constexpr size_t kHeadBytes = kStatusBytes + UNIT_CAP * sizeof(unsigned);  // status word + unit counters
+constexpr size_t kHeadBytes = kStatusBytes + 2 * UNIT_CAP * sizeof(unsigned);  // status word + unit counters
 static_assert(kHeadBytes == IQ_WORKSPACE_HEAD_BYTES, "workspace head size in iqkv.h");
 
 template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES>
@@ -1387,6 +1480,15 @@ int blocks_per_sm() {
                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, true>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_MASK);
+    // CTAs of different kernels share an SM only under one L1 / shared-memory
+    // split: the combine asks for the attention kernels' (all shared), so its
+    // small CTAs can sit beside theirs
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, false>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, true>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(combine_kernel<C::GT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, false>,
                                                       C::THREADS, C::SMEM) !=
             cudaSuccess ||
@@ -1500,6 +1602,7 @@ int make_plan(const iq_cache* c, int q_heads, int nq, int causal, Plan* pl, cons
                            std::max(1LL, W / MIN_TILES_PER_CTA));
     G = std::max<long long>(halves, G / halves * halves);  // whole CTAs
     pl->grid[l] = static_cast<int>(G);
+    pl->full[l] = bps == 1 && G == slots_hw;
     pl->slots = std::max(pl->slots, nu + static_cast<size_t>(G));
   }
   if (!tiles)  // independent of the tile counts, so it bounds every later plan
@@ -1565,6 +1668,23 @@ int validate(const iq_cache* c, const void* q, int q_heads, int nq, int causal, 
   return IQ_OK;
 }
 
+// Partial blocks the combine can stage while its CTA still fits in the shared
+// memory an attention CTA of this configuration leaves on an SM (at least one:
+// beside the masked verify kernel it then waits for an SM of its own).
+template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES>
+int combine_blocks_for(bool masked) {
+  using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>;
+  static int per_sm = -1, reserved = 0;
+  if (per_sm < 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) per_sm = 0;
+    if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) reserved = 1024;
+  }
+  const long long left = static_cast<long long>(per_sm) - (masked ? C::SMEM_MASK : C::SMEM) - 2LL * reserved - 128;
+  return static_cast<int>(std::max(1LL, std::min(8LL, left / kCombineBlockBytes)));
+}
+
 template <int NT, int DS, int STREAMS, int NSTAGE, int MINB, int TILE_, int PAIR, int HALVES>
 int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStream_t s) {
   using C = Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES>;
@@ -1601,8 +1721,8 @@ int launch_attend(const Params& prm, const CUtensorMap& map, int grid, cudaStrea
     IQ_CUDA(cudaLaunchKernelEx(&cfg, attend_kernel<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HALVES, false>, prm, map));
   // the split combine, after the attention grid
   cfg.gridDim = dim3(static_cast<unsigned>(prm.num_units));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(prm.combine_blocks) * kCombineBlockBytes;
   IQ_CUDA(cudaLaunchKernelEx(&cfg, combine_kernel<C::GT>, prm));
   return IQ_OK;
 }
@@ -1666,6 +1786,35 @@ class ReadMarks {
 ReadMarks& read_marks() {
   static ReadMarks m;
   return m;
+}
+
+// The unit-counter set of the next split-KV launch on a workspace: launches on
+// one workspace alternate between the two sets.  next() returns false when the
+// previous launch on it is not on record (first use; the table is bounded);
+// such a launch releases its combine late, the order that needs no second set.
+class CounterSets {
+ public:
+  bool next(const void* ws, int* set) {
+    std::lock_guard<std::mutex> lk(mu_);
+    auto it = sets_.find(ws);
+    if (it == sets_.end()) {
+      if (sets_.size() >= 4096) sets_.clear();
+      sets_[ws] = 0;
+      *set = 0;
+      return false;
+    }
+    it->second ^= 1;
+    *set = it->second;
+    return true;
+  }
+
+ private:
+  std::mutex mu_;
+  std::unordered_map<const void*, int> sets_;
+};
+CounterSets& counter_sets() {
+  static CounterSets c;
+  return c;
 }
 
 // Attention over the cache; with n_new > 0 the last n_new rows of every
@@ -1773,6 +1922,12 @@ int attend_impl(const iq_cache* c, const void* q_in, int q_heads, int n_queries,
     prm.prefix[0] = 0;
     for (int u = 0; u < nu; ++u) prm.prefix[u + 1] = prm.prefix[u] + tiles[u0 + u];
     split_ranges(prm.prefix, nu, prm.grid, pl.nt == 1 ? IQ_DECODE_BOUNDARY : IQ_MULTI_BOUNDARY, prm.cstart);
+    int set = 0;
+    const bool known = counter_sets().next(workspace, &set);
+    prm.counters = counters + static_cast<size_t>(set) * UNIT_CAP;
+    prm.early = known && pl.full[l] ? 1 : 0;
+    prm.combine_blocks = pl.nt == 1 ? combine_blocks_for<IQ_DECODE_CFG>(mask_kind >= 2)
+                                    : combine_blocks_for<IQ_MULTI_CFG>(mask_kind >= 2);
     st = pl.nt == 1 ? launch_attend<IQ_DECODE_CFG>(prm, map, prm.grid, s)
                     : launch_attend<IQ_MULTI_CFG>(prm, map, prm.grid, s);
     if (st != IQ_OK) return st;
