@@ -47,8 +47,8 @@ def row_bytes(bits: int, group_size: int) -> int:
 # combine_kernel).  Reported only while the attention source is the one that
 # was measured.
 TRAFFIC = {"source": "rotated_bit_quantized_gb300/csrc/iq_attend.cu",
-           "sha256": "a9322bafef25b26dbed25735ddbd62bd66c8ff0578ca2eeda07ef56df781a4f6",
-           "bytes": ((539.406592 + 3.501056 + 2.929408) + (539.395328 + 0.417024 + 2.929664)) / 2 * 1e6}
+           "sha256": "cbbbb95d64b8b220ea973719827cb7cd8301895c913d25bf158bc5ca87bee80b",
+           "bytes": ((539.462144 + 3.067648 + 2.936320) + (539.398656 + 0.088576 + 2.934272)) / 2 * 1e6}
 
 
 def measured_traffic():
