@@ -22,9 +22,12 @@
 //    P <= 2^8) through shared memory, then each writes its half of P (fp16 MMA
 //    operand); at the end they add their row sums, normalise, undo the
 //    rotation and store half of the output dims each;
-//  * warps 4-7: turn each staged tile's 4-bit key codes into fp16 (exact
-//    integers, the S MMA operand) and its 3-bit value codes into fp16 values
-//    s*c+b, transposed to dims x keys (the P.V MMA operand);
+//  * warps 4-7: turn each staged tile's 4-bit key codes into bare fp16 fields
+//    (a code masked in place is the subnormal c * 2^(L-24), L = 0 or 4: one AND
+//    per two codes; the tensor cores take these subnormals exactly, and the
+//    query operand is permuted and scaled to match, so every product carries
+//    2^-24) and its 3-bit value codes into fp16 values s*c+b, transposed to
+//    dims x keys (the P.V MMA operand);
 //  * warp 8, one lane: bulk copies of the packed tiles into a two-stage ring;
 //  * warp 9, one lane: issues the MMAs: S_g = Q_g . Khat_g^T (M=128 rows,
 //    N=64 keys, K=64 dims, one accumulator per group) and O += P . Vhat
@@ -308,20 +311,17 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       }
       float* sci = sc + (i & 1) * KT * 8;  // read by the row threads of tile i (tile i-2 was done before S(i-1))
       const uint8_t* g = smem + OFF_STG + st * STG_BYTES;
-      // key codes -> fp16 c (exact): item (key t, 8-dim chunk c), the chunk is word c of the row
+      // key codes -> bare fp16 fields: item (key t, 8-dim chunk c), the chunk is
+      // word c of the row (dims 8c+k at bits 4k); a code masked in place is the
+      // fp16 subnormal c * 2^(L-24) (L = 0 or 4), so the chunk holds dims
+      // (0, 4, 1, 5, 2, 6, 3, 7) with L = (0, 0, 4, 4, 0, 0, 4, 4), and the
+      // query operand is laid out and scaled to match (every product carries 2^-24)
       for (int it = dt; it < KT * 32; it += 128) {
         const int t = it >> 5, c = it & 31;
         const uint32_t w = reinterpret_cast<const uint32_t*>(g + STG_KC)[t * 32 + c];
-        uint32_t hv[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t x = ((w >> (8 * j)) & 0xFu) | (((w >> (8 * j + 4)) & 0xFu) << 16);
-          uint32_t y;
-          asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(x | 0x64006400u), "r"(0x64006400u));
-          hv[j] = y;  // (c_2j, c_2j+1) as fp16
-        }
+        const uint32_t w8 = w >> 8;
         *reinterpret_cast<uint4*>(smem + OFF_K + (c >> 3) * KT * 128 + swz(t, c & 7)) =
-            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            make_uint4(w & 0x000F000Fu, w & 0x00F000F0u, w8 & 0x000F000Fu, w8 & 0x00F000F0u);
       }
       // the key scales and biases of the tile, for the row threads
       for (int it = dt; it < KT * 4; it += 128) {
@@ -357,11 +357,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           const uint16_t* vb = reinterpret_cast<const uint16_t*>(g + STG_VB) + t * 4;
           const float s = bf16_to_f32(vs[gi]), bb = bf16_to_f32(vb[gi]);
           const bool stale = i * KT + t >= T;  // rows past the length may hold anything: P is 0 there, and 0 * NaN is not
+          // the group's values lie between b and b + 7 s (codes 0 .. 7)
+          if (!stale) vmax = fmaxf(vmax, fmaxf(fabsf(bb), fabsf(fmaf(s, 7.0f, bb))));
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
+          for (int e = 0; e < 8; ++e)
             v[k][e] = stale ? 0.f : fmaf(s, __uint_as_float(0x4B000000u | ((f >> (3 * e)) & 7u)) - 8388608.0f, bb);
-            vmax = fmaxf(vmax, fabsf(v[k][e]));
-          }
         }
         // dequantised values enter the P.V product as fp16: a value at or above
         // 2^15 in magnitude (a value group spanning more than about 3e4) is
@@ -432,13 +432,15 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       int e = 0;
       if (m > 0.f) e = min(max(static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127 - 12, -100), 100);
       const float down = __int_as_float((127 - e) << 23);
-      kmul = LOG2E * __int_as_float((127 + e) << 23);
+      // the scores accumulate in units of 2^-24 (key fields), so the multiplier
+      // carries 2^24 and the bias sums below 2^-24
+      kmul = LOG2E * __int_as_float((127 + e + 24) << 23);
       float qh[2] = {0.f, 0.f};  // sums of this thread's two groups
       for (int c = 16 * hf; c < 16 * hf + 16; ++c) {  // 8-dim chunk c: rotation blocks 2c, 2c+1
         uint4 raw = make_uint4(0, 0, 0, 0);
         if (live) raw = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c));
         const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t hv[4];
+        float yy[8];  // q_s of the chunk's 8 dims
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
           float x[4], y[4];
@@ -455,24 +457,28 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             for (int k = 1; k < 4; ++k) a = __fadd_rn(a, __fmul_rn(x[k], bf16_to_f32(__ldg(mb + 4 * k + j))));
             y[j] = __fmul_rn(round_bf16(__fmul_rn(round_bf16(a), p.scale)), down);  // exact: a power of two
           }
-          const uint32_t h0 = pack_h2(y[0], y[1]), h1 = pack_h2(y[2], y[3]);
-          hv[2 * blk] = h0;
-          hv[2 * blk + 1] = h1;
-          // the sums use the fp16 values the MMA multiplies
-          const __half2 a0 = *reinterpret_cast<const __half2*>(&h0), a1 = *reinterpret_cast<const __half2*>(&h1);
-          qh[(c >> 3) & 1] += __low2float(a0) + __high2float(a0) + __low2float(a1) + __high2float(a1);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) yy[4 * blk + j] = y[j];
         }
-        *reinterpret_cast<uint4*>(smem + OFF_Q + (c >> 3) * ROWS * 128 + swz(r, c & 7)) =
-            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        // the key chunk's layout: dims (0, 4, 1, 5, 2, 6, 3, 7), the odd pairs
+        // scaled by 2^-4 (their key fields sit 4 bits higher)
+        const uint32_t h0 = pack_h2(yy[0], yy[4]), h1 = pack_h2(yy[1] * 0.0625f, yy[5] * 0.0625f);
+        const uint32_t h2 = pack_h2(yy[2], yy[6]), h3 = pack_h2(yy[3] * 0.0625f, yy[7] * 0.0625f);
+        // the sums use the fp16 values the MMA multiplies, in the query's own scale
+        const __half2 a0 = *reinterpret_cast<const __half2*>(&h0), a1 = *reinterpret_cast<const __half2*>(&h1);
+        const __half2 a2 = *reinterpret_cast<const __half2*>(&h2), a3 = *reinterpret_cast<const __half2*>(&h3);
+        qh[(c >> 3) & 1] += __low2float(a0) + __high2float(a0) + 16.0f * (__low2float(a1) + __high2float(a1)) +
+                            __low2float(a2) + __high2float(a2) + 16.0f * (__low2float(a3) + __high2float(a3));
+        *reinterpret_cast<uint4*>(smem + OFF_Q + (c >> 3) * ROWS * 128 + swz(r, c & 7)) = make_uint4(h0, h1, h2, h3);
       }
       // exchange the group sums: this thread holds groups 2 hf, 2 hf + 1
       xch[XCH_QS + hf * ROWS * 2 + 2 * r] = qh[0];
       xch[XCH_QS + hf * ROWS * 2 + 2 * r + 1] = qh[1];
       ok = row_sync() && ok;
-      qs[2 * hf] = qh[0];
-      qs[2 * hf + 1] = qh[1];
-      qs[2 - 2 * hf] = xch[XCH_QS + (1 - hf) * ROWS * 2 + 2 * r];
-      qs[3 - 2 * hf] = xch[XCH_QS + (1 - hf) * ROWS * 2 + 2 * r + 1];
+      qs[2 * hf] = qh[0] * 0x1p-24f;
+      qs[2 * hf + 1] = qh[1] * 0x1p-24f;
+      qs[2 - 2 * hf] = xch[XCH_QS + (1 - hf) * ROWS * 2 + 2 * r] * 0x1p-24f;
+      qs[3 - 2 * hf] = xch[XCH_QS + (1 - hf) * ROWS * 2 + 2 * r + 1] * 0x1p-24f;
     }
     proxy_fence();
     named_bar(1, 2 * 128 + 32);  // (arrive side for the MMA warp)
