@@ -420,8 +420,9 @@ def append_throughput(dev, rot, reps: int = 10):
     """Appended tokens/s of the append kernel (rotate + quantise + pack + store)
     on two shapes: the batched-decode prefill chunks (32 sequences x 2 kv heads x
     4096 tokens per call) and one chunked-prefill chunk (1 sequence x 2 kv heads
-    x 2048 tokens).  CUDA events around `reps` calls; each call is undone by a
-    host-side trim, so every call writes the same rows."""
+    x 2048 tokens).  CUDA events around `reps` calls, queued behind a spin
+    kernel so the region times the device, not the host's calls; each call is
+    undone by a host-side trim, so every call writes the same rows."""
     from rotated_bit_quantized_gb300 import IQCache
     stream = torch.cuda.current_stream(dev)
     res = []
@@ -435,6 +436,7 @@ def append_throughput(dev, rot, reps: int = 10):
             cache.trim(n)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
+        preroll(dev, reps, 100e-6)
         e0.record(stream)
         for _ in range(reps):
             cache.append(k, v, rot)
