@@ -318,14 +318,24 @@ struct Stage {
 // grid (nch, B*Hkv, rtiles), 128 threads.  CTA (x, bh, z): the 8 query rows of
 // tile z over key split x (a multiple of 32 keys).  The split's keys pass
 // through shared memory in 32-key tiles, two in flight (cp.async, 16-byte
-// pieces: every row and every tile's scale block starts 16-byte aligned); warp
-// w owns rows 2w and 2w+1 over every key, lane l dims 8l .. 8l+7.  Softmax
-// state in log2 units.  F32: float32 queries, rotation, scales and biases.
+// pieces: every row and every tile's scale block starts 16-byte aligned).
+// Warp w takes keys 8w .. 8w+7 of each tile, four at a time, for all 8 rows,
+// so every key is dequantised once: lane l holds dims 8l .. 8l+7 of the rows'
+// queries and of the keys and values; the 32 (key, row) dot products of a
+// batch are summed over the lanes by a butterfly that leaves the sum for key
+// l/8 and row l%8 in lane l, which applies the masks and the row's lazily
+// moving reference max (softmax in log2 units, P <= 2^8); the 32
+// probabilities are gathered back for P.V.  At the end the four warps' states
+// merge through shared memory into the CTA's partial.  F32: float32 queries,
+// rotation, scales and biases.
 template <bool F32>
 __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__ AttendArgs p) {
   constexpr float LOG2E = 1.4426950408889634f;
   constexpr float NEG = -__builtin_huge_valf();
+  constexpr float TAU = 8.0f;  // a row's reference moves only when a score passes it by 2^8
   __shared__ __align__(16) Stage st[2];
+  static_assert(sizeof(Stage) * 2 >= 4 * 8 * kHeadDim * 4 + 4 * 8 * 2 * 4 && sizeof(Stage) >= 8 * kHeadDim * 4,
+                "the stages hold the query rows and, after the loop, the warps' states");
   const int x = blockIdx.x, bh = blockIdx.y, z = blockIdx.z;
   const int b = bh / p.kv_heads, h = bh % p.kv_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -333,32 +343,48 @@ __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__
   const int per = ((T + p.nch - 1) / p.nch + kTileKeys - 1) / kTileKeys * kTileKeys;
   const int c0 = x * per;
 
-  float m[2][4][4];
-  load_rotation<F32>(p.rot, lane, m);
-  // q'' = rnd(rnd(q @ M) * scale) of the warp's two rows, the lane's 8 dims,
-  // rnd rounding to the data dtype (M = M_b for bfloat16 data)
-  float qq[2][8];
-  int qpos[2], qidx[2];
-  int cmax = -1;  // the last key some row of the tile may see
+  // q'' = rnd(rnd(q @ M) * scale) of the tile's 8 rows (warp w rotates rows 2w,
+  // 2w+1), rnd rounding to the data dtype (M = M_b for bfloat16 data); every
+  // warp then reads the lane's 8 dims of all 8 rows
+  float* qsh = reinterpret_cast<float*>(&st[1]);  // [8 rows][256] (st[1] is staged after this)
+  {
+    float m[2][4][4];
+    load_rotation<F32>(p.rot, lane, m);
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int R = 8 * z + 2 * warp + j, i = R / p.rep, hr = R % p.rep;
-    const bool rv = R < p.rows;
-    qidx[j] = min(i, p.nq - 1);
-    qpos[j] = rv ? (p.causal ? T - p.nq + i : T - 1) : -1;
-    float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (rv) {
-      const long long qrow = (static_cast<long long>(b) * p.kv_heads * p.rep + h * p.rep + hr) * p.nq + i;
-      load_rotate_row<F32>(p.q, qrow, lane, m, y);
+    for (int j = 0; j < 2; ++j) {
+      const int R = 8 * z + 2 * warp + j, i = R / p.rep, hr = R % p.rep;
+      float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (R < p.rows) {
+        const long long qrow = (static_cast<long long>(b) * p.kv_heads * p.rep + h * p.rep + hr) * p.nq + i;
+        load_rotate_row<F32>(p.q, qrow, lane, m, y);
+      }
+#pragma unroll
+      for (int d = 0; d < 8; ++d)
+        qsh[(2 * warp + j) * kHeadDim + 8 * lane + d] =
+            F32 ? __fmul_rn(y[d], p.scale) : round_bf16(__fmul_rn(y[d], p.scale));
     }
-#pragma unroll
-    for (int d = 0; d < 8; ++d) qq[j][d] = F32 ? __fmul_rn(y[d], p.scale) : round_bf16(__fmul_rn(y[d], p.scale));
   }
+  __syncthreads();
+  float qq[8][8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int d = 0; d < 8; ++d) qq[r][d] = qsh[r * kHeadDim + 8 * lane + d];
+  // this lane's row in the softmax phase: row (lane % 8) of the tile
+  const int myr = lane & 7;
+  int qpos_l, qidx_l;
+  {
+    const int R = 8 * z + myr, i = R / p.rep;
+    qidx_l = min(i, p.nq - 1);
+    qpos_l = R < p.rows ? (p.causal ? T - p.nq + i : T - 1) : -1;
+  }
+  int cmax;  // the last key some row of the tile may see
   {
     const int R = min(8 * z + 7, p.rows - 1), i = R / p.rep;
     cmax = p.causal ? T - p.nq + i : T - 1;
   }
   const int c1 = min(min(T, c0 + per), cmax + 1);  // keys [c0, c1) of the split matter to the tile
+  __syncthreads();  // every warp has its query dims before st[1] is staged
 
   // staging of tile [t, t + 32): codes rows, then the scale and bias blocks
   const int kbytes = kTileKeys * 32 * p.kbits, vbytes = kTileKeys * 32 * p.vbits;
@@ -382,11 +408,13 @@ __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__
     }
   };
 
-  float mrow[2] = {NEG, NEG}, lrow[2] = {0.f, 0.f}, o[2][8];
+  // softmax state: the lane's row reference and partial row sum; O of all 8
+  // rows over the lane's 8 dims
+  float mref = NEG, lpart = 0.f, o[8][8];
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
+  for (int r = 0; r < 8; ++r)
 #pragma unroll
-    for (int d = 0; d < 8; ++d) o[j][d] = 0.f;
+    for (int d = 0; d < 8; ++d) o[r][d] = 0.f;
 
   const int ntiles = c1 > c0 ? (c1 - c0 + kTileKeys - 1) / kTileKeys : 0;
   if (ntiles > 0) stage(0, c0);
@@ -399,69 +427,133 @@ __global__ void __launch_bounds__(128) attend_any_kernel(const __grid_constant__
     const Stage& S = st[it & 1];
     const int tbase = c0 + it * kTileKeys;
     const int nk = min(kTileKeys, c1 - tbase);
-    for (int r0 = 0; r0 < nk; r0 += 2) {
-      float k[2][8], v[2][8], sc[2][2];
+#pragma unroll 1
+    for (int k0 = 8 * warp; k0 < 8 * warp + 8 && k0 < nk; k0 += 4) {
+      // partial dot products of the batch's 4 keys with the 8 rows: value key*8 + row
+      float val[32];
+      {
+        float kx[4][8];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int r = min(r0 + u, nk - 1);  // a second key past the end repeats the first (masked below)
-        dequant_lane<F32>(S.kc, S.ks, S.kb, r, p.kbits, ng, klb, k[u]);
-        dequant_lane<F32>(S.vc, S.vs, S.vb, r, p.vbits, ng, vlb, v[u]);
-      }
+        for (int u = 0; u < 4; ++u) dequant_lane<F32>(S.kc, S.ks, S.kb, min(k0 + u, nk - 1), p.kbits, ng, klb, kx[u]);
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+        for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float s = 0.f;
+          for (int r = 0; r < 8; ++r) {
+            float acc = 0.f;
 #pragma unroll
-          for (int d = 0; d < 8; ++d) s = fmaf(qq[j][d], k[u][d], s);
-          sc[u][j] = s;
-        }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) sc[u][j] += __shfl_xor_sync(0xffffffffu, sc[u][j], off);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int t = tbase + r0 + u;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float s = sc[u][j] * LOG2E;
-          if (r0 + u >= nk || t > qpos[j]) s = NEG;  // warp-uniform
-          if (s != NEG && p.mask_kind == 2) {
-            s = fmaf(__ldg(static_cast<const float*>(p.mask) +
-                           (static_cast<long long>(b) * p.nq + qidx[j]) * p.mask_stride + t),
-                     LOG2E, s);
-          } else if (s != NEG && p.mask_kind == 3) {
-            if (__ldg(static_cast<const uint8_t*>(p.mask) + (static_cast<long long>(b) * p.nq + qidx[j]) *
-                                                                p.mask_stride + t) == 0)
-              s = kMaskedScore * LOG2E;
+            for (int d = 0; d < 8; ++d) acc = fmaf(qq[r][d], kx[u][d], acc);
+            val[8 * u + r] = acc;
           }
-          if (s == NEG) continue;
-          const float mn = fmaxf(mrow[j], s);
-          const float a = mrow[j] == NEG ? 0.f : ex2_approx(mrow[j] - mn);
-          const float pr = ex2_approx(s - mn);
-          lrow[j] = fmaf(lrow[j], a, pr);
+      }
+      // butterfly reduce-scatter: after step b the lane keeps the half of its
+      // values whose index bit (4 - b) equals its lane bit (4 - b); lane l ends
+      // with the full sum of value l
 #pragma unroll
-          for (int d = 0; d < 8; ++d) o[j][d] = fmaf(o[j][d], a, pr * v[u][d]);
-          mrow[j] = mn;
+      for (int lev = 0; lev < 5; ++lev) {
+        const int hn = 16 >> lev, msk = 16 >> lev;
+        const bool up = (lane & msk) != 0;
+#pragma unroll
+        for (int i = 0; i < hn; ++i) {
+          const float send = up ? val[i] : val[i + hn];
+          const float keep = up ? val[i + hn] : val[i];
+          val[i] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
+        }
+      }
+      // the lane's (key, row): masks, then the lazily moving row reference
+      const int kr = k0 + (lane >> 3), t = tbase + kr;
+      float s = val[0] * LOG2E;
+      if (kr >= nk || t > qpos_l) s = NEG;
+      if (s != NEG && p.mask_kind == 2) {
+        s = fmaf(__ldg(static_cast<const float*>(p.mask) + (static_cast<long long>(b) * p.nq + qidx_l) * p.mask_stride + t),
+                 LOG2E, s);
+      } else if (s != NEG && p.mask_kind == 3) {
+        if (__ldg(static_cast<const uint8_t*>(p.mask) + (static_cast<long long>(b) * p.nq + qidx_l) * p.mask_stride + t) ==
+            0)
+          s = kMaskedScore * LOG2E;
+      }
+      const bool move = s != NEG && (mref == NEG || s > mref + TAU);
+      if (__any_sync(0xffffffffu, move)) {
+        float mx = s;  // the row's max over the batch's 4 keys (lanes l, l^8, l^16, l^24)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const bool mv = mx != NEG && (mref == NEG || mx > mref + TAU);
+        const float mnew = mv ? (mref == NEG ? mx : fmaxf(mref, mx)) : mref;
+        const float al = !mv ? 1.f : mref == NEG ? 0.f : ex2_approx(mref - mnew);
+        lpart *= al;
+        mref = mnew;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {  // every lane's O of row r: the factor of lane r
+          const float ar = __shfl_sync(0xffffffffu, al, r);
+#pragma unroll
+          for (int d = 0; d < 8; ++d) o[r][d] *= ar;
+        }
+      }
+      const float pr = s == NEG ? 0.f : ex2_approx(s - mref);
+      lpart += pr;
+      // P.V: the values of the 4 keys, each weighted by the row's probability
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float vx[8];
+        dequant_lane<F32>(S.vc, S.vs, S.vb, min(k0 + u, nk - 1), p.vbits, ng, vlb, vx);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const float pw = __shfl_sync(0xffffffffu, pr, 8 * u + r);  // 0 for keys past the tile
+#pragma unroll
+          for (int d = 0; d < 8; ++d) o[r][d] = fmaf(pw, vx[d], o[r][d]);
         }
       }
     }
     __syncthreads();  // every warp is done with this stage before it is refilled
   }
-  // the split's partial of the warp's rows
+  // merge the four warps' states through shared memory (the stages are free):
+  // per warp and row the reference max and the row sum, then O
+  float lrow = lpart;
+  lrow += __shfl_xor_sync(0xffffffffu, lrow, 8);
+  lrow += __shfl_xor_sync(0xffffffffu, lrow, 16);
+  float* wo = reinterpret_cast<float*>(&st[0]);  // [4 warps][8 rows][256]
+  float* wml = wo + 4 * 8 * kHeadDim;            // [4 warps][8 rows][2]
+  cp_async_wait_1();
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  if (lane < 8) {
+    wml[(warp * 8 + lane) * 2] = mref;
+    wml[(warp * 8 + lane) * 2 + 1] = lrow;
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    float4* dst = reinterpret_cast<float4*>(wo + (warp * 8 + r) * kHeadDim + 8 * lane);
+    dst[0] = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
+    dst[1] = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
+  }
+  __syncthreads();
+  // the split's partial of the tile's rows: thread (row r = warp*2 + j, lane) merges dims 8*lane .. +7
   const long long slot = (static_cast<long long>(bh) * p.rtiles + z) * p.nch + x;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const long long r = slot * 8 + 2 * warp + j;
-    float4* dst = reinterpret_cast<float4*>(p.part_o + r * kHeadDim + 8 * lane);
-    dst[0] = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
-    dst[1] = make_float4(o[j][4], o[j][5], o[j][6], o[j][7]);
+    const int r = 2 * warp + j;
+    float M = NEG;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, wml[(w * 8 + r) * 2]);
+    float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float mw = wml[(w * 8 + r) * 2];
+      if (mw == NEG) continue;
+      const float a = ex2_approx(mw - M);
+      L = fmaf(wml[(w * 8 + r) * 2 + 1], a, L);
+      const float4* src = reinterpret_cast<const float4*>(wo + (w * 8 + r) * kHeadDim + 8 * lane);
+      const float4 u0 = src[0], u1 = src[1];
+      const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int d = 0; d < 8; ++d) acc[d] = fmaf(u[d], a, acc[d]);
+    }
+    const long long rr = slot * 8 + r;
+    float4* dst = reinterpret_cast<float4*>(p.part_o + rr * kHeadDim + 8 * lane);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     if (lane == 0) {
-      p.part_ml[r * 2] = mrow[j];
-      p.part_ml[r * 2 + 1] = lrow[j];
+      p.part_ml[rr * 2] = M;
+      p.part_ml[rr * 2 + 1] = L;
     }
   }
 }
