@@ -1172,34 +1172,70 @@ __global__ void __maxnreg__((Cfg<NT, DS, STREAMS, NSTAGE, MINB, TILE_, PAIR, HAL
         a_row[j][e] = msc[j][e] == NEG_INF ? 0.f : ex2_approx(msc[j][e] - M);
         if (dg == 0 && g == 0) lbuf[stream * GT + row] = lrow[j][e] * a_row[j][e];
       }
-#pragma unroll 1
-    for (int turn = 0; turn < STREAMS; ++turn) {
-      if (stream == turn) {
+    if (u == u0) {
+      // the range's last unit: the ring is idle (every tile consumed), so each
+      // stream writes its scaled O to a slot of its own there, in parallel, and
+      // every thread then sums the streams of its elements in stream order
+      // (the same sums, in the same order, as the turns below)
+      static_assert(STREAMS * GT * kHeadDim * 4 <= NSTAGE * STAGE, "the ring holds every stream's O");
+      float* slot = reinterpret_cast<float*>(smem) + stream * GT * kHeadDim;
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
+      for (int j = 0; j < NT; ++j)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int row = 8 * j + 2 * t + e;
-            const float a = a_row[j][e];
+        for (int e = 0; e < 2; ++e) {
+          const int row = 8 * j + 2 * t + e;
+          const float a = a_row[j][e];
 #pragma unroll
-            for (int gi = 0; gi < GPW; ++gi) {
-              const int col = 64 * (dg * GPW + gi) + 8 * g;
-              float4 v0 = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a, O[gi][1][j][e] * a,
-                                      O[gi][1][j][e + 2] * a);
-              float4 v1 = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a, O[gi][3][j][e] * a,
-                                      O[gi][3][j][e + 2] * a);
-              float4* acc = reinterpret_cast<float4*>(obuf + row * kHeadDim + col);
-              if (turn > 0) {
-                const float4 p0 = acc[0], p1 = acc[1];
-                v0.x += p0.x; v0.y += p0.y; v0.z += p0.z; v0.w += p0.w;
-                v1.x += p1.x; v1.y += p1.y; v1.z += p1.z; v1.w += p1.w;
-              }
-              acc[0] = v0;
-              acc[1] = v1;
-            }
+          for (int gi = 0; gi < GPW; ++gi) {
+            float4* dst = reinterpret_cast<float4*>(slot + row * kHeadDim + 64 * (dg * GPW + gi) + 8 * g);
+            dst[0] = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a, O[gi][1][j][e] * a,
+                                 O[gi][1][j][e + 2] * a);
+            dst[1] = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a, O[gi][3][j][e] * a,
+                                 O[gi][3][j][e + 2] * a);
           }
+        }
+      named_bar(bar_all, NCT);
+      const float4* slots = reinterpret_cast<const float4*>(smem);
+      for (int idx = ctid; idx < GT * kHeadDim / 4; idx += NCT) {
+        float4 acc = slots[idx];
+#pragma unroll
+        for (int st = 1; st < STREAMS; ++st) {
+          const float4 v = slots[st * GT * kHeadDim / 4 + idx];
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        reinterpret_cast<float4*>(obuf)[idx] = acc;
       }
       named_bar(bar_all, NCT);
+    } else {
+#pragma unroll 1
+      for (int turn = 0; turn < STREAMS; ++turn) {
+        if (stream == turn) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int row = 8 * j + 2 * t + e;
+              const float a = a_row[j][e];
+#pragma unroll
+              for (int gi = 0; gi < GPW; ++gi) {
+                const int col = 64 * (dg * GPW + gi) + 8 * g;
+                float4 v0 = make_float4(O[gi][0][j][e] * a, O[gi][0][j][e + 2] * a, O[gi][1][j][e] * a,
+                                        O[gi][1][j][e + 2] * a);
+                float4 v1 = make_float4(O[gi][2][j][e] * a, O[gi][2][j][e + 2] * a, O[gi][3][j][e] * a,
+                                        O[gi][3][j][e + 2] * a);
+                float4* acc = reinterpret_cast<float4*>(obuf + row * kHeadDim + col);
+                if (turn > 0) {
+                  const float4 p0 = acc[0], p1 = acc[1];
+                  v0.x += p0.x; v0.y += p0.y; v0.z += p0.z; v0.w += p0.w;
+                  v1.x += p1.x; v1.y += p1.y; v1.z += p1.z; v1.w += p1.w;
+                }
+                acc[0] = v0;
+                acc[1] = v1;
+              }
+            }
+        }
+        named_bar(bar_all, NCT);
+      }
     }
     // obuf holds the range's O for the unit; per row M = max and L = sum over the streams
     for (int r = ctid; r < GT; r += NCT) {
