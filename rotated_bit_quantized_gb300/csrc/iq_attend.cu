@@ -1879,9 +1879,10 @@ int attend_impl(const iq_cache* c, const void* q_in, int q_heads, int n_queries,
   st = make_plan(c, q_heads, n_queries, causal, &bound, nullptr);
   if (st != IQ_OK) return st;
   if (workspace_bytes < bound.bytes) return fail(IQ_ERR_WORKSPACE, "workspace smaller than iq_attend_workspace()");
-  if (n_new == 0 && prefill_shape(c, q_heads, n_queries, mask_kind)) {
+  if (prefill_shape(c, q_heads, n_queries, mask_kind)) {  // n_new > 0: the caller checked prefill_fusable
     st = prefill_attend(c, q, q_heads, n_queries, scale, causal, rot_bf16, out, out_f32,
-                        reinterpret_cast<unsigned*>(workspace), stream);
+                        reinterpret_cast<unsigned*>(workspace), stream, k_new, v_new, n_new,
+                        reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + kStatusBytes));
     if (st == IQ_OK) read_marks().record(c);
     return st;
   }
@@ -1999,21 +2000,26 @@ int iq_cache_append_attend(iq_cache* c, const void* keys, const void* values, in
     if (static_cast<long long>(c->lens[b]) + n > c->capacity)
       return fail(IQ_ERR_CAPACITY, "append past capacity (grow the cache first)");
   // One kernel when every (sequence, kv head) is one query tile and the new
-  // rows of each sequence sit in one key tile; otherwise the append, then the
-  // attention.
+  // rows of each sequence sit in one key tile (the split-KV kernel encodes
+  // them), or when the call takes the tensor-memory prefill kernel (its CTAs
+  // encode the new rows' key tiles, each tile once, before streaming them);
+  // otherwise the append, then the attention.
   const int tile = Cfg<IQ_DECODE_CFG>::TILE;
-  bool fused = tuned_format(c) && q_heads >= c->kv_heads && q_heads % c->kv_heads == 0 &&
-               static_cast<long long>(q_heads / c->kv_heads) * n_queries <= 8;
+  const bool shape_ok = tuned_format(c) && q_heads >= c->kv_heads && q_heads % c->kv_heads == 0;
+  bool fused = shape_ok && static_cast<long long>(q_heads / c->kv_heads) * n_queries <= 8;
   for (int b = 0; b < c->batch && fused; ++b)
     fused = c->lens[b] / tile == (c->lens[b] + n - 1) / tile;
-  if (!fused) {
+  const long long pflags = shape_ok && prefill_shape(c, q_heads, n_queries, causal ? 1 : 0) ? prefill_fuse_flags(c, n) : 0;
+  const bool fused_prefill = pflags > 0 && kStatusBytes + pflags * sizeof(unsigned) <= kHeadBytes;
+  if (!fused && !fused_prefill) {
     st = iq_cache_append(c, keys, values, n, rot, stream);
     if (st != IQ_OK) return st;
     return iq_attend(c, q, q_heads, n_queries, scale, causal, rot, out, out_f32, workspace, workspace_bytes,
                      stream);
   }
   static_assert(Cfg<IQ_DECODE_CFG>::TILE <= kFreshRows, "a fused append writes at most kFreshRows rows");
-  const int encode_wait = read_marks().append_clear(c) ? 0 : 1;
+  // (the prefill kernel waits for the previous grids before it stores)
+  const int encode_wait = fused_prefill || read_marks().append_clear(c) ? 0 : 1;
   for (int b = 0; b < c->batch; ++b) c->lens[b] += n;
   st = attend_impl(c, q, q_heads, n_queries, scale, causal, rot, out, out_f32, workspace, workspace_bytes,
                    stream, keys, values, n, 0, nullptr, 0, encode_wait);

@@ -37,7 +37,12 @@ int attend_any_workspace(const iq_cache* c, int q_heads, int n_queries, size_t* 
 // no explicit mask: the tensor-memory kernel.
 bool prefill_shape(const iq_cache* c, int q_heads, int n_queries, int mask_kind);
 int prefill_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
-                   const uint16_t* rot, void* out, int out_f32, unsigned* status, iq_stream_t stream);
+                   const uint16_t* rot, void* out, int out_f32, unsigned* status, iq_stream_t stream,
+                   const uint16_t* k_new = nullptr, const uint16_t* v_new = nullptr, int n_new = 0,
+                   unsigned* flags = nullptr);
+// Counter words the fused prefill append needs in the workspace's unit-counter
+// area (two, plus one per sequence and kv head).
+long long prefill_fuse_flags(const iq_cache* c, int n_new);
 int attend_any(const iq_cache* c, const void* q, int q_heads, int n_queries, float scale, int causal,
                const void* rot, void* out, int out_f32, void* workspace, size_t workspace_bytes,
                iq_stream_t stream, int mask_kind, const void* mask, long long mask_stride);

@@ -48,6 +48,7 @@
 #include <cstring>
 
 #include "iq_common.cuh"
+#include "iq_encode.cuh"
 
 namespace iq {
 namespace pre {
@@ -72,8 +73,10 @@ constexpr int OFF_XCH = OFF_SC + 2 * KT * 8 * 4;  // row threads' exchange area 
 constexpr int XCH_QS = 2 * 2 * ROWS, XCH_L = XCH_QS + 2 * ROWS * 2;
 constexpr int OFF_BAR = OFF_XCH + (XCH_L + 2 * ROWS) * 4;
 constexpr int SMEM = OFF_BAR + 128 + 1024;  // + alignment slack
+static_assert(13 * 8 + 4 <= 128, "the 13 barriers and the tensor-memory slot fit their area");
 static_assert(STG_BYTES == 16384 && OFF_STG % 1024 == 0 && OFF_SC % 16 == 0, "layout");
 constexpr int THREADS = 448;
+constexpr int ENC_CHUNK = 2 * (THREADS / 32);  // new rows per take of the fused append (two per warp)
 
 struct Params {
   const uint32_t* k_codes;
@@ -86,6 +89,32 @@ struct Params {
   const uint16_t* rot;
   void* out;
   unsigned* status;
+  int out_f32, kv_heads, rep, nq, cap, causal, rtiles;
+  float scale;
+  int lens[IQ_MAX_BATCH];
+};
+// The fused launch's parameters: the same fields (same names, so one kernel
+// body serves both) plus the fused append's.  The n_new new rows of every
+// (sequence, kv head), bf16 [B][Hkv][n_new][256], unrotated, are encoded into
+// the cache at rows lens[b] - n_new .. lens[b] - 1 by the grid; flags (zero at
+// launch, zero again when the grid ends): [0] chunks taken, [1] CTAs finished,
+// then per (sequence, kv head) the count of its new rows stored.  (The field
+// order of each struct is the one measured fastest for its kernel.)
+struct FusedParams {
+  const uint32_t* k_codes;
+  const uint16_t* k_scales;
+  const uint16_t* k_biases;
+  const uint32_t* v_codes;
+  const uint16_t* v_scales;
+  const uint16_t* v_biases;
+  const uint16_t* q;
+  const uint16_t* rot;
+  void* out;
+  unsigned* status;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  unsigned* flags;
+  int n_new;
   int out_f32, kv_heads, rep, nq, cap, causal, rtiles;
   float scale;
   int lens[IQ_MAX_BATCH];
@@ -104,6 +133,19 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
   for (;;) {
     if (mbar_try_wait(bar, parity, 2000u)) return true;
     if (now_ns() - t0 > 100000000ull) return false;
+  }
+}
+
+// Bounded wait for new rows (other CTAs may still be storing them): true once
+// their count reaches want, false after 4 s.
+__device__ __forceinline__ bool wait_stored(const unsigned* count, unsigned want) {
+  const unsigned long long t0 = now_ns();
+  for (;;) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+    if (v >= want) return true;
+    if (now_ns() - t0 > 4000000000ull) return false;
+    __nanosleep(128);
   }
 }
 
@@ -168,14 +210,65 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return d;
 }
 
-__global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ Params p) {
+// The fused append's encoding, every CTA of the grid taking ENC_CHUNK rows at
+// a time (kept out of line: its registers stay out of the pipeline's budget).
+__device__ __noinline__ void encode_new_rows(const FusedParams& p, int nbh, uint8_t* smem, int warp, int lane) {
+  unsigned* const row_count = p.flags + 2;  // [bh]: new rows stored
+  int* slot = reinterpret_cast<int*>(smem + OFF_SC);
+  const long long total = static_cast<long long>(nbh) * p.n_new;
+  float m[2][4][4];
+  load_row_rotation(p.rot, lane, m);
+  for (;;) {
+    if (threadIdx.x == 0) *slot = static_cast<int>(atomicAdd(p.flags, 1u));
+    __syncthreads();
+    const long long c0 = static_cast<long long>(*slot) * ENC_CHUNK;
+    __syncthreads();  // the slot is read before the next take overwrites it
+    if (c0 >= total) break;
+    // two rows per warp, both rows' loads issued before either is encoded
+    uint4 rk[2], rv[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const long long item = c0 + warp + h * (THREADS / 32);
+      if (item < total) {
+        const long long src = item * kHeadDim + lane * 8;
+        rk[h] = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
+        rv[h] = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const long long item = c0 + warp + h * (THREADS / 32);
+      if (item >= total) break;
+      const int ebh = static_cast<int>(item / p.n_new), j = static_cast<int>(item % p.n_new);
+      const long long dst = static_cast<long long>(ebh) * p.cap + p.lens[ebh / p.kv_heads] - p.n_new + j;
+      encode_row<4>(rk[h], m, lane, dst, const_cast<uint32_t*>(p.k_codes), const_cast<uint16_t*>(p.k_scales),
+                    const_cast<uint16_t*>(p.k_biases));
+      encode_row<3>(rv[h], m, lane, dst, const_cast<uint32_t*>(p.v_codes), const_cast<uint16_t*>(p.v_scales),
+                    const_cast<uint16_t*>(p.v_biases));
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // the stores before other CTAs' bulk copies
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        atomicAdd(row_count + ebh, 1u);
+      }
+    }
+  }
+}
+
+// FUSED: the grid also encodes the call's new rows (the fused append); a
+// separate instantiation, so attention-only launches carry none of its code.
+template <bool FUSED, typename P>
+__global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ P p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // [NSTG]
   uint64_t* empty = full + NSTG;                                  // [NSTG]
   uint64_t* k_ready = empty + NSTG;                               // key operand (and key scales) of tile i written
-  uint64_t* v_ready = k_ready + 1;                                // value operand of tile i written
-  uint64_t* s_ready = v_ready + 1;                                // S_g of tile i in tensor memory
+  // [2]: value operand of tile i written, on v_ready[i & 1] (phase i / 2).  One
+  // barrier would not do: the builders may finish V(i+1) while the MMA lane
+  // still waits for P(i), and a parity wait cannot tell phase i from phase i+2
+  uint64_t* v_ready = k_ready + 1;
+  uint64_t* s_ready = v_ready + 2;                                // S_g of tile i in tensor memory
   uint64_t* p_ready = s_ready + 1;                                // P of tile i written (and O rescaled)
   uint64_t* o_ready = p_ready + 1;  // [2]: P.V of tile i done, on o_ready[i & 1] (phase i / 2)
   uint64_t* s_free = o_ready + 2;                                 // S of tile i read (S(i+1) may be issued)
@@ -199,13 +292,25 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // ---- fused append.  The new rows (B x Hkv x n_new of them, in (sequence,
+  // kv head, row) order) are encoded in chunks of ENC_CHUNK rows that every CTA
+  // takes from one counter (flags[0]) until none is left, a warp per row; each
+  // stored row adds one to its (sequence, kv head)'s count (release).  A CTA's
+  // producer, at its first tile holding new rows, waits for the count to reach
+  // n_new only once every chunk has been taken, so the rows it waits for are
+  // owed only by CTAs already encoding (which wait for nothing), never by a CTA
+  // that has not started: the grid needs no co-residency.  The last CTA to
+  // finish returns the counters to zero (flags[1] counts finished CTAs).
+  if constexpr (FUSED) encode_new_rows(p, nbh, smem, warp, lane);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTG; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 4);
     }
     mbar_init(k_ready, 4);
-    mbar_init(v_ready, 4);
+    mbar_init(&v_ready[0], 4);
+    mbar_init(&v_ready[1], 4);
     mbar_init(s_ready, 1);
     mbar_init(p_ready, 8);
     mbar_init(&o_ready[0], 1);
@@ -228,11 +333,22 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int issued = 0;
+      int i_new = -1;  // the first tile holding new rows
+      if constexpr (FUSED) i_new = (T - p.n_new) / KT;
       for (int i = 0; i < ntiles; ++i, ++issued) {
         const int st = i % NSTG;
         if (i >= NSTG && !wait_phase(&empty[st], static_cast<uint32_t>(i / NSTG - 1) & 1)) {
           atomicOr(p.status, 1u | 0x100u);
           break;
+        }
+        if constexpr (FUSED) {
+          if (i == i_new) {  // the first tile with new rows: wait until all are stored
+            if (!wait_stored(p.flags + 2 + bh, static_cast<unsigned>(p.n_new))) {
+              atomicOr(p.status, 1u | 0x20000u);
+              break;
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
         }
         uint8_t* g = smem + OFF_STG + st * STG_BYTES;
         const long long r = row0 + static_cast<long long>(i) * KT;
@@ -280,7 +396,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           }
           issue_s(i + 1);
         }
-        if (!wait_phase(p_ready, static_cast<uint32_t>(i) & 1) || !wait_phase(v_ready, static_cast<uint32_t>(i) & 1)) {
+        if (!wait_phase(p_ready, static_cast<uint32_t>(i) & 1) ||
+            !wait_phase(&v_ready[i & 1], static_cast<uint32_t>(i >> 1) & 1)) {
           atomicOr(p.status, 2u | 0x400u);
           break;
         }
@@ -378,7 +495,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       proxy_fence();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(v_ready);
+        mbar_arrive(&v_ready[i & 1]);
         mbar_arrive(&empty[st]);
       }
     }
@@ -642,6 +759,18 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     tc_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
+  if constexpr (FUSED) {  // the grid's last CTA (every take and wait is over) zeroes the fused append's counters
+    int* last = reinterpret_cast<int*>(smem + OFF_SC);
+    if (threadIdx.x == 0) {
+      __threadfence();
+      *last = atomicAdd(p.flags + 1, 1u) == gridDim.x - 1u;
+    }
+    __syncthreads();
+    if (*last) {
+      __threadfence();
+      for (int i = threadIdx.x; i < 2 + nbh; i += THREADS) p.flags[i] = 0u;
+    }
+  }
 }
 
 }  // namespace pre
@@ -655,37 +784,48 @@ bool prefill_shape(const iq_cache* c, int q_heads, int n_queries, int mask_kind)
   return tuned_format(c) && mask_kind <= 1 && (q_heads / c->kv_heads) * n_queries >= IQ_PREFILL_MIN_ROWS;
 }
 
+long long prefill_fuse_flags(const iq_cache* c, int n_new) {
+  return n_new > 0 ? 2 + static_cast<long long>(c->batch) * c->kv_heads : 0;
+}
+
 int prefill_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_queries, float scale, int causal,
-                   const uint16_t* rot, void* out, int out_f32, unsigned* status, iq_stream_t stream) {
+                   const uint16_t* rot, void* out, int out_f32, unsigned* status, iq_stream_t stream,
+                   const uint16_t* k_new, const uint16_t* v_new, int n_new, unsigned* flags) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    IQ_CUDA(cudaFuncSetAttribute(pre::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pre::SMEM));
+    IQ_CUDA(cudaFuncSetAttribute(pre::prefill_kernel<false, pre::Params>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 pre::SMEM));
+    IQ_CUDA(cudaFuncSetAttribute(pre::prefill_kernel<true, pre::FusedParams>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, pre::SMEM));
     attr_set[dev] = true;
   }
-  pre::Params p;
-  std::memset(&p, 0, sizeof(p));
-  p.k_codes = c->k_codes;
-  p.k_scales = static_cast<const uint16_t*>(c->k_scales);
-  p.k_biases = static_cast<const uint16_t*>(c->k_biases);
-  p.v_codes = c->v_codes;
-  p.v_scales = static_cast<const uint16_t*>(c->v_scales);
-  p.v_biases = static_cast<const uint16_t*>(c->v_biases);
-  p.q = q;
-  p.rot = rot;
-  p.out = out;
-  p.status = status;
-  p.out_f32 = out_f32 ? 1 : 0;
-  p.kv_heads = c->kv_heads;
-  p.rep = q_heads / c->kv_heads;
-  p.nq = n_queries;
-  p.cap = c->capacity;
-  p.causal = causal;
-  p.rtiles = (p.rep * n_queries + pre::ROWS - 1) / pre::ROWS;
-  p.scale = scale;
-  for (int b = 0; b < c->batch; ++b) p.lens[b] = c->lens[b];
-  const long long grid = static_cast<long long>(c->batch) * c->kv_heads * p.rtiles;
+  if (n_new > 0 && (!flags || !k_new || !v_new)) return fail(IQ_ERR_INVALID_ARG, "fused prefill append arguments");
+  auto fill = [&](auto& p) {
+    std::memset(&p, 0, sizeof(p));
+    p.k_codes = c->k_codes;
+    p.k_scales = static_cast<const uint16_t*>(c->k_scales);
+    p.k_biases = static_cast<const uint16_t*>(c->k_biases);
+    p.v_codes = c->v_codes;
+    p.v_scales = static_cast<const uint16_t*>(c->v_scales);
+    p.v_biases = static_cast<const uint16_t*>(c->v_biases);
+    p.q = q;
+    p.rot = rot;
+    p.out = out;
+    p.status = status;
+    p.out_f32 = out_f32 ? 1 : 0;
+    p.kv_heads = c->kv_heads;
+    p.rep = q_heads / c->kv_heads;
+    p.nq = n_queries;
+    p.cap = c->capacity;
+    p.causal = causal;
+    p.rtiles = (p.rep * n_queries + pre::ROWS - 1) / pre::ROWS;
+    p.scale = scale;
+    for (int b = 0; b < c->batch; ++b) p.lens[b] = c->lens[b];
+  };
+  const int rtiles = ((q_heads / c->kv_heads) * n_queries + pre::ROWS - 1) / pre::ROWS;
+  const long long grid = static_cast<long long>(c->batch) * c->kv_heads * rtiles;
   if (grid > 0x7FFFFFFFLL) return fail(IQ_ERR_UNSUPPORTED, "too many query tiles");
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -697,7 +837,21 @@ int prefill_attend(const iq_cache* c, const uint16_t* q, int q_heads, int n_quer
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  IQ_CUDA(cudaLaunchKernelEx(&cfg, pre::prefill_kernel, p));
+  if (n_new > 0) {
+    // (the fused append's counters share the workspace's unit counters, zero
+    // at every call's start; the grid leaves them zero)
+    pre::FusedParams f;
+    fill(f);
+    f.k_new = k_new;
+    f.v_new = v_new;
+    f.n_new = n_new;
+    f.flags = flags;
+    IQ_CUDA(cudaLaunchKernelEx(&cfg, pre::prefill_kernel<true, pre::FusedParams>, f));
+  } else {
+    pre::Params p;
+    fill(p);
+    IQ_CUDA(cudaLaunchKernelEx(&cfg, pre::prefill_kernel<false, pre::Params>, p));
+  }
   return IQ_OK;
 }
 
