@@ -290,12 +290,18 @@ int iq_attend_mask(const iq_cache* cache, const void* q, int q_heads, int n_quer
  * iq_cache_append_attend — iq_cache_append(keys, values, n) followed by
  * iq_attend(q, ...), the page's decode step (quant_kv.py: `update_and_fetch`,
  * then `asym_quantized_sdpa` over the updated cache), with the same results
- * as the two calls.  For a bfloat16 cache of the tuned format, when every
- * (sequence, kv head) holds at most 8 query
- * rows (q_heads / kv_heads * n_queries <= 8) and each sequence's n new rows
- * fall in one 128-token tile, it is one attention launch whose CTAs encode the
- * new rows themselves before streaming the tiles that hold them; otherwise it
- * is the append launch followed by the attention.
+ * as the two calls.  For a bfloat16 cache of the tuned format it is one
+ * launch in two cases:
+ *  - every (sequence, kv head) holds at most 8 query rows (q_heads / kv_heads
+ *    * n_queries <= 8) and each sequence's n new rows fall in one 128-token
+ *    tile: the split-KV attention, whose CTAs encode the new rows themselves
+ *    before streaming the tiles that hold them;
+ *  - 128 or more query rows per kv head and at most 2046 (sequence, kv head)
+ *    pairs: the tensor-memory prefill kernel, whose CTAs take the new rows in
+ *    chunks from a counter in the workspace head, encode them, and stream a
+ *    sequence's tiles holding new rows only once all of that sequence's new
+ *    rows are stored (a wait that runs out sets status bit 0x20000).
+ * Otherwise it is the append launch followed by the attention.
  * Arguments, layouts and workspace as iq_cache_append and iq_attend; lens[b]
  * grows by n on success (the causal mask and the scanned length use the
  * grown lengths).  Errors: as both (nothing is launched on an error).
