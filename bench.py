@@ -47,8 +47,8 @@ def row_bytes(bits: int, group_size: int) -> int:
 # combine_kernel).  Reported only while the attention source is the one that
 # was measured.
 TRAFFIC = {"source": "rotated_bit_quantized_gb300/csrc/iq_attend.cu",
-           "sha256": "cbbbb95d64b8b220ea973719827cb7cd8301895c913d25bf158bc5ca87bee80b",
-           "bytes": ((539.462144 + 3.067648 + 2.936320) + (539.398656 + 0.088576 + 2.934272)) / 2 * 1e6}
+           "sha256": "a338e6b50448f303315622c9ec90818b34a5646a7475357717509774e45c4edd",
+           "bytes": ((539.385088 + 2.726912 + 2.936576 + 0.0) + (539.399680 + 0.105728 + 2.934528 + 0.002048)) / 2 * 1e6}
 
 
 def measured_traffic():
