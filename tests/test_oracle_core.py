@@ -30,6 +30,24 @@ def _bf16_candidates(x):
     return lo.view(np.float32), hi.view(np.float32)
 
 
+def test_ulp_bf16_is_the_gap_to_the_next_bf16():
+    """ulp_bf16(x) (the output tolerance's bf16 term) equals the distance from
+    the bf16 value at or below |x| to the next one, found on the bit pattern
+    (+1 in the 16-bit representation): normals, powers of two (the gap above),
+    the subnormal range (a fixed 2^-133) and zero."""
+    rng = np.random.default_rng(5)
+    mags = np.concatenate([
+        np.exp(rng.uniform(np.log(2.0 ** -125), np.log(2.0 ** 120), 4000)),  # normals, anywhere in range
+        2.0 ** np.arange(-126, 127, dtype=np.float64),                          # exact powers of two
+        rng.uniform(0, 2.0 ** -126, 200),                                       # subnormal range
+        [0.0, 1.0, 1.5, 3.0, 255.0, 256.0, 65504.0]])
+    xs = np.concatenate([mags, -mags]).astype(np.float32)
+    for x in xs:
+        lo, hi = _bf16_candidates(abs(x))  # truncation: the bf16 at or below |x|, and the next one
+        gap = float(hi) - float(lo)
+        assert bf16.ulp_bf16(x) == gap, (x, bf16.ulp_bf16(x), gap)
+
+
 def test_bf16_is_nearest_with_ties_to_even():
     rng = np.random.default_rng(0)
     xs = np.concatenate([rng.standard_normal(20000).astype(np.float32) * 10,
