@@ -38,6 +38,12 @@
 // P(i) is written, and the row threads write P(i+1) after P.V(i) is done.  The
 // value operand is double-buffered by tile parity: tile i's is built while
 // P.V(i-1) runs.
+// Fused append (the FUSED instantiation, for iq_cache_append_attend): before
+// its pipeline every CTA encodes chunks of the call's new rows (the append's
+// row encoder: rotate, group-quantise, pack, store; page "quant_kv.py",
+// `update_and_fetch`), taken from a counter in the workspace, and the
+// producer streams a sequence's tiles holding new rows only once all of them
+// are stored.
 // Shared-memory operands use the 128-byte swizzle (K-major, 8-row groups
 // 1024 bytes apart).  Tensor memory: S_0..S_3 in columns 0..255, O in
 // 256..511.
