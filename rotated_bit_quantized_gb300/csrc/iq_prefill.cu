@@ -143,14 +143,14 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for new rows (other CTAs may still be storing them): true once
-// their count reaches want, false after 4 s.
+// their count reaches want, false after 1 s (the encode takes microseconds).
 __device__ __forceinline__ bool wait_stored(const unsigned* count, unsigned want) {
   const unsigned long long t0 = now_ns();
   for (;;) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
     if (v >= want) return true;
-    if (now_ns() - t0 > 4000000000ull) return false;
+    if (now_ns() - t0 > 1000000000ull) return false;
     __nanosleep(128);
   }
 }

@@ -53,3 +53,38 @@ def test_wait_runs_out_then_next_call_is_correct(setup, flags, spin, wait_ns, bi
         out = cache.attend(q.cuda(), rot, causal=False, out_dtype=torch.float32)
         compare_out(out, attention.attend(f32(q), oc, mb), f"after injected failure {flags}, call {call}")
         assert cache.device_status() == 0
+
+
+def test_fused_prefill_row_wait_runs_out_then_next_call_is_correct():
+    """The fused prefill's wait for its new rows, made to run out from the host:
+    the workspace's chunk counter is preset past every chunk (2^30 takes), so
+    no CTA encodes and every producer's row count stays below n.  The call
+    returns within the waits' limits with status bit 0x20000; the grid leaves
+    its counters at zero, so the same call after a trim is correct."""
+    from rotated_bit_quantized_gb300 import IQCache, Rotation
+    rot = Rotation(0, 256)
+    mb = oracle_blocks(0)
+    B, H, Hq, n = 1, 2, 16, 256  # 2048 query rows per kv head: 32 CTAs, one wave
+    cache = IQCache(B, H)
+    k0, v0 = si.kv_tokens(74, B, H, 300, outliers=True)
+    cache.append(k0.cuda(), v0.cuda(), rot)
+    oc = OracleCache(B, H)
+    oc.append(f32(k0), f32(v0), mb)
+    k, v = si.kv_tokens(75, B, H, n, outliers=True, step=1)
+    q = si.queries(76, B, Hq, n)
+    cache.append_attend(k.cuda(), v.cuda(), q.cuda(), rot, causal=True)  # creates the workspace
+    cache.trim(n)
+    assert cache.device_status() == 0
+    cache._workspace[256:260].view(torch.int32)[0] = 1 << 30  # the unit-counter area: chunks taken
+    cache.append_attend(k.cuda(), v.cuda(), q.cuda(), rot, causal=True)  # returns; its output is not meaningful
+    torch.cuda.synchronize()
+    # the grid's last CTA zeroed the counters (taken, finished, rows per kv head)
+    # before the status read below, which would also clear them after a failure
+    assert cache._workspace[256:256 + 4 * (2 + B * H)].view(torch.int32).tolist() == [0] * (2 + B * H)
+    st = cache.device_status()
+    assert st & 0x20000, f"status {st:#x} lacks the fused append's wait bit"
+    cache.trim(n)
+    out = cache.append_attend(k.cuda(), v.cuda(), q.cuda(), rot, causal=True, out_dtype=torch.float32)
+    assert cache.device_status() == 0
+    oc.append(f32(k), f32(v), mb)
+    compare_out(out, attention.attend(f32(q), oc, mb, causal=True), "fused prefill after an injected wait failure")
