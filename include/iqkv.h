@@ -346,7 +346,7 @@ int iq_cache_append_attend(iq_cache* cache, const void* keys, const void* values
  * them.
  * Errors: as iq_attend, plus WORKSPACE when the call needs more scratch than
  * IQ_NOALLOC_SCRATCH_BYTES (use iq_attend with a caller workspace then); calls
- * that take the tensor-memory prefill kernel need only the 4352-byte head.
+ * that take the tensor-memory prefill kernel need only the IQ_WORKSPACE_HEAD_BYTES head.
  * Kernel-side failures land in the shared status word: read it with
  * iq_noalloc_read_status.
  */
